@@ -1,0 +1,206 @@
+/*
+ * moe.h -- C ABI of libmoe: the forward pass of a Kimi K3-style sparse MoE
+ * layer (top-k of E routed experts in a latent space, plus always-on shared
+ * experts) on one NVIDIA GB300 (sm_103a).
+ *
+ * What the layer computes, per token x (bf16, width D):
+ *   xq  = MXFP8(x)                                   activations enter as MXFP8
+ *   z   = xq P_down^T           (D -> L latent)      "Kimi K3 and the New
+ *   l   = z R^T                 (router logits)       Open-Weights Moat",
+ *   top-k on sigmoid(l) + bias; w = sigmoid(l_j) / sum over the winners
+ *                                                     section "How the router
+ *                                                     picks 16 of 896", Fig. 2
+ *   for each winner e_j: h = SiLU(zq W_gate[e]^T) * (zq W_up[e]^T)
+ *                        o_j = MXFP8(h) W_down[e]^T
+ *   c   = sum_j w_j o_j                                weighted sum in the latent
+ *   y   = MXFP8(c) P_up^T + sum_s MXFP8(h_s) S_down[s]^T
+ *   h_s = SiLU(xq S_gate[s]^T) * (xq S_up[s]^T)       shared experts, full width
+ * (section "Sparse computation: latent experts and routing": routed path in a
+ * latent, shared experts at full width, branches summed).  All weights are
+ * MXFP4 (E2M1 elements, one E8M0 scale per 32 along the reduction dim) and
+ * every GEMM input activation is MXFP8 (E4M3, one E8M0 scale per 32):
+ * section "Precision and deployment", Fig. 6.  The dispatch (stable sort of
+ * (token, slot) pairs by expert, per-expert counts/offsets), one GEMM per
+ * expert segment and the gate-weighted combine follow the one-page data path
+ * of "Kimi K3: 2.8 Trillion Parameters, Four Bits at a Time", section "What
+ * it takes to serve it".  With score_fn = MOE_SCORE_SOFTMAX the gates are the
+ * softmax of the winners' logits instead (that page's toy router).
+ *
+ * Byte layouts.  An MXFP4 matrix W[rows][K] is `codes` uint8 [rows][K/2]
+ * (element 2i in the low nibble of byte i, bit 3 of a nibble = sign) plus
+ * `scales` uint8 [rows][K/32] (E8M0, value 2^(code-127)); rows are output
+ * features, K is the reduction dim.  MXFP8 activations are codes uint8
+ * [T][K] (E4M3) plus scales uint8 [T][K/32].  All pointers in this header are
+ * DEVICE pointers on the plan's device unless stated otherwise.
+ *
+ * Errors.  Every call validates its arguments before enqueuing anything and
+ * returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED with nothing enqueued.
+ * CUDA API failures return MOE_ERR_CUDA.  Kernels never trap: a device-side
+ * failure (a bounded wait that ran out) is recorded in a sticky device status
+ * word read by moe_get_device_status().
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* bad pointer, size or shape; nothing enqueued */
+    MOE_ERR_UNSUPPORTED = 2,   /* valid config this build does not run (e.g. no sm_103a device) */
+    MOE_ERR_OOM = 3,           /* device allocation failed inside moe_plan */
+    MOE_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
+    MOE_ERR_TIMEOUT = 5,       /* a kernel's bounded wait ran out (device status) */
+    MOE_ERR_DEVICE = 6         /* other device-side error (device status) */
+} moe_status;
+
+typedef enum {
+    MOE_SCORE_SIGMOID_BIAS = 0, /* sigmoid score, top-k on score + bias, sum-normalised */
+    MOE_SCORE_SOFTMAX = 1       /* top-k on the logit, softmax over the k winners */
+} moe_score_fn;
+
+/* Layer shape.  Constraints (checked by moe_plan): d_model and d_latent
+ * multiples of 128; expert_inter and shared_inter multiples of 64;
+ * 1 <= top_k <= min(n_experts, 32); 1 <= n_experts <= 4096; n_shared >= 0;
+ * 1 <= max_tokens <= 65536. */
+typedef struct {
+    int32_t d_model;       /* D */
+    int32_t d_latent;      /* L */
+    int32_t n_experts;     /* E */
+    int32_t top_k;         /* k */
+    int32_t expert_inter;  /* I: routed expert inner width */
+    int32_t n_shared;      /* S */
+    int32_t shared_inter;  /* Is: shared expert inner width */
+    int32_t max_tokens;    /* largest T a forward call may pass */
+    int32_t score_fn;      /* moe_score_fn */
+} moe_config;
+
+typedef struct {
+    const uint8_t *codes;  /* [rows][K/2] */
+    const uint8_t *scales; /* [rows][K/32] */
+} moe_mx4;
+
+/* Layer weights (device pointers; read only during moe_plan, which copies
+ * and repacks them into plan-owned memory -- the caller may free them when
+ * moe_plan returns). */
+typedef struct {
+    moe_mx4 p_down;           /* [L][D]       latent down-projection */
+    moe_mx4 p_up;             /* [D][L]       latent up-projection   */
+    moe_mx4 w_gate;           /* [E][I][L]    routed gate            */
+    moe_mx4 w_up;             /* [E][I][L]    routed up              */
+    moe_mx4 w_down;           /* [E][L][I]    routed down            */
+    moe_mx4 s_gate;           /* [S][Is][D]   shared gate            */
+    moe_mx4 s_up;             /* [S][Is][D]   shared up              */
+    moe_mx4 s_down;           /* [S][D][Is]   shared down            */
+    const float *router_w;    /* [E][L] fp32 router on the latent    */
+    const float *router_bias; /* [E] fp32 selection bias, or NULL (= 0) */
+} moe_weights;
+
+/* Optional intermediate outputs of one forward call (device pointers; NULL
+ * skips a field).  Row counts use the T of that call.  "Sorted order" is the
+ * stable sort of the flat (token, slot) pairs by expert: row p of a sorted
+ * tensor belongs to token sorted_token[p]. */
+typedef struct {
+    uint8_t *xq, *xs;         /* [T][D], [T][D/32]           MXFP8 of x            */
+    float *z;                 /* [T][L]                      latent, fp32          */
+    uint8_t *zq, *zs;         /* [T][L], [T][L/32]           MXFP8 of z            */
+    uint8_t *hsq, *hss;       /* [T][S*Is], [T][S*Is/32]     MXFP8 shared activation */
+    float *logits;            /* [T][E]                      router logits         */
+    int32_t *topk_idx;        /* [T][k]   slot order: descending key, tie -> lower id */
+    float *topk_w;            /* [T][k]                      gates                 */
+    int32_t *counts;          /* [E]                         tokens per expert     */
+    int32_t *offsets;         /* [E+1]                       exclusive scan        */
+    int32_t *sorted_token;    /* [T*k]                       token of sorted row   */
+    uint8_t *hq, *hqs;        /* [T*k][I], [T*k][I/32]       MXFP8 expert activation, sorted */
+    float *o;                 /* [T*k][L]                    expert outputs, sorted */
+    uint8_t *cq, *cs;         /* [T][L], [T][L/32]           MXFP8 of the combine  */
+    /* Optional array of MOE_NUM_STAGES + 1 cudaEvent_t (created by the caller):
+     * event i is recorded on the forward's stream before stage i, the last one
+     * after the final stage, so the caller can time each stage. */
+    void **stage_events;
+} moe_debug;
+
+/* Stages of moe_forward, in launch order (indices into stage_events):
+ *  0 quantise x      1 down-projection + shared gate/up GEMM   2 router
+ *  3 top-k + gates   4 per-expert counts   5 offsets + work lists
+ *  6 dispatch (ranks, gather)   7 grouped gate/up GEMM   8 grouped down GEMM
+ *  9 combine         10 up-projection + shared down GEMM */
+#define MOE_NUM_STAGES 11
+
+/* Validate `cfg`, allocate all device memory for up to cfg->max_tokens
+ * tokens on `device`, copy and repack `w`, build TMA descriptors.
+ * Host-synchronous; the only call that allocates.  On failure *plan_out is
+ * NULL.  Needs a compute capability 10.3 device. */
+MOE_API moe_status moe_plan(const moe_config *cfg, const moe_weights *w, int device, void **plan_out);
+
+/* Forward pass: x bf16 [T][D] (device, rows 16-byte aligned) -> y fp32
+ * [T][D] (device).  Enqueued on `stream` (a cudaStream_t; NULL = legacy
+ * default stream); no host synchronisation, no allocation.  1 <= T <=
+ * max_tokens.  `dbg` may be NULL.  One plan serves one stream at a time:
+ * calls on different streams that overlap race on the plan's workspace. */
+MOE_API moe_status moe_forward(void *plan, const void *x, int32_t T, float *y, void *stream,
+                       const moe_debug *dbg);
+
+/* Same as moe_forward with HOST buffers: copies x (host, bf16 [T][D]) to the
+ * device, runs the layer and copies y back to host memory y_host ([T][D]
+ * fp32), all on `stream`, then synchronises the stream.  Page-locked host
+ * buffers make the copies asynchronous. */
+MOE_API moe_status moe_forward_host(void *plan, const uint16_t *x_host, int32_t T, float *y_host,
+                            void *stream);
+
+/* Sticky device-side status of the plan (call after synchronising the stream
+ * of the last forward): MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE.  Reading it
+ * clears it. */
+MOE_API moe_status moe_get_device_status(void *plan);
+
+/* Bytes of device memory the plan owns (weights + workspace). */
+MOE_API size_t moe_workspace_bytes(const void *plan);
+
+/* Release everything the plan owns.  NULL-safe.  Synchronises the device. */
+MOE_API void moe_free(void *plan);
+
+/* Static string naming a status code. */
+MOE_API const char *moe_status_str(moe_status s);
+
+/* Weight preparation (not part of the forward pass): MXFP4-encode fp32
+ * w[rows][K] (device) into codes [rows][K/2] and scales [rows][K/32]
+ * (device), with the block encoder of "Kimi K3: 2.8 Trillion Parameters,
+ * Four Bits at a Time", section "Four bits from the start": per 32-block,
+ * shared exponent floor(log2 amax) - 2 (clamped to [-127, 127]; an all-zero
+ * block gets codes 0 and scale code 0), elements |v|/2^e clipped to 6 and
+ * rounded to the nearest E2M1 level, the smaller level on a tie.  K must be a
+ * multiple of 32.  Enqueued on `stream` on the current device. */
+MOE_API moe_status moe_mxfp4_encode(const float *w, int64_t rows, int64_t K, uint8_t *codes,
+                            uint8_t *scales, void *stream);
+
+/* One block-scaled GEMM on the layer's tcgen05 engine, for callers that
+ * need the raw product:
+ *   out[n][m] = sum_k dq(B[n][k]) * dq(A[m][k])      (fp32 accumulate)
+ * A: MXFP4 [M][K] (a_codes [M][K/2], 32-byte aligned; a_scales [M][K/32]);
+ * B: MXFP8 [N][K] (b_codes [N][K], 16-byte aligned; b_scales [N][K/32]);
+ * out: fp32 [N][M].  All device pointers on the current device.  M and K
+ * multiples of 128, 1 <= N <= 2^24.  The scale factors are re-arranged into
+ * the engine's layouts in scratch memory that this call obtains with
+ * cudaMallocAsync on `stream` and releases with cudaFreeAsync before it
+ * returns.  dev_status (device int32, optional) receives a non-zero code if a
+ * bounded wait inside the kernel ran out.  Asynchronous on `stream`. */
+MOE_API moe_status moe_mx_gemm(const uint8_t *a_codes, const uint8_t *a_scales, int32_t M, const uint8_t *b_codes,
+                       const uint8_t *b_scales, int32_t N, int32_t K, float *out, int32_t *dev_status,
+                       void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

@@ -1,0 +1,681 @@
+// C ABI of libmoe (declared in include/moe.h): plan creation (validation,
+// allocation, weight repacking, TMA descriptors), the forward pass as a fixed
+// sequence of kernel launches on the caller's stream, and utilities.
+//
+// Forward pass (steps of the layer; see include/moe.h for the math):
+//   1 quant_x       x bf16 -> MXFP8 codes + scale planes
+//   2 GEMM (dense)  [P_down ; shared gate/up] x xq: z (fp32 + MXFP8) and the
+//                   shared experts' SiLU-gated activation (MXFP8) in one pass
+//   3 router        logits = z R^T (fp32)
+//   4 top-k         expert ids, gates, per-expert token bitmaps
+//   5 scan          per-expert counts / prefix popcounts
+//   6 work lists    offsets (exact and 16-row padded) + grouped GEMM items
+//   7 scatter       stable ranks -> permuted rows; gather zq rows
+//   8 GEMM grouped  gate/up per expert segment, SiLU * up -> MXFP8
+//   9 GEMM grouped  down per expert segment -> o (fp32)
+//  10 combine       c = sum_j w_j o_j (slot order) -> MXFP8 into the
+//                   concatenated [c | h_shared] activation buffer
+//  11 GEMM (dense)  y = [cq | h_sq] [P_up | S_down]^T: the routed branch's
+//                   up-projection and the shared experts' down-projection
+//                   summed in one accumulator
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/moe.h"
+#include "internal.h"
+
+using namespace moe;
+
+namespace {
+
+// Bytes that one 128x128 MXFP4 TMA box (16U4_ALIGN16B) counts toward the
+// mbarrier transaction: the shared-memory footprint of the unpacked box.
+#ifndef MOE_A_TX_BYTES
+#define MOE_A_TX_BYTES 16384
+#endif
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// MXFP4 weights [rows][K] (packed codes), 128x128-element boxes.
+bool map_mx4(CUtensorMap* m, const void* codes, int64_t rows, int64_t K) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+    cuuint32_t box[2] = {128, 128};
+    cuuint32_t es[2] = {1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(codes), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// MXFP8 activation codes [rows][K], 128-wide x 16-row boxes.
+bool map_mx8(CUtensorMap* m, const void* codes, int64_t rows, int64_t K) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+    cuuint32_t box[2] = {128, 16};
+    cuuint32_t es[2] = {1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(codes), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline int64_t rup(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
+
+struct Plan {
+    moe_config cfg;
+    int device = 0, num_sms = 0;
+    int D, L, E, k, I, Ip, S, Is, SIs, Kcat, rowsA2, T_max, T_pad, W_max;
+    int64_t R_pad, items_cap7, items_cap8;
+    size_t bytes = 0;
+    std::vector<void*> allocs;
+    // weights
+    uint8_t *a2c, *a2sf, *w13c, *w13sf, *w2c, *w2sf, *a10c, *a10sf;
+    float *router, *bias;
+    // workspace
+    uint8_t *xq, *xsf, *zq, *zsf, *act, *actsf, *zqp, *zqpsf, *hq, *hqsf;
+    float *z, *logits, *gw, *o;
+    uint32_t* sel;
+    int32_t *idx, *wpre, *counts, *offsets, *seg, *slot_pos, *canon_to_pad, *sorted_token;
+    int4 *items7, *items8;
+    int* n_items;   // [2]
+    int* status;
+    void* x_stage;
+    float* y_stage;
+    CUtensorMap tA2, tB2, tA7, tB7, tA8, tB8, tA10, tB10;
+};
+
+template <typename T>
+cudaError_t palloc(Plan* p, T** out, size_t bytes) {
+    void* ptr = nullptr;
+    bytes = (bytes + 255) & ~size_t(255);
+    if (bytes == 0) bytes = 256;
+    cudaError_t err = cudaMalloc(&ptr, bytes);
+    if (err != cudaSuccess) return err;
+    err = cudaMemset(ptr, 0, bytes);
+    if (err != cudaSuccess) {
+        cudaFree(ptr);
+        return err;
+    }
+    p->allocs.push_back(ptr);
+    p->bytes += bytes;
+    *out = static_cast<T*>(ptr);
+    return cudaSuccess;
+}
+
+void plan_release(Plan* p) {
+    if (!p) return;
+    int cur = 0;
+    cudaGetDevice(&cur);
+    cudaSetDevice(p->device);
+    cudaDeviceSynchronize();
+    for (void* a : p->allocs) cudaFree(a);
+    cudaSetDevice(cur);
+    delete p;
+}
+
+struct DevGuard {
+    int prev = -1;
+    explicit DevGuard(int d) {
+        cudaGetDevice(&prev);
+        if (prev != d) cudaSetDevice(d);
+    }
+    ~DevGuard() {
+        if (prev >= 0) cudaSetDevice(prev);
+    }
+};
+
+// Copy rows described by host-side source row pointers into dst (device).
+cudaError_t copy_rows(uint8_t* dst, int64_t dst_stride, const std::vector<const uint8_t*>& rows, int64_t row_bytes) {
+    if (rows.empty()) return cudaSuccess;
+    const uint8_t** d_rows = nullptr;
+    cudaError_t err = cudaMalloc(&d_rows, rows.size() * sizeof(void*));
+    if (err != cudaSuccess) return err;
+    err = cudaMemcpy(d_rows, rows.data(), rows.size() * sizeof(void*), cudaMemcpyHostToDevice);
+    if (err == cudaSuccess)
+        err = launch_copy_rows(dst, dst_stride, d_rows, static_cast<int64_t>(rows.size()), row_bytes, 0);
+    if (err == cudaSuccess) err = cudaDeviceSynchronize();
+    cudaFree(d_rows);
+    return err;
+}
+
+// Repack one weight operand: `rows` destination rows, each filled from up to
+// `nseg` K-segments (source row pointers for codes and scales, and the K
+// width of the segment).  Produces packed codes [rows][Kp/2] and the scale
+// atoms [rows/128][Kp/128][512]; columns not covered stay zero.
+struct Segment {
+    std::vector<const uint8_t*> code_rows, scale_rows;
+    int64_t k_off, k_len;
+};
+cudaError_t repack(Plan* p, const std::vector<Segment>& segs, int64_t rows, int64_t Kp, uint8_t** codes_out,
+                   uint8_t** atoms_out) {
+    cudaError_t err = palloc(p, codes_out, static_cast<size_t>(rows * Kp / 2));
+    if (err != cudaSuccess) return err;
+    err = palloc(p, atoms_out, static_cast<size_t>(rows * Kp / 32));
+    if (err != cudaSuccess) return err;
+    uint8_t* rm = nullptr;
+    err = cudaMalloc(&rm, static_cast<size_t>(rows * Kp / 32));
+    if (err != cudaSuccess) return err;
+    err = cudaMemset(rm, 0, static_cast<size_t>(rows * Kp / 32));
+    for (const Segment& s : segs) {
+        if (err != cudaSuccess) break;
+        err = copy_rows(*codes_out + s.k_off / 2, Kp / 2, s.code_rows, s.k_len / 2);
+        if (err == cudaSuccess) err = copy_rows(rm + s.k_off / 32, Kp / 32, s.scale_rows, s.k_len / 32);
+    }
+    if (err == cudaSuccess) err = launch_sf_atoms(rm, rows, Kp / 32, *atoms_out, 0);
+    if (err == cudaSuccess) err = cudaDeviceSynchronize();
+    cudaFree(rm);
+    return err;
+}
+
+moe_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return MOE_OK;
+    if (e == cudaErrorMemoryAllocation) return MOE_ERR_OOM;
+    return MOE_ERR_CUDA;
+}
+
+GemmParams gemm_base(const CUtensorMap& A, const CUtensorMap& B, const uint8_t* sfa, const uint8_t* sfb,
+                     int64_t sfb_pitch, int K, int n_max, int a_rows, int b_rows, int* status) {
+    GemmParams g;
+    std::memset(&g, 0, sizeof(g));
+    g.tmA = A;
+    g.tmB = B;
+    g.sfa = sfa;
+    g.sfb = sfb;
+    g.sfb_pitch = sfb_pitch;
+    g.KT = K / kBlockK;
+    g.n_max = n_max;
+    g.stages = gemm_stages(n_max);
+    g.stage_bytes = gemm_stage_bytes(n_max);
+    g.a_tx_bytes = MOE_A_TX_BYTES;
+    g.a_rows = a_rows;
+    g.b_rows = b_rows;
+    g.status = status;
+    return g;
+}
+
+int pick_n_max(int T) {
+    const int tiles = (T + kNMax - 1) / kNMax;
+    const int per = (T + tiles - 1) / tiles;
+    return static_cast<int>(rup(per, 16));
+}
+
+moe_status validate(const moe_config* c) {
+    if (!c) return MOE_ERR_INVALID_ARG;
+    if (c->d_model <= 0 || c->d_latent <= 0 || c->d_model % 128 || c->d_latent % 128) return MOE_ERR_INVALID_ARG;
+    if (c->expert_inter <= 0 || c->expert_inter % 64) return MOE_ERR_INVALID_ARG;
+    if (c->n_shared < 0 || (c->n_shared > 0 && (c->shared_inter <= 0 || c->shared_inter % 64)))
+        return MOE_ERR_INVALID_ARG;
+    if (c->n_experts < 1 || c->n_experts > 4096) return MOE_ERR_INVALID_ARG;
+    if (c->top_k < 1 || c->top_k > 32 || c->top_k > c->n_experts) return MOE_ERR_INVALID_ARG;
+    if (c->max_tokens < 1 || c->max_tokens > 65536) return MOE_ERR_INVALID_ARG;
+    if (c->score_fn != MOE_SCORE_SIGMOID_BIAS && c->score_fn != MOE_SCORE_SOFTMAX) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+bool mx_ok(const moe_mx4& m) { return m.codes && m.scales; }
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_str(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported";
+        case MOE_ERR_OOM: return "out of device memory";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_TIMEOUT: return "device wait timed out";
+        case MOE_ERR_DEVICE: return "device-side error";
+    }
+    return "unknown status";
+}
+
+moe_status moe_plan(const moe_config* cfg, const moe_weights* w, int device, void** plan_out) {
+    if (!plan_out) return MOE_ERR_INVALID_ARG;
+    *plan_out = nullptr;
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    if (!w || !mx_ok(w->p_down) || !mx_ok(w->p_up) || !mx_ok(w->w_gate) || !mx_ok(w->w_up) || !mx_ok(w->w_down) ||
+        !w->router_w)
+        return MOE_ERR_INVALID_ARG;
+    if (cfg->n_shared > 0 && (!mx_ok(w->s_gate) || !mx_ok(w->s_up) || !mx_ok(w->s_down))) return MOE_ERR_INVALID_ARG;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return MOE_ERR_UNSUPPORTED;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return MOE_ERR_CUDA;
+    if (prop.major != 10 || prop.minor != 3) return MOE_ERR_UNSUPPORTED;
+    if (!encode_fn()) return MOE_ERR_UNSUPPORTED;
+
+    DevGuard guard(device);
+    Plan* p = new (std::nothrow) Plan();
+    if (!p) return MOE_ERR_OOM;
+    p->cfg = *cfg;
+    p->device = device;
+    p->num_sms = prop.multiProcessorCount;
+    p->D = cfg->d_model;
+    p->L = cfg->d_latent;
+    p->E = cfg->n_experts;
+    p->k = cfg->top_k;
+    p->I = cfg->expert_inter;
+    p->Ip = static_cast<int>(rup(p->I, 128));
+    p->S = cfg->n_shared;
+    p->Is = p->S > 0 ? cfg->shared_inter : 0;
+    p->SIs = p->S * p->Is;
+    p->Kcat = static_cast<int>(rup(p->L + p->SIs, 128));
+    p->rowsA2 = p->L + 2 * p->SIs;
+    p->T_max = cfg->max_tokens;
+    p->T_pad = static_cast<int>(rup(p->T_max, 16));
+    p->W_max = (p->T_max + 31) / 32;
+    p->R_pad = rup(static_cast<int64_t>(p->T_max) * p->k + 15LL * p->E, 16);
+    p->items_cap7 = (static_cast<int64_t>(p->T_max) * p->k / 16 + p->E + 1) * (2 * p->I / 128);
+    p->items_cap8 = (static_cast<int64_t>(p->T_max) * p->k / 16 + p->E + 1) * (p->L / 128);
+
+    cudaError_t err = gemm_setup();
+    if (err == cudaSuccess) err = kernels_setup();
+    const int D = p->D, L = p->L, E = p->E, I = p->I, Ip = p->Ip, S = p->S, Is = p->Is;
+    const int64_t Tp = p->T_pad, Rp = p->R_pad;
+#define TRY(x)                          \
+    do {                                \
+        if (err == cudaSuccess) err = (x); \
+    } while (0)
+    // ---------------------------------------------------------------- weights
+    {
+        // A2: rows [0, L) = P_down; then per shared expert, 128-row tiles of
+        // 64 gate rows followed by the 64 matching up rows.
+        Segment s;
+        s.k_off = 0;
+        s.k_len = D;
+        for (int r = 0; r < p->rowsA2; ++r) {
+            const uint8_t *c, *sc;
+            if (r < L) {
+                c = w->p_down.codes + static_cast<int64_t>(r) * (D / 2);
+                sc = w->p_down.scales + static_cast<int64_t>(r) * (D / 32);
+            } else {
+                const int rr = r - L, sh = rr / (2 * Is), within = rr % (2 * Is);
+                const int t = within / 128, h = within % 128;
+                const moe_mx4& src = (h < 64) ? w->s_gate : w->s_up;
+                const int64_t srow = static_cast<int64_t>(sh) * Is + 64 * t + (h % 64);
+                c = src.codes + srow * (D / 2);
+                sc = src.scales + srow * (D / 32);
+            }
+            s.code_rows.push_back(c);
+            s.scale_rows.push_back(sc);
+        }
+        TRY(repack(p, {s}, p->rowsA2, D, &p->a2c, &p->a2sf));
+    }
+    {
+        // W13: per expert, 128-row tiles of 64 gate rows + the 64 matching up rows.
+        Segment s;
+        s.k_off = 0;
+        s.k_len = L;
+        const int64_t rows = static_cast<int64_t>(E) * 2 * I;
+        s.code_rows.reserve(rows);
+        s.scale_rows.reserve(rows);
+        for (int64_t r = 0; r < rows; ++r) {
+            const int64_t e = r / (2 * I), within = r % (2 * I), t = within / 128, h = within % 128;
+            const moe_mx4& src = (h < 64) ? w->w_gate : w->w_up;
+            const int64_t srow = e * I + 64 * t + (h % 64);
+            s.code_rows.push_back(src.codes + srow * (L / 2));
+            s.scale_rows.push_back(src.scales + srow * (L / 32));
+        }
+        TRY(repack(p, {s}, rows, L, &p->w13c, &p->w13sf));
+    }
+    {
+        // W2: [E*L][Ip], K zero-padded from I to a multiple of 128.
+        Segment s;
+        s.k_off = 0;
+        s.k_len = I;
+        const int64_t rows = static_cast<int64_t>(E) * L;
+        for (int64_t r = 0; r < rows; ++r) {
+            s.code_rows.push_back(w->w_down.codes + r * (I / 2));
+            s.scale_rows.push_back(w->w_down.scales + r * (I / 32));
+        }
+        TRY(repack(p, {s}, rows, Ip, &p->w2c, &p->w2sf));
+    }
+    {
+        // A10: [D][Kcat] = [P_up | S_down[0] | S_down[1] | ...] along K.
+        std::vector<Segment> segs(1 + S);
+        segs[0].k_off = 0;
+        segs[0].k_len = L;
+        for (int d = 0; d < D; ++d) {
+            segs[0].code_rows.push_back(w->p_up.codes + static_cast<int64_t>(d) * (L / 2));
+            segs[0].scale_rows.push_back(w->p_up.scales + static_cast<int64_t>(d) * (L / 32));
+        }
+        for (int sh = 0; sh < S; ++sh) {
+            Segment& g = segs[1 + sh];
+            g.k_off = L + static_cast<int64_t>(sh) * Is;
+            g.k_len = Is;
+            for (int d = 0; d < D; ++d) {
+                const int64_t srow = static_cast<int64_t>(sh) * D + d;
+                g.code_rows.push_back(w->s_down.codes + srow * (Is / 2));
+                g.scale_rows.push_back(w->s_down.scales + srow * (Is / 32));
+            }
+        }
+        TRY(repack(p, segs, D, p->Kcat, &p->a10c, &p->a10sf));
+    }
+    TRY(palloc(p, &p->router, sizeof(float) * E * L));
+    TRY(cudaMemcpy(p->router, w->router_w, sizeof(float) * E * L, cudaMemcpyDeviceToDevice));
+    p->bias = nullptr;
+    if (w->router_bias) {
+        TRY(palloc(p, &p->bias, sizeof(float) * E));
+        TRY(cudaMemcpy(p->bias, w->router_bias, sizeof(float) * E, cudaMemcpyDeviceToDevice));
+    }
+    // ---------------------------------------------------------------- workspace
+    TRY(palloc(p, &p->xq, Tp * D));
+    TRY(palloc(p, &p->xsf, (D / 128) * Tp * 4));
+    TRY(palloc(p, &p->z, sizeof(float) * Tp * L));
+    TRY(palloc(p, &p->zq, Tp * L));
+    TRY(palloc(p, &p->zsf, (L / 128) * Tp * 4));
+    TRY(palloc(p, &p->act, Tp * p->Kcat));
+    TRY(palloc(p, &p->actsf, (p->Kcat / 128) * Tp * 4));
+    TRY(palloc(p, &p->logits, sizeof(float) * p->T_max * E));
+    TRY(palloc(p, &p->idx, sizeof(int32_t) * p->T_max * p->k));
+    TRY(palloc(p, &p->gw, sizeof(float) * p->T_max * p->k));
+    TRY(palloc(p, &p->sel, sizeof(uint32_t) * E * p->W_max));
+    TRY(palloc(p, &p->wpre, sizeof(int32_t) * E * p->W_max));
+    TRY(palloc(p, &p->counts, sizeof(int32_t) * E));
+    TRY(palloc(p, &p->offsets, sizeof(int32_t) * (E + 1)));
+    TRY(palloc(p, &p->seg, sizeof(int32_t) * (E + 1)));
+    TRY(palloc(p, &p->slot_pos, sizeof(int32_t) * p->T_max * p->k));
+    TRY(palloc(p, &p->canon_to_pad, sizeof(int32_t) * p->T_max * p->k));
+    TRY(palloc(p, &p->sorted_token, sizeof(int32_t) * p->T_max * p->k));
+    TRY(palloc(p, &p->zqp, Rp * L));
+    TRY(palloc(p, &p->zqpsf, (L / 128) * Rp * 4));
+    TRY(palloc(p, &p->hq, Rp * Ip));
+    TRY(palloc(p, &p->hqsf, (Ip / 128) * Rp * 4));
+    TRY(palloc(p, &p->o, sizeof(float) * Rp * L));
+    TRY(palloc(p, &p->items7, sizeof(int4) * p->items_cap7));
+    TRY(palloc(p, &p->items8, sizeof(int4) * p->items_cap8));
+    TRY(palloc(p, &p->n_items, sizeof(int) * 4));
+    TRY(palloc(p, &p->status, sizeof(int) * 4));
+    TRY(palloc(p, &p->x_stage, sizeof(uint16_t) * p->T_max * D));
+    TRY(palloc(p, &p->y_stage, sizeof(float) * p->T_max * D));
+#undef TRY
+    if (err != cudaSuccess) {
+        st = cuda_status(err);
+        plan_release(p);
+        return st;
+    }
+    // ---------------------------------------------------------------- TMA descriptors
+    bool ok = map_mx4(&p->tA2, p->a2c, p->rowsA2, D) && map_mx8(&p->tB2, p->xq, Tp, D) &&
+              map_mx4(&p->tA7, p->w13c, static_cast<int64_t>(E) * 2 * I, L) && map_mx8(&p->tB7, p->zqp, Rp, L) &&
+              map_mx4(&p->tA8, p->w2c, static_cast<int64_t>(E) * L, Ip) && map_mx8(&p->tB8, p->hq, Rp, Ip) &&
+              map_mx4(&p->tA10, p->a10c, D, p->Kcat) && map_mx8(&p->tB10, p->act, Tp, p->Kcat);
+    if (!ok) {
+        plan_release(p);
+        return MOE_ERR_CUDA;
+    }
+    *plan_out = p;
+    return MOE_OK;
+}
+
+moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* stream, const moe_debug* dbg) {
+    Plan* p = static_cast<Plan*>(plan);
+    if (!p || !x || !y) return MOE_ERR_INVALID_ARG;
+    if (T < 1 || T > p->T_max) return MOE_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(y) & 3)) return MOE_ERR_INVALID_ARG;
+    DevGuard guard(p->device);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int D = p->D, L = p->L, E = p->E, k = p->k, I = p->I, Ip = p->Ip;
+    const int W = (T + 31) / 32;
+    const int64_t Tp = p->T_pad, Rp = p->R_pad;
+    const int nmax_dense = pick_n_max(T);
+    const int nmax_grp = static_cast<int>(std::min<int64_t>(kNMax, rup(T, 16)));
+    cudaError_t err = cudaSuccess;
+#define TRY(x)                          \
+    do {                                \
+        if (err == cudaSuccess) err = (x); \
+    } while (0)
+    cudaEvent_t* ev = (dbg && dbg->stage_events) ? reinterpret_cast<cudaEvent_t*>(dbg->stage_events) : nullptr;
+    auto mark = [&](int i) {
+        if (ev && err == cudaSuccess) err = cudaEventRecord(ev[i], s);
+    };
+    TRY(cudaMemsetAsync(p->sel, 0, sizeof(uint32_t) * E * W, s));
+    mark(0);
+    // 1. x -> MXFP8
+    TRY(launch_quant_x(static_cast<const __nv_bfloat16*>(x), T, D, p->xq, p->xsf, Tp, s));
+    mark(1);
+    // 2. latent down-projection + shared gate/up
+    {
+        GemmParams g = gemm_base(p->tA2, p->tB2, p->a2sf, p->xsf, Tp, D, nmax_dense, p->rowsA2, static_cast<int>(Tp),
+                                 p->status);
+        g.dense = 1;
+        g.m_tiles = p->rowsA2 / kBlockM;
+        g.n_tokens = T;
+        g.epi_split = L / kBlockM;
+        g.epi[0] = EpiParams{EPI_QUANT, 0, 0, 0, p->z, L, p->zq, L, p->zsf, Tp};
+        g.epi[1] = EpiParams{EPI_SILU_QUANT, L / kBlockM, L, 0, nullptr, 0, p->act, p->Kcat, p->actsf, Tp};
+        const int items = g.m_tiles * ((T + g.n_max - 1) / g.n_max);
+        TRY(launch_gemm(g, std::min(items, p->num_sms), s));
+    }
+    // 3. router logits, 4. top-k + gates + bitmaps
+    mark(2);
+    TRY(launch_router(p->z, p->router, p->logits, T, E, L, s));
+    mark(3);
+    TRY(launch_topk(p->logits, p->bias, T, E, k, p->cfg.score_fn == MOE_SCORE_SOFTMAX, p->idx, p->gw, p->sel, W, s));
+    // 5. per-expert prefix counts, 6. offsets + work lists
+    mark(4);
+    TRY(launch_expert_scan(p->sel, E, W, p->wpre, p->counts, s));
+    mark(5);
+    {
+        WorkListArgs a;
+        a.counts = p->counts;
+        a.E = E;
+        a.offsets = p->offsets;
+        a.seg = p->seg;
+        a.items1 = p->items7;
+        a.n_items1 = p->n_items;
+        a.n_max1 = nmax_grp;
+        a.mt1 = 2 * I / kBlockM;
+        a.a_rows_per_e1 = 2 * I;
+        a.items2 = p->items8;
+        a.n_items2 = p->n_items + 1;
+        a.n_max2 = nmax_grp;
+        a.mt2 = L / kBlockM;
+        a.a_rows_per_e2 = L;
+        TRY(launch_worklist(a, s));
+    }
+    // 7. stable ranks, permuted rows, gather of zq
+    mark(6);
+    {
+        ScatterArgs a;
+        a.idx = p->idx;
+        a.T = T;
+        a.k = k;
+        a.W = W;
+        a.sel = p->sel;
+        a.wpre = p->wpre;
+        a.offsets = p->offsets;
+        a.seg = p->seg;
+        a.slot_pos = p->slot_pos;
+        a.canon_to_pad = p->canon_to_pad;
+        a.sorted_token = p->sorted_token;
+        a.zq = p->zq;
+        a.zsf = p->zsf;
+        a.zsf_pitch = Tp;
+        a.L = L;
+        a.zq_perm = p->zqp;
+        a.zq_perm_sf = p->zqpsf;
+        a.perm_pitch = Rp;
+        TRY(launch_scatter(a, s));
+    }
+    // 8. routed gate/up + SiLU -> MXFP8
+    mark(7);
+    {
+        GemmParams g = gemm_base(p->tA7, p->tB7, p->w13sf, p->zqpsf, Rp, L, nmax_grp, E * 2 * I,
+                                 static_cast<int>(Rp), p->status);
+        g.dense = 0;
+        g.items = p->items7;
+        g.n_items = p->n_items;
+        g.epi[0] = EpiParams{EPI_SILU_QUANT, 0, 0, 0, nullptr, 0, p->hq, Ip, p->hqsf, Rp};
+        TRY(launch_gemm(g, p->num_sms, s));
+    }
+    // 9. routed down -> o
+    mark(8);
+    {
+        GemmParams g = gemm_base(p->tA8, p->tB8, p->w2sf, p->hqsf, Rp, Ip, nmax_grp, E * L, static_cast<int>(Rp),
+                                 p->status);
+        g.dense = 0;
+        g.items = p->items8;
+        g.n_items = p->n_items + 1;
+        g.epi[0] = EpiParams{EPI_F32, 0, 0, 0, p->o, L, nullptr, 0, nullptr, 0};
+        TRY(launch_gemm(g, p->num_sms, s));
+    }
+    // 10. weighted combine -> MXFP8 into columns [0, L) of the concatenated activation
+    mark(9);
+    TRY(launch_combine(p->o, p->slot_pos, p->gw, T, k, L, p->act, p->Kcat, p->actsf, Tp, s));
+    // 11. y = [cq | h_sq] [P_up | S_down]^T
+    mark(10);
+    {
+        GemmParams g = gemm_base(p->tA10, p->tB10, p->a10sf, p->actsf, Tp, p->Kcat, nmax_dense, D,
+                                 static_cast<int>(Tp), p->status);
+        g.dense = 1;
+        g.m_tiles = D / kBlockM;
+        g.n_tokens = T;
+        g.epi_split = 1 << 30;
+        g.epi[0] = EpiParams{EPI_F32, 0, 0, 0, y, D, nullptr, 0, nullptr, 0};
+        const int items = g.m_tiles * ((T + g.n_max - 1) / g.n_max);
+        TRY(launch_gemm(g, std::min(items, p->num_sms), s));
+    }
+    mark(MOE_NUM_STAGES);
+    // intermediate outputs on request
+    if (dbg && err == cudaSuccess) {
+        const int S = p->S, SIs = p->SIs;
+        const int64_t TK = static_cast<int64_t>(T) * k;
+        if (dbg->xq) TRY(cudaMemcpyAsync(dbg->xq, p->xq, static_cast<size_t>(T) * D, cudaMemcpyDeviceToDevice, s));
+        if (dbg->xs) TRY(launch_export_sf(p->xsf, Tp, nullptr, T, D / 32, 0, dbg->xs, s));
+        if (dbg->z) TRY(cudaMemcpyAsync(dbg->z, p->z, sizeof(float) * T * L, cudaMemcpyDeviceToDevice, s));
+        if (dbg->zq) TRY(cudaMemcpyAsync(dbg->zq, p->zq, static_cast<size_t>(T) * L, cudaMemcpyDeviceToDevice, s));
+        if (dbg->zs) TRY(launch_export_sf(p->zsf, Tp, nullptr, T, L / 32, 0, dbg->zs, s));
+        if (S > 0 && dbg->hsq)
+            TRY(cudaMemcpy2DAsync(dbg->hsq, SIs, p->act + L, p->Kcat, SIs, T, cudaMemcpyDeviceToDevice, s));
+        if (S > 0 && dbg->hss) TRY(launch_export_sf(p->actsf, Tp, nullptr, T, SIs / 32, L / 32, dbg->hss, s));
+        if (dbg->logits)
+            TRY(cudaMemcpyAsync(dbg->logits, p->logits, sizeof(float) * T * E, cudaMemcpyDeviceToDevice, s));
+        if (dbg->topk_idx) TRY(cudaMemcpyAsync(dbg->topk_idx, p->idx, sizeof(int32_t) * TK, cudaMemcpyDeviceToDevice, s));
+        if (dbg->topk_w) TRY(cudaMemcpyAsync(dbg->topk_w, p->gw, sizeof(float) * TK, cudaMemcpyDeviceToDevice, s));
+        if (dbg->counts) TRY(cudaMemcpyAsync(dbg->counts, p->counts, sizeof(int32_t) * E, cudaMemcpyDeviceToDevice, s));
+        if (dbg->offsets)
+            TRY(cudaMemcpyAsync(dbg->offsets, p->offsets, sizeof(int32_t) * (E + 1), cudaMemcpyDeviceToDevice, s));
+        if (dbg->sorted_token)
+            TRY(cudaMemcpyAsync(dbg->sorted_token, p->sorted_token, sizeof(int32_t) * TK, cudaMemcpyDeviceToDevice, s));
+        if (dbg->hq) TRY(launch_gather_rows(p->hq, Ip, p->canon_to_pad, TK, I, dbg->hq, I, s));
+        if (dbg->hqs) TRY(launch_export_sf(p->hqsf, Rp, p->canon_to_pad, TK, I / 32, 0, dbg->hqs, s));
+        if (dbg->o)
+            TRY(launch_gather_rows(reinterpret_cast<const uint8_t*>(p->o), sizeof(float) * L, p->canon_to_pad, TK,
+                                   sizeof(float) * L, reinterpret_cast<uint8_t*>(dbg->o), sizeof(float) * L, s));
+        if (dbg->cq) TRY(cudaMemcpy2DAsync(dbg->cq, L, p->act, p->Kcat, L, T, cudaMemcpyDeviceToDevice, s));
+        if (dbg->cs) TRY(launch_export_sf(p->actsf, Tp, nullptr, T, L / 32, 0, dbg->cs, s));
+    }
+#undef TRY
+    return cuda_status(err);
+}
+
+moe_status moe_forward_host(void* plan, const uint16_t* x_host, int32_t T, float* y_host, void* stream) {
+    Plan* p = static_cast<Plan*>(plan);
+    if (!p || !x_host || !y_host) return MOE_ERR_INVALID_ARG;
+    if (T < 1 || T > p->T_max) return MOE_ERR_INVALID_ARG;
+    DevGuard guard(p->device);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t err = cudaMemcpyAsync(p->x_stage, x_host, sizeof(uint16_t) * T * p->D, cudaMemcpyHostToDevice, s);
+    if (err != cudaSuccess) return cuda_status(err);
+    moe_status st = moe_forward(plan, p->x_stage, T, p->y_stage, stream, nullptr);
+    if (st != MOE_OK) return st;
+    err = cudaMemcpyAsync(y_host, p->y_stage, sizeof(float) * T * p->D, cudaMemcpyDeviceToHost, s);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(s);
+    return cuda_status(err);
+}
+
+moe_status moe_get_device_status(void* plan) {
+    Plan* p = static_cast<Plan*>(plan);
+    if (!p) return MOE_ERR_INVALID_ARG;
+    DevGuard guard(p->device);
+    int code = 0;
+    if (cudaMemcpy(&code, p->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    if (code == 0) return MOE_OK;
+    cudaMemset(p->status, 0, sizeof(int));
+    return (code == DEV_BAD_WORK) ? MOE_ERR_DEVICE : MOE_ERR_TIMEOUT;
+}
+
+size_t moe_workspace_bytes(const void* plan) {
+    const Plan* p = static_cast<const Plan*>(plan);
+    return p ? p->bytes : 0;
+}
+
+void moe_free(void* plan) { plan_release(static_cast<Plan*>(plan)); }
+
+moe_status moe_mxfp4_encode(const float* w, int64_t rows, int64_t K, uint8_t* codes, uint8_t* scales,
+                            void* stream) {
+    if (!w || !codes || !scales || rows < 0 || K <= 0 || K % 32) return MOE_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(w) & 15 || reinterpret_cast<uintptr_t>(codes) & 15) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_mxfp4_encode(w, rows, K, codes, scales, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_mx_gemm(const uint8_t* a_codes, const uint8_t* a_scales, int32_t M, const uint8_t* b_codes,
+                       const uint8_t* b_scales, int32_t N, int32_t K, float* out, int32_t* dev_status,
+                       void* stream) {
+    if (!a_codes || !a_scales || !b_codes || !b_scales || !out) return MOE_ERR_INVALID_ARG;
+    if (M <= 0 || M % 128 || K <= 0 || K % 128 || N <= 0 || N > (1 << 24)) return MOE_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(a_codes) & 31) || (reinterpret_cast<uintptr_t>(b_codes) & 15) ||
+        (reinterpret_cast<uintptr_t>(out) & 3))
+        return MOE_ERR_INVALID_ARG;
+    if (!encode_fn()) return MOE_ERR_UNSUPPORTED;
+    int dev = 0, sms = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err == cudaSuccess) err = gemm_setup();
+    if (err != cudaSuccess) return cuda_status(err);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t Np = rup(N, 16);
+    const size_t atom_bytes = static_cast<size_t>(M) * K / 32;
+    const size_t plane_bytes = static_cast<size_t>(K / 128) * Np * 4;
+    CUtensorMap tA, tB;
+    if (!map_mx4(&tA, a_codes, M, K) || !map_mx8(&tB, b_codes, N, K)) return MOE_ERR_INVALID_ARG;
+    uint8_t* scratch = nullptr;
+    err = cudaMallocAsync(reinterpret_cast<void**>(&scratch), atom_bytes + plane_bytes + 256, s);
+    if (err != cudaSuccess) return cuda_status(err);
+    uint8_t* atoms = scratch;
+    uint8_t* planes = scratch + atom_bytes;
+    int32_t* st = dev_status ? dev_status : reinterpret_cast<int32_t*>(scratch + atom_bytes + plane_bytes);
+    err = cudaMemsetAsync(planes, 0, plane_bytes + 256, s);
+    if (err == cudaSuccess) err = launch_sf_atoms(a_scales, M, K / 32, atoms, s);
+    if (err == cudaSuccess) err = launch_sf_planes(b_scales, N, K / 32, planes, Np, s);
+    if (err == cudaSuccess) {
+        const int nmax = pick_n_max(N);
+        GemmParams g = gemm_base(tA, tB, atoms, planes, Np, K, nmax, M, static_cast<int>(Np), st);
+        g.dense = 1;
+        g.m_tiles = M / kBlockM;
+        g.n_tokens = N;
+        g.epi_split = 1 << 30;
+        g.epi[0] = EpiParams{EPI_F32, 0, 0, 0, out, M, nullptr, 0, nullptr, 0};
+        const int items = g.m_tiles * ((N + nmax - 1) / nmax);
+        err = launch_gemm(g, std::min(items, sms), s);
+    }
+    cudaError_t ferr = cudaFreeAsync(scratch, s);
+    if (err == cudaSuccess) err = ferr;
+    return cuda_status(err);
+}
+
+}  // extern "C"

@@ -1,0 +1,118 @@
+// Declarations shared by the translation units of libmoe (not installed).
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace moe {
+
+// Device status codes (sticky; read by moe_get_device_status).
+enum : int { DEV_OK = 0, DEV_TIMEOUT_PRODUCER = 1, DEV_TIMEOUT_MMA = 2, DEV_TIMEOUT_EPILOGUE = 3,
+             DEV_TIMEOUT_TEARDOWN = 4, DEV_BAD_WORK = 5 };
+
+// ------------------------------------------------------------------ GEMM engine
+// Tiles: 128 weight rows (MMA M, the A operand, MXFP4) x up to kNMax tokens
+// (MMA N, the B operand, MXFP8) x 128 along K per pipeline stage.
+constexpr int kBlockM = 128;
+constexpr int kBlockK = 128;
+constexpr int kNMax = 240;        // 2 accumulators of kNMax fp32 columns + scale columns fit 512 TMEM columns
+constexpr int kGemmThreads = 192; // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kSmemLimit = 227 * 1024;
+
+enum EpiMode : int {
+    EPI_F32 = 0,        // store fp32 accumulators
+    EPI_QUANT = 1,      // optionally store fp32, and store MXFP8 of the row segment (blocks along M)
+    EPI_SILU_QUANT = 2  // rows 0..63 gate, 64..127 up: store MXFP8 of SiLU(gate) * up
+};
+
+// Where an epilogue region writes.  Output row = item.b_row0 + token index;
+// output column = col0 + (item.mt - m_tile0) * cols_per_mtile + row-in-tile.
+struct EpiParams {
+    int mode;
+    int m_tile0;
+    int col0;
+    int pad0;
+    float* out_f32;     // [rows][ld_f32]
+    int64_t ld_f32;
+    uint8_t* out_q;     // E4M3 codes [rows][ld_q]
+    int64_t ld_q;
+    uint8_t* out_sf;    // scale planes: uint32 word per (col/128, row), byte (col%128)/32
+    int64_t sf_pitch;   // rows per plane
+};
+
+struct GemmParams {
+    CUtensorMap tmA;        // MXFP4 weights, 16U4_ALIGN16B, box {128, 128}, 128B swizzle
+    CUtensorMap tmB;        // MXFP8 activations, UINT8, box {128, 16}, 128B swizzle
+    const uint8_t* sfa;     // weight scales, pre-arranged: [rows/128][KT][512]
+    const uint8_t* sfb;     // activation scale planes: [KT][sfb_pitch] uint32
+    int64_t sfb_pitch;
+    int KT;                 // 128-wide K tiles
+    int n_max;              // tokens per work item (multiple of 16, <= kNMax)
+    int stages;
+    int stage_bytes;
+    int a_tx_bytes;         // bytes a 128x128 MXFP4 TMA box delivers to the mbarrier
+    int dense;              // 1: items = m_tiles x ceil(n_tokens / n_max); 0: item list
+    int m_tiles;
+    int n_tokens;
+    int a_rows;             // rows of A (bounds check of list items)
+    int b_rows;             // rows of B / scale planes (bounds check)
+    const int4* items;      // {a_row0, b_row0, n, mt}
+    const int* n_items;
+    int epi_split;          // dense: m-tiles >= epi_split use epi[1]
+    int pad1;
+    EpiParams epi[2];
+    int* status;
+};
+
+int gemm_stage_bytes(int n_max);
+int gemm_stages(int n_max);
+size_t gemm_smem_bytes(int n_max, int stages);
+cudaError_t gemm_setup();   // raise the dynamic shared memory limit once
+cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s);
+
+// ------------------------------------------------------------------ other kernels
+cudaError_t launch_quant_x(const __nv_bfloat16* x, int T, int D, uint8_t* xq, uint8_t* xsf, int64_t pitch,
+                           cudaStream_t s);
+cudaError_t launch_router(const float* z, const float* R, float* logits, int T, int E, int L, cudaStream_t s);
+cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int softmax, int32_t* idx,
+                        float* w, uint32_t* sel, int W, cudaStream_t s);
+cudaError_t launch_expert_scan(const uint32_t* sel, int E, int W, int32_t* wpre, int32_t* counts, cudaStream_t s);
+struct WorkListArgs {
+    const int32_t* counts;
+    int E;
+    int32_t* offsets;    // [E+1] exclusive scan of counts
+    int32_t* seg;        // [E+1] exclusive scan of counts rounded up to 16 (row starts in permuted buffers)
+    int4* items1; int* n_items1; int n_max1; int mt1; int a_rows_per_e1;
+    int4* items2; int* n_items2; int n_max2; int mt2; int a_rows_per_e2;
+};
+cudaError_t launch_worklist(const WorkListArgs& a, cudaStream_t s);
+struct ScatterArgs {
+    const int32_t* idx; int T; int k; int W;
+    const uint32_t* sel; const int32_t* wpre; const int32_t* offsets; const int32_t* seg;
+    int32_t* slot_pos;        // [T*k] row of (t, j) in the permuted buffers
+    int32_t* canon_to_pad;    // [T*k] sorted (unpadded) position -> permuted row
+    int32_t* sorted_token;    // [T*k] token of each sorted position
+    const uint8_t* zq; const uint8_t* zsf; int64_t zsf_pitch; int L;
+    uint8_t* zq_perm; uint8_t* zq_perm_sf; int64_t perm_pitch;
+};
+cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s);
+cudaError_t launch_combine(const float* o, const int32_t* slot_pos, const float* w, int T, int k, int L,
+                           uint8_t* out_q, int64_t ld_q, uint8_t* out_sf, int64_t sf_pitch, cudaStream_t s);
+cudaError_t launch_mxfp4_encode(const float* w, int64_t rows, int64_t K, uint8_t* codes, uint8_t* scales,
+                                cudaStream_t s);
+cudaError_t kernels_setup();   // per-device kernel attributes
+// row-major scales [rows][kb] -> scale planes [kb/4][pitch] (uint32 words)
+cudaError_t launch_sf_planes(const uint8_t* scales_rm, int64_t rows, int64_t kb, uint8_t* planes, int64_t pitch,
+                             cudaStream_t s);
+// plan-time repacking
+cudaError_t launch_copy_rows(uint8_t* dst, int64_t dst_stride, const uint8_t* const* src_rows, int64_t nrows,
+                             int64_t row_bytes, cudaStream_t s);
+cudaError_t launch_sf_atoms(const uint8_t* scales_rm, int64_t rows, int64_t kb, uint8_t* atoms, cudaStream_t s);
+// debug export
+cudaError_t launch_export_sf(const uint8_t* planes, int64_t pitch, const int32_t* row_map, int64_t rows,
+                             int64_t nblocks, int64_t col_block0, uint8_t* out, cudaStream_t s);
+cudaError_t launch_gather_rows(const uint8_t* src, int64_t src_stride, const int32_t* row_map, int64_t rows,
+                               int64_t row_bytes, uint8_t* dst, int64_t dst_stride, cudaStream_t s);
+
+}  // namespace moe

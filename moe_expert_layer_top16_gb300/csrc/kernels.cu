@@ -1,0 +1,541 @@
+// The non-GEMM kernels of the layer: MXFP8 quantisation of the input, the
+// router GEMM, top-k selection with gate normalisation, the dispatch
+// (per-expert counts, offsets, stable ranks, work lists, gather), the
+// weighted combine with MXFP8 re-quantisation, the MXFP4 weight encoder, and
+// plan-time repacking / debug export helpers.
+#include "internal.h"
+#include "mx.cuh"
+
+namespace moe {
+
+namespace {
+
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// ------------------------------------------------------------------ A1: x -> MXFP8
+// One warp per (row, 128-wide column tile); lane l owns elements 4l..4l+3, so
+// 8 lanes form one 32-element block.  Scale planes as in mx.cuh.
+__global__ void quant_x_kernel(const __nv_bfloat16* __restrict__ x, int T, int D, uint8_t* __restrict__ xq,
+                               uint32_t* __restrict__ xsf, int64_t pitch) {
+    const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const int tiles = D / 128;
+    if (gw >= static_cast<int64_t>(T) * tiles) return;
+    const int64_t row = gw / tiles;
+    const int tile = static_cast<int>(gw % tiles);
+    const int64_t off = row * D + tile * 128 + lane * 4;
+    const uint2 raw = *reinterpret_cast<const uint2*>(x + off);
+    float v[4];
+    v[0] = __uint_as_float(raw.x << 16);
+    v[1] = __uint_as_float(raw.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(raw.y << 16);
+    v[3] = __uint_as_float(raw.y & 0xFFFF0000u);
+    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const int e = mx8_exponent(amax);
+    const float inv = exp2i(-e);
+    uint32_t packed = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) packed |= static_cast<uint32_t>(f32_to_e4m3(v[i] * inv)) << (8 * i);
+    *reinterpret_cast<uint32_t*>(xq + off) = packed;
+    // gather the 4 block scales (lanes 0, 8, 16, 24) into one word
+    const uint32_t sc = static_cast<uint32_t>(e + 127);
+    uint32_t word = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) word |= __shfl_sync(0xffffffffu, sc, b * 8) << (8 * b);
+    if (lane == 0) xsf[tile * pitch + row] = word;
+}
+
+// ------------------------------------------------------------------ A3: router logits
+// logits[t][e] = sum_l z[t][l] * R[e][l], fp32 with one sequential FMA chain
+// per output (deterministic).  64 tokens x 64 experts per CTA, 16-wide K
+// slices staged through shared memory, 4x4 outputs per thread.
+constexpr int RT = 64, RE = 64, RK = 16;
+__global__ void __launch_bounds__(256) router_kernel(const float* __restrict__ z, const float* __restrict__ R,
+                                                     float* __restrict__ logits, int T, int E, int L) {
+    __shared__ float zs[RK][RT + 4];
+    __shared__ float rs[RK][RE + 4];
+    const int t0 = blockIdx.y * RT, e0 = blockIdx.x * RE;
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    float acc[4][4] = {};
+    for (int k0 = 0; k0 < L; k0 += RK) {
+        for (int i = threadIdx.x; i < RT * RK; i += 256) {
+            const int r = i / RK, c = i % RK;
+            zs[c][r] = (t0 + r < T) ? z[static_cast<int64_t>(t0 + r) * L + k0 + c] : 0.0f;
+            rs[c][r] = (e0 + r < E) ? R[static_cast<int64_t>(e0 + r) * L + k0 + c] : 0.0f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < RK; ++kk) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = zs[kk][ty * 4 + i];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) b[j] = rs[kk][tx * 4 + j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int t = t0 + ty * 4 + i;
+        if (t >= T) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int e = e0 + tx * 4 + j;
+            if (e < E) logits[static_cast<int64_t>(t) * E + e] = acc[i][j];
+        }
+    }
+}
+
+// ------------------------------------------------------------------ A4: top-k + gates
+// One warp per token.  Selection key: the logit itself when there is no
+// bias (sigmoid is monotonic, so this orders experts exactly like the
+// sigmoid score) or in softmax mode; sigmoid(l) + bias evaluated in fp64
+// otherwise.  k rounds of "largest remaining key, lower id on a tie".
+// Gates: sigmoid(l_j) / sum over the winners (fp32), or softmax over the
+// winners' logits.  Each selection sets bit t of the expert's token bitmap.
+constexpr int kTopkWarps = 4;
+constexpr int kMaxE = 4096;
+__global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(const float* __restrict__ logits,
+                                                                const float* __restrict__ bias, int T, int E, int k,
+                                                                int softmax, int32_t* __restrict__ idx_out,
+                                                                float* __restrict__ w_out, uint32_t* __restrict__ sel,
+                                                                int W) {
+    extern __shared__ double keys_all[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kTopkWarps + warp;
+    if (t >= T) return;
+    double* key = keys_all + static_cast<int64_t>(warp) * E;
+    const float* l = logits + static_cast<int64_t>(t) * E;
+    const bool use_bias = (bias != nullptr) && !softmax;
+    for (int e = lane; e < E; e += 32) {
+        const double lv = static_cast<double>(l[e]);
+        key[e] = use_bias ? 1.0 / (1.0 + exp(-lv)) + static_cast<double>(bias[e]) : lv;
+    }
+    __syncwarp();
+    // Lane `lane` owns candidates e = lane + 32 i (i < 128 since E <= 4096);
+    // `taken` marks the ones already selected.  NaN keys rank as -inf and
+    // every round still returns an untaken, in-range id.
+    uint32_t taken[kMaxE / 32 / 32] = {};
+    int my_id = 0;             // lane j < k ends up holding slot j's expert
+    for (int j = 0; j < k; ++j) {
+        double best = -INFINITY;
+        int bid = 0x7fffffff;
+        for (int e = lane, i = 0; e < E; e += 32, ++i) {
+            if (taken[i >> 5] & (1u << (i & 31))) continue;
+            double kv = key[e];
+            if (kv != kv) kv = -INFINITY;
+            if (bid == 0x7fffffff || kv > best || (kv == best && e < bid)) {
+                best = kv;
+                bid = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const double ob = __shfl_xor_sync(0xffffffffu, best, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bid, o);
+            if (oi != 0x7fffffff && (bid == 0x7fffffff || ob > best || (ob == best && oi < bid))) {
+                best = ob;
+                bid = oi;
+            }
+        }
+        if (bid < 0 || bid >= E) bid = 0;        // unreachable while k <= E
+        if (lane == j) my_id = bid;
+        if ((bid & 31) == lane) {
+            const int i = bid >> 5;
+            taken[i >> 5] |= 1u << (i & 31);    // the owner removes the winner
+        }
+    }
+    float s = 0.0f;
+    if (lane < k) s = l[my_id];
+    if (softmax) {
+        const float lmax = __shfl_sync(0xffffffffu, s, 0);    // slot 0 holds the largest logit
+        s = (lane < k) ? expf(s - lmax) : 0.0f;
+    } else {
+        s = (lane < k) ? 1.0f / (1.0f + expf(-s)) : 0.0f;
+    }
+    float sum = s;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane < k) {
+        idx_out[static_cast<int64_t>(t) * k + lane] = my_id;
+        w_out[static_cast<int64_t>(t) * k + lane] = s / sum;
+        atomicOr(&sel[static_cast<int64_t>(my_id) * W + (t >> 5)], 1u << (t & 31));
+    }
+}
+
+// ------------------------------------------------------------------ A5: per-expert scan
+// One warp per expert: prefix popcounts of its token bitmap.  wpre[e][w] =
+// number of tokens < 32w that selected e; counts[e] = total.
+__global__ void expert_scan_kernel(const uint32_t* __restrict__ sel, int E, int W, int32_t* __restrict__ wpre,
+                                   int32_t* __restrict__ counts) {
+    const int e = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (e >= E) return;
+    int running = 0;
+    for (int w0 = 0; w0 < W; w0 += 32) {
+        const int w = w0 + lane;
+        const int c = (w < W) ? __popc(sel[static_cast<int64_t>(e) * W + w]) : 0;
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        if (w < W) wpre[static_cast<int64_t>(e) * W + w] = running + incl - c;
+        running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) counts[e] = running;
+}
+
+// Block-wide exclusive scan (blockDim.x == 1024) over `n` values, sequential
+// chunks of 1024; returns the total.  `tmp` holds 32 ints of shared memory.
+template <typename F, typename G>
+__device__ int block_exclusive_scan(int n, F value, G store, int* tmp) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int carry = 0;
+    for (int base = 0; base < n; base += 1024) {
+        const int i = base + threadIdx.x;
+        const int v = (i < n) ? value(i) : 0;
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        if (lane == 31) tmp[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            int s = tmp[lane];
+            int si = s;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, si, o);
+                if (lane >= o) si += t;
+            }
+            tmp[lane] = si - s;   // exclusive warp offsets
+        }
+        __syncthreads();
+        const int excl = carry + tmp[warp] + incl - v;
+        if (i < n) store(i, excl);
+        __syncthreads();
+        // total of this chunk = exclusive offset of the last warp + its inclusive sum
+        int chunk_total = 0;
+        if (threadIdx.x == 1023) tmp[0] = tmp[31] + incl;
+        __syncthreads();
+        chunk_total = tmp[0];
+        __syncthreads();
+        carry += chunk_total;
+    }
+    return carry;
+}
+
+// Offsets (exact and padded to 16 rows per expert) and the work lists of the
+// two grouped GEMMs: for every expert with n_e > 0, ceil(n_e / n_max) token
+// tiles x mt weight tiles, item = {weight row, first permuted row, tokens, mt}.
+__global__ void __launch_bounds__(1024) worklist_kernel(WorkListArgs a) {
+    __shared__ int tmp[32];
+    const int E = a.E;
+    const int32_t* counts = a.counts;
+    int total = block_exclusive_scan(
+        E, [&](int e) { return counts[e]; }, [&](int e, int v) { a.offsets[e] = v; }, tmp);
+    if (threadIdx.x == 0) a.offsets[E] = total;
+    total = block_exclusive_scan(
+        E, [&](int e) { return (counts[e] + 15) & ~15; }, [&](int e, int v) { a.seg[e] = v; }, tmp);
+    if (threadIdx.x == 0) a.seg[E] = total;
+    __syncthreads();
+    for (int pass = 0; pass < 2; ++pass) {
+        int4* items = pass ? a.items2 : a.items1;
+        int* n_items = pass ? a.n_items2 : a.n_items1;
+        const int nmax = pass ? a.n_max2 : a.n_max1;
+        const int mt = pass ? a.mt2 : a.mt1;
+        const int rpe = pass ? a.a_rows_per_e2 : a.a_rows_per_e1;
+        // item offsets per expert, written into a scratch view of `items`?  No:
+        // recompute with a second scan and write directly.
+        total = block_exclusive_scan(
+            E, [&](int e) { return ceil_div(counts[e], nmax) * mt; },
+            [&](int e, int off) {
+                const int n_e = counts[e];
+                const int tiles = ceil_div(n_e, nmax);
+                int o = off;
+                for (int j = 0; j < tiles; ++j) {
+                    const int nj = min(nmax, n_e - j * nmax);
+                    for (int m = 0; m < mt; ++m)
+                        items[o++] = make_int4(e * rpe + m * 128, a.seg[e] + j * nmax, nj, m);
+                }
+            },
+            tmp);
+        if (threadIdx.x == 0) *n_items = total;
+        __syncthreads();
+    }
+}
+
+// ------------------------------------------------------------------ A5/A6: ranks + gather
+// One warp per (token, slot).  The rank of token t inside expert e's segment
+// is the number of tokens < t that selected e (bitmap prefix + popcount), so
+// the resulting order is the stable sort of (token, slot) pairs by expert.
+__global__ void scatter_kernel(ScatterArgs a) {
+    const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (gw >= static_cast<int64_t>(a.T) * a.k) return;
+    const int t = static_cast<int>(gw / a.k);
+    const int e = a.idx[gw];
+    const int w = t >> 5;
+    const uint32_t bits = a.sel[static_cast<int64_t>(e) * a.W + w] & ((1u << (t & 31)) - 1u);
+    const int rank = a.wpre[static_cast<int64_t>(e) * a.W + w] + __popc(bits);
+    const int pos = a.seg[e] + rank;
+    const int canon = a.offsets[e] + rank;
+    if (lane == 0) {
+        a.slot_pos[gw] = pos;
+        a.canon_to_pad[canon] = pos;
+        a.sorted_token[canon] = t;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(a.zq + static_cast<int64_t>(t) * a.L);
+    uint4* dst = reinterpret_cast<uint4*>(a.zq_perm + static_cast<int64_t>(pos) * a.L);
+    for (int i = lane; i < a.L / 16; i += 32) dst[i] = src[i];
+    const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(a.zsf);
+    uint32_t* sdst = reinterpret_cast<uint32_t*>(a.zq_perm_sf);
+    for (int kt = lane; kt < a.L / 128; kt += 32) sdst[kt * a.perm_pitch + pos] = ssrc[kt * a.zsf_pitch + t];
+}
+
+// ------------------------------------------------------------------ A9: combine + MXFP8
+// c[t][l] = sum_j w[t][j] * o[slot_pos[t][j]][l], slots in order, then MXFP8
+// along l.  One CTA per token; a warp owns 32 consecutive columns = one block.
+__global__ void combine_kernel(const float* __restrict__ o, const int32_t* __restrict__ slot_pos,
+                               const float* __restrict__ w, int T, int k, int L, uint8_t* __restrict__ out_q,
+                               int64_t ld_q, uint8_t* __restrict__ out_sf, int64_t sf_pitch) {
+    const int t = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nw = blockDim.x >> 5;
+    __shared__ int pos_s[32];
+    __shared__ float w_s[32];
+    if (threadIdx.x < k) {
+        pos_s[threadIdx.x] = slot_pos[static_cast<int64_t>(t) * k + threadIdx.x];
+        w_s[threadIdx.x] = w[static_cast<int64_t>(t) * k + threadIdx.x];
+    }
+    __syncthreads();
+    for (int blk = warp; blk < L / 32; blk += nw) {
+        const int col = blk * 32 + lane;
+        float acc = 0.0f;
+        for (int j = 0; j < k; ++j) acc = fmaf(w_s[j], o[static_cast<int64_t>(pos_s[j]) * L + col], acc);
+        uint8_t sc;
+        const uint8_t code = warp_mx8_quant(acc, &sc);
+        out_q[static_cast<int64_t>(t) * ld_q + col] = code;
+        if (lane == 0) out_sf[sf_byte_offset(t, col, sf_pitch)] = sc;
+    }
+}
+
+// ------------------------------------------------------------------ MXFP4 weight encoder
+// One thread per 32-element block.  Shared exponent floor(log2 amax) - 2;
+// level = number of grid midpoints {0.25,0.75,1.25,1.75,2.5,3.5,5} strictly
+// below |v|/2^e (a value on a midpoint takes the smaller level; anything
+// above 5 -- including beyond the clip at 6 -- takes level 7).
+__global__ void mxfp4_encode_kernel(const float* __restrict__ w, int64_t rows, int64_t K,
+                                    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+    const int64_t nb = K / 32;
+    const int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (b >= rows * nb) return;
+    const int64_t r = b / nb, j = b % nb;
+    const float* v = w + r * K + j * 32;
+    float x[32];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+        const float4 q = *reinterpret_cast<const float4*>(v + i);
+        x[i] = q.x;
+        x[i + 1] = q.y;
+        x[i + 2] = q.z;
+        x[i + 3] = q.w;
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    uint8_t* c = codes + r * (K / 2) + j * 16;
+    if (amax == 0.0f) {
+        *reinterpret_cast<uint4*>(c) = make_uint4(0, 0, 0, 0);
+        scales[b] = 0;
+        return;
+    }
+    const uint32_t ab = __float_as_uint(amax);
+    int fl;
+    const int biased = static_cast<int>((ab >> 23) & 0xFFu);
+    if (biased != 0) {
+        fl = biased - 127;
+    } else {
+        const uint32_t m = ab & 0x7FFFFFu;             // subnormal: value = m * 2^-149
+        fl = -149 + (31 - __clz(m));
+    }
+    int e = fl - 2;
+    e = e < -127 ? -127 : (e > 127 ? 127 : e);
+    // |v| * 2^-e; split the power of two so each factor is a normal float
+    const int ne = -e;
+    const float s1 = exp2i(ne / 2), s2 = exp2i(ne - ne / 2);
+    uint32_t packed[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const float a = (fabsf(x[i]) * s1) * s2;
+        const int lvl = (a > 0.25f) + (a > 0.75f) + (a > 1.25f) + (a > 1.75f) + (a > 2.5f) + (a > 3.5f) + (a > 5.0f);
+        const uint32_t code = static_cast<uint32_t>(lvl) | ((__float_as_uint(x[i]) >> 31) << 3);
+        packed[i / 8] |= code << (4 * (i % 8));
+    }
+    *reinterpret_cast<uint4*>(c) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    scales[b] = static_cast<uint8_t>(e + 127);
+}
+
+// ------------------------------------------------------------------ plan-time repacking
+__global__ void copy_rows_kernel(uint8_t* __restrict__ dst, int64_t dst_stride, const uint8_t* const* src_rows,
+                                 int64_t nrows, int64_t row_bytes) {
+    const int64_t r = blockIdx.x;
+    if (r >= nrows) return;
+    const uint8_t* s = src_rows[r];
+    uint8_t* d = dst + r * dst_stride;
+    if (((reinterpret_cast<uintptr_t>(s) | reinterpret_cast<uintptr_t>(d) | row_bytes) & 15) == 0) {
+        const uint4* s4 = reinterpret_cast<const uint4*>(s);
+        uint4* d4 = reinterpret_cast<uint4*>(d);
+        for (int64_t i = threadIdx.x; i < row_bytes / 16; i += blockDim.x) d4[i] = s4[i];
+        return;
+    }
+    for (int64_t i = threadIdx.x; i < row_bytes; i += blockDim.x) d[i] = s[i];
+}
+
+// Row-major scales [rows][kb] -> MMA scale atoms [rows/128][kb/4][512]:
+// atom byte 16*i + 4*c + j = scale of row 32*c + i, K-block j of the tile.
+__global__ void sf_atoms_kernel(const uint8_t* __restrict__ rm, int64_t rows, int64_t kb, uint8_t* __restrict__ atoms) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= rows * kb) return;
+    const int64_t row = i / kb, b = i % kb;
+    const int64_t rb = row / 128, rr = row % 128, kt = b / 4, j = b % 4;
+    const int64_t KT = kb / 4;
+    atoms[(rb * KT + kt) * 512 + (rr % 32) * 16 + (rr / 32) * 4 + j] = rm[i];
+}
+
+__global__ void sf_planes_kernel(const uint8_t* __restrict__ rm, int64_t rows, int64_t kb, uint8_t* __restrict__ planes,
+                                 int64_t pitch) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= rows * kb) return;
+    const int64_t row = i / kb, b = i % kb;
+    planes[((b / 4) * pitch + row) * 4 + (b % 4)] = rm[i];
+}
+
+// ------------------------------------------------------------------ debug export
+__global__ void export_sf_kernel(const uint8_t* __restrict__ planes, int64_t pitch, const int32_t* __restrict__ row_map,
+                                 int64_t rows, int64_t nblocks, int64_t col_block0, uint8_t* __restrict__ out) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= rows * nblocks) return;
+    const int64_t r = i / nblocks, b = i % nblocks;
+    const int64_t src_row = row_map ? row_map[r] : r;
+    const int64_t cb = col_block0 + b;
+    out[i] = planes[((cb / 4) * pitch + src_row) * 4 + (cb % 4)];
+}
+
+__global__ void gather_rows_kernel(const uint8_t* __restrict__ src, int64_t src_stride, const int32_t* __restrict__ row_map,
+                                   int64_t rows, int64_t row_bytes, uint8_t* __restrict__ dst, int64_t dst_stride) {
+    const int64_t r = blockIdx.x;
+    if (r >= rows) return;
+    const uint8_t* s = src + static_cast<int64_t>(row_map ? row_map[r] : r) * src_stride;
+    uint8_t* d = dst + r * dst_stride;
+    for (int64_t i = threadIdx.x; i < row_bytes; i += blockDim.x) d[i] = s[i];
+}
+
+}  // namespace
+
+cudaError_t launch_quant_x(const __nv_bfloat16* x, int T, int D, uint8_t* xq, uint8_t* xsf, int64_t pitch,
+                           cudaStream_t s) {
+    const int64_t warps = static_cast<int64_t>(T) * (D / 128);
+    const int blocks = static_cast<int>((warps * 32 + 255) / 256);
+    quant_x_kernel<<<blocks, 256, 0, s>>>(x, T, D, xq, reinterpret_cast<uint32_t*>(xsf), pitch);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_router(const float* z, const float* R, float* logits, int T, int E, int L, cudaStream_t s) {
+    dim3 grid((E + RE - 1) / RE, (T + RT - 1) / RT);
+    router_kernel<<<grid, 256, 0, s>>>(z, R, logits, T, E, L);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int softmax, int32_t* idx,
+                        float* w, uint32_t* sel, int W, cudaStream_t s) {
+    const size_t smem = sizeof(double) * kTopkWarps * E;
+    topk_kernel<<<(T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, smem, s>>>(logits, bias, T, E, k, softmax,
+                                                                               idx, w, sel, W);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_expert_scan(const uint32_t* sel, int E, int W, int32_t* wpre, int32_t* counts, cudaStream_t s) {
+    expert_scan_kernel<<<(E * 32 + 255) / 256, 256, 0, s>>>(sel, E, W, wpre, counts);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_worklist(const WorkListArgs& a, cudaStream_t s) {
+    worklist_kernel<<<1, 1024, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s) {
+    const int64_t warps = static_cast<int64_t>(a.T) * a.k;
+    scatter_kernel<<<static_cast<int>((warps * 32 + 255) / 256), 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const float* o, const int32_t* slot_pos, const float* w, int T, int k, int L,
+                           uint8_t* out_q, int64_t ld_q, uint8_t* out_sf, int64_t sf_pitch, cudaStream_t s) {
+    combine_kernel<<<T, 256, 0, s>>>(o, slot_pos, w, T, k, L, out_q, ld_q, out_sf, sf_pitch);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mxfp4_encode(const float* w, int64_t rows, int64_t K, uint8_t* codes, uint8_t* scales,
+                                cudaStream_t s) {
+    const int64_t n = rows * (K / 32);
+    if (n == 0) return cudaSuccess;
+    mxfp4_encode_kernel<<<static_cast<unsigned>((n + 127) / 128), 128, 0, s>>>(w, rows, K, codes, scales);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_rows(uint8_t* dst, int64_t dst_stride, const uint8_t* const* src_rows, int64_t nrows,
+                             int64_t row_bytes, cudaStream_t s) {
+    if (nrows == 0) return cudaSuccess;
+    copy_rows_kernel<<<static_cast<unsigned>(nrows), 128, 0, s>>>(dst, dst_stride, src_rows, nrows, row_bytes);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sf_atoms(const uint8_t* scales_rm, int64_t rows, int64_t kb, uint8_t* atoms, cudaStream_t s) {
+    const int64_t n = rows * kb;
+    sf_atoms_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(scales_rm, rows, kb, atoms);
+    return cudaGetLastError();
+}
+
+cudaError_t kernels_setup() {
+    return cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(sizeof(double) * kTopkWarps * kMaxE));
+}
+
+cudaError_t launch_sf_planes(const uint8_t* scales_rm, int64_t rows, int64_t kb, uint8_t* planes, int64_t pitch,
+                             cudaStream_t s) {
+    const int64_t n = rows * kb;
+    if (n == 0) return cudaSuccess;
+    sf_planes_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(scales_rm, rows, kb, planes, pitch);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_export_sf(const uint8_t* planes, int64_t pitch, const int32_t* row_map, int64_t rows,
+                             int64_t nblocks, int64_t col_block0, uint8_t* out, cudaStream_t s) {
+    const int64_t n = rows * nblocks;
+    if (n == 0) return cudaSuccess;
+    export_sf_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(planes, pitch, row_map, rows, nblocks,
+                                                                          col_block0, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const uint8_t* src, int64_t src_stride, const int32_t* row_map, int64_t rows,
+                               int64_t row_bytes, uint8_t* dst, int64_t dst_stride, cudaStream_t s) {
+    if (rows == 0) return cudaSuccess;
+    gather_rows_kernel<<<static_cast<unsigned>(rows), 128, 0, s>>>(src, src_stride, row_map, rows, row_bytes, dst,
+                                                                   dst_stride);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -149,13 +149,17 @@ void orc_mxfp4_encode_f64(const double *w, int64_t rows, int64_t K,
 void orc_mxfp4_encode_f32(const float *w, int64_t rows, int64_t K,
                           uint8_t *codes, uint8_t *scales)
 {
-    double *tmp = (double *)malloc(sizeof(double) * (size_t)K);
-    for (int64_t r = 0; r < rows; ++r) {
-        for (int64_t i = 0; i < K; ++i)
-            tmp[i] = (double)w[r * K + i];
-        orc_mxfp4_encode_f64(tmp, 1, K, codes + r * (K / 2), scales + r * (K / 32));
+#pragma omp parallel
+    {
+        double *tmp = (double *)malloc(sizeof(double) * (size_t)K);
+#pragma omp for schedule(static)
+        for (int64_t r = 0; r < rows; ++r) {
+            for (int64_t i = 0; i < K; ++i)
+                tmp[i] = (double)w[r * K + i];
+            orc_mxfp4_encode_f64(tmp, 1, K, codes + r * (K / 2), scales + r * (K / 32));
+        }
+        free(tmp);
     }
-    free(tmp);
 }
 
 /* ------------------------------------------------------------------ */

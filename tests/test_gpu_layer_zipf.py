@@ -1,0 +1,26 @@
+"""The K3-shaped layer with a Zipf(s=1.1)-shaped selection bias, 16384
+tokens: hot experts take many times the mean load, so the grouped GEMMs see
+very ragged segments (several full 240-token tiles for one expert, many
+empty experts).  Same parity contract as the uniform workloads; the bias
+enters the selection key only (sigmoid(l) + b, evaluated in fp64)."""
+import numpy as np
+import pytest
+
+import synth
+from gpu_util import OracleLayer, gpu_plan, run_sampled_parity
+
+pytestmark = pytest.mark.gpu
+
+
+def test_zipf16384():
+    wl = synth.workload("zipf16384")
+    plan, _ = gpu_plan(wl)
+    ol = OracleLayer(wl)
+    try:
+        accepted, errs, counts = run_sampled_parity(wl, plan, ol, 16384, [0, 5000, 12345, 16383])
+    finally:
+        plan.close()
+    assert len(accepted) <= 1
+    mean = 16384 * 16 / 896
+    assert counts.max() > 10 * mean, f"hottest expert {counts.max()} vs mean {mean:.1f}"
+    assert (counts == 0).sum() > 0
