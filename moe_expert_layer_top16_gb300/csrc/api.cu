@@ -32,9 +32,11 @@ using namespace moe;
 namespace {
 
 // Bytes that one 128x128 MXFP4 TMA box (16U4_ALIGN16B) counts toward the
-// mbarrier transaction: the shared-memory footprint of the unpacked box.
+// mbarrier transaction: the packed size (128 rows x 64 B).  In shared memory
+// the box occupies 16 KB -- each 16-byte chunk holds 8 bytes of packed
+// elements and an 8-byte gap that the copy leaves unwritten.
 #ifndef MOE_A_TX_BYTES
-#define MOE_A_TX_BYTES 16384
+#define MOE_A_TX_BYTES 8192
 #endif
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,

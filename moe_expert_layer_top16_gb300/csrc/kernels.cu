@@ -92,6 +92,48 @@ __global__ void __launch_bounds__(256) router_kernel(const float* __restrict__ z
     }
 }
 
+// Decode-sized batches (T <= 128): 8 experts per CTA so that ~E/8 CTAs
+// stream R from HBM in parallel; the tokens' latent rows come through shared
+// memory in 64-wide K chunks (z is small and L2-resident).  Warp w owns
+// expert e0 + w; lane l owns tokens l, l+32, l+64, l+96.  One sequential FMA
+// chain per output, like the tiled kernel.
+constexpr int RS_E = 8, RS_K = 64, RS_TMAX = 128;
+__global__ void __launch_bounds__(256) router_small_kernel(const float* __restrict__ z, const float* __restrict__ R,
+                                                           float* __restrict__ logits, int T, int E, int L) {
+    __shared__ float zs[RS_TMAX][RS_K + 1];
+    __shared__ float rs[RS_E][RS_K];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e0 = blockIdx.x * RS_E;
+    const int e = e0 + warp;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k0 = 0; k0 < L; k0 += RS_K) {
+        for (int i = threadIdx.x; i < T * RS_K; i += 256) {
+            const int r = i / RS_K, c = i % RS_K;
+            zs[r][c] = z[static_cast<int64_t>(r) * L + k0 + c];
+        }
+        for (int i = threadIdx.x; i < RS_E * RS_K; i += 256) {
+            const int r = i / RS_K, c = i % RS_K;
+            rs[r][c] = (e0 + r < E) ? R[static_cast<int64_t>(e0 + r) * L + k0 + c] : 0.0f;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int kk = 0; kk < RS_K; ++kk) {
+            const float rv = rs[warp][kk];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (lane + 32 * j < T) acc[j] = fmaf(zs[lane + 32 * j][kk], rv, acc[j]);
+        }
+        __syncthreads();
+    }
+    if (e < E) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int t = lane + 32 * j;
+            if (t < T) logits[static_cast<int64_t>(t) * E + e] = acc[j];
+        }
+    }
+}
+
 // ------------------------------------------------------------------ A4: top-k + gates
 // One warp per token.  Selection key: the logit itself when there is no
 // bias (sigmoid is monotonic, so this orders experts exactly like the
@@ -452,6 +494,10 @@ cudaError_t launch_quant_x(const __nv_bfloat16* x, int T, int D, uint8_t* xq, ui
 }
 
 cudaError_t launch_router(const float* z, const float* R, float* logits, int T, int E, int L, cudaStream_t s) {
+    if (T <= RS_TMAX && L % RS_K == 0) {
+        router_small_kernel<<<(E + RS_E - 1) / RS_E, 256, 0, s>>>(z, R, logits, T, E, L);
+        return cudaGetLastError();
+    }
     dim3 grid((E + RE - 1) / RE, (T + RT - 1) / RT);
     router_kernel<<<grid, 256, 0, s>>>(z, R, logits, T, E, L);
     return cudaGetLastError();
