@@ -199,6 +199,26 @@ MOE_API moe_status moe_mx_gemm(const uint8_t *a_codes, const uint8_t *a_scales, 
                        const uint8_t *b_scales, int32_t N, int32_t K, float *out, int32_t *dev_status,
                        void *stream);
 
+/* moe_mx_gemm without any allocation (the paper has no counterpart: this is
+ * an entry point for callers that cannot allocate device memory -- e.g. code
+ * whose device memory is owned by another allocator under a fixed budget, or
+ * code that must not pay the device-wide synchronisation of cudaFree).
+ * Arguments, layouts and the result are those of moe_mx_gemm.  Instead of
+ * cudaMallocAsync it uses a fixed scratch array of MOE_NOALLOC_SCRATCH_BYTES
+ * that lives in the library's device image: every GPU that loads the library
+ * holds it until the process exits.  Limit: M*K/32 + (K/128)*round16(N)*4 +
+ * 256 <= MOE_NOALLOC_SCRATCH_BYTES (e.g. M = K = 4096 with N up to ~24000);
+ * larger calls return MOE_ERR_INVALID_ARG with nothing enqueued.  The first
+ * call on a device looks up the array's device address (once per device, on
+ * the current device); make that first call before any stream capture.  All
+ * calls share the one array and it keeps the previous call's contents: calls
+ * whose executions overlap on the GPU (other streams, other host threads)
+ * race on it.  Makes no cudaMalloc / cudaFree call. */
+#define MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
+MOE_API moe_status moe_mx_gemm_noalloc(const uint8_t *a_codes, const uint8_t *a_scales, int32_t M,
+                                       const uint8_t *b_codes, const uint8_t *b_scales, int32_t N, int32_t K,
+                                       float *out, int32_t *dev_status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

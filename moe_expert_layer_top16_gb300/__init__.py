@@ -29,7 +29,7 @@ SCORE_SIGMOID_BIAS, SCORE_SOFTMAX = 0, 1
 
 # Entry points declared in include/moe.h.
 ENTRY_POINTS = ("moe_plan", "moe_forward", "moe_forward_host", "moe_get_device_status", "moe_workspace_bytes",
-                "moe_free", "moe_status_str", "moe_mxfp4_encode", "moe_mx_gemm")
+                "moe_free", "moe_status_str", "moe_mxfp4_encode", "moe_mx_gemm", "moe_mx_gemm_noalloc")
 
 
 class MoeError(RuntimeError):
@@ -99,6 +99,8 @@ def lib(build_if_missing: bool = False):
             L.moe_mxfp4_encode.argtypes = [P, i64, i64, P, P, P]
             L.moe_mx_gemm.restype = C.c_int
             L.moe_mx_gemm.argtypes = [P, P, i32, P, P, i32, i32, P, P, P]
+            L.moe_mx_gemm_noalloc.restype = C.c_int
+            L.moe_mx_gemm_noalloc.argtypes = [P, P, i32, P, P, i32, i32, P, P, P]
             _lib = L
     return _lib
 

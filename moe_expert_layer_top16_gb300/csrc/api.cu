@@ -21,6 +21,7 @@
 #include <algorithm>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -681,3 +682,78 @@ moe_status moe_mx_gemm(const uint8_t* a_codes, const uint8_t* a_scales, int32_t 
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// moe_mx_gemm_noalloc: the same block-scaled GEMM for callers that may not
+// allocate device memory themselves or through us.  Its scratch (the
+// re-arranged scale factors and a status word) lives in this fixed, file-scope
+// device array instead of cudaMallocAsync memory.  Every device that loads
+// the library holds the array until the process exits; all calls share it.
+static __device__ __align__(256) uint8_t moe_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_noalloc_mu;
+constexpr int kNoAllocMaxDevices = 64;
+uint8_t* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on `dev` (which must be current).  In
+// host code the array's name is only a host-side stand-in, so the address is
+// looked up once per device and cached.
+cudaError_t noalloc_scratch(int dev, uint8_t** out) {
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        const cudaError_t err = cudaGetSymbolAddress(&p, moe_noalloc_scratch);
+        if (err != cudaSuccess) return err;
+        g_noalloc_ptr[dev] = static_cast<uint8_t*>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return cudaSuccess;
+}
+}  // namespace
+
+extern "C" moe_status moe_mx_gemm_noalloc(const uint8_t* a_codes, const uint8_t* a_scales, int32_t M,
+                                          const uint8_t* b_codes, const uint8_t* b_scales, int32_t N, int32_t K,
+                                          float* out, int32_t* dev_status, void* stream) {
+    if (!a_codes || !a_scales || !b_codes || !b_scales || !out) return MOE_ERR_INVALID_ARG;
+    if (M <= 0 || M % 128 || K <= 0 || K % 128 || N <= 0 || N > (1 << 24)) return MOE_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(a_codes) & 31) || (reinterpret_cast<uintptr_t>(b_codes) & 15) ||
+        (reinterpret_cast<uintptr_t>(out) & 3))
+        return MOE_ERR_INVALID_ARG;
+    const int64_t Np = rup(N, 16);
+    const size_t atom_bytes = static_cast<size_t>(M) * K / 32;
+    const size_t plane_bytes = static_cast<size_t>(K / 128) * Np * 4;
+    if (atom_bytes + plane_bytes + 256 > MOE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_INVALID_ARG;
+    if (!encode_fn()) return MOE_ERR_UNSUPPORTED;
+    int dev = 0, sms = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err == cudaSuccess) err = gemm_setup();
+    uint8_t* scratch = nullptr;
+    if (err == cudaSuccess) err = noalloc_scratch(dev, &scratch);
+    if (err != cudaSuccess) return cuda_status(err);
+    CUtensorMap tA, tB;
+    if (!map_mx4(&tA, a_codes, M, K) || !map_mx8(&tB, b_codes, N, K)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* atoms = scratch;
+    uint8_t* planes = scratch + atom_bytes;
+    int32_t* st = dev_status ? dev_status : reinterpret_cast<int32_t*>(planes + plane_bytes);
+    // the array keeps the previous call's contents: clear the scale planes
+    // (their padding rows) and the internal status word
+    err = cudaMemsetAsync(planes, 0, plane_bytes + 256, s);
+    if (err == cudaSuccess) err = launch_sf_atoms(a_scales, M, K / 32, atoms, s);
+    if (err == cudaSuccess) err = launch_sf_planes(b_scales, N, K / 32, planes, Np, s);
+    if (err == cudaSuccess) {
+        const int nmax = pick_n_max(N);
+        GemmParams g = gemm_base(tA, tB, atoms, planes, Np, K, nmax, M, static_cast<int>(Np), st);
+        g.dense = 1;
+        g.m_tiles = M / kBlockM;
+        g.n_tokens = N;
+        g.epi_split = 1 << 30;
+        g.epi[0] = EpiParams{EPI_F32, 0, 0, 0, out, M, nullptr, 0, nullptr, 0};
+        const int items = g.m_tiles * ((N + nmax - 1) / nmax);
+        err = launch_gemm(g, std::min(items, sms), s);
+    }
+    return cuda_status(err);
+}
