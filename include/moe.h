@@ -72,7 +72,7 @@ typedef enum {
 
 /* Layer shape.  Constraints (checked by moe_plan): d_model and d_latent
  * multiples of 128; expert_inter and shared_inter multiples of 64;
- * 1 <= top_k <= min(n_experts, 32); 1 <= n_experts <= 4096; n_shared >= 0;
+ * 1 <= top_k <= min(n_experts, 32); 1 <= n_experts <= 1024; n_shared >= 0;
  * 1 <= max_tokens <= 65536. */
 typedef struct {
     int32_t d_model;       /* D */

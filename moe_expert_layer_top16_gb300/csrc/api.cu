@@ -229,7 +229,7 @@ moe_status validate(const moe_config* c) {
     if (c->expert_inter <= 0 || c->expert_inter % 64) return MOE_ERR_INVALID_ARG;
     if (c->n_shared < 0 || (c->n_shared > 0 && (c->shared_inter <= 0 || c->shared_inter % 64)))
         return MOE_ERR_INVALID_ARG;
-    if (c->n_experts < 1 || c->n_experts > 4096) return MOE_ERR_INVALID_ARG;
+    if (c->n_experts < 1 || c->n_experts > 1024) return MOE_ERR_INVALID_ARG;
     if (c->top_k < 1 || c->top_k > 32 || c->top_k > c->n_experts) return MOE_ERR_INVALID_ARG;
     if (c->max_tokens < 1 || c->max_tokens > 65536) return MOE_ERR_INVALID_ARG;
     if (c->score_fn != MOE_SCORE_SIGMOID_BIAS && c->score_fn != MOE_SCORE_SOFTMAX) return MOE_ERR_INVALID_ARG;

@@ -54,7 +54,7 @@ def _cfg(**kw):
 
 
 @pytest.mark.parametrize("bad", [dict(d_model=200), dict(d_latent=96), dict(expert_inter=48), dict(top_k=0),
-                                 dict(top_k=33), dict(top_k=40, n_experts=32), dict(n_experts=0),
+                                 dict(top_k=33), dict(top_k=40, n_experts=32), dict(n_experts=0), dict(n_experts=2048),
                                  dict(max_tokens=0), dict(max_tokens=70000), dict(score_fn=7),
                                  dict(n_shared=1, shared_inter=0)])
 def test_plan_rejects_bad_config_without_a_device(L, bad):
