@@ -70,6 +70,19 @@ bool map_mx4(CUtensorMap* m, const void* codes, int64_t rows, int64_t K) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 matrix [rows][K] for the TF32 path: 32-wide (128-byte) x box_rows boxes.
+bool map_f32(CUtensorMap* m, const void* base, int64_t rows, int64_t K, uint32_t box_rows) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K * 4)};
+    cuuint32_t box[2] = {32, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // MXFP8 activation codes [rows][K], 128-wide x 16-row boxes.
 bool map_mx8(CUtensorMap* m, const void* codes, int64_t rows, int64_t K) {
     EncodeTiledFn f = encode_fn();
@@ -94,10 +107,10 @@ struct Plan {
     std::vector<void*> allocs;
     // weights
     uint8_t *a2c, *a2sf, *w13c, *w13sf, *w2c, *w2sf, *a10c, *a10sf;
-    float *router, *bias;
+    float *router, *router2, *bias;   // router2: [E][2L] = TF32 high part | remainder
     // workspace
     uint8_t *xq, *xsf, *zq, *zsf, *act, *actsf, *zqp, *zqpsf, *hq, *hqsf;
-    float *z, *logits, *gw, *o;
+    float *z, *logits, *rpart, *gw, *o;   // rpart: router K-split partials (batches <= 128 tokens)
     uint32_t* sel;
     int32_t *idx, *wpre, *counts, *offsets, *seg, *slot_pos, *canon_to_pad, *sorted_token;
     int4 *items7, *items8;
@@ -105,7 +118,8 @@ struct Plan {
     int* status;
     void* x_stage;
     float* y_stage;
-    CUtensorMap tA2, tB2, tA7, tB7, tA8, tB8, tA10, tB10;
+    CUtensorMap tA2, tB2, tA7, tB7, tA8, tB8, tA10, tB10, tAR, tBR;
+    bool tc_router;    // router logits on the tensor cores (3xTF32) for batches above 128 tokens
 };
 
 template <typename T>
@@ -211,6 +225,8 @@ GemmParams gemm_base(const CUtensorMap& A, const CUtensorMap& B, const uint8_t* 
     g.stages = gemm_stages(n_max);
     g.stage_bytes = gemm_stage_bytes(n_max);
     g.a_tx_bytes = MOE_A_TX_BYTES;
+    g.kind = KIND_MX;
+    g.kseg_tiles = g.KT;
     g.a_rows = a_rows;
     g.b_rows = b_rows;
     g.status = status;
@@ -380,6 +396,9 @@ moe_status moe_plan(const moe_config* cfg, const moe_weights* w, int device, voi
     }
     TRY(palloc(p, &p->router, sizeof(float) * E * L));
     TRY(cudaMemcpy(p->router, w->router_w, sizeof(float) * E * L, cudaMemcpyDeviceToDevice));
+    TRY(palloc(p, &p->router2, sizeof(float) * E * 2 * L));
+    TRY(launch_tf32_split(p->router, E, L, p->router2, 0));
+    TRY(cudaDeviceSynchronize());
     p->bias = nullptr;
     if (w->router_bias) {
         TRY(palloc(p, &p->bias, sizeof(float) * E));
@@ -388,12 +407,14 @@ moe_status moe_plan(const moe_config* cfg, const moe_weights* w, int device, voi
     // ---------------------------------------------------------------- workspace
     TRY(palloc(p, &p->xq, Tp * D));
     TRY(palloc(p, &p->xsf, (D / 128) * Tp * 4));
-    TRY(palloc(p, &p->z, sizeof(float) * Tp * L));
+    TRY(palloc(p, &p->z, sizeof(float) * Tp * 2 * L));     // TF32 high part | remainder
     TRY(palloc(p, &p->zq, Tp * L));
     TRY(palloc(p, &p->zsf, (L / 128) * Tp * 4));
     TRY(palloc(p, &p->act, Tp * p->Kcat));
     TRY(palloc(p, &p->actsf, (p->Kcat / 128) * Tp * 4));
     TRY(palloc(p, &p->logits, sizeof(float) * p->T_max * E));
+    TRY(palloc(p, &p->rpart, sizeof(float) * router_partials(std::min(p->T_max, 128), L) *
+                                 std::min(p->T_max, 128) * E));
     TRY(palloc(p, &p->idx, sizeof(int32_t) * p->T_max * p->k));
     TRY(palloc(p, &p->gw, sizeof(float) * p->T_max * p->k));
     TRY(palloc(p, &p->sel, sizeof(uint32_t) * E * p->W_max));
@@ -425,7 +446,9 @@ moe_status moe_plan(const moe_config* cfg, const moe_weights* w, int device, voi
     bool ok = map_mx4(&p->tA2, p->a2c, p->rowsA2, D) && map_mx8(&p->tB2, p->xq, Tp, D) &&
               map_mx4(&p->tA7, p->w13c, static_cast<int64_t>(E) * 2 * I, L) && map_mx8(&p->tB7, p->zqp, Rp, L) &&
               map_mx4(&p->tA8, p->w2c, static_cast<int64_t>(E) * L, Ip) && map_mx8(&p->tB8, p->hq, Rp, Ip) &&
-              map_mx4(&p->tA10, p->a10c, D, p->Kcat) && map_mx8(&p->tB10, p->act, Tp, p->Kcat);
+              map_mx4(&p->tA10, p->a10c, D, p->Kcat) && map_mx8(&p->tB10, p->act, Tp, p->Kcat) &&
+              map_f32(&p->tAR, p->router2, E, 2 * L, 128) && map_f32(&p->tBR, p->z, Tp, 2 * L, 16);
+    p->tc_router = (E % 128 == 0) && (L % 32 == 0);
     if (!ok) {
         plan_release(p);
         return MOE_ERR_CUDA;
@@ -468,16 +491,39 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
         g.m_tiles = p->rowsA2 / kBlockM;
         g.n_tokens = T;
         g.epi_split = L / kBlockM;
-        g.epi[0] = EpiParams{EPI_QUANT, 0, 0, 0, p->z, L, p->zq, L, p->zsf, Tp};
+        g.epi[0] = EpiParams{EPI_QUANT, 0, 0, L, p->z, 2 * L, p->zq, L, p->zsf, Tp};
         g.epi[1] = EpiParams{EPI_SILU_QUANT, L / kBlockM, L, 0, nullptr, 0, p->act, p->Kcat, p->actsf, Tp};
         const int items = g.m_tiles * ((T + g.n_max - 1) / g.n_max);
         TRY(launch_gemm(g, std::min(items, p->num_sms), s));
     }
     // 3. router logits, 4. top-k + gates + bitmaps
     mark(2);
-    TRY(launch_router(p->z, p->router, p->logits, T, E, L, s));
+    int nparts = 1;
+    if (p->tc_router && T > 128) {
+        // logits = z R^T as three TF32 products, z_hi R_hi + z_lo R_hi + z_hi R_lo,
+        // K-concatenated through the maps' coordinates into one accumulator
+        GemmParams g = gemm_base(p->tAR, p->tBR, nullptr, nullptr, 0, 3 * L * 4, nmax_dense, E,
+                                 static_cast<int>(Tp), p->status);
+        g.kind = KIND_TF32;
+        g.KT = 3 * L / 32;
+        g.kseg_tiles = L / 32;
+        g.a_seg_x[0] = 0; g.a_seg_x[1] = 0; g.a_seg_x[2] = L;
+        g.b_seg_x[0] = 0; g.b_seg_x[1] = L; g.b_seg_x[2] = 0;
+        g.dense = 1;
+        g.m_tiles = E / kBlockM;
+        g.n_tokens = T;
+        g.epi_split = 1 << 30;
+        g.epi[0] = EpiParams{EPI_F32, 0, 0, 0, p->logits, E, nullptr, 0, nullptr, 0};
+        const int items = g.m_tiles * ((T + g.n_max - 1) / g.n_max);
+        TRY(launch_gemm(g, std::min(items, p->num_sms), s));
+        nparts = 1;
+    } else {
+        nparts = router_partials(T, L);
+        TRY(launch_router(p->z, p->router, p->logits, p->rpart, T, E, L, s));
+    }
     mark(3);
-    TRY(launch_topk(p->logits, p->bias, T, E, k, p->cfg.score_fn == MOE_SCORE_SOFTMAX, p->idx, p->gw, p->sel, W, s));
+    TRY(launch_topk(p->logits, p->rpart, nparts, p->bias, T, E, k, p->cfg.score_fn == MOE_SCORE_SOFTMAX, p->idx,
+                    p->gw, p->sel, W, s));
     // 5. per-expert prefix counts, 6. offsets + work lists
     mark(4);
     TRY(launch_expert_scan(p->sel, E, W, p->wpre, p->counts, s));
@@ -569,7 +615,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
         const int64_t TK = static_cast<int64_t>(T) * k;
         if (dbg->xq) TRY(cudaMemcpyAsync(dbg->xq, p->xq, static_cast<size_t>(T) * D, cudaMemcpyDeviceToDevice, s));
         if (dbg->xs) TRY(launch_export_sf(p->xsf, Tp, nullptr, T, D / 32, 0, dbg->xs, s));
-        if (dbg->z) TRY(cudaMemcpyAsync(dbg->z, p->z, sizeof(float) * T * L, cudaMemcpyDeviceToDevice, s));
+        if (dbg->z) TRY(launch_add_halves(p->z, T, L, dbg->z, s));
         if (dbg->zq) TRY(cudaMemcpyAsync(dbg->zq, p->zq, static_cast<size_t>(T) * L, cudaMemcpyDeviceToDevice, s));
         if (dbg->zs) TRY(launch_export_sf(p->zsf, Tp, nullptr, T, L / 32, 0, dbg->zs, s));
         if (S > 0 && dbg->hsq)

@@ -116,7 +116,10 @@ __device__ __forceinline__ bool mbar_wait_teardown(uint64_t* bar, uint32_t parit
     return true;
 }
 
+template <int KIND>
 __global__ void __launch_bounds__(kGemmThreads, 1) mx_gemm_kernel(const __grid_constant__ GemmParams p) {
+    constexpr bool kMX = (KIND == KIND_MX);
+    constexpr int kTileElems = kMX ? kBlockK : 32;      // K elements per 128-byte row of a stage
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = p.stages;
@@ -173,22 +176,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1) mx_gemm_kernel(const __grid_c
                     continue;
                 }
                 const int nm = (w.n + 15) & ~15;
-                const uint32_t tx = static_cast<uint32_t>(p.a_tx_bytes + (nm / 16) * 2048 + 512 + nm * 4);
-                const uint8_t* sfa_tile = p.sfa + static_cast<size_t>(w.a_row0 / kBlockM) * p.KT * 512;
+                const uint32_t tx = kMX ? static_cast<uint32_t>(p.a_tx_bytes + (nm / 16) * 2048 + 512 + nm * 4)
+                                        : static_cast<uint32_t>(kBlockM * 128 + (nm / 16) * 2048);
+                const uint8_t* sfa_tile = kMX ? p.sfa + static_cast<size_t>(w.a_row0 / kBlockM) * p.KT * 512 : nullptr;
                 bool ok = true;
                 for (int kt = 0; kt < p.KT; ++kt) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_PRODUCER)) {
                         ok = false;
                         break;
                     }
+                    const int seg = kt / p.kseg_tiles;
+                    const int kin = (kt - seg * p.kseg_tiles) * kTileElems;
                     uint8_t* sb = base + stage * p.stage_bytes;
                     mbar_arrive_expect_tx(&full[stage], tx);
-                    tma_load_2d(sb, &p.tmA, &full[stage], kt * kBlockK, w.a_row0);
+                    tma_load_2d(sb, &p.tmA, &full[stage], p.a_seg_x[seg] + kin, w.a_row0);
                     for (int c = 0; c < nm / 16; ++c)
-                        tma_load_2d(sb + L.offB + c * 2048, &p.tmB, &full[stage], kt * kBlockK, w.b_row0 + c * 16);
-                    bulk_load(sb + L.offSFA, sfa_tile + static_cast<size_t>(kt) * 512, 512, &full[stage]);
-                    bulk_load(sb + L.offSFBraw, p.sfb + (static_cast<size_t>(kt) * p.sfb_pitch + w.b_row0) * 4,
-                              static_cast<uint32_t>(nm * 4), &full[stage]);
+                        tma_load_2d(sb + L.offB + c * 2048, &p.tmB, &full[stage], p.b_seg_x[seg] + kin,
+                                    w.b_row0 + c * 16);
+                    if constexpr (kMX) {
+                        bulk_load(sb + L.offSFA, sfa_tile + static_cast<size_t>(kt) * 512, 512, &full[stage]);
+                        bulk_load(sb + L.offSFBraw,
+                                  p.sfb + (static_cast<size_t>(kt) * p.sfb_pitch + w.b_row0) * 4,
+                                  static_cast<uint32_t>(nm * 4), &full[stage]);
+                    }
                     issued |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == static_cast<uint32_t>(S)) {
@@ -222,7 +232,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) mx_gemm_kernel(const __grid_c
                 ok = mbar_wait(&full[stage], phase, abort_flag, p.status, DEV_TIMEOUT_MMA);
                 if (!__all_sync(0xffffffffu, ok)) goto mma_done;
                 tc_fence_after();
-                {
+                if constexpr (!kMX) {
+                    uint8_t* sb = base + stage * p.stage_bytes;
+                    if (lane == 0) {
+                        const uint64_t adesc = sdesc_sw128(smem_u32(sb));
+                        const uint64_t bdesc = sdesc_sw128(smem_u32(sb + L.offB));
+                        const uint32_t idesc = idesc_tf32(kBlockM, static_cast<int>(idesc_n));
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            mma_tf32(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, (kt | j) != 0 ? 1u : 0u);
+                        tc_commit(&empty[stage]);
+                    }
+                    any = true;
+                    __syncwarp();
+                } else {
                     uint8_t* sb = base + stage * p.stage_bytes;
                     // B scales arrive as one uint32 per token row (4 bytes = the 4
                     // K-blocks of this tile).  The 32x128b copy wants 32 rows of
@@ -326,7 +349,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) mx_gemm_kernel(const __grid_c
                         const int n = n0 + i;
                         if (n < w.n) {
                             const int64_t row = w.b_row0 + n;
-                            if (E.out_f32) E.out_f32[row * E.ld_f32 + col] = v[i];
+                            if (E.out_f32) {
+                                if (E.f32_split) {
+                                    const float hi = tf32_round(v[i]);
+                                    E.out_f32[row * E.ld_f32 + col] = hi;
+                                    E.out_f32[row * E.ld_f32 + col + E.f32_split] = v[i] - hi;
+                                } else {
+                                    E.out_f32[row * E.ld_f32 + col] = v[i];
+                                }
+                            }
                             if (E.mode == EPI_QUANT) {
                                 uint8_t sc;
                                 const uint8_t code = warp_mx8_quant(v[i], &sc);
@@ -374,12 +405,19 @@ int gemm_stages(int n_max) {
 }
 
 cudaError_t gemm_setup() {
-    return cudaFuncSetAttribute(mx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    cudaError_t err =
+        cudaFuncSetAttribute(mx_gemm_kernel<KIND_MX>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    if (err != cudaSuccess) return err;
+    return cudaFuncSetAttribute(mx_gemm_kernel<KIND_TF32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
 }
 
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s) {
     const size_t smem = gemm_smem_bytes(p.n_max, p.stages);
-    mx_gemm_kernel<<<grid, kGemmThreads, smem, s>>>(p);
+    if (p.kseg_tiles <= 0 || p.KT > 3 * p.kseg_tiles) return cudaErrorInvalidValue;
+    if (p.kind == KIND_TF32)
+        mx_gemm_kernel<KIND_TF32><<<grid, kGemmThreads, smem, s>>>(p);
+    else
+        mx_gemm_kernel<KIND_MX><<<grid, kGemmThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 

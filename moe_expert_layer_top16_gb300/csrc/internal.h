@@ -32,7 +32,7 @@ struct EpiParams {
     int mode;
     int m_tile0;
     int col0;
-    int pad0;
+    int f32_split;      // > 0: store the fp32 output as TF32 hi at col and the remainder lo at col + f32_split
     float* out_f32;     // [rows][ld_f32]
     int64_t ld_f32;
     uint8_t* out_q;     // E4M3 codes [rows][ld_q]
@@ -41,9 +41,14 @@ struct EpiParams {
     int64_t sf_pitch;   // rows per plane
 };
 
+enum GemmKind : int {
+    KIND_MX = 0,        // MXFP4 A x MXFP8 B, block-scaled (kind::mxf8f6f4)
+    KIND_TF32 = 1       // fp32 A x fp32 B as TF32 (kind::tf32), no scales
+};
+
 struct GemmParams {
-    CUtensorMap tmA;        // MXFP4 weights, 16U4_ALIGN16B, box {128, 128}, 128B swizzle
-    CUtensorMap tmB;        // MXFP8 activations, UINT8, box {128, 16}, 128B swizzle
+    CUtensorMap tmA;        // MX: MXFP4 weights, 16U4_ALIGN16B, box {128, 128}; TF32: fp32, box {32, 128}
+    CUtensorMap tmB;        // MX: MXFP8 activations, UINT8, box {128, 16}; TF32: fp32, box {32, 16}
     const uint8_t* sfa;     // weight scales, pre-arranged: [rows/128][KT][512]
     const uint8_t* sfb;     // activation scale planes: [KT][sfb_pitch] uint32
     int64_t sfb_pitch;
@@ -60,7 +65,10 @@ struct GemmParams {
     const int4* items;      // {a_row0, b_row0, n, mt}
     const int* n_items;
     int epi_split;          // dense: m-tiles >= epi_split use epi[1]
-    int pad1;
+    int kind;               // GemmKind
+    int kseg_tiles;         // K tiles per K segment (K-concatenation through map coordinates)
+    int a_seg_x[3];         // element offset along K of each segment in A's map
+    int b_seg_x[3];         // element offset along K of each segment in B's map
     EpiParams epi[2];
     int* status;
 };
@@ -74,9 +82,16 @@ cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s);
 // ------------------------------------------------------------------ other kernels
 cudaError_t launch_quant_x(const __nv_bfloat16* x, int T, int D, uint8_t* xq, uint8_t* xsf, int64_t pitch,
                            cudaStream_t s);
-cudaError_t launch_router(const float* z, const float* R, float* logits, int T, int E, int L, cudaStream_t s);
-cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int softmax, int32_t* idx,
-                        float* w, uint32_t* sel, int W, cudaStream_t s);
+// SIMT router on z = hi + lo ([T][2L]).  Batches of at most 128 tokens write
+// router_partials(T, L) K-split partial sums to part[split][T][E] (summed by
+// the top-k kernel); larger ones write logits directly.
+int router_partials(int T, int L);
+cudaError_t launch_router(const float* z, const float* R, float* logits, float* part, int T, int E, int L,
+                          cudaStream_t s);
+// top-k + gates; with nparts > 1 the logits are first summed from `part`
+// (and written to `logits`).
+cudaError_t launch_topk(float* logits, const float* part, int nparts, const float* bias, int T, int E, int k,
+                        int softmax, int32_t* idx, float* w, uint32_t* sel, int W, cudaStream_t s);
 cudaError_t launch_expert_scan(const uint32_t* sel, int E, int W, int32_t* wpre, int32_t* counts, cudaStream_t s);
 struct WorkListArgs {
     const int32_t* counts;
@@ -102,6 +117,10 @@ cudaError_t launch_combine(const float* o, const int32_t* slot_pos, const float*
 cudaError_t launch_mxfp4_encode(const float* w, int64_t rows, int64_t K, uint8_t* codes, uint8_t* scales,
                                 cudaStream_t s);
 cudaError_t kernels_setup();   // per-device kernel attributes
+// fp32 [rows][K] -> [rows][2K] = nearest TF32 | exact remainder
+cudaError_t launch_tf32_split(const float* src, int64_t rows, int64_t K, float* dst, cudaStream_t s);
+// [rows][2K] (hi | lo) -> [rows][K] = hi + lo
+cudaError_t launch_add_halves(const float* src, int64_t rows, int64_t K, float* dst, cudaStream_t s);
 // row-major scales [rows][kb] -> scale planes [kb/4][pitch] (uint32 words)
 cudaError_t launch_sf_planes(const uint8_t* scales_rm, int64_t rows, int64_t kb, uint8_t* planes, int64_t pitch,
                              cudaStream_t s);

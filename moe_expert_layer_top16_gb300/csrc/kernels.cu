@@ -54,6 +54,7 @@ __global__ void quant_x_kernel(const __nv_bfloat16* __restrict__ x, int T, int D
 constexpr int RT = 64, RE = 64, RK = 16;
 __global__ void __launch_bounds__(256) router_kernel(const float* __restrict__ z, const float* __restrict__ R,
                                                      float* __restrict__ logits, int T, int E, int L) {
+    // z: [T][2L] = TF32 high part | remainder; z = hi + lo exactly
     __shared__ float zs[RK][RT + 4];
     __shared__ float rs[RK][RE + 4];
     const int t0 = blockIdx.y * RT, e0 = blockIdx.x * RE;
@@ -62,7 +63,8 @@ __global__ void __launch_bounds__(256) router_kernel(const float* __restrict__ z
     for (int k0 = 0; k0 < L; k0 += RK) {
         for (int i = threadIdx.x; i < RT * RK; i += 256) {
             const int r = i / RK, c = i % RK;
-            zs[c][r] = (t0 + r < T) ? z[static_cast<int64_t>(t0 + r) * L + k0 + c] : 0.0f;
+            const float* zr = z + static_cast<int64_t>(t0 + r) * 2 * L + k0 + c;
+            zs[c][r] = (t0 + r < T) ? zr[0] + zr[L] : 0.0f;
             rs[c][r] = (e0 + r < E) ? R[static_cast<int64_t>(e0 + r) * L + k0 + c] : 0.0f;
         }
         __syncthreads();
@@ -94,22 +96,30 @@ __global__ void __launch_bounds__(256) router_kernel(const float* __restrict__ z
 
 // Decode-sized batches (T <= 128): 8 experts per CTA so that ~E/8 CTAs
 // stream R from HBM in parallel; the tokens' latent rows come through shared
-// memory in 64-wide K chunks (z is small and L2-resident).  Warp w owns
+// memory in 64-wide K chunks (z is small and L2-resident; it is stored as
+// TF32 high part | remainder, [T][2L], and z = hi + lo exactly).  Warp w owns
 // expert e0 + w; lane l owns tokens l, l+32, l+64, l+96.  One sequential FMA
 // chain per output, like the tiled kernel.
-constexpr int RS_E = 8, RS_K = 64, RS_TMAX = 128;
+// K is split RS_KSPLIT ways across blockIdx.y (many CTAs per SM hide the L2
+// latency of the z chunks); each split writes its partial sums to
+// part[split][T][E] and the top-k kernel adds the splits in a fixed order.
+constexpr int RS_E = 8, RS_K = 64, RS_TMAX = 128, RS_KSPLIT = 8;
 __global__ void __launch_bounds__(256) router_small_kernel(const float* __restrict__ z, const float* __restrict__ R,
-                                                           float* __restrict__ logits, int T, int E, int L) {
+                                                           float* __restrict__ part, int T, int E, int L) {
     __shared__ float zs[RS_TMAX][RS_K + 1];
     __shared__ float rs[RS_E][RS_K];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e0 = blockIdx.x * RS_E;
     const int e = e0 + warp;
+    const int klen = L / RS_KSPLIT;
+    const int kbeg = blockIdx.y * klen;
+    float* logits = part + static_cast<int64_t>(blockIdx.y) * T * E;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int k0 = 0; k0 < L; k0 += RS_K) {
+    for (int k0 = kbeg; k0 < kbeg + klen; k0 += RS_K) {
         for (int i = threadIdx.x; i < T * RS_K; i += 256) {
             const int r = i / RS_K, c = i % RS_K;
-            zs[r][c] = z[static_cast<int64_t>(r) * L + k0 + c];
+            const float* zr = z + static_cast<int64_t>(r) * 2 * L + k0 + c;
+            zs[r][c] = zr[0] + zr[L];
         }
         for (int i = threadIdx.x; i < RS_E * RS_K; i += 256) {
             const int r = i / RS_K, c = i % RS_K;
@@ -178,15 +188,24 @@ __device__ __forceinline__ double key64(float l, const float* bias, int e) {
     return 1.0 / (1.0 + exp(-static_cast<double>(l))) + static_cast<double>(bias[e]);
 }
 
-__global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(const float* __restrict__ logits,
-                                                                const float* __restrict__ bias, int T, int E, int k,
-                                                                int softmax, int32_t* __restrict__ idx_out,
-                                                                float* __restrict__ w_out, uint32_t* __restrict__ sel,
-                                                                int W) {
+__global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(float* __restrict__ logits, const float* __restrict__ part,
+                                                                int nparts, const float* __restrict__ bias, int T,
+                                                                int E, int k, int softmax,
+                                                                int32_t* __restrict__ idx_out, float* __restrict__ w_out,
+                                                                uint32_t* __restrict__ sel, int W) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * kTopkWarps + warp;
     if (t >= T) return;
-    const float* l = logits + static_cast<int64_t>(t) * E;
+    float* l = logits + static_cast<int64_t>(t) * E;
+    if (nparts > 1) {
+        // logits = sum of the router's K-split partials, in split order
+        for (int e = lane; e < E; e += 32) {
+            float v = 0.0f;
+            for (int q = 0; q < nparts; ++q) v += part[(static_cast<int64_t>(q) * T + t) * E + e];
+            l[e] = v;
+        }
+        __syncwarp();
+    }
     const bool use_bias = (bias != nullptr) && !softmax;
     const int nper = (E + 31) / 32;
     float lv[kTopkPerLane], key[kTopkPerLane];
@@ -549,6 +568,27 @@ __global__ void sf_planes_kernel(const uint8_t* __restrict__ rm, int64_t rows, i
     planes[((b / 4) * pitch + row) * 4 + (b % 4)] = rm[i];
 }
 
+// [rows][K] fp32 -> [rows][2K]: nearest TF32 value, then the exact remainder.
+__global__ void tf32_split_kernel(const float* __restrict__ src, int64_t rows, int64_t K, float* __restrict__ dst) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= rows * K) return;
+    const int64_t r = i / K, c = i % K;
+    const float v = src[i];
+    uint32_t hb;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hb) : "f"(v));
+    const float hi = __uint_as_float(hb);
+    dst[r * 2 * K + c] = hi;
+    dst[r * 2 * K + K + c] = v - hi;
+}
+
+// [rows][2K] (hi | lo) -> [rows][K] fp32 sums.
+__global__ void add_halves_kernel(const float* __restrict__ src, int64_t rows, int64_t K, float* __restrict__ dst) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= rows * K) return;
+    const int64_t r = i / K, c = i % K;
+    dst[i] = src[r * 2 * K + c] + src[r * 2 * K + K + c];
+}
+
 // ------------------------------------------------------------------ debug export
 __global__ void export_sf_kernel(const uint8_t* __restrict__ planes, int64_t pitch, const int32_t* __restrict__ row_map,
                                  int64_t rows, int64_t nblocks, int64_t col_block0, uint8_t* __restrict__ out) {
@@ -579,9 +619,13 @@ cudaError_t launch_quant_x(const __nv_bfloat16* x, int T, int D, uint8_t* xq, ui
     return cudaGetLastError();
 }
 
-cudaError_t launch_router(const float* z, const float* R, float* logits, int T, int E, int L, cudaStream_t s) {
-    if (T <= RS_TMAX && L % RS_K == 0) {
-        router_small_kernel<<<(E + RS_E - 1) / RS_E, 256, 0, s>>>(z, R, logits, T, E, L);
+int router_partials(int T, int L) { return (T <= RS_TMAX && L % (RS_K * RS_KSPLIT) == 0) ? RS_KSPLIT : 1; }
+
+cudaError_t launch_router(const float* z, const float* R, float* logits, float* part, int T, int E, int L,
+                          cudaStream_t s) {
+    if (T <= RS_TMAX && L % (RS_K * RS_KSPLIT) == 0) {
+        dim3 grid((E + RS_E - 1) / RS_E, RS_KSPLIT);
+        router_small_kernel<<<grid, 256, 0, s>>>(z, R, part, T, E, L);
         return cudaGetLastError();
     }
     dim3 grid((E + RE - 1) / RE, (T + RT - 1) / RT);
@@ -589,11 +633,11 @@ cudaError_t launch_router(const float* z, const float* R, float* logits, int T, 
     return cudaGetLastError();
 }
 
-cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int softmax, int32_t* idx,
-                        float* w, uint32_t* sel, int W, cudaStream_t s) {
+cudaError_t launch_topk(float* logits, const float* part, int nparts, const float* bias, int T, int E, int k,
+                        int softmax, int32_t* idx, float* w, uint32_t* sel, int W, cudaStream_t s) {
     if (E > kMaxE || k > 32) return cudaErrorInvalidValue;
-    topk_kernel<<<(T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, s>>>(logits, bias, T, E, k, softmax, idx,
-                                                                            w, sel, W);
+    topk_kernel<<<(T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, s>>>(logits, part, nparts, bias, T, E, k,
+                                                                            softmax, idx, w, sel, W);
     return cudaGetLastError();
 }
 
@@ -643,6 +687,20 @@ cudaError_t launch_sf_atoms(const uint8_t* scales_rm, int64_t rows, int64_t kb, 
 }
 
 cudaError_t kernels_setup() { return cudaSuccess; }
+
+cudaError_t launch_tf32_split(const float* src, int64_t rows, int64_t K, float* dst, cudaStream_t s) {
+    const int64_t n = rows * K;
+    if (n == 0) return cudaSuccess;
+    tf32_split_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(src, rows, K, dst);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_add_halves(const float* src, int64_t rows, int64_t K, float* dst, cudaStream_t s) {
+    const int64_t n = rows * K;
+    if (n == 0) return cudaSuccess;
+    add_halves_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(src, rows, K, dst);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_sf_planes(const uint8_t* scales_rm, int64_t rows, int64_t kb, uint8_t* planes, int64_t pitch,
                              cudaStream_t s) {

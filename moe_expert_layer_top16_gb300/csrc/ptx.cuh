@@ -127,6 +127,17 @@ __device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t adesc, ui
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
         : "memory");
 }
+// D[tmem] (+)= A[smem] * B[smem]^T, TF32 operands (fp32 in shared memory,
+// the low 13 mantissa bits ignored), fp32 accumulate.
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // Copy a 32-row x 128-bit block from shared memory into 4 TMEM columns of
 // all four 32-lane quarters.
 __device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
@@ -184,6 +195,25 @@ __host__ __device__ __forceinline__ uint32_t idesc_mxf8f6f4(int M, int N, int a_
     d |= static_cast<uint32_t>((M >> 4) & 31) << 24;
     d |= static_cast<uint32_t>(sfa_id & 3) << 29;
     return d;
+}
+
+// Instruction descriptor for kind::tf32: fp32 accumulator, A and B TF32,
+// both K-major.
+__host__ __device__ __forceinline__ uint32_t idesc_tf32(int M, int N) {
+    uint32_t d = 0;
+    d |= 1u << 4;                                           // accumulator format F32
+    d |= 2u << 7;                                           // A: TF32
+    d |= 2u << 10;                                          // B: TF32
+    d |= static_cast<uint32_t>((N >> 3) & 63) << 17;
+    d |= static_cast<uint32_t>((M >> 4) & 31) << 24;
+    return d;
+}
+
+// fp32 -> nearest TF32 value (10 mantissa bits, ties away from zero), as fp32.
+__device__ __forceinline__ float tf32_round(float v) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
+    return __uint_as_float(r);
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
