@@ -98,11 +98,17 @@ bool map_mx8(CUtensorMap* m, const void* codes, int64_t rows, int64_t K) {
 
 inline int64_t rup(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
 
+// Bound on |tensor-core logit - fp32 logit| assumed by the top-k refinement.
+// The 3xTF32 product accumulated by the tensor core (which rounds its fp32
+// accumulator toward zero at every step) stays within ~5e-4 of the fp64
+// logit on the K3-shaped layer; the bound leaves a factor 8.
+constexpr float kTcRouterDelta = 4.0e-3f;
+
 struct Plan {
     moe_config cfg;
     int device = 0, num_sms = 0;
     int D, L, E, k, I, Ip, S, Is, SIs, Kcat, rowsA2, T_max, T_pad, W_max;
-    int64_t R_pad, items_cap7, items_cap8;
+    int64_t R_pad;
     size_t bytes = 0;
     std::vector<void*> allocs;
     // weights
@@ -113,8 +119,7 @@ struct Plan {
     float *z, *logits, *rpart, *gw, *o;   // rpart: router K-split partials (batches <= 128 tokens)
     uint32_t* sel;
     int32_t *idx, *wpre, *counts, *offsets, *seg, *slot_pos, *canon_to_pad, *sorted_token;
-    int4 *items7, *items8;
-    int* n_items;   // [2]
+    int32_t *ioff7, *ioff8;   // [E+1] per-expert item offsets of the grouped GEMMs
     int* status;
     void* x_stage;
     float* y_stage;
@@ -222,7 +227,6 @@ GemmParams gemm_base(const CUtensorMap& A, const CUtensorMap& B, const uint8_t* 
     g.sfb_pitch = sfb_pitch;
     g.KT = K / kBlockK;
     g.n_max = n_max;
-    g.stages = gemm_stages(n_max);
     g.stage_bytes = gemm_stage_bytes(n_max);
     g.a_tx_bytes = MOE_A_TX_BYTES;
     g.kind = KIND_MX;
@@ -233,10 +237,39 @@ GemmParams gemm_base(const CUtensorMap& A, const CUtensorMap& B, const uint8_t* 
     return g;
 }
 
-int pick_n_max(int T) {
-    const int tiles = (T + kNMax - 1) / kNMax;
+// Tokens per dense work item: the batch split into equal 16-row multiples of
+// at most `cap` rows.
+int pick_n_max(int T, int cap = kNMax) {
+    const int tiles = (T + cap - 1) / cap;
     const int per = (T + tiles - 1) / tiles;
     return static_cast<int>(rup(per, 16));
+}
+
+// Largest per-item token count at batch size T: small batches use narrow
+// items (several groups, two TMEM buffers each), larger ones wide items.
+int item_cap(int T) { return T <= 256 ? 48 : kNMax; }
+
+// Groups / accumulator buffers / stages for a GEMM whose items hold up to
+// g.n_max tokens and span g.KT K tiles.  E > 0 for grouped items.
+void shape_gemm(GemmParams& g, int E) {
+    // narrow items: up to four groups, each with at least 4 K tiles; wide
+    // items: one group with two accumulators (epilogue overlap)
+    const int want = (g.n_max <= 64) ? 4 : 1;
+    for (int G = want; G >= 1; G >>= 1) {
+        if (G > 1 && g.KT < 4 * G) continue;
+        for (int NB = 2; NB >= 1; --NB) {
+            if (!gemm_config_ok(g.n_max, G, NB)) continue;
+            const int S = gemm_stages(g.n_max, G, E);
+            if (gemm_smem_bytes(g.n_max, G, S, E) > static_cast<size_t>(kSmemLimit)) continue;
+            g.groups = G;
+            g.acc_bufs = NB;
+            g.stages = S;
+            return;
+        }
+    }
+    g.groups = 1;
+    g.acc_bufs = 1;
+    g.stages = gemm_stages(g.n_max, 1, E);
 }
 
 moe_status validate(const moe_config* c) {
@@ -308,8 +341,6 @@ moe_status moe_plan(const moe_config* cfg, const moe_weights* w, int device, voi
     p->T_pad = static_cast<int>(rup(p->T_max, 16));
     p->W_max = (p->T_max + 31) / 32;
     p->R_pad = rup(static_cast<int64_t>(p->T_max) * p->k + 15LL * p->E, 16);
-    p->items_cap7 = (static_cast<int64_t>(p->T_max) * p->k / 16 + p->E + 1) * (2 * p->I / 128);
-    p->items_cap8 = (static_cast<int64_t>(p->T_max) * p->k / 16 + p->E + 1) * (p->L / 128);
 
     cudaError_t err = gemm_setup();
     if (err == cudaSuccess) err = kernels_setup();
@@ -430,9 +461,8 @@ moe_status moe_plan(const moe_config* cfg, const moe_weights* w, int device, voi
     TRY(palloc(p, &p->hq, Rp * Ip));
     TRY(palloc(p, &p->hqsf, (Ip / 128) * Rp * 4));
     TRY(palloc(p, &p->o, sizeof(float) * Rp * L));
-    TRY(palloc(p, &p->items7, sizeof(int4) * p->items_cap7));
-    TRY(palloc(p, &p->items8, sizeof(int4) * p->items_cap8));
-    TRY(palloc(p, &p->n_items, sizeof(int) * 4));
+    TRY(palloc(p, &p->ioff7, sizeof(int32_t) * (E + 1)));
+    TRY(palloc(p, &p->ioff8, sizeof(int32_t) * (E + 1)));
     TRY(palloc(p, &p->status, sizeof(int) * 4));
     TRY(palloc(p, &p->x_stage, sizeof(uint16_t) * p->T_max * D));
     TRY(palloc(p, &p->y_stage, sizeof(float) * p->T_max * D));
@@ -467,8 +497,8 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
     const int D = p->D, L = p->L, E = p->E, k = p->k, I = p->I, Ip = p->Ip;
     const int W = (T + 31) / 32;
     const int64_t Tp = p->T_pad, Rp = p->R_pad;
-    const int nmax_dense = pick_n_max(T);
-    const int nmax_grp = static_cast<int>(std::min<int64_t>(kNMax, rup(T, 16)));
+    const int nmax_dense = pick_n_max(T, item_cap(T));
+    const int nmax_grp = static_cast<int>(std::min<int64_t>(item_cap(T), rup(T, 16)));
     cudaError_t err = cudaSuccess;
 #define TRY(x)                          \
     do {                                \
@@ -493,13 +523,15 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
         g.epi_split = L / kBlockM;
         g.epi[0] = EpiParams{EPI_QUANT, 0, 0, L, p->z, 2 * L, p->zq, L, p->zsf, Tp};
         g.epi[1] = EpiParams{EPI_SILU_QUANT, L / kBlockM, L, 0, nullptr, 0, p->act, p->Kcat, p->actsf, Tp};
+        shape_gemm(g, 0);
         const int items = g.m_tiles * ((T + g.n_max - 1) / g.n_max);
         TRY(launch_gemm(g, std::min(items, p->num_sms), s));
     }
     // 3. router logits, 4. top-k + gates + bitmaps
     mark(2);
     int nparts = 1;
-    if (p->tc_router && T > 128) {
+    const bool tc_logits = p->tc_router && T > 128;
+    if (tc_logits) {
         // logits = z R^T as three TF32 products, z_hi R_hi + z_lo R_hi + z_hi R_lo,
         // K-concatenated through the maps' coordinates into one accumulator
         GemmParams g = gemm_base(p->tAR, p->tBR, nullptr, nullptr, 0, 3 * L * 4, nmax_dense, E,
@@ -514,6 +546,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
         g.n_tokens = T;
         g.epi_split = 1 << 30;
         g.epi[0] = EpiParams{EPI_F32, 0, 0, 0, p->logits, E, nullptr, 0, nullptr, 0};
+        shape_gemm(g, 0);
         const int items = g.m_tiles * ((T + g.n_max - 1) / g.n_max);
         TRY(launch_gemm(g, std::min(items, p->num_sms), s));
         nparts = 1;
@@ -522,8 +555,27 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
         TRY(launch_router(p->z, p->router, p->logits, p->rpart, T, E, L, s));
     }
     mark(3);
-    TRY(launch_topk(p->logits, p->rpart, nparts, p->bias, T, E, k, p->cfg.score_fn == MOE_SCORE_SOFTMAX, p->idx,
-                    p->gw, p->sel, W, s));
+    {
+        TopkArgs a;
+        a.logits = p->logits;
+        a.part = p->rpart;
+        a.nparts = nparts;
+        a.bias = p->bias;
+        a.T = T;
+        a.E = E;
+        a.k = k;
+        a.softmax = p->cfg.score_fn == MOE_SCORE_SOFTMAX;
+        a.refine = tc_logits ? 1 : 0;
+        a.delta = kTcRouterDelta;
+        a.z = p->z;
+        a.R = p->router;
+        a.L = L;
+        a.idx = p->idx;
+        a.w = p->gw;
+        a.sel = p->sel;
+        a.W = W;
+        TRY(launch_topk(a, s));
+    }
     // 5. per-expert prefix counts, 6. offsets + work lists
     mark(4);
     TRY(launch_expert_scan(p->sel, E, W, p->wpre, p->counts, s));
@@ -534,16 +586,12 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
         a.E = E;
         a.offsets = p->offsets;
         a.seg = p->seg;
-        a.items1 = p->items7;
-        a.n_items1 = p->n_items;
+        a.ioff1 = p->ioff7;
         a.n_max1 = nmax_grp;
         a.mt1 = 2 * I / kBlockM;
-        a.a_rows_per_e1 = 2 * I;
-        a.items2 = p->items8;
-        a.n_items2 = p->n_items + 1;
+        a.ioff2 = p->ioff8;
         a.n_max2 = nmax_grp;
         a.mt2 = L / kBlockM;
-        a.a_rows_per_e2 = L;
         TRY(launch_worklist(a, s));
     }
     // 7. stable ranks, permuted rows, gather of zq
@@ -576,8 +624,13 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
         GemmParams g = gemm_base(p->tA7, p->tB7, p->w13sf, p->zqpsf, Rp, L, nmax_grp, E * 2 * I,
                                  static_cast<int>(Rp), p->status);
         g.dense = 0;
-        g.items = p->items7;
-        g.n_items = p->n_items;
+        g.ioff = p->ioff7;
+        g.seg = p->seg;
+        g.counts = p->counts;
+        g.E = E;
+        g.mt_per_e = 2 * I / kBlockM;
+        g.rows_per_e = 2 * I;
+        shape_gemm(g, E);
         g.epi[0] = EpiParams{EPI_SILU_QUANT, 0, 0, 0, nullptr, 0, p->hq, Ip, p->hqsf, Rp};
         TRY(launch_gemm(g, p->num_sms, s));
     }
@@ -587,8 +640,13 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
         GemmParams g = gemm_base(p->tA8, p->tB8, p->w2sf, p->hqsf, Rp, Ip, nmax_grp, E * L, static_cast<int>(Rp),
                                  p->status);
         g.dense = 0;
-        g.items = p->items8;
-        g.n_items = p->n_items + 1;
+        g.ioff = p->ioff8;
+        g.seg = p->seg;
+        g.counts = p->counts;
+        g.E = E;
+        g.mt_per_e = L / kBlockM;
+        g.rows_per_e = L;
+        shape_gemm(g, E);
         g.epi[0] = EpiParams{EPI_F32, 0, 0, 0, p->o, L, nullptr, 0, nullptr, 0};
         TRY(launch_gemm(g, p->num_sms, s));
     }
@@ -605,6 +663,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
         g.n_tokens = T;
         g.epi_split = 1 << 30;
         g.epi[0] = EpiParams{EPI_F32, 0, 0, 0, y, D, nullptr, 0, nullptr, 0};
+        shape_gemm(g, 0);
         const int items = g.m_tiles * ((T + g.n_max - 1) / g.n_max);
         TRY(launch_gemm(g, std::min(items, p->num_sms), s));
     }
@@ -712,13 +771,14 @@ moe_status moe_mx_gemm(const uint8_t* a_codes, const uint8_t* a_scales, int32_t 
     if (err == cudaSuccess) err = launch_sf_atoms(a_scales, M, K / 32, atoms, s);
     if (err == cudaSuccess) err = launch_sf_planes(b_scales, N, K / 32, planes, Np, s);
     if (err == cudaSuccess) {
-        const int nmax = pick_n_max(N);
+        const int nmax = pick_n_max(N, item_cap(N));
         GemmParams g = gemm_base(tA, tB, atoms, planes, Np, K, nmax, M, static_cast<int>(Np), st);
         g.dense = 1;
         g.m_tiles = M / kBlockM;
         g.n_tokens = N;
         g.epi_split = 1 << 30;
         g.epi[0] = EpiParams{EPI_F32, 0, 0, 0, out, M, nullptr, 0, nullptr, 0};
+        shape_gemm(g, 0);
         const int items = g.m_tiles * ((N + nmax - 1) / nmax);
         err = launch_gemm(g, std::min(items, sms), s);
     }
@@ -791,13 +851,14 @@ extern "C" moe_status moe_mx_gemm_noalloc(const uint8_t* a_codes, const uint8_t*
     if (err == cudaSuccess) err = launch_sf_atoms(a_scales, M, K / 32, atoms, s);
     if (err == cudaSuccess) err = launch_sf_planes(b_scales, N, K / 32, planes, Np, s);
     if (err == cudaSuccess) {
-        const int nmax = pick_n_max(N);
+        const int nmax = pick_n_max(N, item_cap(N));
         GemmParams g = gemm_base(tA, tB, atoms, planes, Np, K, nmax, M, static_cast<int>(Np), st);
         g.dense = 1;
         g.m_tiles = M / kBlockM;
         g.n_tokens = N;
         g.epi_split = 1 << 30;
         g.epi[0] = EpiParams{EPI_F32, 0, 0, 0, out, M, nullptr, 0, nullptr, 0};
+        shape_gemm(g, 0);
         const int items = g.m_tiles * ((N + nmax - 1) / nmax);
         err = launch_gemm(g, std::min(items, sms), s);
     }

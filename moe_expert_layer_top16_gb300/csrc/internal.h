@@ -16,8 +16,9 @@ enum : int { DEV_OK = 0, DEV_TIMEOUT_PRODUCER = 1, DEV_TIMEOUT_MMA = 2, DEV_TIME
 // (MMA N, the B operand, MXFP8) x 128 along K per pipeline stage.
 constexpr int kBlockM = 128;
 constexpr int kBlockK = 128;
-constexpr int kNMax = 240;        // 2 accumulators of kNMax fp32 columns + scale columns fit 512 TMEM columns
-constexpr int kGemmThreads = 192; // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kNMax = 240;        // tokens per work item at most (TMEM: accumulators + scale columns <= 512)
+constexpr int kMaxGroups = 4;     // producer / MMA warp pairs per CTA
+constexpr int kGemmMaxThreads = (2 * kMaxGroups + 4) * 32;
 constexpr int kSmemLimit = 227 * 1024;
 
 enum EpiMode : int {
@@ -54,7 +55,9 @@ struct GemmParams {
     int64_t sfb_pitch;
     int KT;                 // 128-wide K tiles
     int n_max;              // tokens per work item (multiple of 16, <= kNMax)
-    int stages;
+    int groups;             // producer / MMA warp pairs; each takes a contiguous 1/groups of every item's K tiles
+    int acc_bufs;           // TMEM accumulator buffers per group (1 or 2)
+    int stages;             // shared-memory stages per group
     int stage_bytes;
     int a_tx_bytes;         // bytes a 128x128 MXFP4 TMA box delivers to the mbarrier
     int dense;              // 1: items = m_tiles x ceil(n_tokens / n_max); 0: item list
@@ -62,8 +65,15 @@ struct GemmParams {
     int n_tokens;
     int a_rows;             // rows of A (bounds check of list items)
     int b_rows;             // rows of B / scale planes (bounds check)
-    const int4* items;      // {a_row0, b_row0, n, mt}
-    const int* n_items;
+    // grouped items (dense == 0): for expert e, ceil(counts[e] / n_max) token
+    // tiles x mt_per_e weight tiles, numbered from ioff[e] (ioff[E] = total);
+    // token tile j starts at permuted row seg[e] + j * n_max.
+    const int* ioff;        // [E+1]
+    const int* seg;         // [E+1]
+    const int* counts;      // [E]
+    int E;
+    int mt_per_e;
+    int rows_per_e;
     int epi_split;          // dense: m-tiles >= epi_split use epi[1]
     int kind;               // GemmKind
     int kseg_tiles;         // K tiles per K segment (K-concatenation through map coordinates)
@@ -74,8 +84,9 @@ struct GemmParams {
 };
 
 int gemm_stage_bytes(int n_max);
-int gemm_stages(int n_max);
-size_t gemm_smem_bytes(int n_max, int stages);
+int gemm_stages(int n_max, int groups, int E);          // E > 0: grouped items (per-expert tables in smem)
+size_t gemm_smem_bytes(int n_max, int groups, int stages, int E);
+bool gemm_config_ok(int n_max, int groups, int acc_bufs);
 cudaError_t gemm_setup();   // raise the dynamic shared memory limit once
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s);
 
@@ -88,18 +99,35 @@ cudaError_t launch_quant_x(const __nv_bfloat16* x, int T, int D, uint8_t* xq, ui
 int router_partials(int T, int L);
 cudaError_t launch_router(const float* z, const float* R, float* logits, float* part, int T, int E, int L,
                           cudaStream_t s);
-// top-k + gates; with nparts > 1 the logits are first summed from `part`
-// (and written to `logits`).
-cudaError_t launch_topk(float* logits, const float* part, int nparts, const float* bias, int T, int E, int k,
-                        int softmax, int32_t* idx, float* w, uint32_t* sel, int W, cudaStream_t s);
+// top-k + gates (kernels.cu): with nparts > 1 the logits are first summed
+// from `part` (and written to `logits`); with refine, the logits are
+// approximate within delta and the candidates' exact logits are recomputed
+// from z ([T][2L], hi | lo) and R ([E][L]).
+struct TopkArgs {
+    float* logits;
+    const float* part;
+    int nparts;
+    const float* bias;
+    int T, E, k, softmax;
+    int refine;
+    float delta;
+    const float* z;
+    const float* R;
+    int L;
+    int32_t* idx;
+    float* w;
+    uint32_t* sel;
+    int W;
+};
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
 cudaError_t launch_expert_scan(const uint32_t* sel, int E, int W, int32_t* wpre, int32_t* counts, cudaStream_t s);
 struct WorkListArgs {
     const int32_t* counts;
     int E;
     int32_t* offsets;    // [E+1] exclusive scan of counts
     int32_t* seg;        // [E+1] exclusive scan of counts rounded up to 16 (row starts in permuted buffers)
-    int4* items1; int* n_items1; int n_max1; int mt1; int a_rows_per_e1;
-    int4* items2; int* n_items2; int n_max2; int mt2; int a_rows_per_e2;
+    int32_t* ioff1; int n_max1; int mt1;   // [E+1] item offsets of the gate/up GEMM
+    int32_t* ioff2; int n_max2; int mt2;   // [E+1] item offsets of the down GEMM
 };
 cudaError_t launch_worklist(const WorkListArgs& a, cudaStream_t s);
 struct ScatterArgs {

@@ -116,14 +116,41 @@ __global__ void __launch_bounds__(256) router_small_kernel(const float* __restri
     float* logits = part + static_cast<int64_t>(blockIdx.y) * T * E;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int k0 = kbeg; k0 < kbeg + klen; k0 += RS_K) {
-        for (int i = threadIdx.x; i < T * RS_K; i += 256) {
-            const int r = i / RS_K, c = i % RS_K;
-            const float* zr = z + static_cast<int64_t>(r) * 2 * L + k0 + c;
-            zs[r][c] = zr[0] + zr[L];
+        // float4 loads, all issued before any is consumed
+        constexpr int kV = RS_TMAX * RS_K / 4 / 256;        // float4 slots per thread (<= 8)
+        float4 zh[kV], zl[kV];
+#pragma unroll
+        for (int u = 0; u < kV; ++u) {
+            const int i = threadIdx.x + u * 256;             // float4 index
+            const int r = i / (RS_K / 4), c = (i % (RS_K / 4)) * 4;
+            if (r < T) {
+                const float* zr = z + static_cast<int64_t>(r) * 2 * L + k0 + c;
+                zh[u] = *reinterpret_cast<const float4*>(zr);
+                zl[u] = *reinterpret_cast<const float4*>(zr + L);
+            }
         }
-        for (int i = threadIdx.x; i < RS_E * RS_K; i += 256) {
-            const int r = i / RS_K, c = i % RS_K;
-            rs[r][c] = (e0 + r < E) ? R[static_cast<int64_t>(e0 + r) * L + k0 + c] : 0.0f;
+        float4 rvec = make_float4(0.f, 0.f, 0.f, 0.f);
+        {
+            const int r = threadIdx.x / (RS_K / 4), c = (threadIdx.x % (RS_K / 4)) * 4;   // 8 x 16 float4
+            if (r < RS_E && e0 + r < E) rvec = *reinterpret_cast<const float4*>(R + static_cast<int64_t>(e0 + r) * L + k0 + c);
+        }
+#pragma unroll
+        for (int u = 0; u < kV; ++u) {
+            const int i = threadIdx.x + u * 256;
+            const int r = i / (RS_K / 4), c = (i % (RS_K / 4)) * 4;
+            if (r < T) {
+                zs[r][c] = zh[u].x + zl[u].x;
+                zs[r][c + 1] = zh[u].y + zl[u].y;
+                zs[r][c + 2] = zh[u].z + zl[u].z;
+                zs[r][c + 3] = zh[u].w + zl[u].w;
+            }
+        }
+        if (threadIdx.x < RS_E * RS_K / 4) {
+            const int r = threadIdx.x / (RS_K / 4), c = (threadIdx.x % (RS_K / 4)) * 4;
+            rs[r][c] = rvec.x;
+            rs[r][c + 1] = rvec.y;
+            rs[r][c + 2] = rvec.z;
+            rs[r][c + 3] = rvec.w;
         }
         __syncthreads();
 #pragma unroll 8
@@ -152,18 +179,21 @@ __global__ void __launch_bounds__(256) router_small_kernel(const float* __restri
 //  * no bias, or softmax gates: the fp32 logit.  sigmoid is strictly
 //    increasing, so ranking logits ranks sigmoid(l) exactly (ties only where
 //    the logits tie).
-//  * with a bias: sigmoid(l) + b decided in fp64.  An fp32 estimate (error
-//    below kKeyErr) picks R = k + 8 candidates; their fp64 keys are ranked
-//    exactly.  That ranking is final when the best key outside the
-//    candidates, at most (R-th fp32 estimate + kKeyErr), is below the k-th
-//    exact key; otherwise every expert's fp64 key is evaluated.
-// Rounds take the largest remaining key, the lower expert id on a tie.
+//  * with a bias: sigmoid(l) + b, decided in fp64.
+// When the logits are approximate (tensor-core router, |error| <= delta) or
+// keys need fp64, R = k + 8 candidates are picked on the estimates; their
+// exact fp32 logits (recomputed from z and R when the logits were
+// approximate) and keys give the final ranking.  That ranking is final when
+// no expert outside the candidates can beat the k-th one: the R-th estimate
+// plus the estimate's error bound is below the k-th exact key; otherwise every
+// expert's logit and key are evaluated exactly.  Rounds take the largest
+// remaining key, the lower expert id on a tie.
 // Gates: sigmoid(l_j) / sum over the winners (fp32), or softmax over the
 // winners' logits.  Each selection sets bit t of the expert's token bitmap.
 constexpr int kTopkWarps = 4;
 constexpr int kTopkPerLane = 32;     // E <= 1024
 constexpr int kMaxE = 32 * kTopkPerLane;
-constexpr float kKeyErr = 4.0e-6f;
+constexpr float kKeyErr = 4.0e-6f;   // error bound of the fp32 sigmoid(l) + b estimate
 
 struct KeyId {
     float key;
@@ -188,25 +218,69 @@ __device__ __forceinline__ double key64(float l, const float* bias, int e) {
     return 1.0 / (1.0 + exp(-static_cast<double>(l))) + static_cast<double>(bias[e]);
 }
 
-__global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(float* __restrict__ logits, const float* __restrict__ part,
-                                                                int nparts, const float* __restrict__ bias, int T,
-                                                                int E, int k, int softmax,
-                                                                int32_t* __restrict__ idx_out, float* __restrict__ w_out,
-                                                                uint32_t* __restrict__ sel, int W) {
+// Exact fp32 logit of expert `e` for the token whose latent is zt = [hi | lo]
+// (z = hi + lo): lane-strided FMA chains, then a fixed butterfly reduction.
+// Every lane returns the same value.
+__device__ __forceinline__ float exact_logit(const float* __restrict__ zt, const float* __restrict__ R, int e, int L,
+                                             int lane) {
+    const float* r = R + static_cast<int64_t>(e) * L;
+    float acc = 0.0f;
+    for (int i = lane; i < L; i += 32) acc = fmaf(zt[i] + zt[L + i], r[i], acc);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    return acc;
+}
+
+// The same for four experts at once (each chain identical to exact_logit's;
+// z is read once for the four).
+__device__ __forceinline__ void exact_logit4(const float* __restrict__ zt, const float* __restrict__ R,
+                                             const int (&e)[4], int L, int lane, float (&out)[4]) {
+    const float* r0 = R + static_cast<int64_t>(e[0]) * L;
+    const float* r1 = R + static_cast<int64_t>(e[1]) * L;
+    const float* r2 = R + static_cast<int64_t>(e[2]) * L;
+    const float* r3 = R + static_cast<int64_t>(e[3]) * L;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 4
+    for (int i = lane; i < L; i += 32) {
+        const float zv = zt[i] + zt[L + i];
+        a0 = fmaf(zv, r0[i], a0);
+        a1 = fmaf(zv, r1[i], a1);
+        a2 = fmaf(zv, r2[i], a2);
+        a3 = fmaf(zv, r3[i], a3);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        a0 += __shfl_xor_sync(0xffffffffu, a0, o);
+        a1 += __shfl_xor_sync(0xffffffffu, a1, o);
+        a2 += __shfl_xor_sync(0xffffffffu, a2, o);
+        a3 += __shfl_xor_sync(0xffffffffu, a3, o);
+    }
+    out[0] = a0;
+    out[1] = a1;
+    out[2] = a2;
+    out[3] = a3;
+}
+
+__global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(TopkArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * kTopkWarps + warp;
-    if (t >= T) return;
-    float* l = logits + static_cast<int64_t>(t) * E;
-    if (nparts > 1) {
+    if (t >= a.T) return;
+    const int E = a.E, k = a.k;
+    float* l = a.logits + static_cast<int64_t>(t) * E;
+    if (a.nparts > 1) {
         // logits = sum of the router's K-split partials, in split order
         for (int e = lane; e < E; e += 32) {
             float v = 0.0f;
-            for (int q = 0; q < nparts; ++q) v += part[(static_cast<int64_t>(q) * T + t) * E + e];
+            for (int q = 0; q < a.nparts; ++q) v += a.part[(static_cast<int64_t>(q) * a.T + t) * E + e];
             l[e] = v;
         }
         __syncwarp();
     }
-    const bool use_bias = (bias != nullptr) && !softmax;
+    const float* bias = a.bias;
+    const bool use_bias = (bias != nullptr) && !a.softmax;
+    const bool approx = a.refine != 0;
+    const bool need_cand = use_bias || approx;
+    const float* zt = a.z + static_cast<int64_t>(t) * 2 * a.L;
     const int nper = (E + 31) / 32;
     float lv[kTopkPerLane], key[kTopkPerLane];
 #pragma unroll
@@ -219,7 +293,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(float* __restrict
         key[i] = (i < nper && e < E) ? kv : -INFINITY;
     }
     uint32_t taken = 0;                                       // bit i: candidate lane + 32 i selected
-    const int R = use_bias ? min(E, min(32, k + 8)) : k;
+    const int R = need_cand ? min(E, min(32, k + 8)) : k;
     int my_id = 0;                                            // lane j < R holds the j-th pick
     float my_est = 0.0f;
     for (int j = 0; j < R; ++j) {
@@ -242,61 +316,107 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(float* __restrict
         if ((b.id & 31) == lane) taken |= 1u << (b.id >> 5);
     }
     int slot = lane;                                          // final slot of this lane's pick
-    if (use_bias) {
-        // exact fp64 ranking of the R candidates
-        const double k64 = (lane < R) ? key64(l[my_id], bias, my_id) : -INFINITY;
+    float my_l = 0.0f;                                        // exact logit of this lane's pick
+    if (need_cand) {
+        if (approx) {
+            for (int c = 0; c < R; c += 4) {
+                int ids[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) ids[u] = __shfl_sync(0xffffffffu, my_id, min(c + u, R - 1));
+                float v[4];
+                exact_logit4(zt, a.R, ids, a.L, lane, v);
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (lane == c + u) my_l = v[u];
+            }
+        } else if (lane < R) {
+            my_l = l[my_id];
+        }
+        // exact ranking of the R candidates
+        const double kx = (lane < R) ? (use_bias ? key64(my_l, bias, my_id) : static_cast<double>(my_l)) : -INFINITY;
         int rank = 0;
         for (int i = 0; i < R; ++i) {
-            const double oi = __shfl_sync(0xffffffffu, k64, i);
+            const double oi = __shfl_sync(0xffffffffu, kx, i);
             const int id = __shfl_sync(0xffffffffu, my_id, i);
-            if (i != lane && (oi > k64 || (oi == k64 && id < my_id))) ++rank;
+            if (i != lane && (oi > kx || (oi == kx && id < my_id))) ++rank;
         }
         slot = (lane < R) ? rank : 32;
-        // the k-th exact key versus anything outside the candidates
-        double kth = -INFINITY;
+        double kth = -INFINITY;                               // k-th exact key
         for (int i = 0; i < R; ++i) {
             const int r = __shfl_sync(0xffffffffu, slot, i);
-            const double v = __shfl_sync(0xffffffffu, k64, i);
+            const double v = __shfl_sync(0xffffffffu, kx, i);
             if (r == k - 1) kth = v;
         }
         const float last_est = __shfl_sync(0xffffffffu, my_est, R - 1);
-        const bool safe = (R == E) || (static_cast<double>(last_est) + static_cast<double>(kKeyErr) < kth);
+        const double err = approx ? (use_bias ? 0.25 * a.delta + kKeyErr : a.delta) : kKeyErr;
+        const bool safe = (R == E) || (static_cast<double>(last_est) + err < kth);
+        if (approx && safe) {
+            if (lane < R) l[my_id] = my_l;                    // export the exact candidate logits
+        }
         if (!safe) {
-            // full fp64 ranking (rare): k rounds over every expert's exact key
+            // rare: exact logits and keys of every expert, k rounds over all of them
+            if (approx) {
+#pragma unroll
+                for (int i = 0; i < kTopkPerLane; ++i) {
+                    if (i < nper) {
+                        for (int c = 0; c < 32; ++c) {
+                            const int e = c + 32 * i;
+                            if (e >= E) break;
+                            const float v = exact_logit(zt, a.R, e, a.L, lane);
+                            if (c == lane) lv[i] = v;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < kTopkPerLane; ++i) {
+                    const int e = lane + 32 * i;
+                    if (i < nper && e < E) l[e] = lv[i];
+                }
+            }
             taken = 0;
             for (int j = 0; j < k; ++j) {
                 double bk = -INFINITY;
                 int bid = 0x7fffffff;
-                for (int i = 0; i < nper; ++i) {
+                float bl = 0.0f;
+#pragma unroll
+                for (int i = 0; i < kTopkPerLane; ++i) {
                     const int e = lane + 32 * i;
-                    if (e >= E || (taken & (1u << i))) continue;
-                    double kv = key64(lv[i], bias, e);
+                    if (i >= nper || e >= E || (taken & (1u << i))) continue;
+                    double kv = use_bias ? key64(lv[i], bias, e) : static_cast<double>(lv[i]);
                     if (kv != kv) kv = -INFINITY;
                     if (bid == 0x7fffffff || kv > bk || (kv == bk && e < bid)) {
                         bk = kv;
                         bid = e;
+                        bl = lv[i];
                     }
                 }
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) {
                     const double ob = __shfl_xor_sync(0xffffffffu, bk, o);
                     const int oi = __shfl_xor_sync(0xffffffffu, bid, o);
+                    const float ol = __shfl_xor_sync(0xffffffffu, bl, o);
                     if (oi != 0x7fffffff && (bid == 0x7fffffff || ob > bk || (ob == bk && oi < bid))) {
                         bk = ob;
                         bid = oi;
+                        bl = ol;
                     }
                 }
                 if (bid < 0 || bid >= E) bid = 0;
-                if (lane == j) my_id = bid;
+                if (lane == j) {
+                    my_id = bid;
+                    my_l = bl;
+                }
                 if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
             }
             slot = lane;
         }
+    } else {
+        my_l = (lane < R) ? l[my_id] : 0.0f;
     }
-    // gates over the k winners (lanes whose slot < k)
+    // gates over the k winners (lanes whose slot < k), from exact logits
     const bool winner = slot < k;
-    float s = winner ? l[my_id] : 0.0f;
-    if (softmax) {
+    float s = winner ? my_l : 0.0f;
+    if (a.softmax) {
         float lmax = winner ? s : -INFINITY;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
@@ -308,9 +428,9 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(float* __restrict
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     if (winner) {
-        idx_out[static_cast<int64_t>(t) * k + slot] = my_id;
-        w_out[static_cast<int64_t>(t) * k + slot] = s / sum;
-        atomicOr(&sel[static_cast<int64_t>(my_id) * W + (t >> 5)], 1u << (t & 31));
+        a.idx[static_cast<int64_t>(t) * k + slot] = my_id;
+        a.w[static_cast<int64_t>(t) * k + slot] = s / sum;
+        atomicOr(&a.sel[static_cast<int64_t>(my_id) * a.W + (t >> 5)], 1u << (t & 31));
     }
 }
 
@@ -338,18 +458,16 @@ __global__ void expert_scan_kernel(const uint32_t* __restrict__ sel, int E, int 
     if (lane == 0) counts[e] = running;
 }
 
-// Offsets (exact, and padded to 16 rows per expert) and the work lists of the
-// two grouped GEMMs, in one CTA of 1024 threads (E <= 1024: thread e owns
-// expert e).  For every expert with n_e > 0: ceil(n_e / n_max) token tiles x
-// mt weight tiles; item = {weight row, first permuted row, tokens, mt},
-// ordered by expert, token tile, weight tile.
+// Offsets (exact, and padded to 16 rows per expert) and the per-expert item
+// offsets of the two grouped GEMMs, in one CTA of 1024 threads (E <= 1024:
+// thread e owns expert e).  Expert e contributes ceil(n_e / n_max) token tiles
+// x mt weight tiles to a GEMM; the GEMM derives each item from these tables.
 __global__ void __launch_bounds__(1024) worklist_kernel(WorkListArgs a) {
     __shared__ int4 warp_tot[32];
-    __shared__ int off1[1025], off2[1025], seg_s[1025];
     const int E = a.E;
     const int e = threadIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int n = (e < E) ? a.counts[e] : 0;
-    int4 v = make_int4(n, (n + 15) & ~15, ceil_div(n, a.n_max1) * a.mt1, ceil_div(n, a.n_max2) * a.mt2);
+    const int4 v = make_int4(n, (n + 15) & ~15, ceil_div(n, a.n_max1) * a.mt1, ceil_div(n, a.n_max2) * a.mt2);
     int4 inc = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -365,7 +483,8 @@ __global__ void __launch_bounds__(1024) worklist_kernel(WorkListArgs a) {
     if (lane == 31) warp_tot[warp] = inc;
     __syncthreads();
     if (warp == 0) {
-        int4 tv = warp_tot[lane], ti = tv;
+        const int4 tv = warp_tot[lane];
+        int4 ti = tv;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int x = __shfl_up_sync(0xffffffffu, ti.x, o), y = __shfl_up_sync(0xffffffffu, ti.y, o);
@@ -385,39 +504,14 @@ __global__ void __launch_bounds__(1024) worklist_kernel(WorkListArgs a) {
     if (e < E) {
         a.offsets[e] = ex.x;
         a.seg[e] = ex.y;
-        seg_s[e] = ex.y;
-        off1[e] = ex.z;
-        off2[e] = ex.w;
+        a.ioff1[e] = ex.z;
+        a.ioff2[e] = ex.w;
     }
     if (e == E - 1) {
         a.offsets[E] = ex.x + v.x;
         a.seg[E] = ex.y + v.y;
-        off1[E] = ex.z + v.z;
-        off2[E] = ex.w + v.w;
-        *a.n_items1 = ex.z + v.z;
-        *a.n_items2 = ex.w + v.w;
-    }
-    __syncthreads();
-    for (int pass = 0; pass < 2; ++pass) {
-        const int* off = pass ? off2 : off1;
-        int4* items = pass ? a.items2 : a.items1;
-        const int nmax = pass ? a.n_max2 : a.n_max1;
-        const int mt = pass ? a.mt2 : a.mt1;
-        const int rpe = pass ? a.a_rows_per_e2 : a.a_rows_per_e1;
-        const int total = off[E];
-        for (int i = threadIdx.x; i < total; i += blockDim.x) {
-            int lo = 0, hi = E - 1;          // expert with off[x] <= i < off[x + 1]
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (off[mid] <= i) lo = mid;
-                else hi = mid - 1;
-            }
-            const int ex_id = lo;
-            const int local = i - off[ex_id];
-            const int j = local / mt, m = local % mt;
-            const int n_e = a.counts[ex_id];
-            items[i] = make_int4(ex_id * rpe + m * 128, seg_s[ex_id] + j * nmax, min(nmax, n_e - j * nmax), m);
-        }
+        a.ioff1[E] = ex.z + v.z;
+        a.ioff2[E] = ex.w + v.w;
     }
 }
 
@@ -633,11 +727,9 @@ cudaError_t launch_router(const float* z, const float* R, float* logits, float* 
     return cudaGetLastError();
 }
 
-cudaError_t launch_topk(float* logits, const float* part, int nparts, const float* bias, int T, int E, int k,
-                        int softmax, int32_t* idx, float* w, uint32_t* sel, int W, cudaStream_t s) {
-    if (E > kMaxE || k > 32) return cudaErrorInvalidValue;
-    topk_kernel<<<(T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, s>>>(logits, part, nparts, bias, T, E, k,
-                                                                            softmax, idx, w, sel, W);
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
+    if (a.E > kMaxE || a.k > 32) return cudaErrorInvalidValue;
+    topk_kernel<<<(a.T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, s>>>(a);
     return cudaGetLastError();
 }
 
