@@ -249,25 +249,35 @@ int pick_n_max(int T, int cap = kNMax) {
 // items (several groups, two TMEM buffers each), larger ones wide items.
 int item_cap(int T) { return T <= 256 ? 48 : kNMax; }
 
-// Groups / accumulator buffers / stages for a GEMM whose items hold up to
-// g.n_max tokens and span g.KT K tiles.  E > 0 for grouped items.
-void shape_gemm(GemmParams& g, int E) {
-    // narrow items: up to four groups, each with at least 4 K tiles; wide
-    // items: one group with two accumulators (epilogue overlap)
-    const int want = (g.n_max <= 64) ? 4 : 1;
-    for (int G = want; G >= 1; G >>= 1) {
-        if (G > 1 && g.KT < 4 * G) continue;
+// Groups / K-splits / accumulator buffers / stages of a GEMM launch whose
+// items hold up to g.n_max tokens and span g.KT K tiles; about est_items
+// items spread over `grid` CTAs; E > 0 for grouped items.
+// Wide items (prefill) run one group with two accumulators: the tensor pipe
+// is busy for a whole item and the epilogue overlaps the next one.  Narrow
+// items are issue-bound, so four groups run side by side: as four item lanes
+// when each CTA has enough items, else as K-splits of fewer items (each
+// split keeping at least 4 K tiles).
+void shape_gemm(GemmParams& g, int E, int64_t est_items, int grid) {
+    const bool narrow = g.n_max <= 64;
+    const int64_t per_cta = std::max<int64_t>(1, (est_items + grid - 1) / std::max(grid, 1));
+    int ks_max = 1;
+    while (ks_max < 4 && g.KT >= 8 * ks_max) ks_max *= 2;
+    for (int G = narrow ? 4 : 1; G >= 1; G >>= 1) {
+        int KS = per_cta >= 4 ? 1 : (per_cta >= 2 ? 2 : 4);
+        KS = std::min(std::min(KS, ks_max), G);
         for (int NB = 2; NB >= 1; --NB) {
-            if (!gemm_config_ok(g.n_max, G, NB)) continue;
+            if (!gemm_config_ok(g.n_max, G, KS, NB)) continue;
             const int S = gemm_stages(g.n_max, G, E);
             if (gemm_smem_bytes(g.n_max, G, S, E) > static_cast<size_t>(kSmemLimit)) continue;
             g.groups = G;
+            g.ksplit = KS;
             g.acc_bufs = NB;
             g.stages = S;
             return;
         }
     }
     g.groups = 1;
+    g.ksplit = 1;
     g.acc_bufs = 1;
     g.stages = gemm_stages(g.n_max, 1, E);
 }
@@ -499,6 +509,8 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
     const int64_t Tp = p->T_pad, Rp = p->R_pad;
     const int nmax_dense = pick_n_max(T, item_cap(T));
     const int nmax_grp = static_cast<int>(std::min<int64_t>(item_cap(T), rup(T, 16)));
+    // experts expected to receive tokens (all of them once T * k >> E)
+    const int64_t est_experts = std::min<int64_t>(E, static_cast<int64_t>(T) * k);
     cudaError_t err = cudaSuccess;
 #define TRY(x)                          \
     do {                                \
@@ -523,8 +535,8 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
         g.epi_split = L / kBlockM;
         g.epi[0] = EpiParams{EPI_QUANT, 0, 0, L, p->z, 2 * L, p->zq, L, p->zsf, Tp};
         g.epi[1] = EpiParams{EPI_SILU_QUANT, L / kBlockM, L, 0, nullptr, 0, p->act, p->Kcat, p->actsf, Tp};
-        shape_gemm(g, 0);
         const int items = g.m_tiles * ((T + g.n_max - 1) / g.n_max);
+        shape_gemm(g, 0, items, std::min(items, p->num_sms));
         TRY(launch_gemm(g, std::min(items, p->num_sms), s));
     }
     // 3. router logits, 4. top-k + gates + bitmaps
@@ -546,8 +558,8 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
         g.n_tokens = T;
         g.epi_split = 1 << 30;
         g.epi[0] = EpiParams{EPI_F32, 0, 0, 0, p->logits, E, nullptr, 0, nullptr, 0};
-        shape_gemm(g, 0);
         const int items = g.m_tiles * ((T + g.n_max - 1) / g.n_max);
+        shape_gemm(g, 0, items, std::min(items, p->num_sms));
         TRY(launch_gemm(g, std::min(items, p->num_sms), s));
         nparts = 1;
     } else {
@@ -630,7 +642,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
         g.E = E;
         g.mt_per_e = 2 * I / kBlockM;
         g.rows_per_e = 2 * I;
-        shape_gemm(g, E);
+        shape_gemm(g, E, est_experts * g.mt_per_e, p->num_sms);
         g.epi[0] = EpiParams{EPI_SILU_QUANT, 0, 0, 0, nullptr, 0, p->hq, Ip, p->hqsf, Rp};
         TRY(launch_gemm(g, p->num_sms, s));
     }
@@ -646,7 +658,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
         g.E = E;
         g.mt_per_e = L / kBlockM;
         g.rows_per_e = L;
-        shape_gemm(g, E);
+        shape_gemm(g, E, est_experts * g.mt_per_e, p->num_sms);
         g.epi[0] = EpiParams{EPI_F32, 0, 0, 0, p->o, L, nullptr, 0, nullptr, 0};
         TRY(launch_gemm(g, p->num_sms, s));
     }
@@ -663,8 +675,8 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
         g.n_tokens = T;
         g.epi_split = 1 << 30;
         g.epi[0] = EpiParams{EPI_F32, 0, 0, 0, y, D, nullptr, 0, nullptr, 0};
-        shape_gemm(g, 0);
         const int items = g.m_tiles * ((T + g.n_max - 1) / g.n_max);
+        shape_gemm(g, 0, items, std::min(items, p->num_sms));
         TRY(launch_gemm(g, std::min(items, p->num_sms), s));
     }
     mark(MOE_NUM_STAGES);
@@ -778,8 +790,8 @@ moe_status moe_mx_gemm(const uint8_t* a_codes, const uint8_t* a_scales, int32_t 
         g.n_tokens = N;
         g.epi_split = 1 << 30;
         g.epi[0] = EpiParams{EPI_F32, 0, 0, 0, out, M, nullptr, 0, nullptr, 0};
-        shape_gemm(g, 0);
         const int items = g.m_tiles * ((N + nmax - 1) / nmax);
+        shape_gemm(g, 0, items, std::min(items, sms));
         err = launch_gemm(g, std::min(items, sms), s);
     }
     cudaError_t ferr = cudaFreeAsync(scratch, s);
@@ -858,8 +870,8 @@ extern "C" moe_status moe_mx_gemm_noalloc(const uint8_t* a_codes, const uint8_t*
         g.n_tokens = N;
         g.epi_split = 1 << 30;
         g.epi[0] = EpiParams{EPI_F32, 0, 0, 0, out, M, nullptr, 0, nullptr, 0};
-        shape_gemm(g, 0);
         const int items = g.m_tiles * ((N + nmax - 1) / nmax);
+        shape_gemm(g, 0, items, std::min(items, sms));
         err = launch_gemm(g, std::min(items, sms), s);
     }
     return cuda_status(err);

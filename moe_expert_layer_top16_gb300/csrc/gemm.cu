@@ -11,12 +11,14 @@
 // block scales are applied inside the MMA (kind::mxf8f6f4.block_scale),
 // with E8M0 scales per 32 elements along K for both operands.
 //
-// Persistent kernel, one CTA per SM.  A thread that issues tcgen05.mma gets
-// one MMA through per ~250 cycles whatever its N, while MMAs from different
-// threads proceed concurrently; a thread issuing TMA copies is similarly
-// limited.  So a CTA runs G "groups" side by side, each with its own
-// producer warp, MMA warp, shared-memory stage ring and TMEM accumulator(s),
-// and splits every work item's K tiles into G contiguous ranges:
+// Persistent kernel, one CTA per SM, organised as G "groups", each with its
+// own TMA producer warp, MMA warp, shared-memory stage ring and TMEM
+// accumulator(s).  Groups form IP item lanes x KS K-splits: the CTA's items
+// (blockIdx.x, +gridDim.x, ...) are dealt round-robin to the item lanes, and
+// the KS groups of a lane split each item's K tiles into contiguous ranges.
+// Independent issuers matter because one thread's tcgen05 / TMA issue rate,
+// not the tensor pipe, bounds small-N items: several item lanes keep the
+// pipe and HBM busy on short-K GEMMs, K-splits on long-K ones.
 //   warps 0..G-1     TMA producers: per 128-wide K tile, one 128x128 MXFP4
 //                    box of A (unpacked into 16-byte groups in shared memory
 //                    by the 16U4_ALIGN16B tensor type), ceil(N/16) 16-row
@@ -24,14 +26,15 @@
 //   warps G..2G-1    MMA issuers: per K tile, re-arrange B's scales,
 //                    tcgen05.cp both scale tiles into TMEM, 4 MMAs (K = 32
 //                    each), commit the stage back to the producer.
-//   warps 2G..2G+3   epilogue: wait for all G partial accumulators of the
-//                    item, add them (group order, fp32), then fp32 stores,
-//                    MXFP8 quantisation (one warp = 32 consecutive output
-//                    features = one MX block) or SiLU-gating + MXFP8.
-// With two accumulator buffers per group the epilogue of one item overlaps
-// the MMAs of the next.  Work items come from per-expert tables (grouped
-// GEMMs) or a dense m-tile x n-tile grid; CTAs take items blockIdx.x,
-// +gridDim.x, ...
+//   warps 2G..2G+3   epilogue, items in CTA order: wait for the KS partial
+//                    accumulators of the item, add them (group order, fp32),
+//                    then fp32 stores, MXFP8 quantisation (one warp = 32
+//                    consecutive output features = one MX block) or
+//                    SiLU-gating + MXFP8.
+// Both roles that issue asynchronous work run warp-converged and issue from
+// one elected lane.  With two accumulator buffers per group the epilogue of
+// one item overlaps the MMAs of the next.  Work items come from per-expert
+// tables (grouped GEMMs) or a dense m-tile x n-tile grid.
 //
 // Every wait is bounded; on a time-out the kernel records a status code,
 // drains what it issued and frees TMEM before returning.
@@ -50,36 +53,77 @@ struct Item {
     int a_row0, b_row0, n, mt;
 };
 
+// Scalar launch parameters held in registers for the whole kernel (reading
+// them from the parameter space would repeat after every asm statement that
+// clobbers memory).
+struct Hot {
+    int KT, n_max, stage_bytes, a_tx_bytes, kseg_tiles;
+    int dense, m_tiles, n_tokens, a_rows, b_rows, E, mt_per_e, rows_per_e, epi_split;
+    int ax0, ax1, ax2, bx0, bx1, bx2;
+    int64_t sfb_pitch;
+    const uint8_t* sfa;
+    const uint8_t* sfb;
+    int* status;
+};
+
+__device__ __forceinline__ Hot load_hot(const GemmParams& p) {
+    Hot h;
+    h.KT = p.KT;
+    h.n_max = p.n_max;
+    h.stage_bytes = p.stage_bytes;
+    h.a_tx_bytes = p.a_tx_bytes;
+    h.kseg_tiles = p.kseg_tiles;
+    h.dense = p.dense;
+    h.m_tiles = p.m_tiles;
+    h.n_tokens = p.n_tokens;
+    h.a_rows = p.a_rows;
+    h.b_rows = p.b_rows;
+    h.E = p.E;
+    h.mt_per_e = p.mt_per_e;
+    h.rows_per_e = p.rows_per_e;
+    h.epi_split = p.epi_split;
+    h.ax0 = p.a_seg_x[0];
+    h.ax1 = p.a_seg_x[1];
+    h.ax2 = p.a_seg_x[2];
+    h.bx0 = p.b_seg_x[0];
+    h.bx1 = p.b_seg_x[1];
+    h.bx2 = p.b_seg_x[2];
+    h.sfb_pitch = p.sfb_pitch;
+    h.sfa = p.sfa;
+    h.sfb = p.sfb;
+    h.status = p.status;
+    return h;
+}
+
 // Item `it`.  Grouped items come from the per-expert tables staged in shared
 // memory (ioff, seg, counts): binary search for the expert, then token tile j
 // and weight tile m of that expert.
-__device__ __forceinline__ Item get_item(const GemmParams& p, int it, const int* ioff, const int* seg,
-                                         const int* cnt) {
+__device__ __forceinline__ Item get_item(const Hot& h, int it, const int* ioff, const int* seg, const int* cnt) {
     Item w;
-    if (p.dense) {
-        const int mt = it % p.m_tiles;
-        const int nt = it / p.m_tiles;
+    if (h.dense) {
+        const int mt = it % h.m_tiles;
+        const int nt = it / h.m_tiles;
         w.a_row0 = mt * kBlockM;
-        w.b_row0 = nt * p.n_max;
-        w.n = min(p.n_max, p.n_tokens - w.b_row0);
+        w.b_row0 = nt * h.n_max;
+        w.n = min(h.n_max, h.n_tokens - w.b_row0);
         w.mt = mt;
     } else {
-        int lo = 0, hi = p.E - 1;
+        int lo = 0, hi = h.E - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
             if (ioff[mid] <= it) lo = mid;
             else hi = mid - 1;
         }
         const int local = it - ioff[lo];
-        const int j = local / p.mt_per_e, m = local - j * p.mt_per_e;
-        w.a_row0 = lo * p.rows_per_e + m * kBlockM;
-        w.b_row0 = seg[lo] + j * p.n_max;
-        w.n = min(p.n_max, cnt[lo] - j * p.n_max);
+        const int j = local / h.mt_per_e, m = local - j * h.mt_per_e;
+        w.a_row0 = lo * h.rows_per_e + m * kBlockM;
+        w.b_row0 = seg[lo] + j * h.n_max;
+        w.n = min(h.n_max, cnt[lo] - j * h.n_max);
         w.mt = m;
         // reject items that would read or write outside the buffers
-        if (w.n <= 0 || w.n > p.n_max || w.a_row0 < 0 || (w.a_row0 & (kBlockM - 1)) ||
-            w.a_row0 + kBlockM > p.a_rows || w.b_row0 < 0 || (w.b_row0 & 3) ||
-            w.b_row0 + ((w.n + 15) & ~15) > p.b_rows || w.mt < 0) {
+        if (w.n <= 0 || w.n > h.n_max || w.a_row0 < 0 || (w.a_row0 & (kBlockM - 1)) ||
+            w.a_row0 + kBlockM > h.a_rows || w.b_row0 < 0 || (w.b_row0 & 3) ||
+            w.b_row0 + ((w.n + 15) & ~15) > h.b_rows || w.mt < 0) {
             w.n = -1;
         }
     }
@@ -99,7 +143,7 @@ __host__ __device__ __forceinline__ SmemLayout stage_layout(int n_max) {
     return l;
 }
 
-// K tiles [kb, ke) of an item handled by group g of G.
+// K tiles [kb, ke) of an item handled by K-split g of G.
 __device__ __forceinline__ void group_range(int KT, int g, int G, int& kb, int& ke) {
     kb = (KT * g) / G;
     ke = (KT * (g + 1)) / G;
@@ -140,17 +184,32 @@ __device__ __forceinline__ bool mbar_wait_teardown(uint64_t* bar, uint32_t parit
     return true;
 }
 
-template <int KIND>
+// Epilogue code compiled into a kernel instance: each launch carries only the
+// output paths it can take.
+enum EpiSet : int {
+    SET_F32 = 0,        // EPI_F32 only
+    SET_QUANT = 1,      // EPI_F32 / EPI_QUANT
+    SET_SILU = 2,       // EPI_SILU_QUANT only
+    SET_DUAL = 3        // EPI_F32 / EPI_QUANT (epi[0]) and EPI_SILU_QUANT (epi[1])
+};
+
+template <int KIND, int SET>
 __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __grid_constant__ GemmParams p) {
     constexpr bool kMX = (KIND == KIND_MX);
+    constexpr bool kSilu = (SET == SET_SILU || SET == SET_DUAL);
+    constexpr bool kQuant = (SET == SET_QUANT || SET == SET_DUAL);
+    constexpr bool kOnlySilu = (SET == SET_SILU);
     constexpr int kTileElems = kMX ? kBlockK : 32;      // K elements per 128-byte row of a stage
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const Hot h = load_hot(p);
     const int G = p.groups;
+    const int KS = p.ksplit;                // groups per item
+    const int IP = G / KS;                  // item lanes
     const int S = p.stages;                 // per group
     const int NB = p.acc_bufs;              // accumulator buffers per group
-    const SmemLayout L = stage_layout(p.n_max);
-    uint8_t* tail = base + G * S * p.stage_bytes;
+    const SmemLayout L = stage_layout(h.n_max);
+    uint8_t* tail = base + G * S * h.stage_bytes;
     float* xbuf = reinterpret_cast<float*>(tail);
     uint64_t* full = reinterpret_cast<uint64_t*>(tail + kXbufBytes);      // [G][kMaxStagesPerGroup]
     uint64_t* empty = full + kMaxGroups * kMaxStagesPerGroup;              // [G][kMaxStagesPerGroup]
@@ -160,8 +219,8 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tdown + kMaxGroups);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* ioff_s = reinterpret_cast<int*>(tail + kXbufBytes + kBarBytes);
-    int* seg_s = ioff_s + (p.dense ? 0 : p.E + 1);
-    int* cnt_s = seg_s + (p.dense ? 0 : p.E + 1);
+    int* seg_s = ioff_s + (h.dense ? 0 : h.E + 1);
+    int* cnt_s = seg_s + (h.dense ? 0 : h.E + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -187,11 +246,11 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
-    if (!p.dense) {
-        for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
+    if (!h.dense) {
+        for (int i = threadIdx.x; i <= h.E; i += blockDim.x) {
             ioff_s[i] = p.ioff[i];
             seg_s[i] = p.seg[i];
-            cnt_s[i] = (i < p.E) ? p.counts[i] : 0;
+            cnt_s[i] = (i < h.E) ? p.counts[i] : 0;
         }
     }
     tc_fence_before();
@@ -199,99 +258,103 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const int n_items = p.dense ? p.m_tiles * ((p.n_tokens + p.n_max - 1) / p.n_max) : ioff_s[p.E];
-    const uint32_t cols_per_group = static_cast<uint32_t>(NB * p.n_max + 24);
+    const int n_items = h.dense ? h.m_tiles * ((h.n_tokens + h.n_max - 1) / h.n_max) : ioff_s[h.E];
+    const uint32_t cols_per_group = static_cast<uint32_t>(NB * h.n_max + 24);
 
     if (warp < G) {
         // ------------------------------------------------------------ producer of group g
+        // The whole warp runs the loop; one elected lane issues the copies.
         const int g = warp;
-        if (lane == 0) {
-            uint64_t* fullg = full + g * kMaxStagesPerGroup;
-            uint64_t* emptyg = empty + g * kMaxStagesPerGroup;
-            uint8_t* ring = base + g * S * p.stage_bytes;
-            uint32_t stage = 0, phase = 0;
-            uint32_t issued = 0, issued_parity = 0;   // per-stage bits for the teardown drain
-            for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-                const Item w = get_item(p, it, ioff_s, seg_s, cnt_s);
-                if (w.n <= 0) {
-                    if (w.n < 0 && g == 0) atomicCAS(p.status, 0, DEV_BAD_WORK);
-                    continue;
+        const int ip = g / KS;
+        int kb, ke;
+        group_range(h.KT, g % KS, KS, kb, ke);
+        uint64_t* fullg = full + g * kMaxStagesPerGroup;
+        uint64_t* emptyg = empty + g * kMaxStagesPerGroup;
+        uint8_t* ring = base + g * S * h.stage_bytes;
+        uint32_t stage = 0, phase = 0;
+        uint32_t issued = 0, issued_parity = 0;   // per-stage bits for the teardown drain
+        bool ok = true;
+        for (int it = blockIdx.x + ip * gridDim.x; ok && it < n_items && ke > kb; it += IP * gridDim.x) {
+            const Item w = get_item(h, it, ioff_s, seg_s, cnt_s);
+            if (w.n <= 0) {
+                if (w.n < 0 && g == 0 && lane == 0) atomicCAS(h.status, 0, DEV_BAD_WORK);
+                continue;
+            }
+            const int nm = (w.n + 15) & ~15;
+            const uint32_t tx = kMX ? static_cast<uint32_t>(h.a_tx_bytes + (nm / 16) * 2048 + 512 + nm * 4)
+                                    : static_cast<uint32_t>(kBlockM * 128 + (nm / 16) * 2048);
+            const uint8_t* sfa_tile = kMX ? h.sfa + static_cast<size_t>(w.a_row0 / kBlockM) * h.KT * 512 : nullptr;
+            for (int kt = kb; kt < ke; ++kt) {
+                ok = mbar_wait(&emptyg[stage], phase ^ 1, abort_flag, h.status, DEV_TIMEOUT_PRODUCER);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
                 }
-                int kb, ke;
-                group_range(p.KT, g, G, kb, ke);
-                const int nm = (w.n + 15) & ~15;
-                const uint32_t tx = kMX ? static_cast<uint32_t>(p.a_tx_bytes + (nm / 16) * 2048 + 512 + nm * 4)
-                                        : static_cast<uint32_t>(kBlockM * 128 + (nm / 16) * 2048);
-                const uint8_t* sfa_tile = kMX ? p.sfa + static_cast<size_t>(w.a_row0 / kBlockM) * p.KT * 512 : nullptr;
-                bool ok = true;
-                for (int kt = kb; kt < ke; ++kt) {
-                    if (!mbar_wait(&emptyg[stage], phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_PRODUCER)) {
-                        ok = false;
-                        break;
-                    }
-                    const int seg = kt / p.kseg_tiles;
-                    const int kin = (kt - seg * p.kseg_tiles) * kTileElems;
-                    uint8_t* sb = ring + stage * p.stage_bytes;
+                const int sg = kt / h.kseg_tiles;
+                const int kin = (kt - sg * h.kseg_tiles) * kTileElems;
+                const int ax = (sg == 0 ? h.ax0 : (sg == 1 ? h.ax1 : h.ax2)) + kin;
+                const int bx = (sg == 0 ? h.bx0 : (sg == 1 ? h.bx1 : h.bx2)) + kin;
+                uint8_t* sb = ring + stage * h.stage_bytes;
+                if (elect_one()) {
                     mbar_arrive_expect_tx(&fullg[stage], tx);
-                    tma_load_2d(sb, &p.tmA, &fullg[stage], p.a_seg_x[seg] + kin, w.a_row0);
+                    tma_load_2d(sb, &p.tmA, &fullg[stage], ax, w.a_row0);
                     for (int c = 0; c < nm / 16; ++c)
-                        tma_load_2d(sb + L.offB + c * 2048, &p.tmB, &fullg[stage], p.b_seg_x[seg] + kin,
-                                    w.b_row0 + c * 16);
+                        tma_load_2d(sb + L.offB + c * 2048, &p.tmB, &fullg[stage], bx, w.b_row0 + c * 16);
                     if constexpr (kMX) {
                         bulk_load(sb + L.offSFA, sfa_tile + static_cast<size_t>(kt) * 512, 512, &fullg[stage]);
-                        bulk_load(sb + L.offSFBraw,
-                                  p.sfb + (static_cast<size_t>(kt) * p.sfb_pitch + w.b_row0) * 4,
+                        bulk_load(sb + L.offSFBraw, h.sfb + (static_cast<size_t>(kt) * h.sfb_pitch + w.b_row0) * 4,
                                   static_cast<uint32_t>(nm * 4), &fullg[stage]);
                     }
-                    issued |= 1u << stage;
-                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-                    if (++stage == static_cast<uint32_t>(S)) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
                 }
-                if (!ok) break;
-            }
-            if (*abort_flag) {
-                // drain: every issued stage's copies must land before exit
-                for (int s = 0; s < S; ++s)
-                    if (issued & (1u << s)) mbar_wait_teardown(&fullg[s], (issued_parity >> s) & 1u, p.status);
+                __syncwarp();
+                issued |= 1u << stage;
+                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == static_cast<uint32_t>(S)) {
+                    stage = 0;
+                    phase ^= 1;
+                }
             }
         }
+        if (*abort_flag && lane == 0) {
+            // drain: every issued stage's copies must land before exit
+            for (int s = 0; s < S; ++s)
+                if (issued & (1u << s)) mbar_wait_teardown(&fullg[s], (issued_parity >> s) & 1u, h.status);
+        }
+        __syncwarp();
     } else if (warp < 2 * G) {
         // ------------------------------------------------------------ MMA issuer of group g
         const int g = warp - G;
+        const int ip = g / KS;
+        int kb, ke;
+        group_range(h.KT, g % KS, KS, kb, ke);
         uint64_t* fullg = full + g * kMaxStagesPerGroup;
         uint64_t* emptyg = empty + g * kMaxStagesPerGroup;
-        uint8_t* ring = base + g * S * p.stage_bytes;
+        uint8_t* ring = base + g * S * h.stage_bytes;
         const uint32_t gcol = tmem + static_cast<uint32_t>(g) * cols_per_group;
-        const uint32_t sf_base = gcol + static_cast<uint32_t>(NB * p.n_max);
+        const uint32_t sf_base = gcol + static_cast<uint32_t>(NB * h.n_max);
         uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
         bool any = false;
-        for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-            const Item w = get_item(p, it, ioff_s, seg_s, cnt_s);
+        for (int it = blockIdx.x + ip * gridDim.x; it < n_items && ke > kb; it += IP * gridDim.x) {
+            const Item w = get_item(h, it, ioff_s, seg_s, cnt_s);
             if (w.n <= 0) continue;
-            int kb, ke;
-            group_range(p.KT, g, G, kb, ke);
-            if (ke <= kb) continue;
             const int nm = (w.n + 15) & ~15;
             const int natoms = (nm + 127) / 128;
-            bool ok = mbar_wait(&tempty[g * 2 + acc], acc_phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_MMA);
+            bool ok = mbar_wait(&tempty[g * 2 + acc], acc_phase ^ 1, abort_flag, h.status, DEV_TIMEOUT_MMA);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
-            const uint32_t d_tmem = gcol + acc * static_cast<uint32_t>(p.n_max);
+            const uint32_t d_tmem = gcol + acc * static_cast<uint32_t>(h.n_max);
             for (int kt = kb; kt < ke; ++kt) {
-                ok = mbar_wait(&fullg[stage], phase, abort_flag, p.status, DEV_TIMEOUT_MMA);
+                ok = mbar_wait(&fullg[stage], phase, abort_flag, h.status, DEV_TIMEOUT_MMA);
                 if (!__all_sync(0xffffffffu, ok)) goto mma_done;
                 tc_fence_after();
                 {
-                    uint8_t* sb = ring + stage * p.stage_bytes;
+                    uint8_t* sb = ring + stage * h.stage_bytes;
                     const uint32_t accum_first = (kt == kb) ? 0u : 1u;
+                    const uint64_t adesc = sdesc_sw128(smem_u32(sb));
+                    const uint64_t bdesc = sdesc_sw128(smem_u32(sb + L.offB));
                     if constexpr (!kMX) {
-                        if (lane == 0) {
-                            const uint64_t adesc = sdesc_sw128(smem_u32(sb));
-                            const uint64_t bdesc = sdesc_sw128(smem_u32(sb + L.offB));
-                            const uint32_t idesc = idesc_tf32(kBlockM, nm);
+                        const uint32_t idesc = idesc_tf32(kBlockM, nm);
+                        if (elect_one()) {
 #pragma unroll
                             for (int j = 0; j < 4; ++j)
                                 mma_tf32(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, (accum_first | j) != 0 ? 1u : 0u);
@@ -313,17 +376,19 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                         }
                         fence_proxy_async_smem();
                         __syncwarp();
-                        if (lane == 0) {
-                            const uint32_t sfa_col = sf_base + static_cast<uint32_t>(kt & 1) * 12u;
-                            const uint32_t sfb_col = sfa_col + 4u;
+                        const uint32_t sfa_col = sf_base + static_cast<uint32_t>(kt & 1) * 12u;
+                        const uint32_t sfb_col = sfa_col + 4u;
+                        const uint32_t idesc0 = idesc_mxf8f6f4(kBlockM, nm, 5, 0, 0, 0);
+                        if (elect_one()) {
                             tc_cp_32x128b_x4(sfa_col, sdesc_rows16(smem_u32(sb + L.offSFA)));
                             for (int a = 0; a < natoms; ++a)
                                 tc_cp_32x128b_x4(sfb_col + 4u * a, sdesc_rows16(smem_u32(sb + L.offSFBatom + a * 512)));
-                            const uint64_t adesc = sdesc_sw128(smem_u32(sb));
-                            const uint64_t bdesc = sdesc_sw128(smem_u32(sb + L.offB));
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
-                                const uint32_t idesc = idesc_mxf8f6f4(kBlockM, nm, 5, 0, j, j);
+                                // scale-factor ids (byte j of each 32-bit scale column) sit
+                                // at bits 4..5 (B) and 29..30 (A) of the instruction descriptor
+                                const uint32_t idesc = idesc0 | (static_cast<uint32_t>(j) << 4) |
+                                                       (static_cast<uint32_t>(j) << 29);
                                 mma_mxf8f6f4(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sfa_col, sfb_col,
                                              (accum_first | j) != 0 ? 1u : 0u);
                             }
@@ -338,7 +403,7 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                     phase ^= 1;
                 }
             }
-            if (lane == 0) tc_commit(&tfull[g * 2 + acc]);
+            if (elect_one()) tc_commit(&tfull[g * 2 + acc]);
             __syncwarp();
             if (++acc == static_cast<uint32_t>(NB)) {
                 acc = 0;
@@ -347,50 +412,71 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
         }
     mma_done:
         // every tcgen05 operation issued above must finish before TMEM is freed
-        if (lane == 0 && any) {
-            tc_commit(&tdown[g]);
-            mbar_wait_teardown(&tdown[g], 0, p.status);
+        if (any) {
+            if (elect_one()) {
+                tc_commit(&tdown[g]);
+                mbar_wait_teardown(&tdown[g], 0, h.status);
+            }
+            __syncwarp();
         }
-        __syncwarp();
     } else if (warp < 2 * G + 4) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;                 // TMEM lane quarter this warp may access
-        uint32_t acc = 0, acc_phase = 0;
+        const uint32_t t_lane = static_cast<uint32_t>(32 * q) << 16;
+        // both output descriptions in registers; an item selects scalars
+        const EpiParams E0 = p.epi[0];
+        const EpiParams E1 = p.epi[1];
+        uint32_t cnts = 0;                      // items consumed per item lane, mod 4 (8 bits each)
         int chunk_parity = 0;
-        for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-            const Item w = get_item(p, it, ioff_s, seg_s, cnt_s);
+        int c = 0;                              // CTA-local item number
+        for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++c) {
+            const Item w = get_item(h, it, ioff_s, seg_s, cnt_s);
             if (w.n <= 0) continue;
+            const int ip = c % IP;
+            const uint32_t cnt = (cnts >> (8 * ip)) & 0xFFu;
+            const uint32_t acc = cnt % static_cast<uint32_t>(NB);
+            const uint32_t acc_phase = (cnt / static_cast<uint32_t>(NB)) & 1u;
+            const int g0 = ip * KS;
             const int nm = (w.n + 15) & ~15;
             bool ok = true;
-            for (int g = 0; g < G; ++g) {
+            for (int ks = 0; ks < KS; ++ks) {
                 int kb, ke;
-                group_range(p.KT, g, G, kb, ke);
+                group_range(h.KT, ks, KS, kb, ke);
                 if (ke > kb && ok)
-                    ok = mbar_wait(&tfull[g * 2 + acc], acc_phase, abort_flag, p.status, DEV_TIMEOUT_EPILOGUE);
+                    ok = mbar_wait(&tfull[(g0 + ks) * 2 + acc], acc_phase, abort_flag, h.status, DEV_TIMEOUT_EPILOGUE);
             }
             if (!epi_all(ok && !*abort_flag)) break;
             tc_fence_after();
-            const int region = (p.dense && w.mt >= p.epi_split) ? 1 : 0;
-            const EpiParams& E = p.epi[region];
-            const uint32_t t_lane = static_cast<uint32_t>(32 * q) << 16;
+            const bool second = h.dense && w.mt >= h.epi_split;
+            EpiParams E;
+            E.mode = second ? E1.mode : E0.mode;
+            E.m_tile0 = second ? E1.m_tile0 : E0.m_tile0;
+            E.col0 = second ? E1.col0 : E0.col0;
+            E.f32_split = second ? E1.f32_split : E0.f32_split;
+            E.out_f32 = second ? E1.out_f32 : E0.out_f32;
+            E.ld_f32 = second ? E1.ld_f32 : E0.ld_f32;
+            E.out_q = second ? E1.out_q : E0.out_q;
+            E.ld_q = second ? E1.ld_q : E0.ld_q;
+            E.out_sf = second ? E1.out_sf : E0.out_sf;
+            E.sf_pitch = second ? E1.sf_pitch : E0.sf_pitch;
             const int rel_mt = w.mt - E.m_tile0;
             for (int n0 = 0; n0 < nm; n0 += 16) {
-                // sum of the groups' partial accumulators, in group order
+                // sum of the K-split partial accumulators, in group order
                 float v[16];
                 bool first = true;
-                for (int g = 0; g < G; ++g) {
+                for (int ks = 0; ks < KS; ++ks) {
                     int kb, ke;
-                    group_range(p.KT, g, G, kb, ke);
+                    group_range(h.KT, ks, KS, kb, ke);
                     if (ke <= kb) continue;
                     float u[16];
-                    tmem_ld16(tmem + t_lane + static_cast<uint32_t>(g) * cols_per_group +
-                                  acc * static_cast<uint32_t>(p.n_max) + static_cast<uint32_t>(n0),
+                    tmem_ld16(tmem + t_lane + static_cast<uint32_t>(g0 + ks) * cols_per_group +
+                                  acc * static_cast<uint32_t>(h.n_max) + static_cast<uint32_t>(n0),
                               u);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) v[i] = first ? u[i] : v[i] + u[i];
                     first = false;
                 }
-                if (E.mode == EPI_SILU_QUANT) {
+                if (kOnlySilu || (kSilu && E.mode == EPI_SILU_QUANT)) {
                     float* xb = xbuf + chunk_parity * (2 * 32 * 16);
                     chunk_parity ^= 1;
                     if (q >= 2) {
@@ -404,9 +490,9 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                         for (int i = 0; i < 16; ++i) {
                             const int n = n0 + i;
                             if (n < w.n) {
-                                const float h = silu_f(v[i]) * xb[q * 512 + i * 32 + lane];
+                                const float hv = silu_f(v[i]) * xb[q * 512 + i * 32 + lane];
                                 uint8_t sc;
-                                const uint8_t code = warp_mx8_quant(h, &sc);
+                                const uint8_t code = warp_mx8_quant(hv, &sc);
                                 const int64_t row = w.b_row0 + n;
                                 E.out_q[row * E.ld_q + col] = code;
                                 if (lane == 0) E.out_sf[sf_byte_offset(row, col, E.sf_pitch)] = sc;
@@ -429,7 +515,7 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                                     E.out_f32[row * E.ld_f32 + col] = v[i];
                                 }
                             }
-                            if (E.mode == EPI_QUANT) {
+                            if (kQuant && E.mode == EPI_QUANT) {
                                 uint8_t sc;
                                 const uint8_t code = warp_mx8_quant(v[i], &sc);
                                 E.out_q[row * E.ld_q + col] = code;
@@ -442,16 +528,14 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                for (int g = 0; g < G; ++g) {
+                for (int ks = 0; ks < KS; ++ks) {
                     int kb, ke;
-                    group_range(p.KT, g, G, kb, ke);
-                    if (ke > kb) mbar_arrive(&tempty[g * 2 + acc]);
+                    group_range(h.KT, ks, KS, kb, ke);
+                    if (ke > kb) mbar_arrive(&tempty[(g0 + ks) * 2 + acc]);
                 }
             }
-            if (++acc == static_cast<uint32_t>(NB)) {
-                acc = 0;
-                acc_phase ^= 1;
-            }
+            const uint32_t nxt = (cnt + 1u) & 3u;
+            cnts = (cnts & ~(0xFFu << (8 * ip))) | (nxt << (8 * ip));
         }
     }
 
@@ -482,31 +566,65 @@ int gemm_stages(int n_max, int groups, int E) {
     return s;
 }
 
-bool gemm_config_ok(int n_max, int groups, int acc_bufs) {
+bool gemm_config_ok(int n_max, int groups, int ksplit, int acc_bufs) {
     if (groups < 1 || groups > kMaxGroups || acc_bufs < 1 || acc_bufs > 2) return false;
+    if (ksplit < 1 || groups % ksplit) return false;
     if (n_max < 16 || n_max > kNMax || (n_max & 15)) return false;
     return groups * (acc_bufs * n_max + 24) <= kTmemCols;
 }
 
+namespace {
+
+template <int KIND, int SET>
+cudaError_t raise_smem() {
+    return cudaFuncSetAttribute(mx_gemm_kernel<KIND, SET>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+}
+
+// The kernel instance whose epilogue covers the launch's output modes.
+int epi_set(const GemmParams& p) {
+    const int m0 = p.epi[0].mode;
+    const bool two = p.dense && p.epi_split < p.m_tiles;
+    const int m1 = two ? p.epi[1].mode : m0;
+    const bool s0 = m0 == EPI_SILU_QUANT, s1 = m1 == EPI_SILU_QUANT;
+    if (!s0 && !s1) return (m0 == EPI_QUANT || m1 == EPI_QUANT) ? SET_QUANT : SET_F32;
+    if (s0 && s1) return SET_SILU;
+    if (s1) return SET_DUAL;
+    return -1;
+}
+
+}  // namespace
+
 cudaError_t gemm_setup() {
-    cudaError_t err =
-        cudaFuncSetAttribute(mx_gemm_kernel<KIND_MX>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-    if (err != cudaSuccess) return err;
-    return cudaFuncSetAttribute(mx_gemm_kernel<KIND_TF32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    cudaError_t err = raise_smem<KIND_MX, SET_F32>();
+    if (err == cudaSuccess) err = raise_smem<KIND_MX, SET_QUANT>();
+    if (err == cudaSuccess) err = raise_smem<KIND_MX, SET_SILU>();
+    if (err == cudaSuccess) err = raise_smem<KIND_MX, SET_DUAL>();
+    if (err == cudaSuccess) err = raise_smem<KIND_TF32, SET_F32>();
+    return err;
 }
 
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s) {
-    if (!gemm_config_ok(p.n_max, p.groups, p.acc_bufs)) return cudaErrorInvalidValue;
+    if (!gemm_config_ok(p.n_max, p.groups, p.ksplit, p.acc_bufs)) return cudaErrorInvalidValue;
     if (p.stages < 2 || p.stages > kMaxStagesPerGroup) return cudaErrorInvalidValue;
     const size_t smem = gemm_smem_bytes(p.n_max, p.groups, p.stages, p.dense ? 0 : p.E);
     if (smem > static_cast<size_t>(kSmemLimit)) return cudaErrorInvalidValue;
     if (p.kseg_tiles <= 0 || p.KT > 3 * p.kseg_tiles) return cudaErrorInvalidValue;
     if (!p.dense && (p.E <= 0 || p.E > 1024)) return cudaErrorInvalidValue;
+    const int set = epi_set(p);
+    if (set < 0) return cudaErrorInvalidValue;
     const int threads = (2 * p.groups + 4) * 32;
-    if (p.kind == KIND_TF32)
-        mx_gemm_kernel<KIND_TF32><<<grid, threads, smem, s>>>(p);
-    else
-        mx_gemm_kernel<KIND_MX><<<grid, threads, smem, s>>>(p);
+    if (p.kind == KIND_TF32) {
+        if (set != SET_F32) return cudaErrorInvalidValue;
+        mx_gemm_kernel<KIND_TF32, SET_F32><<<grid, threads, smem, s>>>(p);
+    } else if (set == SET_F32) {
+        mx_gemm_kernel<KIND_MX, SET_F32><<<grid, threads, smem, s>>>(p);
+    } else if (set == SET_QUANT) {
+        mx_gemm_kernel<KIND_MX, SET_QUANT><<<grid, threads, smem, s>>>(p);
+    } else if (set == SET_SILU) {
+        mx_gemm_kernel<KIND_MX, SET_SILU><<<grid, threads, smem, s>>>(p);
+    } else {
+        mx_gemm_kernel<KIND_MX, SET_DUAL><<<grid, threads, smem, s>>>(p);
+    }
     return cudaGetLastError();
 }
 

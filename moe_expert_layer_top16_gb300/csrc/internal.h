@@ -55,7 +55,8 @@ struct GemmParams {
     int64_t sfb_pitch;
     int KT;                 // 128-wide K tiles
     int n_max;              // tokens per work item (multiple of 16, <= kNMax)
-    int groups;             // producer / MMA warp pairs; each takes a contiguous 1/groups of every item's K tiles
+    int groups;             // producer / MMA warp pairs = item lanes x ksplit
+    int ksplit;             // groups per item; each takes a contiguous 1/ksplit of the item's K tiles
     int acc_bufs;           // TMEM accumulator buffers per group (1 or 2)
     int stages;             // shared-memory stages per group
     int stage_bytes;
@@ -86,7 +87,7 @@ struct GemmParams {
 int gemm_stage_bytes(int n_max);
 int gemm_stages(int n_max, int groups, int E);          // E > 0: grouped items (per-expert tables in smem)
 size_t gemm_smem_bytes(int n_max, int groups, int stages, int E);
-bool gemm_config_ok(int n_max, int groups, int acc_bufs);
+bool gemm_config_ok(int n_max, int groups, int ksplit, int acc_bufs);
 cudaError_t gemm_setup();   // raise the dynamic shared memory limit once
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s);
 

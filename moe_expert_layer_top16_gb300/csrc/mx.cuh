@@ -33,10 +33,10 @@ __device__ __forceinline__ uint8_t f32_to_e4m3(float v) {
     return static_cast<uint8_t>(r & 0xFFu);
 }
 
+// Maximum over the warp of a non-negative float (its bit pattern orders like
+// an unsigned integer), in one warp reduction.
 __device__ __forceinline__ float warp_max32(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
+    return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(v)));
 }
 
 // Quantise one value per lane of a full warp (the 32 lanes form one MX

@@ -110,6 +110,19 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
+// True in exactly one lane of a converged warp (the same lane every time the
+// full warp executes it).  Issuing tcgen05 and TMA instructions from a
+// converged warp through this predicate is markedly cheaper per instruction
+// than issuing them from a lane-0 branch.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, e;\n\t}"
+        : "=r"(r));
+    return r != 0;
+}
 // Arrive on `bar` once every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
