@@ -256,7 +256,8 @@ int item_cap(int T) { return T <= 256 ? 48 : kNMax; }
 // is busy for a whole item and the epilogue overlaps the next one.  Narrow
 // items are issue-bound, so four groups run side by side: as four item lanes
 // when each CTA has enough items, else as K-splits of fewer items (each
-// split keeping at least 4 K tiles).
+// split keeping at least 4 K tiles); a CTA then takes a contiguous range of
+// items, so that successive items mostly belong to one expert.
 void shape_gemm(GemmParams& g, int E, int64_t est_items, int grid) {
     const bool narrow = g.n_max <= 64;
     const int64_t per_cta = std::max<int64_t>(1, (est_items + grid - 1) / std::max(grid, 1));
@@ -273,11 +274,13 @@ void shape_gemm(GemmParams& g, int E, int64_t est_items, int grid) {
             g.ksplit = KS;
             g.acc_bufs = NB;
             g.stages = S;
+            g.contiguous = narrow ? 1 : 0;
             return;
         }
     }
     g.groups = 1;
     g.ksplit = 1;
+    g.contiguous = 0;
     g.acc_bufs = 1;
     g.stages = gemm_stages(g.n_max, 1, E);
 }

@@ -68,37 +68,53 @@ struct Hot {
 
 __device__ __forceinline__ Hot load_hot(const GemmParams& p) {
     Hot h;
-    h.KT = p.KT;
-    h.n_max = p.n_max;
-    h.stage_bytes = p.stage_bytes;
-    h.a_tx_bytes = p.a_tx_bytes;
-    h.kseg_tiles = p.kseg_tiles;
-    h.dense = p.dense;
-    h.m_tiles = p.m_tiles;
-    h.n_tokens = p.n_tokens;
-    h.a_rows = p.a_rows;
-    h.b_rows = p.b_rows;
-    h.E = p.E;
-    h.mt_per_e = p.mt_per_e;
-    h.rows_per_e = p.rows_per_e;
-    h.epi_split = p.epi_split;
-    h.ax0 = p.a_seg_x[0];
-    h.ax1 = p.a_seg_x[1];
-    h.ax2 = p.a_seg_x[2];
-    h.bx0 = p.b_seg_x[0];
-    h.bx1 = p.b_seg_x[1];
-    h.bx2 = p.b_seg_x[2];
-    h.sfb_pitch = p.sfb_pitch;
-    h.sfa = p.sfa;
-    h.sfb = p.sfb;
-    h.status = p.status;
+    h.KT = pin(p.KT);
+    h.n_max = pin(p.n_max);
+    h.stage_bytes = pin(p.stage_bytes);
+    h.a_tx_bytes = pin(p.a_tx_bytes);
+    h.kseg_tiles = pin(p.kseg_tiles);
+    h.dense = pin(p.dense);
+    h.m_tiles = pin(p.m_tiles);
+    h.n_tokens = pin(p.n_tokens);
+    h.a_rows = pin(p.a_rows);
+    h.b_rows = pin(p.b_rows);
+    h.E = pin(p.E);
+    h.mt_per_e = pin(p.mt_per_e);
+    h.rows_per_e = pin(p.rows_per_e);
+    h.epi_split = pin(p.epi_split);
+    h.ax0 = pin(p.a_seg_x[0]);
+    h.ax1 = pin(p.a_seg_x[1]);
+    h.ax2 = pin(p.a_seg_x[2]);
+    h.bx0 = pin(p.b_seg_x[0]);
+    h.bx1 = pin(p.b_seg_x[1]);
+    h.bx2 = pin(p.b_seg_x[2]);
+    h.sfb_pitch = pin(p.sfb_pitch);
+    h.sfa = pin(p.sfa);
+    h.sfb = pin(p.sfb);
+    h.status = pin(p.status);
     return h;
 }
 
+__device__ __forceinline__ void pin_epi(EpiParams& e) {
+    e.mode = pin(e.mode);
+    e.m_tile0 = pin(e.m_tile0);
+    e.col0 = pin(e.col0);
+    e.f32_split = pin(e.f32_split);
+    e.out_f32 = pin(e.out_f32);
+    e.ld_f32 = pin(e.ld_f32);
+    e.out_q = pin(e.out_q);
+    e.ld_q = pin(e.ld_q);
+    e.out_sf = pin(e.out_sf);
+    e.sf_pitch = pin(e.sf_pitch);
+}
+
 // Item `it`.  Grouped items come from the per-expert tables staged in shared
-// memory (ioff, seg, counts): binary search for the expert, then token tile j
-// and weight tile m of that expert.
-__device__ __forceinline__ Item get_item(const Hot& h, int it, const int* ioff, const int* seg, const int* cnt) {
+// memory (ioff, seg, counts): the expert is found from `e`, the expert of the
+// caller's previous item (callers visit their items in increasing order), by
+// a short walk forward, else a binary search; then token tile j and weight
+// tile m of that expert.
+__device__ __forceinline__ Item get_item(const Hot& h, int it, const int* ioff, const int* seg, const int* cnt,
+                                         int& e) {
     Item w;
     if (h.dense) {
         const int mt = it % h.m_tiles;
@@ -108,12 +124,17 @@ __device__ __forceinline__ Item get_item(const Hot& h, int it, const int* ioff, 
         w.n = min(h.n_max, h.n_tokens - w.b_row0);
         w.mt = mt;
     } else {
-        int lo = 0, hi = h.E - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (ioff[mid] <= it) lo = mid;
-            else hi = mid - 1;
+        int lo = (e < 0 || ioff[e] > it) ? 0 : e;
+        for (int step = 0; step < 4 && lo + 1 < h.E && ioff[lo + 1] <= it; ++step) ++lo;
+        if (lo + 1 < h.E && ioff[lo + 1] <= it) {
+            int hi = h.E - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (ioff[mid] <= it) lo = mid;
+                else hi = mid - 1;
+            }
         }
+        e = lo;
         const int local = it - ioff[lo];
         const int j = local / h.mt_per_e, m = local - j * h.mt_per_e;
         w.a_row0 = lo * h.rows_per_e + m * kBlockM;
@@ -153,7 +174,8 @@ __device__ __forceinline__ void group_range(int KT, int g, int G, int& kb, int& 
 // 32 lanes x 16 floats), then the barriers, then the grouped-item tables.
 constexpr int kXbufBytes = 2 * 2 * 32 * 16 * 4;
 constexpr int kMaxStagesPerGroup = 16;
-constexpr int kBarBytes = (kMaxGroups * (2 * kMaxStagesPerGroup + 2 * 2 + 1)) * 8 + 16;
+// barriers, TMEM slot + abort flag (16 bytes), then the [G][2] item slots
+constexpr int kBarBytes = (kMaxGroups * (2 * kMaxStagesPerGroup + 2 * 2 + 1)) * 8 + 16 + kMaxGroups * 2 * 16;
 __host__ __device__ __forceinline__ int table_bytes(int E) { return E > 0 ? ((3 * (E + 1) * 4 + 15) & ~15) : 0; }
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
@@ -203,11 +225,11 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const Hot h = load_hot(p);
-    const int G = p.groups;
-    const int KS = p.ksplit;                // groups per item
+    const int G = pin(p.groups);
+    const int KS = pin(p.ksplit);           // groups per item
     const int IP = G / KS;                  // item lanes
-    const int S = p.stages;                 // per group
-    const int NB = p.acc_bufs;              // accumulator buffers per group
+    const int S = pin(p.stages);            // per group
+    const int NB = pin(p.acc_bufs);         // accumulator buffers per group
     const SmemLayout L = stage_layout(h.n_max);
     uint8_t* tail = base + G * S * h.stage_bytes;
     float* xbuf = reinterpret_cast<float*>(tail);
@@ -218,6 +240,8 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
     uint64_t* tdown = tempty + kMaxGroups * 2;                             // [G]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tdown + kMaxGroups);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    // item handed from each group's MMA warp to the epilogue with its accumulator
+    Item* item_slot = reinterpret_cast<Item*>(reinterpret_cast<uint8_t*>(tmem_slot) + 16);    // [G][2]
     int* ioff_s = reinterpret_cast<int*>(tail + kXbufBytes + kBarBytes);
     int* seg_s = ioff_s + (h.dense ? 0 : h.E + 1);
     int* cnt_s = seg_s + (h.dense ? 0 : h.E + 1);
@@ -232,7 +256,7 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                 mbar_init(&empty[g * kMaxStagesPerGroup + s], 1);
             }
             for (int b = 0; b < 2; ++b) {
-                mbar_init(&tfull[g * 2 + b], 1);
+                mbar_init(&tfull[g * 2 + b], 2);      // the MMAs' commit + the item slot
                 mbar_init(&tempty[g * 2 + b], 4);
             }
             mbar_init(&tdown[g], 1);
@@ -259,6 +283,15 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
     const uint32_t tmem = *tmem_slot;
 
     const int n_items = h.dense ? h.m_tiles * ((h.n_tokens + h.n_max - 1) / h.n_max) : ioff_s[h.E];
+    // this CTA's items: it_begin + c * it_step for c = 0, 1, ... while below
+    // it_end -- a contiguous range (narrow items: consecutive items mostly
+    // share an expert), or every gridDim.x-th item
+    const bool contiguous = p.contiguous != 0;
+    const int it_begin = contiguous ? static_cast<int>(static_cast<int64_t>(n_items) * blockIdx.x / gridDim.x)
+                                    : static_cast<int>(blockIdx.x);
+    const int it_end = contiguous ? static_cast<int>(static_cast<int64_t>(n_items) * (blockIdx.x + 1) / gridDim.x)
+                                  : n_items;
+    const int it_step = contiguous ? 1 : static_cast<int>(gridDim.x);
     const uint32_t cols_per_group = static_cast<uint32_t>(NB * h.n_max + 24);
 
     if (warp < G) {
@@ -274,8 +307,9 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
         uint32_t stage = 0, phase = 0;
         uint32_t issued = 0, issued_parity = 0;   // per-stage bits for the teardown drain
         bool ok = true;
-        for (int it = blockIdx.x + ip * gridDim.x; ok && it < n_items && ke > kb; it += IP * gridDim.x) {
-            const Item w = get_item(h, it, ioff_s, seg_s, cnt_s);
+        int ecur = -1;
+        for (int it = it_begin + ip * it_step; ok && it < it_end && ke > kb; it += IP * it_step) {
+            const Item w = get_item(h, it, ioff_s, seg_s, cnt_s, ecur);
             if (w.n <= 0) {
                 if (w.n < 0 && g == 0 && lane == 0) atomicCAS(h.status, 0, DEV_BAD_WORK);
                 continue;
@@ -334,16 +368,19 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
         const uint32_t sf_base = gcol + static_cast<uint32_t>(NB * h.n_max);
         uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
         bool any = false;
-        for (int it = blockIdx.x + ip * gridDim.x; it < n_items && ke > kb; it += IP * gridDim.x) {
-            const Item w = get_item(h, it, ioff_s, seg_s, cnt_s);
-            if (w.n <= 0) continue;
+        int ecur = -1;
+        for (int it = it_begin + ip * it_step; it < it_end && ke > kb; it += IP * it_step) {
+            // every item takes an accumulator turn, so that the epilogue can
+            // follow the item lanes round-robin; a rejected item (n <= 0)
+            // issues no MMAs
+            const Item w = get_item(h, it, ioff_s, seg_s, cnt_s, ecur);
             const int nm = (w.n + 15) & ~15;
             const int natoms = (nm + 127) / 128;
             bool ok = mbar_wait(&tempty[g * 2 + acc], acc_phase ^ 1, abort_flag, h.status, DEV_TIMEOUT_MMA);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
             const uint32_t d_tmem = gcol + acc * static_cast<uint32_t>(h.n_max);
-            for (int kt = kb; kt < ke; ++kt) {
+            for (int kt = kb; kt < (w.n > 0 ? ke : kb); ++kt) {
                 ok = mbar_wait(&fullg[stage], phase, abort_flag, h.status, DEV_TIMEOUT_MMA);
                 if (!__all_sync(0xffffffffu, ok)) goto mma_done;
                 tc_fence_after();
@@ -403,7 +440,11 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                     phase ^= 1;
                 }
             }
-            if (elect_one()) tc_commit(&tfull[g * 2 + acc]);
+            if (elect_one()) {
+                item_slot[g * 2 + acc] = w;
+                mbar_arrive(&tfull[g * 2 + acc]);      // release: the slot is visible with the phase
+                tc_commit(&tfull[g * 2 + acc]);
+            }
             __syncwarp();
             if (++acc == static_cast<uint32_t>(NB)) {
                 acc = 0;
@@ -424,20 +465,19 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
         const int q = warp & 3;                 // TMEM lane quarter this warp may access
         const uint32_t t_lane = static_cast<uint32_t>(32 * q) << 16;
         // both output descriptions in registers; an item selects scalars
-        const EpiParams E0 = p.epi[0];
-        const EpiParams E1 = p.epi[1];
+        EpiParams E0 = p.epi[0];
+        EpiParams E1 = p.epi[1];
+        pin_epi(E0);
+        pin_epi(E1);
         uint32_t cnts = 0;                      // items consumed per item lane, mod 4 (8 bits each)
         int chunk_parity = 0;
-        int c = 0;                              // CTA-local item number
-        for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++c) {
-            const Item w = get_item(h, it, ioff_s, seg_s, cnt_s);
-            if (w.n <= 0) continue;
-            const int ip = c % IP;
+        const int n_mine = (it_end > it_begin) ? (it_end - it_begin + it_step - 1) / it_step : 0;
+        int ip = 0;                             // item lane of item c
+        for (int c = 0; c < n_mine; ++c) {
             const uint32_t cnt = (cnts >> (8 * ip)) & 0xFFu;
-            const uint32_t acc = cnt % static_cast<uint32_t>(NB);
-            const uint32_t acc_phase = (cnt / static_cast<uint32_t>(NB)) & 1u;
+            const uint32_t acc = (NB == 2) ? (cnt & 1u) : 0u;
+            const uint32_t acc_phase = (NB == 2) ? ((cnt >> 1) & 1u) : (cnt & 1u);
             const int g0 = ip * KS;
-            const int nm = (w.n + 15) & ~15;
             bool ok = true;
             for (int ks = 0; ks < KS; ++ks) {
                 int kb, ke;
@@ -445,8 +485,13 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                 if (ke > kb && ok)
                     ok = mbar_wait(&tfull[(g0 + ks) * 2 + acc], acc_phase, abort_flag, h.status, DEV_TIMEOUT_EPILOGUE);
             }
-            if (!epi_all(ok && !*abort_flag)) break;
+            // the SiLU exchange synchronises the four warps, so there all of
+            // them must leave together; elsewhere each warp decides alone
+            // (every wait is bounded, and a failure raises the abort flag)
+            if (kSilu ? !epi_all(ok && !*abort_flag) : !__all_sync(0xffffffffu, ok && !*abort_flag)) break;
             tc_fence_after();
+            const Item w = item_slot[g0 * 2 + acc];
+            const int nm = (w.n > 0) ? ((w.n + 15) & ~15) : 0;
             const bool second = h.dense && w.mt >= h.epi_split;
             EpiParams E;
             E.mode = second ? E1.mode : E0.mode;
@@ -486,26 +531,47 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                     named_bar_sync(2, 128);
                     if (q < 2) {
                         const int64_t col = E.col0 + static_cast<int64_t>(rel_mt) * 64 + 32 * q + lane;
+                        const int nv = min(16, w.n - n0);
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const int n = n0 + i;
-                            if (n < w.n) {
-                                const float hv = silu_f(v[i]) * xb[q * 512 + i * 32 + lane];
-                                uint8_t sc;
-                                const uint8_t code = warp_mx8_quant(hv, &sc);
-                                const int64_t row = w.b_row0 + n;
-                                E.out_q[row * E.ld_q + col] = code;
-                                if (lane == 0) E.out_sf[sf_byte_offset(row, col, E.sf_pitch)] = sc;
-                            }
+                            if (i >= nv) break;
+                            const float hv = silu_f(v[i]) * xb[q * 512 + i * 32 + lane];
+                            uint8_t sc;
+                            const uint8_t code = warp_mx8_quant(hv, &sc);
+                            const int64_t row = w.b_row0 + n0 + i;
+                            E.out_q[row * E.ld_q + col] = code;
+                            if (lane == 0) E.out_sf[sf_byte_offset(row, col, E.sf_pitch)] = sc;
                         }
                     }
                 } else {
                     const int64_t col = E.col0 + static_cast<int64_t>(rel_mt) * 128 + 32 * q + lane;
+                    const int nv = min(16, w.n - n0);                 // valid tokens of this chunk
+                    const int64_t row0 = w.b_row0 + n0;
+                    if (!kQuant || E.mode != EPI_QUANT) {
+                        // fp32 only: one store per valid token through a running pointer
+                        float* o = E.out_f32 + row0 * E.ld_f32 + col;
+                        if (E.f32_split) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int n = n0 + i;
-                        if (n < w.n) {
-                            const int64_t row = w.b_row0 + n;
+                            for (int i = 0; i < 16; ++i) {
+                                if (i >= nv) break;
+                                const float hi = tf32_round(v[i]);
+                                o[0] = hi;
+                                o[E.f32_split] = v[i] - hi;
+                                o += E.ld_f32;
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                if (i >= nv) break;
+                                o[0] = v[i];
+                                o += E.ld_f32;
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            if (i >= nv) break;
+                            const int64_t row = row0 + i;
                             if (E.out_f32) {
                                 if (E.f32_split) {
                                     const float hi = tf32_round(v[i]);
@@ -515,12 +581,10 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                                     E.out_f32[row * E.ld_f32 + col] = v[i];
                                 }
                             }
-                            if (kQuant && E.mode == EPI_QUANT) {
-                                uint8_t sc;
-                                const uint8_t code = warp_mx8_quant(v[i], &sc);
-                                E.out_q[row * E.ld_q + col] = code;
-                                if (lane == 0) E.out_sf[sf_byte_offset(row, col, E.sf_pitch)] = sc;
-                            }
+                            uint8_t sc;
+                            const uint8_t code = warp_mx8_quant(v[i], &sc);
+                            E.out_q[row * E.ld_q + col] = code;
+                            if (lane == 0) E.out_sf[sf_byte_offset(row, col, E.sf_pitch)] = sc;
                         }
                     }
                 }
@@ -536,6 +600,7 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
             }
             const uint32_t nxt = (cnt + 1u) & 3u;
             cnts = (cnts & ~(0xFFu << (8 * ip))) | (nxt << (8 * ip));
+            ip = (ip + 1 == IP) ? 0 : ip + 1;
         }
     }
 

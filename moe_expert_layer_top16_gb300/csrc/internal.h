@@ -57,6 +57,7 @@ struct GemmParams {
     int n_max;              // tokens per work item (multiple of 16, <= kNMax)
     int groups;             // producer / MMA warp pairs = item lanes x ksplit
     int ksplit;             // groups per item; each takes a contiguous 1/ksplit of the item's K tiles
+    int contiguous;         // 1: each CTA takes a contiguous range of items; 0: every gridDim.x-th item
     int acc_bufs;           // TMEM accumulator buffers per group (1 or 2)
     int stages;             // shared-memory stages per group
     int stage_bytes;

@@ -16,6 +16,22 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Opaque copy of a value: the compiler must keep it in a register from here
+// on instead of re-reading its source (a kernel parameter) at every use.
+__device__ __forceinline__ int pin(int v) {
+    asm volatile("" : "+r"(v));
+    return v;
+}
+__device__ __forceinline__ int64_t pin(int64_t v) {
+    asm volatile("" : "+l"(v));
+    return v;
+}
+template <class T>
+__device__ __forceinline__ T* pin(T* v) {
+    asm volatile("" : "+l"(v));
+    return v;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -54,12 +70,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status,
                                           int code) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
+    uint64_t t0 = 0;                                  // the clock is read only once a wait has spun a while
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63) == 0) {
             if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > kWaitLimitNs) {
                 *abort = 1;
                 if (status) atomicCAS(status, 0, code);
                 return false;
