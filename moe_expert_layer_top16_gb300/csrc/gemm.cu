@@ -26,11 +26,11 @@
 //   warps G..2G-1    MMA issuers: per K tile, re-arrange B's scales,
 //                    tcgen05.cp both scale tiles into TMEM, 4 MMAs (K = 32
 //                    each), commit the stage back to the producer.
-//   warps 2G..2G+3   epilogue, items in CTA order: wait for the KS partial
-//                    accumulators of the item, add them (group order, fp32),
-//                    then fp32 stores, MXFP8 quantisation (one warp = 32
-//                    consecutive output features = one MX block) or
-//                    SiLU-gating + MXFP8.
+//   warps 2G..2G+7   epilogue, two warpgroups taking the CTA's items in
+//                    turn: wait for the KS partial accumulators of the item,
+//                    add them (group order, fp32), then fp32 stores, MXFP8
+//                    quantisation (one warp = 32 consecutive output features
+//                    = one MX block) or SiLU-gating + MXFP8.
 // Both roles that issue asynchronous work run warp-converged and issue from
 // one elected lane.  With two accumulator buffers per group the epilogue of
 // one item overlaps the MMAs of the next.  Work items come from per-expert
@@ -172,7 +172,7 @@ __device__ __forceinline__ void group_range(int KT, int g, int G, int& kb, int& 
 
 // Shared memory after the stages: epilogue exchange buffer (2 x 2 warps x
 // 32 lanes x 16 floats), then the barriers, then the grouped-item tables.
-constexpr int kXbufBytes = 2 * 2 * 32 * 16 * 4;
+constexpr int kXbufBytes = kEpiGroups * 2 * 2 * 32 * 16 * 4;    // per epilogue warpgroup: 2 chunks x 2 warps
 constexpr int kMaxStagesPerGroup = 16;
 // barriers, TMEM slot + abort flag (16 bytes), then the [G][2] item slots
 constexpr int kBarBytes = (kMaxGroups * (2 * kMaxStagesPerGroup + 2 * 2 + 1)) * 8 + 16 + kMaxGroups * 2 * 16;
@@ -180,16 +180,17 @@ __host__ __device__ __forceinline__ int table_bytes(int E) { return E > 0 ? ((3 
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
-// All 128 epilogue threads agree on `ok` (named barrier 1 with an AND reduction).
-__device__ __forceinline__ bool epi_all(bool ok) {
+// The 128 threads of an epilogue warpgroup agree on `ok` (named barrier
+// `bar` with an AND reduction).
+__device__ __forceinline__ bool epi_all(bool ok, int bar) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "bar.red.and.pred q, %2, 128, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
-        : "r"(ok ? 1u : 0u)
+        : "r"(ok ? 1u : 0u), "r"(bar)
         : "memory");
     return r != 0;
 }
@@ -460,23 +461,28 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
             }
             __syncwarp();
         }
-    } else if (warp < 2 * G + 4) {
+    } else if (warp < 2 * G + 4 * kEpiGroups) {
         // ------------------------------------------------------------ epilogue
+        // kEpiGroups warpgroups take the CTA's items in turn; the four warps of
+        // a warpgroup cover the four TMEM lane quarters of an accumulator
         const int q = warp & 3;                 // TMEM lane quarter this warp may access
+        const int wg = (warp - 2 * G) >> 2;
+        const int bar_agree = 1 + 2 * wg, bar_xchg = 2 + 2 * wg;     // named barriers of this warpgroup
         const uint32_t t_lane = static_cast<uint32_t>(32 * q) << 16;
         // both output descriptions in registers; an item selects scalars
         EpiParams E0 = p.epi[0];
         EpiParams E1 = p.epi[1];
         pin_epi(E0);
         pin_epi(E1);
-        uint32_t cnts = 0;                      // items consumed per item lane, mod 4 (8 bits each)
         int chunk_parity = 0;
         const int n_mine = (it_end > it_begin) ? (it_end - it_begin + it_step - 1) / it_step : 0;
-        int ip = 0;                             // item lane of item c
-        for (int c = 0; c < n_mine; ++c) {
-            const uint32_t cnt = (cnts >> (8 * ip)) & 0xFFu;
-            const uint32_t acc = (NB == 2) ? (cnt & 1u) : 0u;
-            const uint32_t acc_phase = (NB == 2) ? ((cnt >> 1) & 1u) : (cnt & 1u);
+        const int ip_shift = (IP == 4) ? 2 : (IP == 2 ? 1 : 0);       // IP is 1, 2 or 4
+        for (int c = wg; c < n_mine; c += kEpiGroups) {
+            // item c: item lane c % IP, that lane's (c / IP)-th accumulator turn
+            const int ip = c & (IP - 1);
+            const uint32_t turn = static_cast<uint32_t>(c >> ip_shift);
+            const uint32_t acc = (NB == 2) ? (turn & 1u) : 0u;
+            const uint32_t acc_phase = (NB == 2) ? ((turn >> 1) & 1u) : (turn & 1u);
             const int g0 = ip * KS;
             bool ok = true;
             for (int ks = 0; ks < KS; ++ks) {
@@ -488,7 +494,7 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
             // the SiLU exchange synchronises the four warps, so there all of
             // them must leave together; elsewhere each warp decides alone
             // (every wait is bounded, and a failure raises the abort flag)
-            if (kSilu ? !epi_all(ok && !*abort_flag) : !__all_sync(0xffffffffu, ok && !*abort_flag)) break;
+            if (kSilu ? !epi_all(ok && !*abort_flag, bar_agree) : !__all_sync(0xffffffffu, ok && !*abort_flag)) break;
             tc_fence_after();
             const Item w = item_slot[g0 * 2 + acc];
             const int nm = (w.n > 0) ? ((w.n + 15) & ~15) : 0;
@@ -522,13 +528,13 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                     first = false;
                 }
                 if (kOnlySilu || (kSilu && E.mode == EPI_SILU_QUANT)) {
-                    float* xb = xbuf + chunk_parity * (2 * 32 * 16);
+                    float* xb = xbuf + (wg * 2 + chunk_parity) * (2 * 32 * 16);
                     chunk_parity ^= 1;
                     if (q >= 2) {
 #pragma unroll
                         for (int i = 0; i < 16; ++i) xb[(q - 2) * 512 + i * 32 + lane] = v[i];
                     }
-                    named_bar_sync(2, 128);
+                    named_bar_sync(bar_xchg, 128);
                     if (q < 2) {
                         const int64_t col = E.col0 + static_cast<int64_t>(rel_mt) * 64 + 32 * q + lane;
                         const int nv = min(16, w.n - n0);
@@ -598,9 +604,6 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                     if (ke > kb) mbar_arrive(&tempty[(g0 + ks) * 2 + acc]);
                 }
             }
-            const uint32_t nxt = (cnt + 1u) & 3u;
-            cnts = (cnts & ~(0xFFu << (8 * ip))) | (nxt << (8 * ip));
-            ip = (ip + 1 == IP) ? 0 : ip + 1;
         }
     }
 
@@ -677,7 +680,7 @@ cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s) {
     if (!p.dense && (p.E <= 0 || p.E > 1024)) return cudaErrorInvalidValue;
     const int set = epi_set(p);
     if (set < 0) return cudaErrorInvalidValue;
-    const int threads = (2 * p.groups + 4) * 32;
+    const int threads = (2 * p.groups + 4 * kEpiGroups) * 32;
     if (p.kind == KIND_TF32) {
         if (set != SET_F32) return cudaErrorInvalidValue;
         mx_gemm_kernel<KIND_TF32, SET_F32><<<grid, threads, smem, s>>>(p);
