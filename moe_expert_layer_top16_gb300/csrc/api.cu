@@ -116,7 +116,7 @@ struct Plan {
     float *router, *router2, *bias;   // router2: [E][2L] = TF32 high part | remainder
     // workspace
     uint8_t *xq, *xsf, *zq, *zsf, *act, *actsf, *zqp, *zqpsf, *hq, *hqsf;
-    float *z, *logits, *rpart, *gw, *o;   // rpart: router K-split partials (batches <= 128 tokens)
+    float *z, *logits, *gw, *o;
     uint32_t* sel;
     int32_t *idx, *wpre, *counts, *offsets, *seg, *slot_pos, *canon_to_pad, *sorted_token;
     int32_t *ioff7, *ioff8;   // [E+1] per-expert item offsets of the grouped GEMMs
@@ -457,8 +457,6 @@ moe_status moe_plan(const moe_config* cfg, const moe_weights* w, int device, voi
     TRY(palloc(p, &p->act, Tp * p->Kcat));
     TRY(palloc(p, &p->actsf, (p->Kcat / 128) * Tp * 4));
     TRY(palloc(p, &p->logits, sizeof(float) * p->T_max * E));
-    TRY(palloc(p, &p->rpart, sizeof(float) * router_partials(std::min(p->T_max, 128), L) *
-                                 std::min(p->T_max, 128) * E));
     TRY(palloc(p, &p->idx, sizeof(int32_t) * p->T_max * p->k));
     TRY(palloc(p, &p->gw, sizeof(float) * p->T_max * p->k));
     TRY(palloc(p, &p->sel, sizeof(uint32_t) * E * p->W_max));
@@ -544,7 +542,6 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
     }
     // 3. router logits, 4. top-k + gates + bitmaps
     mark(2);
-    int nparts = 1;
     const bool tc_logits = p->tc_router && T > 128;
     if (tc_logits) {
         // logits = z R^T as three TF32 products, z_hi R_hi + z_lo R_hi + z_hi R_lo,
@@ -564,17 +561,13 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
         const int items = g.m_tiles * ((T + g.n_max - 1) / g.n_max);
         shape_gemm(g, 0, items, std::min(items, p->num_sms));
         TRY(launch_gemm(g, std::min(items, p->num_sms), s));
-        nparts = 1;
     } else {
-        nparts = router_partials(T, L);
-        TRY(launch_router(p->z, p->router, p->logits, p->rpart, T, E, L, s));
+        TRY(launch_router(p->z, p->router, p->logits, T, E, L, s));
     }
     mark(3);
     {
         TopkArgs a;
         a.logits = p->logits;
-        a.part = p->rpart;
-        a.nparts = nparts;
         a.bias = p->bias;
         a.T = T;
         a.E = E;

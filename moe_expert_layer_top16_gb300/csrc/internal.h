@@ -96,20 +96,16 @@ cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s);
 // ------------------------------------------------------------------ other kernels
 cudaError_t launch_quant_x(const __nv_bfloat16* x, int T, int D, uint8_t* xq, uint8_t* xsf, int64_t pitch,
                            cudaStream_t s);
-// SIMT router on z = hi + lo ([T][2L]).  Batches of at most 128 tokens write
-// router_partials(T, L) K-split partial sums to part[split][T][E] (summed by
-// the top-k kernel); larger ones write logits directly.
-int router_partials(int T, int L);
-cudaError_t launch_router(const float* z, const float* R, float* logits, float* part, int T, int E, int L,
-                          cudaStream_t s);
-// top-k + gates (kernels.cu): with nparts > 1 the logits are first summed
-// from `part` (and written to `logits`); with refine, the logits are
+// SIMT router on z = hi + lo ([T][2L]) writing logits [T][E]; batches of at
+// most kRouterSplitTokens tokens split K kRouterSplit ways over a cluster.
+constexpr int kRouterSplit = 8;
+constexpr int kRouterSplitTokens = 128;
+cudaError_t launch_router(const float* z, const float* R, float* logits, int T, int E, int L, cudaStream_t s);
+// top-k + gates (kernels.cu): with refine, the logits are
 // approximate within delta and the candidates' exact logits are recomputed
 // from z ([T][2L], hi | lo) and R ([E][L]).
 struct TopkArgs {
     float* logits;
-    const float* part;
-    int nparts;
     const float* bias;
     int T, E, k, softmax;
     int refine;

@@ -3,14 +3,18 @@
 // (per-expert counts, offsets, stable ranks, work lists, gather), the
 // weighted combine with MXFP8 re-quantisation, the MXFP4 weight encoder, and
 // plan-time repacking / debug export helpers.
+#include <cooperative_groups.h>
+
 #include "internal.h"
 #include "mx.cuh"
 
 namespace moe {
 
+namespace cg = cooperative_groups;
+
 namespace {
 
-__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+__host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // ------------------------------------------------------------------ A1: x -> MXFP8
 // One warp per (row, 128-wide column tile); lane l owns elements 4l..4l+3, so
@@ -94,81 +98,91 @@ __global__ void __launch_bounds__(256) router_kernel(const float* __restrict__ z
     }
 }
 
-// Decode-sized batches (T <= 128): 8 experts per CTA so that ~E/8 CTAs
-// stream R from HBM in parallel; the tokens' latent rows come through shared
-// memory in 64-wide K chunks (z is small and L2-resident; it is stored as
-// TF32 high part | remainder, [T][2L], and z = hi + lo exactly).  Warp w owns
-// expert e0 + w; lane l owns tokens l, l+32, l+64, l+96.  One sequential FMA
-// chain per output, like the tiled kernel.
-// K is split RS_KSPLIT ways across blockIdx.y (many CTAs per SM hide the L2
-// latency of the z chunks); each split writes its partial sums to
-// part[split][T][E] and the top-k kernel adds the splits in a fixed order.
-constexpr int RS_E = 8, RS_K = 64, RS_TMAX = 128, RS_KSPLIT = 8;
-__global__ void __launch_bounds__(256) router_small_kernel(const float* __restrict__ z, const float* __restrict__ R,
-                                                           float* __restrict__ part, int T, int E, int L) {
-    __shared__ float zs[RS_TMAX][RS_K + 1];
-    __shared__ float rs[RS_E][RS_K];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e0 = blockIdx.x * RS_E;
-    const int e = e0 + warp;
-    const int klen = L / RS_KSPLIT;
-    const int kbeg = blockIdx.y * klen;
-    float* logits = part + static_cast<int64_t>(blockIdx.y) * T * E;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int k0 = kbeg; k0 < kbeg + klen; k0 += RS_K) {
-        // float4 loads, all issued before any is consumed
-        constexpr int kV = RS_TMAX * RS_K / 4 / 256;        // float4 slots per thread (<= 8)
-        float4 zh[kV], zl[kV];
+// Decode-sized batches (T <= 128): 32 experts x 64 tokens per output tile,
+// its K range split over the kRouterSplit CTAs of a thread-block cluster, so
+// that ~E/32 x 8 CTAs stream R from HBM in parallel while z (L2-resident) is
+// re-read only E/32 times.  Each CTA accumulates its K range in registers
+// (one sequential FMA chain per output, the next 32-wide K slice prefetched
+// into registers during the current one), leaves its partial tile in shared
+// memory, and after a cluster barrier reduces 1/8 of the tile by adding the 8
+// partials, read through distributed shared memory, in split order -- a
+// fixed order, so the logits are deterministic.
+constexpr int RC_T = 64, RC_E = 32, RC_K = 32;
+__global__ void __cluster_dims__(1, 1, kRouterSplit) __launch_bounds__(256)
+    router_cluster_kernel(const float* __restrict__ z, const float* __restrict__ R, float* __restrict__ logits, int T,
+                          int E, int L, int kper) {
+    __shared__ __align__(16) float zs[RC_K][RC_T + 4];     // [k][token]
+    __shared__ __align__(16) float rs[RC_K][RC_E + 4];     // [k][expert]
+    __shared__ float red[RC_T * RC_E];                     // this split's partial tile [token][expert]
+    cg::cluster_group cluster = cg::this_cluster();
+    const int t0 = blockIdx.y * RC_T, e0 = blockIdx.x * RC_E;
+    const int ks = static_cast<int>(cluster.block_rank());
+    const int kb = ks * kper, ke = min(L, kb + kper);
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;   // experts 2tx, 2tx+1; tokens 4ty..4ty+3
+    float acc[4][2] = {};
+    // one K slice: z rows t0..t0+63 (hi and lo, 2 float4 each per thread), R rows e0..e0+31 (1 float4)
+    float4 zh[2], zl[2], rv;
+    auto load = [&](int k0) {
 #pragma unroll
-        for (int u = 0; u < kV; ++u) {
-            const int i = threadIdx.x + u * 256;             // float4 index
-            const int r = i / (RS_K / 4), c = (i % (RS_K / 4)) * 4;
-            if (r < T) {
-                const float* zr = z + static_cast<int64_t>(r) * 2 * L + k0 + c;
-                zh[u] = *reinterpret_cast<const float4*>(zr);
-                zl[u] = *reinterpret_cast<const float4*>(zr + L);
-            }
+        for (int u = 0; u < 2; ++u) {
+            const int i = threadIdx.x + 256 * u;
+            const int r = i >> 3, c = (i & 7) * 4;
+            const float* zr = z + static_cast<int64_t>(t0 + r) * 2 * L + k0 + c;
+            const bool tv = t0 + r < T;
+            zh[u] = tv ? *reinterpret_cast<const float4*>(zr) : make_float4(0.f, 0.f, 0.f, 0.f);
+            zl[u] = tv ? *reinterpret_cast<const float4*>(zr + L) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        float4 rvec = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int r = threadIdx.x >> 3, c = (threadIdx.x & 7) * 4;
+        rv = (e0 + r < E) ? *reinterpret_cast<const float4*>(R + static_cast<int64_t>(e0 + r) * L + k0 + c)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    if (kb < ke) load(kb);
+    for (int k0 = kb; k0 < ke; k0 += RC_K) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int i = threadIdx.x + 256 * u;
+            const int r = i >> 3, c = (i & 7) * 4;
+            zs[c][r] = zh[u].x + zl[u].x;
+            zs[c + 1][r] = zh[u].y + zl[u].y;
+            zs[c + 2][r] = zh[u].z + zl[u].z;
+            zs[c + 3][r] = zh[u].w + zl[u].w;
+        }
         {
-            const int r = threadIdx.x / (RS_K / 4), c = (threadIdx.x % (RS_K / 4)) * 4;   // 8 x 16 float4
-            if (r < RS_E && e0 + r < E) rvec = *reinterpret_cast<const float4*>(R + static_cast<int64_t>(e0 + r) * L + k0 + c);
+            const int r = threadIdx.x >> 3, c = (threadIdx.x & 7) * 4;
+            rs[c][r] = rv.x;
+            rs[c + 1][r] = rv.y;
+            rs[c + 2][r] = rv.z;
+            rs[c + 3][r] = rv.w;
         }
+        __syncthreads();
+        if (k0 + RC_K < ke) load(k0 + RC_K);
+#pragma unroll 8
+        for (int kk = 0; kk < RC_K; ++kk) {
+            const float4 a4 = *reinterpret_cast<const float4*>(&zs[kk][ty * 4]);
+            const float2 b2 = *reinterpret_cast<const float2*>(&rs[kk][tx * 2]);
+            const float a[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
-        for (int u = 0; u < kV; ++u) {
-            const int i = threadIdx.x + u * 256;
-            const int r = i / (RS_K / 4), c = (i % (RS_K / 4)) * 4;
-            if (r < T) {
-                zs[r][c] = zh[u].x + zl[u].x;
-                zs[r][c + 1] = zh[u].y + zl[u].y;
-                zs[r][c + 2] = zh[u].z + zl[u].z;
-                zs[r][c + 3] = zh[u].w + zl[u].w;
+            for (int i2 = 0; i2 < 4; ++i2) {
+                acc[i2][0] = fmaf(a[i2], b2.x, acc[i2][0]);
+                acc[i2][1] = fmaf(a[i2], b2.y, acc[i2][1]);
             }
         }
-        if (threadIdx.x < RS_E * RS_K / 4) {
-            const int r = threadIdx.x / (RS_K / 4), c = (threadIdx.x % (RS_K / 4)) * 4;
-            rs[r][c] = rvec.x;
-            rs[r][c + 1] = rvec.y;
-            rs[r][c + 2] = rvec.z;
-            rs[r][c + 3] = rvec.w;
-        }
-        __syncthreads();
-#pragma unroll 8
-        for (int kk = 0; kk < RS_K; ++kk) {
-            const float rv = rs[warp][kk];
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (lane + 32 * j < T) acc[j] = fmaf(zs[lane + 32 * j][kk], rv, acc[j]);
-        }
         __syncthreads();
     }
-    if (e < E) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int t = lane + 32 * j;
-            if (t < T) logits[static_cast<int64_t>(t) * E + e] = acc[j];
-        }
+    for (int i2 = 0; i2 < 4; ++i2) {
+        red[(ty * 4 + i2) * RC_E + tx * 2] = acc[i2][0];
+        red[(ty * 4 + i2) * RC_E + tx * 2 + 1] = acc[i2][1];
     }
+    cluster.sync();
+    // this CTA's eighth of the tile: 256 outputs, one per thread
+    const int o = ks * 256 + threadIdx.x;
+    const int tt = o / RC_E, ee = o % RC_E;
+    float v = 0.0f;
+#pragma unroll
+    for (int q = 0; q < kRouterSplit; ++q) v += cluster.map_shared_rank(red, q)[o];
+    if (t0 + tt < T && e0 + ee < E) logits[static_cast<int64_t>(t0 + tt) * E + e0 + ee] = v;
+    cluster.sync();     // no CTA leaves while another still reads its tile
 }
 
 // ------------------------------------------------------------------ A4: top-k + gates
@@ -181,13 +195,13 @@ __global__ void __launch_bounds__(256) router_small_kernel(const float* __restri
 //    the logits tie).
 //  * with a bias: sigmoid(l) + b, decided in fp64.
 // When the logits are approximate (tensor-core router, |error| <= delta) or
-// keys need fp64, R = k + 8 candidates are picked on the estimates; their
-// exact fp32 logits (recomputed from z and R when the logits were
-// approximate) and keys give the final ranking.  That ranking is final when
-// no expert outside the candidates can beat the k-th one: the R-th estimate
-// plus the estimate's error bound is below the k-th exact key; otherwise every
-// expert's logit and key are evaluated exactly.  Rounds take the largest
-// remaining key, the lower expert id on a tie.
+// keys need fp64, candidates are picked on the estimates: the k best and
+// every expert within twice the estimate's error bound of the k-th (no expert
+// outside that band can be in the exact top-k).  Their exact fp32 logits
+// (recomputed from z and R when the logits were approximate) and keys give
+// the final ranking; with more than 32 candidates every expert's logit and key
+// are evaluated exactly instead.  Rounds take the largest remaining key, the
+// lower expert id on a tie.
 // Gates: sigmoid(l_j) / sum over the winners (fp32), or softmax over the
 // winners' logits.  Each selection sets bit t of the expert's token bitmap.
 constexpr int kTopkWarps = 4;
@@ -267,15 +281,6 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(TopkArgs a) {
     if (t >= a.T) return;
     const int E = a.E, k = a.k;
     float* l = a.logits + static_cast<int64_t>(t) * E;
-    if (a.nparts > 1) {
-        // logits = sum of the router's K-split partials, in split order
-        for (int e = lane; e < E; e += 32) {
-            float v = 0.0f;
-            for (int q = 0; q < a.nparts; ++q) v += a.part[(static_cast<int64_t>(q) * a.T + t) * E + e];
-            l[e] = v;
-        }
-        __syncwarp();
-    }
     const float* bias = a.bias;
     const bool use_bias = (bias != nullptr) && !a.softmax;
     const bool approx = a.refine != 0;
@@ -293,10 +298,18 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(TopkArgs a) {
         key[i] = (i < nper && e < E) ? kv : -INFINITY;
     }
     uint32_t taken = 0;                                       // bit i: candidate lane + 32 i selected
-    const int R = need_cand ? min(E, min(32, k + 8)) : k;
+    // Candidates, in estimate order: the k best estimates, then every further
+    // expert whose estimate is within 2 * err of the k-th one.  An expert
+    // outside that band has a true key below k-th estimate - err, and each of
+    // the k best has a true key above it, so the exact top-k lies among the
+    // candidates.  More than 32 candidates (lane capacity): exact fallback.
+    const double err = approx ? (use_bias ? 0.25 * a.delta + kKeyErr : a.delta) : kKeyErr;
+    int R = 0;
+    bool overflow = false;
     int my_id = 0;                                            // lane j < R holds the j-th pick
-    float my_est = 0.0f;
-    for (int j = 0; j < R; ++j) {
+    float kth_est = 0.0f;
+    for (int j = 0; j <= 32; ++j) {
+        if (j >= k && !need_cand) break;
         KeyId b = {-INFINITY, 0x7fffffff};
 #pragma unroll
         for (int i = 0; i < kTopkPerLane; ++i) {
@@ -308,12 +321,20 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(TopkArgs a) {
             }
         }
         b = warp_best(b);
-        if (b.id < 0 || b.id >= E) b.id = 0;                 // unreachable while k <= E
-        if (lane == j) {
-            my_id = b.id;
-            my_est = b.key;
+        if (j >= k) {
+            // band test in double: kth_est - 2 err is not rounded toward the candidate
+            if (b.id < 0 || b.id >= E || !(static_cast<double>(b.key) >= static_cast<double>(kth_est) - 2.0 * err))
+                break;
+            if (j == 32) {
+                overflow = true;
+                break;
+            }
         }
+        if (b.id < 0 || b.id >= E) b.id = 0;                 // unreachable while k <= E
+        if (j == k - 1) kth_est = b.key;
+        if (lane == j) my_id = b.id;
         if ((b.id & 31) == lane) taken |= 1u << (b.id >> 5);
+        R = j + 1;
     }
     int slot = lane;                                          // final slot of this lane's pick
     float my_l = 0.0f;                                        // exact logit of this lane's pick
@@ -341,15 +362,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(TopkArgs a) {
             if (i != lane && (oi > kx || (oi == kx && id < my_id))) ++rank;
         }
         slot = (lane < R) ? rank : 32;
-        double kth = -INFINITY;                               // k-th exact key
-        for (int i = 0; i < R; ++i) {
-            const int r = __shfl_sync(0xffffffffu, slot, i);
-            const double v = __shfl_sync(0xffffffffu, kx, i);
-            if (r == k - 1) kth = v;
-        }
-        const float last_est = __shfl_sync(0xffffffffu, my_est, R - 1);
-        const double err = approx ? (use_bias ? 0.25 * a.delta + kKeyErr : a.delta) : kKeyErr;
-        const bool safe = (R == E) || (static_cast<double>(last_est) + err < kth);
+        const bool safe = !overflow;
         if (approx && safe) {
             if (lane < R) l[my_id] = my_l;                    // export the exact candidate logits
         }
@@ -713,13 +726,13 @@ cudaError_t launch_quant_x(const __nv_bfloat16* x, int T, int D, uint8_t* xq, ui
     return cudaGetLastError();
 }
 
-int router_partials(int T, int L) { return (T <= RS_TMAX && L % (RS_K * RS_KSPLIT) == 0) ? RS_KSPLIT : 1; }
-
-cudaError_t launch_router(const float* z, const float* R, float* logits, float* part, int T, int E, int L,
-                          cudaStream_t s) {
-    if (T <= RS_TMAX && L % (RS_K * RS_KSPLIT) == 0) {
-        dim3 grid((E + RS_E - 1) / RS_E, RS_KSPLIT);
-        router_small_kernel<<<grid, 256, 0, s>>>(z, R, part, T, E, L);
+cudaError_t launch_router(const float* z, const float* R, float* logits, int T, int E, int L, cudaStream_t s) {
+    if (L % 4) return cudaErrorInvalidValue;
+    if (T <= kRouterSplitTokens && L % RC_K == 0) {
+        static_assert(RC_T * RC_E == 256 * kRouterSplit, "one reduced output per thread");
+        const int kper = ceil_div(L / RC_K, kRouterSplit) * RC_K;
+        dim3 grid((E + RC_E - 1) / RC_E, (T + RC_T - 1) / RC_T, kRouterSplit);
+        router_cluster_kernel<<<grid, 256, 0, s>>>(z, R, logits, T, E, L, kper);
         return cudaGetLastError();
     }
     dim3 grid((E + RE - 1) / RE, (T + RT - 1) / RT);
