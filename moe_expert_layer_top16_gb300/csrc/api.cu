@@ -508,7 +508,9 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
     const int D = p->D, L = p->L, E = p->E, k = p->k, I = p->I, Ip = p->Ip;
     const int W = (T + 31) / 32;
     const int64_t Tp = p->T_pad, Rp = p->R_pad;
-    const int nmax_dense = pick_n_max(T, item_cap(T));
+    // dense GEMMs stream their weights once per token tile: a batch of up to
+    // 64 tokens is one tile
+    const int nmax_dense = (T <= 64) ? static_cast<int>(rup(T, 16)) : pick_n_max(T, item_cap(T));
     const int nmax_grp = static_cast<int>(std::min<int64_t>(item_cap(T), rup(T, 16)));
     // experts expected to receive tokens (all of them once T * k >> E)
     const int64_t est_experts = std::min<int64_t>(E, static_cast<int64_t>(T) * k);
