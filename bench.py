@@ -46,6 +46,17 @@ def peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+CPU_BASELINE_SECONDS = 10.0
+
+# DRAM bytes (read + write) per launch of a stage's kernel from one ncu
+# capture, and the commit the capture was taken at; a capture stands only
+# until its kernel changes (summaries under profiles/).
+NCU_TRAFFIC = {
+    ("decode64", "gemm_gate_up"): (1.306458e9 + 3.840256e6, "f8c2b48", "profiles/gate_up_decode64.md"),
+    ("prefill8192", "gemm_gate_up"): (2.256906e9 + 68.11776e6, "f8c2b48", "profiles/gate_up_prefill8192.md"),
+}
+
+
 def algorithmic_work(wl, T, counts):
     """Per-stage algorithmic bytes and MX FLOPs of one forward of T tokens.
     `counts` = realised tokens per expert (touched experts are those > 0)."""
@@ -322,6 +333,8 @@ def run_cuda(args, wl, world, rank, local):
     dom_name = names[dom]
     bytes_, flops = work.get(dom_name, (0.0, 0.0))
     stage_s = mean_stage[dom] / 1e3
+    key = (wl.name, dom_name)
+    traffic = NCU_TRAFFIC[key][0] if key in NCU_TRAFFIC else None
     # decode-sized batches are judged on HBM bytes, prefill-sized on the tensor pipe
     tensor_bound = flops / max(bytes_, 1.0) > 560.0 and flops > 0
     if tensor_bound:
@@ -329,12 +342,15 @@ def run_cuda(args, wl, world, rank, local):
         peak = bf16 * 2.0
         achieved = flops / stage_s / 1e12
         roof = {"bound": "tensor", "kernel": dom_name, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": None,
+                "frac": achieved / peak, "traffic": traffic,
                 "peak_source": f"{peak_kind} bf16 burst {bf16} TFLOP/s x 2 (nominal fp8/bf16 ratio)"}
     else:
         achieved = bytes_ / stage_s / 1e9
         roof = {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "traffic": None, "peak_source": f"{peak_kind} copy bandwidth"}
+                "frac": achieved / hbm, "traffic": traffic, "peak_source": f"{peak_kind} copy bandwidth"}
+    if traffic is not None:
+        roof["traffic_source"] = f"ncu dram__bytes_read.sum + dram__bytes_write.sum, {NCU_TRAFFIC[key][2]}, " \
+                                 f"commit {NCU_TRAFFIC[key][1]}"
     layer_bytes = sum(b for b, _ in work.values())
     layer_flops = sum(f for _, f in work.values())
     step_s = ms_per_step / 1e3
@@ -364,14 +380,22 @@ def run_cuda(args, wl, world, rank, local):
     plan.close()
     del flush
     if rank == 0 and not args.no_cpu_baseline:
-        run, n_exp = oracle_sample(wl, args.cpu_tokens, dev)
-        t0 = time.perf_counter()
-        run()
-        dt = time.perf_counter() - t0
-        result["cpu_baseline"] = {"value": args.cpu_tokens / dt, "unit": "tokens/s", "cores": cpu_cores(),
+        # the oracle as it stands, repeated over the same token sample until
+        # about CPU_BASELINE_SECONDS of work have been timed
+        n_tok = min(args.cpu_tokens, T)
+        run, n_exp = oracle_sample(wl, n_tok, dev)
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            run()
+            reps += 1
+            dt = time.perf_counter() - t0
+            if dt >= CPU_BASELINE_SECONDS or reps >= 100:
+                break
+        result["cpu_baseline"] = {"value": n_tok * reps / dt, "unit": "tokens/s", "cores": cpu_cores(),
                                   "kind": "oracle",
-                                  "sample": f"{args.cpu_tokens} tokens of {wl.name} ({n_exp} experts), fp64 C "
-                                            f"oracle with OpenMP on {cpu_model()}; weight encoding excluded"}
+                                  "sample": f"{n_tok} tokens of {wl.name} ({n_exp} experts) x {reps} passes "
+                                            f"({dt:.1f} s); fp64 C oracle with OpenMP on {cpu_model()}; "
+                                            f"weight encoding excluded"}
     if rank == 0:
         print(json.dumps(result), flush=True)
     return 0
@@ -384,7 +408,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="decode64")
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
-    ap.add_argument("--cpu-tokens", type=int, default=8)
+    ap.add_argument("--cpu-tokens", type=int, default=64)
     ap.add_argument("--reference-tokens", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
