@@ -206,8 +206,9 @@ MOE_API moe_status moe_mx_gemm(const uint8_t *a_codes, const uint8_t *a_scales, 
  * Arguments, layouts and the result are those of moe_mx_gemm.  Instead of
  * cudaMallocAsync it uses a fixed scratch array of MOE_NOALLOC_SCRATCH_BYTES
  * that lives in the library's device image: every GPU that loads the library
- * holds it until the process exits.  Limit: M*K/32 + (K/128)*round16(N)*4 +
- * 256 <= MOE_NOALLOC_SCRATCH_BYTES (e.g. M = K = 4096 with N up to ~24000);
+ * holds it until the process exits.  Limit: M*K/32 + (K/128)*(round16(N) +
+ * 32)*16 + 256 <= MOE_NOALLOC_SCRATCH_BYTES (e.g. M = K = 4096 with N up to
+ * about 7100);
  * larger calls return MOE_ERR_INVALID_ARG with nothing enqueued.  The first
  * call on a device looks up the array's device address (once per device, on
  * the current device); make that first call before any stream capture.  All

@@ -450,12 +450,13 @@ moe_status moe_plan(const moe_config* cfg, const moe_weights* w, int device, voi
     }
     // ---------------------------------------------------------------- workspace
     TRY(palloc(p, &p->xq, Tp * D));
-    TRY(palloc(p, &p->xsf, (D / 128) * Tp * 4));
+    // token-operand scales of the GEMMs: item-atom planes with 32 spare slots
+    TRY(palloc(p, &p->xsf, (D / 128) * (Tp + 32) * 16));
     TRY(palloc(p, &p->z, sizeof(float) * Tp * 2 * L));     // TF32 high part | remainder
     TRY(palloc(p, &p->zq, Tp * L));
     TRY(palloc(p, &p->zsf, (L / 128) * Tp * 4));
     TRY(palloc(p, &p->act, Tp * p->Kcat));
-    TRY(palloc(p, &p->actsf, (p->Kcat / 128) * Tp * 4));
+    TRY(palloc(p, &p->actsf, (p->Kcat / 128) * (Tp + 32) * 16));
     TRY(palloc(p, &p->logits, sizeof(float) * p->T_max * E));
     TRY(palloc(p, &p->idx, sizeof(int32_t) * p->T_max * p->k));
     TRY(palloc(p, &p->gw, sizeof(float) * p->T_max * p->k));
@@ -468,9 +469,9 @@ moe_status moe_plan(const moe_config* cfg, const moe_weights* w, int device, voi
     TRY(palloc(p, &p->canon_to_pad, sizeof(int32_t) * p->T_max * p->k));
     TRY(palloc(p, &p->sorted_token, sizeof(int32_t) * p->T_max * p->k));
     TRY(palloc(p, &p->zqp, Rp * L));
-    TRY(palloc(p, &p->zqpsf, (L / 128) * Rp * 4));
+    TRY(palloc(p, &p->zqpsf, (L / 128) * (Rp + 32) * 16));
     TRY(palloc(p, &p->hq, Rp * Ip));
-    TRY(palloc(p, &p->hqsf, (Ip / 128) * Rp * 4));
+    TRY(palloc(p, &p->hqsf, (Ip / 128) * (Rp + 32) * 16));
     TRY(palloc(p, &p->o, sizeof(float) * Rp * L));
     TRY(palloc(p, &p->ioff7, sizeof(int32_t) * (E + 1)));
     TRY(palloc(p, &p->ioff8, sizeof(int32_t) * (E + 1)));
@@ -508,6 +509,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
     const int D = p->D, L = p->L, E = p->E, k = p->k, I = p->I, Ip = p->Ip;
     const int W = (T + 31) / 32;
     const int64_t Tp = p->T_pad, Rp = p->R_pad;
+    const int64_t Tps = Tp + 32, Rps = Rp + 32;   // slots per item-atom scale plane
     // dense GEMMs stream their weights once per token tile: a batch of up to
     // 64 tokens is one tile
     const int nmax_dense = (T <= 64) ? static_cast<int>(rup(T, 16)) : pick_n_max(T, item_cap(T));
@@ -526,18 +528,18 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
     TRY(cudaMemsetAsync(p->sel, 0, sizeof(uint32_t) * E * W, s));
     mark(0);
     // 1. x -> MXFP8
-    TRY(launch_quant_x(static_cast<const __nv_bfloat16*>(x), T, D, p->xq, p->xsf, Tp, s));
+    TRY(launch_quant_x(static_cast<const __nv_bfloat16*>(x), T, D, p->xq, p->xsf, Tps, nmax_dense, s));
     mark(1);
     // 2. latent down-projection + shared gate/up
     {
-        GemmParams g = gemm_base(p->tA2, p->tB2, p->a2sf, p->xsf, Tp, D, nmax_dense, p->rowsA2, static_cast<int>(Tp),
+        GemmParams g = gemm_base(p->tA2, p->tB2, p->a2sf, p->xsf, Tps, D, nmax_dense, p->rowsA2, static_cast<int>(Tp),
                                  p->status);
         g.dense = 1;
         g.m_tiles = p->rowsA2 / kBlockM;
         g.n_tokens = T;
         g.epi_split = L / kBlockM;
         g.epi[0] = EpiParams{EPI_QUANT, 0, 0, L, p->z, 2 * L, p->zq, L, p->zsf, Tp};
-        g.epi[1] = EpiParams{EPI_SILU_QUANT, L / kBlockM, L, 0, nullptr, 0, p->act, p->Kcat, p->actsf, Tp};
+        g.epi[1] = EpiParams{EPI_SILU_QUANT, L / kBlockM, L, 0, nullptr, 0, p->act, p->Kcat, p->actsf, Tps, 1};
         const int items = g.m_tiles * ((T + g.n_max - 1) / g.n_max);
         shape_gemm(g, 0, items, std::min(items, p->num_sms));
         TRY(launch_gemm(g, std::min(items, p->num_sms), s));
@@ -625,13 +627,14 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
         a.L = L;
         a.zq_perm = p->zqp;
         a.zq_perm_sf = p->zqpsf;
-        a.perm_pitch = Rp;
+        a.perm_pitch = Rps;
+        a.n_max = nmax_grp;
         TRY(launch_scatter(a, s));
     }
     // 8. routed gate/up + SiLU -> MXFP8
     mark(7);
     {
-        GemmParams g = gemm_base(p->tA7, p->tB7, p->w13sf, p->zqpsf, Rp, L, nmax_grp, E * 2 * I,
+        GemmParams g = gemm_base(p->tA7, p->tB7, p->w13sf, p->zqpsf, Rps, L, nmax_grp, E * 2 * I,
                                  static_cast<int>(Rp), p->status);
         g.dense = 0;
         g.ioff = p->ioff7;
@@ -641,13 +644,13 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
         g.mt_per_e = 2 * I / kBlockM;
         g.rows_per_e = 2 * I;
         shape_gemm(g, E, est_experts * g.mt_per_e, p->num_sms);
-        g.epi[0] = EpiParams{EPI_SILU_QUANT, 0, 0, 0, nullptr, 0, p->hq, Ip, p->hqsf, Rp};
+        g.epi[0] = EpiParams{EPI_SILU_QUANT, 0, 0, 0, nullptr, 0, p->hq, Ip, p->hqsf, Rps, 1};
         TRY(launch_gemm(g, p->num_sms, s));
     }
     // 9. routed down -> o
     mark(8);
     {
-        GemmParams g = gemm_base(p->tA8, p->tB8, p->w2sf, p->hqsf, Rp, Ip, nmax_grp, E * L, static_cast<int>(Rp),
+        GemmParams g = gemm_base(p->tA8, p->tB8, p->w2sf, p->hqsf, Rps, Ip, nmax_grp, E * L, static_cast<int>(Rp),
                                  p->status);
         g.dense = 0;
         g.ioff = p->ioff8;
@@ -662,11 +665,11 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
     }
     // 10. weighted combine -> MXFP8 into columns [0, L) of the concatenated activation
     mark(9);
-    TRY(launch_combine(p->o, p->slot_pos, p->gw, T, k, L, p->act, p->Kcat, p->actsf, Tp, s));
+    TRY(launch_combine(p->o, p->slot_pos, p->gw, T, k, L, p->act, p->Kcat, p->actsf, Tps, nmax_dense, s));
     // 11. y = [cq | h_sq] [P_up | S_down]^T
     mark(10);
     {
-        GemmParams g = gemm_base(p->tA10, p->tB10, p->a10sf, p->actsf, Tp, p->Kcat, nmax_dense, D,
+        GemmParams g = gemm_base(p->tA10, p->tB10, p->a10sf, p->actsf, Tps, p->Kcat, nmax_dense, D,
                                  static_cast<int>(Tp), p->status);
         g.dense = 1;
         g.m_tiles = D / kBlockM;
@@ -683,13 +686,14 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
         const int S = p->S, SIs = p->SIs;
         const int64_t TK = static_cast<int64_t>(T) * k;
         if (dbg->xq) TRY(cudaMemcpyAsync(dbg->xq, p->xq, static_cast<size_t>(T) * D, cudaMemcpyDeviceToDevice, s));
-        if (dbg->xs) TRY(launch_export_sf(p->xsf, Tp, nullptr, T, D / 32, 0, dbg->xs, s));
+        if (dbg->xs) TRY(launch_export_sf(p->xsf, Tps, nullptr, T, D / 32, 0, dbg->xs, nmax_dense, nullptr, 0, s));
         if (dbg->z) TRY(launch_add_halves(p->z, T, L, dbg->z, s));
         if (dbg->zq) TRY(cudaMemcpyAsync(dbg->zq, p->zq, static_cast<size_t>(T) * L, cudaMemcpyDeviceToDevice, s));
-        if (dbg->zs) TRY(launch_export_sf(p->zsf, Tp, nullptr, T, L / 32, 0, dbg->zs, s));
+        if (dbg->zs) TRY(launch_export_sf(p->zsf, Tp, nullptr, T, L / 32, 0, dbg->zs, 0, nullptr, 0, s));
         if (S > 0 && dbg->hsq)
             TRY(cudaMemcpy2DAsync(dbg->hsq, SIs, p->act + L, p->Kcat, SIs, T, cudaMemcpyDeviceToDevice, s));
-        if (S > 0 && dbg->hss) TRY(launch_export_sf(p->actsf, Tp, nullptr, T, SIs / 32, L / 32, dbg->hss, s));
+        if (S > 0 && dbg->hss)
+            TRY(launch_export_sf(p->actsf, Tps, nullptr, T, SIs / 32, L / 32, dbg->hss, nmax_dense, nullptr, 0, s));
         if (dbg->logits)
             TRY(cudaMemcpyAsync(dbg->logits, p->logits, sizeof(float) * T * E, cudaMemcpyDeviceToDevice, s));
         if (dbg->topk_idx) TRY(cudaMemcpyAsync(dbg->topk_idx, p->idx, sizeof(int32_t) * TK, cudaMemcpyDeviceToDevice, s));
@@ -700,12 +704,13 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
         if (dbg->sorted_token)
             TRY(cudaMemcpyAsync(dbg->sorted_token, p->sorted_token, sizeof(int32_t) * TK, cudaMemcpyDeviceToDevice, s));
         if (dbg->hq) TRY(launch_gather_rows(p->hq, Ip, p->canon_to_pad, TK, I, dbg->hq, I, s));
-        if (dbg->hqs) TRY(launch_export_sf(p->hqsf, Rp, p->canon_to_pad, TK, I / 32, 0, dbg->hqs, s));
+        if (dbg->hqs)
+            TRY(launch_export_sf(p->hqsf, Rps, p->canon_to_pad, TK, I / 32, 0, dbg->hqs, nmax_grp, p->seg, E, s));
         if (dbg->o)
             TRY(launch_gather_rows(reinterpret_cast<const uint8_t*>(p->o), sizeof(float) * L, p->canon_to_pad, TK,
                                    sizeof(float) * L, reinterpret_cast<uint8_t*>(dbg->o), sizeof(float) * L, s));
         if (dbg->cq) TRY(cudaMemcpy2DAsync(dbg->cq, L, p->act, p->Kcat, L, T, cudaMemcpyDeviceToDevice, s));
-        if (dbg->cs) TRY(launch_export_sf(p->actsf, Tp, nullptr, T, L / 32, 0, dbg->cs, s));
+        if (dbg->cs) TRY(launch_export_sf(p->actsf, Tps, nullptr, T, L / 32, 0, dbg->cs, nmax_dense, nullptr, 0, s));
     }
 #undef TRY
     return cuda_status(err);
@@ -768,7 +773,7 @@ moe_status moe_mx_gemm(const uint8_t* a_codes, const uint8_t* a_scales, int32_t 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t Np = rup(N, 16);
     const size_t atom_bytes = static_cast<size_t>(M) * K / 32;
-    const size_t plane_bytes = static_cast<size_t>(K / 128) * Np * 4;
+    const size_t plane_bytes = static_cast<size_t>(K / 128) * (Np + 32) * 16;    // item-atom planes
     CUtensorMap tA, tB;
     if (!map_mx4(&tA, a_codes, M, K) || !map_mx8(&tB, b_codes, N, K)) return MOE_ERR_INVALID_ARG;
     uint8_t* scratch = nullptr;
@@ -779,10 +784,10 @@ moe_status moe_mx_gemm(const uint8_t* a_codes, const uint8_t* a_scales, int32_t 
     int32_t* st = dev_status ? dev_status : reinterpret_cast<int32_t*>(scratch + atom_bytes + plane_bytes);
     err = cudaMemsetAsync(planes, 0, plane_bytes + 256, s);
     if (err == cudaSuccess) err = launch_sf_atoms(a_scales, M, K / 32, atoms, s);
-    if (err == cudaSuccess) err = launch_sf_planes(b_scales, N, K / 32, planes, Np, s);
+    const int nmax = pick_n_max(N, item_cap(N));
+    if (err == cudaSuccess) err = launch_sf_item_planes(b_scales, N, K / 32, planes, Np + 32, nmax, s);
     if (err == cudaSuccess) {
-        const int nmax = pick_n_max(N, item_cap(N));
-        GemmParams g = gemm_base(tA, tB, atoms, planes, Np, K, nmax, M, static_cast<int>(Np), st);
+        GemmParams g = gemm_base(tA, tB, atoms, planes, Np + 32, K, nmax, M, static_cast<int>(Np), st);
         g.dense = 1;
         g.m_tiles = M / kBlockM;
         g.n_tokens = N;
@@ -839,7 +844,7 @@ extern "C" moe_status moe_mx_gemm_noalloc(const uint8_t* a_codes, const uint8_t*
         return MOE_ERR_INVALID_ARG;
     const int64_t Np = rup(N, 16);
     const size_t atom_bytes = static_cast<size_t>(M) * K / 32;
-    const size_t plane_bytes = static_cast<size_t>(K / 128) * Np * 4;
+    const size_t plane_bytes = static_cast<size_t>(K / 128) * (Np + 32) * 16;    // item-atom planes
     if (atom_bytes + plane_bytes + 256 > MOE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_INVALID_ARG;
     if (!encode_fn()) return MOE_ERR_UNSUPPORTED;
     int dev = 0, sms = 0;
@@ -859,10 +864,10 @@ extern "C" moe_status moe_mx_gemm_noalloc(const uint8_t* a_codes, const uint8_t*
     // (their padding rows) and the internal status word
     err = cudaMemsetAsync(planes, 0, plane_bytes + 256, s);
     if (err == cudaSuccess) err = launch_sf_atoms(a_scales, M, K / 32, atoms, s);
-    if (err == cudaSuccess) err = launch_sf_planes(b_scales, N, K / 32, planes, Np, s);
+    const int nmax = pick_n_max(N, item_cap(N));
+    if (err == cudaSuccess) err = launch_sf_item_planes(b_scales, N, K / 32, planes, Np + 32, nmax, s);
     if (err == cudaSuccess) {
-        const int nmax = pick_n_max(N, item_cap(N));
-        GemmParams g = gemm_base(tA, tB, atoms, planes, Np, K, nmax, M, static_cast<int>(Np), st);
+        GemmParams g = gemm_base(tA, tB, atoms, planes, Np + 32, K, nmax, M, static_cast<int>(Np), st);
         g.dense = 1;
         g.m_tiles = M / kBlockM;
         g.n_tokens = N;

@@ -106,6 +106,7 @@ __device__ __forceinline__ void pin_epi(EpiParams& e) {
     e.ld_q = pin(e.ld_q);
     e.out_sf = pin(e.out_sf);
     e.sf_pitch = pin(e.sf_pitch);
+    e.sf_item = pin(e.sf_item);
 }
 
 // Item `it`.  Grouped items come from the per-expert tables staged in shared
@@ -152,15 +153,16 @@ __device__ __forceinline__ Item get_item(const Hot& h, int it, const int* ioff, 
 }
 
 struct SmemLayout {
-    int offB, offSFA, offSFBatom, offSFBraw;
+    int offB, offSFA, offSFB;
 };
 
+// One stage: A tile, B rows, then the scale atoms of A (512 B) and of B
+// (512 B per started 128 tokens), both copied as they sit in global memory.
 __host__ __device__ __forceinline__ SmemLayout stage_layout(int n_max) {
     SmemLayout l;
     l.offB = kABytes;
     l.offSFA = l.offB + n_max * kBlockK;
-    l.offSFBatom = l.offSFA + 512;
-    l.offSFBraw = l.offSFBatom + ((n_max + 127) / 128) * 512;
+    l.offSFB = l.offSFA + 512;
     return l;
 }
 
@@ -316,7 +318,8 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                 continue;
             }
             const int nm = (w.n + 15) & ~15;
-            const uint32_t tx = kMX ? static_cast<uint32_t>(h.a_tx_bytes + (nm / 16) * 2048 + 512 + nm * 4)
+            const int natoms = (nm + 127) / 128;
+            const uint32_t tx = kMX ? static_cast<uint32_t>(h.a_tx_bytes + (nm / 16) * 2048 + 512 + natoms * 512)
                                     : static_cast<uint32_t>(kBlockM * 128 + (nm / 16) * 2048);
             const uint8_t* sfa_tile = kMX ? h.sfa + static_cast<size_t>(w.a_row0 / kBlockM) * h.KT * 512 : nullptr;
             for (int kt = kb; kt < ke; ++kt) {
@@ -337,8 +340,8 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                         tma_load_2d(sb + L.offB + c * 2048, &p.tmB, &fullg[stage], bx, w.b_row0 + c * 16);
                     if constexpr (kMX) {
                         bulk_load(sb + L.offSFA, sfa_tile + static_cast<size_t>(kt) * 512, 512, &fullg[stage]);
-                        bulk_load(sb + L.offSFBraw, h.sfb + (static_cast<size_t>(kt) * h.sfb_pitch + w.b_row0) * 4,
-                                  static_cast<uint32_t>(nm * 4), &fullg[stage]);
+                        bulk_load(sb + L.offSFB, h.sfb + (static_cast<size_t>(kt) * h.sfb_pitch + w.b_row0) * 16,
+                                  static_cast<uint32_t>(natoms * 512), &fullg[stage]);
                     }
                 }
                 __syncwarp();
@@ -399,28 +402,14 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                             tc_commit(&emptyg[stage]);
                         }
                     } else {
-                        // B scales arrive as one uint32 per token row (4 bytes = the 4
-                        // K-blocks of this tile).  The 32x128b copy wants 32 rows of
-                        // 16 bytes where row i holds tokens i, i+32, i+64, i+96.
-                        const uint32_t* raw = reinterpret_cast<const uint32_t*>(sb + L.offSFBraw);
-                        for (int a = 0; a < natoms; ++a) {
-                            const int r0 = a * 128 + lane;
-                            uint4 v;
-                            v.x = (r0 < nm) ? raw[r0] : 0u;
-                            v.y = (r0 + 32 < nm) ? raw[r0 + 32] : 0u;
-                            v.z = (r0 + 64 < nm) ? raw[r0 + 64] : 0u;
-                            v.w = (r0 + 96 < nm) ? raw[r0 + 96] : 0u;
-                            *reinterpret_cast<uint4*>(sb + L.offSFBatom + a * 512 + lane * 16) = v;
-                        }
-                        fence_proxy_async_smem();
-                        __syncwarp();
+                        // both scale operands arrive as 32x128b copy images
                         const uint32_t sfa_col = sf_base + static_cast<uint32_t>(kt & 1) * 12u;
                         const uint32_t sfb_col = sfa_col + 4u;
                         const uint32_t idesc0 = idesc_mxf8f6f4(kBlockM, nm, 5, 0, 0, 0);
                         if (elect_one()) {
                             tc_cp_32x128b_x4(sfa_col, sdesc_rows16(smem_u32(sb + L.offSFA)));
                             for (int a = 0; a < natoms; ++a)
-                                tc_cp_32x128b_x4(sfb_col + 4u * a, sdesc_rows16(smem_u32(sb + L.offSFBatom + a * 512)));
+                                tc_cp_32x128b_x4(sfb_col + 4u * a, sdesc_rows16(smem_u32(sb + L.offSFB + a * 512)));
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
                                 // scale-factor ids (byte j of each 32-bit scale column) sit
@@ -510,6 +499,7 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
             E.ld_q = second ? E1.ld_q : E0.ld_q;
             E.out_sf = second ? E1.out_sf : E0.out_sf;
             E.sf_pitch = second ? E1.sf_pitch : E0.sf_pitch;
+            E.sf_item = second ? E1.sf_item : E0.sf_item;
             const int rel_mt = w.mt - E.m_tile0;
             for (int n0 = 0; n0 < nm; n0 += 16) {
                 // sum of the K-split partial accumulators, in group order
@@ -546,7 +536,9 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                             const uint8_t code = warp_mx8_quant(hv, &sc);
                             const int64_t row = w.b_row0 + n0 + i;
                             E.out_q[row * E.ld_q + col] = code;
-                            if (lane == 0) E.out_sf[sf_byte_offset(row, col, E.sf_pitch)] = sc;
+                            if (lane == 0)
+                                E.out_sf[E.sf_item ? sf_atom_offset(w.b_row0, n0 + i, col, E.sf_pitch)
+                                                   : sf_byte_offset(row, col, E.sf_pitch)] = sc;
                         }
                     }
                 } else {
@@ -590,7 +582,9 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                             uint8_t sc;
                             const uint8_t code = warp_mx8_quant(v[i], &sc);
                             E.out_q[row * E.ld_q + col] = code;
-                            if (lane == 0) E.out_sf[sf_byte_offset(row, col, E.sf_pitch)] = sc;
+                            if (lane == 0)
+                                E.out_sf[E.sf_item ? sf_atom_offset(w.b_row0, n0 + i, col, E.sf_pitch)
+                                                   : sf_byte_offset(row, col, E.sf_pitch)] = sc;
                         }
                     }
                 }
@@ -619,7 +613,7 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
 
 int gemm_stage_bytes(int n_max) {
     const SmemLayout l = stage_layout(n_max);
-    const int bytes = l.offSFBraw + ((n_max * 4 + 15) & ~15);
+    const int bytes = l.offSFB + ((n_max + 127) / 128) * 512;
     return (bytes + 1023) & ~1023;
 }
 

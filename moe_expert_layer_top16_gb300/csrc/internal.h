@@ -40,7 +40,8 @@ struct EpiParams {
     uint8_t* out_q;     // E4M3 codes [rows][ld_q]
     int64_t ld_q;
     uint8_t* out_sf;    // scale planes: uint32 word per (col/128, row), byte (col%128)/32
-    int64_t sf_pitch;   // rows per plane
+    int64_t sf_pitch;   // rows (raw planes) or 16-byte slots (item-atom planes) per plane
+    int sf_item;        // 1: item-atom planes keyed by the output item's first row; 0: raw planes
 };
 
 enum GemmKind : int {
@@ -52,7 +53,7 @@ struct GemmParams {
     CUtensorMap tmA;        // MX: MXFP4 weights, 16U4_ALIGN16B, box {128, 128}; TF32: fp32, box {32, 128}
     CUtensorMap tmB;        // MX: MXFP8 activations, UINT8, box {128, 16}; TF32: fp32, box {32, 16}
     const uint8_t* sfa;     // weight scales, pre-arranged: [rows/128][KT][512]
-    const uint8_t* sfb;     // activation scale planes: [KT][sfb_pitch] uint32
+    const uint8_t* sfb;     // activation scales, item-atom planes: [KT][sfb_pitch] 16-byte slots
     int64_t sfb_pitch;
     int KT;                 // 128-wide K tiles
     int n_max;              // tokens per work item (multiple of 16, <= kNMax)
@@ -94,7 +95,8 @@ cudaError_t gemm_setup();   // raise the dynamic shared memory limit once
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s);
 
 // ------------------------------------------------------------------ other kernels
-cudaError_t launch_quant_x(const __nv_bfloat16* x, int T, int D, uint8_t* xq, uint8_t* xsf, int64_t pitch,
+// xsf: item-atom planes of a dense GEMM with token tiles of n_max
+cudaError_t launch_quant_x(const __nv_bfloat16* x, int T, int D, uint8_t* xq, uint8_t* xsf, int64_t pitch, int n_max,
                            cudaStream_t s);
 // SIMT router on z = hi + lo ([T][2L]) writing logits [T][E]; batches of at
 // most kRouterSplitTokens tokens split K kRouterSplit ways over a cluster.
@@ -136,11 +138,13 @@ struct ScatterArgs {
     int32_t* canon_to_pad;    // [T*k] sorted (unpadded) position -> permuted row
     int32_t* sorted_token;    // [T*k] token of each sorted position
     const uint8_t* zq; const uint8_t* zsf; int64_t zsf_pitch; int L;
-    uint8_t* zq_perm; uint8_t* zq_perm_sf; int64_t perm_pitch;
+    uint8_t* zq_perm; uint8_t* zq_perm_sf; int64_t perm_pitch;   // zq_perm_sf: item-atom planes
+    int n_max;                // token tile of the grouped GEMM that reads zq_perm
 };
 cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s);
+// out_sf: item-atom planes of a dense GEMM with token tiles of n_max
 cudaError_t launch_combine(const float* o, const int32_t* slot_pos, const float* w, int T, int k, int L,
-                           uint8_t* out_q, int64_t ld_q, uint8_t* out_sf, int64_t sf_pitch, cudaStream_t s);
+                           uint8_t* out_q, int64_t ld_q, uint8_t* out_sf, int64_t sf_pitch, int n_max, cudaStream_t s);
 cudaError_t launch_mxfp4_encode(const float* w, int64_t rows, int64_t K, uint8_t* codes, uint8_t* scales,
                                 cudaStream_t s);
 cudaError_t kernels_setup();   // per-device kernel attributes
@@ -148,16 +152,20 @@ cudaError_t kernels_setup();   // per-device kernel attributes
 cudaError_t launch_tf32_split(const float* src, int64_t rows, int64_t K, float* dst, cudaStream_t s);
 // [rows][2K] (hi | lo) -> [rows][K] = hi + lo
 cudaError_t launch_add_halves(const float* src, int64_t rows, int64_t K, float* dst, cudaStream_t s);
-// row-major scales [rows][kb] -> scale planes [kb/4][pitch] (uint32 words)
-cudaError_t launch_sf_planes(const uint8_t* scales_rm, int64_t rows, int64_t kb, uint8_t* planes, int64_t pitch,
-                             cudaStream_t s);
+// row-major scales [rows][kb] -> item-atom planes [kb/4][pitch] of a dense
+// GEMM with token tiles of n_max
+cudaError_t launch_sf_item_planes(const uint8_t* scales_rm, int64_t rows, int64_t kb, uint8_t* planes, int64_t pitch,
+                                  int n_max, cudaStream_t s);
 // plan-time repacking
 cudaError_t launch_copy_rows(uint8_t* dst, int64_t dst_stride, const uint8_t* const* src_rows, int64_t nrows,
                              int64_t row_bytes, cudaStream_t s);
 cudaError_t launch_sf_atoms(const uint8_t* scales_rm, int64_t rows, int64_t kb, uint8_t* atoms, cudaStream_t s);
-// debug export
+// debug export of scales to [rows][nblocks] bytes: raw planes (item_n == 0)
+// or item-atom planes of token tiles of item_n (dense when seg is null, else
+// tiles within the expert segments seg[0..E])
 cudaError_t launch_export_sf(const uint8_t* planes, int64_t pitch, const int32_t* row_map, int64_t rows,
-                             int64_t nblocks, int64_t col_block0, uint8_t* out, cudaStream_t s);
+                             int64_t nblocks, int64_t col_block0, uint8_t* out, int item_n, const int32_t* seg, int E,
+                             cudaStream_t s);
 cudaError_t launch_gather_rows(const uint8_t* src, int64_t src_stride, const int32_t* row_map, int64_t rows,
                                int64_t row_bytes, uint8_t* dst, int64_t dst_stride, cudaStream_t s);
 

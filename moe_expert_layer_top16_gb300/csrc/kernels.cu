@@ -18,9 +18,10 @@ __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b -
 
 // ------------------------------------------------------------------ A1: x -> MXFP8
 // One warp per (row, 128-wide column tile); lane l owns elements 4l..4l+3, so
-// 8 lanes form one 32-element block.  Scale planes as in mx.cuh.
+// 8 lanes form one 32-element block.  Scales go to the item-atom planes of
+// the GEMM that reads xq (token tiles of n_max rows; mx.cuh).
 __global__ void quant_x_kernel(const __nv_bfloat16* __restrict__ x, int T, int D, uint8_t* __restrict__ xq,
-                               uint32_t* __restrict__ xsf, int64_t pitch) {
+                               uint8_t* __restrict__ xsf, int64_t pitch, int n_max) {
     const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     const int tiles = D / 128;
@@ -48,7 +49,10 @@ __global__ void quant_x_kernel(const __nv_bfloat16* __restrict__ x, int T, int D
     uint32_t word = 0;
 #pragma unroll
     for (int b = 0; b < 4; ++b) word |= __shfl_sync(0xffffffffu, sc, b * 8) << (8 * b);
-    if (lane == 0) xsf[tile * pitch + row] = word;
+    if (lane == 0) {
+        const int64_t b0 = (row / n_max) * n_max;
+        *reinterpret_cast<uint32_t*>(xsf + sf_atom_offset(b0, static_cast<int>(row - b0), tile * 128, pitch)) = word;
+    }
 }
 
 // ------------------------------------------------------------------ A3: router logits
@@ -551,9 +555,13 @@ __global__ void scatter_kernel(ScatterArgs a) {
     const uint4* src = reinterpret_cast<const uint4*>(a.zq + static_cast<int64_t>(t) * a.L);
     uint4* dst = reinterpret_cast<uint4*>(a.zq_perm + static_cast<int64_t>(pos) * a.L);
     for (int i = lane; i < a.L / 16; i += 32) dst[i] = src[i];
+    // scales: raw planes in, item-atom planes of the grouped GEMM's token tile out
     const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(a.zsf);
-    uint32_t* sdst = reinterpret_cast<uint32_t*>(a.zq_perm_sf);
-    for (int kt = lane; kt < a.L / 128; kt += 32) sdst[kt * a.perm_pitch + pos] = ssrc[kt * a.zsf_pitch + t];
+    const int64_t b0 = a.seg[e] + (rank / a.n_max) * a.n_max;
+    const int l = rank % a.n_max;
+    for (int kt = lane; kt < a.L / 128; kt += 32)
+        *reinterpret_cast<uint32_t*>(a.zq_perm_sf + sf_atom_offset(b0, l, static_cast<int64_t>(kt) * 128, a.perm_pitch)) =
+            ssrc[kt * a.zsf_pitch + t];
 }
 
 // ------------------------------------------------------------------ A9: combine + MXFP8
@@ -563,7 +571,7 @@ __global__ void scatter_kernel(ScatterArgs a) {
 constexpr int kCombineWarps = 8;
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(
     const float* __restrict__ o, const int32_t* __restrict__ slot_pos, const float* __restrict__ w, int T, int k,
-    int L, uint8_t* __restrict__ out_q, int64_t ld_q, uint8_t* __restrict__ out_sf, int64_t sf_pitch) {
+    int L, uint8_t* __restrict__ out_q, int64_t ld_q, uint8_t* __restrict__ out_sf, int64_t sf_pitch, int n_max) {
     const int t = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __shared__ int pos_s[32];
@@ -581,7 +589,10 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(
     uint8_t sc;
     const uint8_t code = warp_mx8_quant(acc, &sc);
     out_q[static_cast<int64_t>(t) * ld_q + col] = code;
-    if (lane == 0) out_sf[sf_byte_offset(t, col, sf_pitch)] = sc;
+    if (lane == 0) {
+        const int b0 = (t / n_max) * n_max;
+        out_sf[sf_atom_offset(b0, t - b0, col, sf_pitch)] = sc;
+    }
 }
 
 // ------------------------------------------------------------------ MXFP4 weight encoder
@@ -667,12 +678,13 @@ __global__ void sf_atoms_kernel(const uint8_t* __restrict__ rm, int64_t rows, in
     atoms[(rb * KT + kt) * 512 + (rr % 32) * 16 + (rr / 32) * 4 + j] = rm[i];
 }
 
-__global__ void sf_planes_kernel(const uint8_t* __restrict__ rm, int64_t rows, int64_t kb, uint8_t* __restrict__ planes,
-                                 int64_t pitch) {
+__global__ void sf_item_planes_kernel(const uint8_t* __restrict__ rm, int64_t rows, int64_t kb,
+                                      uint8_t* __restrict__ planes, int64_t pitch, int n_max) {
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= rows * kb) return;
     const int64_t row = i / kb, b = i % kb;
-    planes[((b / 4) * pitch + row) * 4 + (b % 4)] = rm[i];
+    const int64_t b0 = (row / n_max) * n_max;
+    planes[sf_atom_offset(b0, static_cast<int>(row - b0), b * 32, pitch)] = rm[i];
 }
 
 // [rows][K] fp32 -> [rows][2K]: nearest TF32 value, then the exact remainder.
@@ -698,13 +710,29 @@ __global__ void add_halves_kernel(const float* __restrict__ src, int64_t rows, i
 
 // ------------------------------------------------------------------ debug export
 __global__ void export_sf_kernel(const uint8_t* __restrict__ planes, int64_t pitch, const int32_t* __restrict__ row_map,
-                                 int64_t rows, int64_t nblocks, int64_t col_block0, uint8_t* __restrict__ out) {
+                                 int64_t rows, int64_t nblocks, int64_t col_block0, uint8_t* __restrict__ out,
+                                 int item_n, const int32_t* __restrict__ seg, int E) {
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= rows * nblocks) return;
     const int64_t r = i / nblocks, b = i % nblocks;
     const int64_t src_row = row_map ? row_map[r] : r;
     const int64_t cb = col_block0 + b;
-    out[i] = planes[((cb / 4) * pitch + src_row) * 4 + (cb % 4)];
+    if (item_n == 0) {
+        out[i] = planes[((cb / 4) * pitch + src_row) * 4 + (cb % 4)];
+        return;
+    }
+    int64_t base = 0;                                   // first row of the segment holding src_row
+    if (seg) {
+        int lo = 0, hi = E - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (seg[mid] <= src_row) lo = mid;
+            else hi = mid - 1;
+        }
+        base = seg[lo];
+    }
+    const int64_t b0 = base + ((src_row - base) / item_n) * item_n;
+    out[i] = planes[sf_atom_offset(b0, static_cast<int>(src_row - b0), cb * 32, pitch)];
 }
 
 __global__ void gather_rows_kernel(const uint8_t* __restrict__ src, int64_t src_stride, const int32_t* __restrict__ row_map,
@@ -718,11 +746,12 @@ __global__ void gather_rows_kernel(const uint8_t* __restrict__ src, int64_t src_
 
 }  // namespace
 
-cudaError_t launch_quant_x(const __nv_bfloat16* x, int T, int D, uint8_t* xq, uint8_t* xsf, int64_t pitch,
+cudaError_t launch_quant_x(const __nv_bfloat16* x, int T, int D, uint8_t* xq, uint8_t* xsf, int64_t pitch, int n_max,
                            cudaStream_t s) {
+    if (n_max <= 0) return cudaErrorInvalidValue;
     const int64_t warps = static_cast<int64_t>(T) * (D / 128);
     const int blocks = static_cast<int>((warps * 32 + 255) / 256);
-    quant_x_kernel<<<blocks, 256, 0, s>>>(x, T, D, xq, reinterpret_cast<uint32_t*>(xsf), pitch);
+    quant_x_kernel<<<blocks, 256, 0, s>>>(x, T, D, xq, xsf, pitch, n_max);
     return cudaGetLastError();
 }
 
@@ -764,9 +793,10 @@ cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_combine(const float* o, const int32_t* slot_pos, const float* w, int T, int k, int L,
-                           uint8_t* out_q, int64_t ld_q, uint8_t* out_sf, int64_t sf_pitch, cudaStream_t s) {
+                           uint8_t* out_q, int64_t ld_q, uint8_t* out_sf, int64_t sf_pitch, int n_max, cudaStream_t s) {
+    if (n_max <= 0) return cudaErrorInvalidValue;
     dim3 grid(T, (L / 32 + kCombineWarps - 1) / kCombineWarps);
-    combine_kernel<<<grid, kCombineWarps * 32, 0, s>>>(o, slot_pos, w, T, k, L, out_q, ld_q, out_sf, sf_pitch);
+    combine_kernel<<<grid, kCombineWarps * 32, 0, s>>>(o, slot_pos, w, T, k, L, out_q, ld_q, out_sf, sf_pitch, n_max);
     return cudaGetLastError();
 }
 
@@ -807,20 +837,23 @@ cudaError_t launch_add_halves(const float* src, int64_t rows, int64_t K, float* 
     return cudaGetLastError();
 }
 
-cudaError_t launch_sf_planes(const uint8_t* scales_rm, int64_t rows, int64_t kb, uint8_t* planes, int64_t pitch,
-                             cudaStream_t s) {
+cudaError_t launch_sf_item_planes(const uint8_t* scales_rm, int64_t rows, int64_t kb, uint8_t* planes, int64_t pitch,
+                                  int n_max, cudaStream_t s) {
     const int64_t n = rows * kb;
     if (n == 0) return cudaSuccess;
-    sf_planes_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(scales_rm, rows, kb, planes, pitch);
+    if (n_max <= 0) return cudaErrorInvalidValue;
+    sf_item_planes_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(scales_rm, rows, kb, planes, pitch,
+                                                                                 n_max);
     return cudaGetLastError();
 }
 
 cudaError_t launch_export_sf(const uint8_t* planes, int64_t pitch, const int32_t* row_map, int64_t rows,
-                             int64_t nblocks, int64_t col_block0, uint8_t* out, cudaStream_t s) {
+                             int64_t nblocks, int64_t col_block0, uint8_t* out, int item_n, const int32_t* seg, int E,
+                             cudaStream_t s) {
     const int64_t n = rows * nblocks;
     if (n == 0) return cudaSuccess;
     export_sf_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(planes, pitch, row_map, rows, nblocks,
-                                                                          col_block0, out);
+                                                                          col_block0, out, item_n, seg, E);
     return cudaGetLastError();
 }
 

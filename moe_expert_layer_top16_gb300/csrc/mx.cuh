@@ -54,4 +54,16 @@ __device__ __forceinline__ int64_t sf_byte_offset(int64_t row, int64_t col, int6
     return ((col >> 7) * pitch + row) * 4 + ((col & 127) >> 5);
 }
 
+// Item-atom scale planes (a GEMM's token-operand scales): per 128-wide K tile
+// a plane of `pitch` 16-byte slots.  The tokens of a GEMM work item that
+// starts at row b0 are placed so that the bytes from slot b0 on are the image
+// of the 32x128b tensor-memory copy: token l of the item (row b0 + l), K-block
+// (col % 128) / 32, lives in slot b0 + 32 * (l / 128) + l % 32, at byte
+// 4 * ((l / 32) % 4) + K-block of that slot.  An item of n <= 240 tokens uses
+// only slots of its own rows; planes carry 32 spare slots so that the copy of
+// a short item's atom stays inside the plane.
+__host__ __device__ __forceinline__ int64_t sf_atom_offset(int64_t b0, int l, int64_t col, int64_t pitch) {
+    return ((col >> 7) * pitch + b0 + 32 * (l >> 7) + (l & 31)) * 16 + ((l >> 5) & 3) * 4 + ((col & 127) >> 5);
+}
+
 }  // namespace moe
