@@ -84,12 +84,12 @@ bool map_f32(CUtensorMap* m, const void* base, int64_t rows, int64_t K, uint32_t
 }
 
 // MXFP8 activation codes [rows][K], 128-wide x 16-row boxes.
-bool map_mx8(CUtensorMap* m, const void* codes, int64_t rows, int64_t K) {
+bool map_mx8(CUtensorMap* m, const void* codes, int64_t rows, int64_t K, int box_rows = 16) {
     EncodeTiledFn f = encode_fn();
     if (!f) return false;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
-    cuuint32_t box[2] = {128, 16};
+    cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
     cuuint32_t es[2] = {1, 1};
     return f(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(codes), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -124,6 +124,10 @@ struct Plan {
     void* x_stage;
     float* y_stage;
     CUtensorMap tA2, tB2, tA7, tB7, tA8, tB8, tA10, tB10, tAR, tBR;
+    // B maps with one box per wide work item (box height = that n_max),
+    // re-encoded when a forward needs another height
+    CUtensorMap tB2w, tB10w, tB7w, tB8w;
+    int wide_dense = 0, wide_grp = 0;
     bool tc_router;    // router logits on the tensor cores (3xTF32) for batches above 128 tokens
 };
 
@@ -231,6 +235,7 @@ GemmParams gemm_base(const CUtensorMap& A, const CUtensorMap& B, const uint8_t* 
     g.a_tx_bytes = MOE_A_TX_BYTES;
     g.kind = KIND_MX;
     g.kseg_tiles = g.KT;
+    g.b_box = 16;
     g.a_rows = a_rows;
     g.b_rows = b_rows;
     g.status = status;
@@ -516,6 +521,20 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
     const int nmax_grp = static_cast<int>(std::min<int64_t>(item_cap(T), rup(T, 16)));
     // experts expected to receive tokens (all of them once T * k >> E)
     const int64_t est_experts = std::min<int64_t>(E, static_cast<int64_t>(T) * k);
+    // wide items load their token rows with one TMA box (height n_max)
+    const bool wide_d = nmax_dense > 64, wide_g = nmax_grp > 64;
+    if (wide_d && p->wide_dense != nmax_dense) {
+        p->wide_dense = 0;
+        if (!map_mx8(&p->tB2w, p->xq, Tp, D, nmax_dense) || !map_mx8(&p->tB10w, p->act, Tp, p->Kcat, nmax_dense))
+            return MOE_ERR_CUDA;
+        p->wide_dense = nmax_dense;
+    }
+    if (wide_g && p->wide_grp != nmax_grp) {
+        p->wide_grp = 0;
+        if (!map_mx8(&p->tB7w, p->zqp, Rp, L, nmax_grp) || !map_mx8(&p->tB8w, p->hq, Rp, Ip, nmax_grp))
+            return MOE_ERR_CUDA;
+        p->wide_grp = nmax_grp;
+    }
     cudaError_t err = cudaSuccess;
 #define TRY(x)                          \
     do {                                \
@@ -534,6 +553,10 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
     {
         GemmParams g = gemm_base(p->tA2, p->tB2, p->a2sf, p->xsf, Tps, D, nmax_dense, p->rowsA2, static_cast<int>(Tp),
                                  p->status);
+        if (wide_d) {
+            g.tmB = p->tB2w;
+            g.b_box = nmax_dense;
+        }
         g.dense = 1;
         g.m_tiles = p->rowsA2 / kBlockM;
         g.n_tokens = T;
@@ -636,6 +659,10 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
     {
         GemmParams g = gemm_base(p->tA7, p->tB7, p->w13sf, p->zqpsf, Rps, L, nmax_grp, E * 2 * I,
                                  static_cast<int>(Rp), p->status);
+        if (wide_g) {
+            g.tmB = p->tB7w;
+            g.b_box = nmax_grp;
+        }
         g.dense = 0;
         g.ioff = p->ioff7;
         g.seg = p->seg;
@@ -652,6 +679,10 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
     {
         GemmParams g = gemm_base(p->tA8, p->tB8, p->w2sf, p->hqsf, Rps, Ip, nmax_grp, E * L, static_cast<int>(Rp),
                                  p->status);
+        if (wide_g) {
+            g.tmB = p->tB8w;
+            g.b_box = nmax_grp;
+        }
         g.dense = 0;
         g.ioff = p->ioff8;
         g.seg = p->seg;
@@ -671,6 +702,10 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
     {
         GemmParams g = gemm_base(p->tA10, p->tB10, p->a10sf, p->actsf, Tps, p->Kcat, nmax_dense, D,
                                  static_cast<int>(Tp), p->status);
+        if (wide_d) {
+            g.tmB = p->tB10w;
+            g.b_box = nmax_dense;
+        }
         g.dense = 1;
         g.m_tiles = D / kBlockM;
         g.n_tokens = T;
@@ -775,7 +810,8 @@ moe_status moe_mx_gemm(const uint8_t* a_codes, const uint8_t* a_scales, int32_t 
     const size_t atom_bytes = static_cast<size_t>(M) * K / 32;
     const size_t plane_bytes = static_cast<size_t>(K / 128) * (Np + 32) * 16;    // item-atom planes
     CUtensorMap tA, tB;
-    if (!map_mx4(&tA, a_codes, M, K) || !map_mx8(&tB, b_codes, N, K)) return MOE_ERR_INVALID_ARG;
+    const int box_rows = pick_n_max(N, item_cap(N)) > 64 ? pick_n_max(N, item_cap(N)) : 16;
+    if (!map_mx4(&tA, a_codes, M, K) || !map_mx8(&tB, b_codes, N, K, box_rows)) return MOE_ERR_INVALID_ARG;
     uint8_t* scratch = nullptr;
     err = cudaMallocAsync(reinterpret_cast<void**>(&scratch), atom_bytes + plane_bytes + 256, s);
     if (err != cudaSuccess) return cuda_status(err);
@@ -788,6 +824,7 @@ moe_status moe_mx_gemm(const uint8_t* a_codes, const uint8_t* a_scales, int32_t 
     if (err == cudaSuccess) err = launch_sf_item_planes(b_scales, N, K / 32, planes, Np + 32, nmax, s);
     if (err == cudaSuccess) {
         GemmParams g = gemm_base(tA, tB, atoms, planes, Np + 32, K, nmax, M, static_cast<int>(Np), st);
+        if (nmax > 64) g.b_box = nmax;      // tB was encoded with one box per item
         g.dense = 1;
         g.m_tiles = M / kBlockM;
         g.n_tokens = N;
@@ -855,7 +892,8 @@ extern "C" moe_status moe_mx_gemm_noalloc(const uint8_t* a_codes, const uint8_t*
     if (err == cudaSuccess) err = noalloc_scratch(dev, &scratch);
     if (err != cudaSuccess) return cuda_status(err);
     CUtensorMap tA, tB;
-    if (!map_mx4(&tA, a_codes, M, K) || !map_mx8(&tB, b_codes, N, K)) return MOE_ERR_INVALID_ARG;
+    const int box_rows = pick_n_max(N, item_cap(N)) > 64 ? pick_n_max(N, item_cap(N)) : 16;
+    if (!map_mx4(&tA, a_codes, M, K) || !map_mx8(&tB, b_codes, N, K, box_rows)) return MOE_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* atoms = scratch;
     uint8_t* planes = scratch + atom_bytes;
@@ -868,6 +906,7 @@ extern "C" moe_status moe_mx_gemm_noalloc(const uint8_t* a_codes, const uint8_t*
     if (err == cudaSuccess) err = launch_sf_item_planes(b_scales, N, K / 32, planes, Np + 32, nmax, s);
     if (err == cudaSuccess) {
         GemmParams g = gemm_base(tA, tB, atoms, planes, Np + 32, K, nmax, M, static_cast<int>(Np), st);
+        if (nmax > 64) g.b_box = nmax;      // tB was encoded with one box per item
         g.dense = 1;
         g.m_tiles = M / kBlockM;
         g.n_tokens = N;

@@ -57,7 +57,7 @@ struct Item {
 // them from the parameter space would repeat after every asm statement that
 // clobbers memory).
 struct Hot {
-    int KT, n_max, stage_bytes, a_tx_bytes, kseg_tiles;
+    int KT, n_max, stage_bytes, a_tx_bytes, kseg_tiles, b_box;
     int dense, m_tiles, n_tokens, a_rows, b_rows, E, mt_per_e, rows_per_e, epi_split;
     int ax0, ax1, ax2, bx0, bx1, bx2;
     int64_t sfb_pitch;
@@ -73,6 +73,7 @@ __device__ __forceinline__ Hot load_hot(const GemmParams& p) {
     h.stage_bytes = pin(p.stage_bytes);
     h.a_tx_bytes = pin(p.a_tx_bytes);
     h.kseg_tiles = pin(p.kseg_tiles);
+    h.b_box = pin(p.b_box);
     h.dense = pin(p.dense);
     h.m_tiles = pin(p.m_tiles);
     h.n_tokens = pin(p.n_tokens);
@@ -319,8 +320,10 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
             }
             const int nm = (w.n + 15) & ~15;
             const int natoms = (nm + 127) / 128;
-            const uint32_t tx = kMX ? static_cast<uint32_t>(h.a_tx_bytes + (nm / 16) * 2048 + 512 + natoms * 512)
-                                    : static_cast<uint32_t>(kBlockM * 128 + (nm / 16) * 2048);
+            const int nbox = (nm + h.b_box - 1) / h.b_box;           // B boxes of b_box rows
+            const uint32_t b_bytes = static_cast<uint32_t>(nbox * h.b_box * kBlockK);
+            const uint32_t tx = kMX ? static_cast<uint32_t>(h.a_tx_bytes) + b_bytes + 512u + natoms * 512u
+                                    : static_cast<uint32_t>(kBlockM * 128) + b_bytes;
             const uint8_t* sfa_tile = kMX ? h.sfa + static_cast<size_t>(w.a_row0 / kBlockM) * h.KT * 512 : nullptr;
             for (int kt = kb; kt < ke; ++kt) {
                 ok = mbar_wait(&emptyg[stage], phase ^ 1, abort_flag, h.status, DEV_TIMEOUT_PRODUCER);
@@ -336,8 +339,9 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                 if (elect_one()) {
                     mbar_arrive_expect_tx(&fullg[stage], tx);
                     tma_load_2d(sb, &p.tmA, &fullg[stage], ax, w.a_row0);
-                    for (int c = 0; c < nm / 16; ++c)
-                        tma_load_2d(sb + L.offB + c * 2048, &p.tmB, &fullg[stage], bx, w.b_row0 + c * 16);
+                    for (int c = 0; c < nbox; ++c)
+                        tma_load_2d(sb + L.offB + c * h.b_box * kBlockK, &p.tmB, &fullg[stage], bx,
+                                    w.b_row0 + c * h.b_box);
                     if constexpr (kMX) {
                         bulk_load(sb + L.offSFA, sfa_tile + static_cast<size_t>(kt) * 512, 512, &fullg[stage]);
                         bulk_load(sb + L.offSFB, h.sfb + (static_cast<size_t>(kt) * h.sfb_pitch + w.b_row0) * 16,
@@ -671,6 +675,7 @@ cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s) {
     const size_t smem = gemm_smem_bytes(p.n_max, p.groups, p.stages, p.dense ? 0 : p.E);
     if (smem > static_cast<size_t>(kSmemLimit)) return cudaErrorInvalidValue;
     if (p.kseg_tiles <= 0 || p.KT > 3 * p.kseg_tiles) return cudaErrorInvalidValue;
+    if (!(p.b_box == 16 || p.b_box == p.n_max)) return cudaErrorInvalidValue;   // boxes must tile the B rows
     if (!p.dense && (p.E <= 0 || p.E > 1024)) return cudaErrorInvalidValue;
     const int set = epi_set(p);
     if (set < 0) return cudaErrorInvalidValue;

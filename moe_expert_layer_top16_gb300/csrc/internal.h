@@ -60,6 +60,7 @@ struct GemmParams {
     int groups;             // producer / MMA warp pairs = item lanes x ksplit
     int ksplit;             // groups per item; each takes a contiguous 1/ksplit of the item's K tiles
     int contiguous;         // 1: each CTA takes a contiguous range of items; 0: every gridDim.x-th item
+    int b_box;              // token rows per TMA box of B (tmB's box height): 16, or n_max for wide items
     int acc_bufs;           // TMEM accumulator buffers per group (1 or 2)
     int stages;             // shared-memory stages per group
     int stage_bytes;
