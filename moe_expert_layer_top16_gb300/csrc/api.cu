@@ -264,7 +264,7 @@ int item_cap(int T) { return T <= 256 ? 48 : kNMax; }
 // split keeping at least 4 K tiles); a CTA then takes a contiguous range of
 // items, so that successive items mostly belong to one expert.
 void shape_gemm(GemmParams& g, int E, int64_t est_items, int grid) {
-    const bool narrow = g.n_max <= 64;
+    const bool narrow = g.n_max <= kNarrowMax;
     const int64_t per_cta = std::max<int64_t>(1, (est_items + grid - 1) / std::max(grid, 1));
     int ks_max = 1;
     while (ks_max < 4 && g.KT >= 8 * ks_max) ks_max *= 2;
@@ -522,7 +522,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
     // experts expected to receive tokens (all of them once T * k >> E)
     const int64_t est_experts = std::min<int64_t>(E, static_cast<int64_t>(T) * k);
     // wide items load their token rows with one TMA box (height n_max)
-    const bool wide_d = nmax_dense > 64, wide_g = nmax_grp > 64;
+    const bool wide_d = nmax_dense > kNarrowMax, wide_g = nmax_grp > kNarrowMax;
     if (wide_d && p->wide_dense != nmax_dense) {
         p->wide_dense = 0;
         if (!map_mx8(&p->tB2w, p->xq, Tp, D, nmax_dense) || !map_mx8(&p->tB10w, p->act, Tp, p->Kcat, nmax_dense))
@@ -810,7 +810,7 @@ moe_status moe_mx_gemm(const uint8_t* a_codes, const uint8_t* a_scales, int32_t 
     const size_t atom_bytes = static_cast<size_t>(M) * K / 32;
     const size_t plane_bytes = static_cast<size_t>(K / 128) * (Np + 32) * 16;    // item-atom planes
     CUtensorMap tA, tB;
-    const int box_rows = pick_n_max(N, item_cap(N)) > 64 ? pick_n_max(N, item_cap(N)) : 16;
+    const int box_rows = pick_n_max(N, item_cap(N)) > kNarrowMax ? pick_n_max(N, item_cap(N)) : 16;
     if (!map_mx4(&tA, a_codes, M, K) || !map_mx8(&tB, b_codes, N, K, box_rows)) return MOE_ERR_INVALID_ARG;
     uint8_t* scratch = nullptr;
     err = cudaMallocAsync(reinterpret_cast<void**>(&scratch), atom_bytes + plane_bytes + 256, s);
@@ -824,7 +824,7 @@ moe_status moe_mx_gemm(const uint8_t* a_codes, const uint8_t* a_scales, int32_t 
     if (err == cudaSuccess) err = launch_sf_item_planes(b_scales, N, K / 32, planes, Np + 32, nmax, s);
     if (err == cudaSuccess) {
         GemmParams g = gemm_base(tA, tB, atoms, planes, Np + 32, K, nmax, M, static_cast<int>(Np), st);
-        if (nmax > 64) g.b_box = nmax;      // tB was encoded with one box per item
+        if (nmax > kNarrowMax) g.b_box = nmax;      // tB was encoded with one box per item
         g.dense = 1;
         g.m_tiles = M / kBlockM;
         g.n_tokens = N;
@@ -892,7 +892,7 @@ extern "C" moe_status moe_mx_gemm_noalloc(const uint8_t* a_codes, const uint8_t*
     if (err == cudaSuccess) err = noalloc_scratch(dev, &scratch);
     if (err != cudaSuccess) return cuda_status(err);
     CUtensorMap tA, tB;
-    const int box_rows = pick_n_max(N, item_cap(N)) > 64 ? pick_n_max(N, item_cap(N)) : 16;
+    const int box_rows = pick_n_max(N, item_cap(N)) > kNarrowMax ? pick_n_max(N, item_cap(N)) : 16;
     if (!map_mx4(&tA, a_codes, M, K) || !map_mx8(&tB, b_codes, N, K, box_rows)) return MOE_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* atoms = scratch;
@@ -906,7 +906,7 @@ extern "C" moe_status moe_mx_gemm_noalloc(const uint8_t* a_codes, const uint8_t*
     if (err == cudaSuccess) err = launch_sf_item_planes(b_scales, N, K / 32, planes, Np + 32, nmax, s);
     if (err == cudaSuccess) {
         GemmParams g = gemm_base(tA, tB, atoms, planes, Np + 32, K, nmax, M, static_cast<int>(Np), st);
-        if (nmax > 64) g.b_box = nmax;      // tB was encoded with one box per item
+        if (nmax > kNarrowMax) g.b_box = nmax;      // tB was encoded with one box per item
         g.dense = 1;
         g.m_tiles = M / kBlockM;
         g.n_tokens = N;

@@ -261,7 +261,8 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
             }
             for (int b = 0; b < 2; ++b) {
                 mbar_init(&tfull[g * 2 + b], 2);      // the MMAs' commit + the item slot
-                mbar_init(&tempty[g * 2 + b], 4);
+                // released by every epilogue warp that works on the item
+                mbar_init(&tempty[g * 2 + b], h.n_max > kNarrowMax ? 4 * kEpiGroups : 4);
             }
             mbar_init(&tdown[g], 1);
         }
@@ -470,7 +471,13 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
         int chunk_parity = 0;
         const int n_mine = (it_end > it_begin) ? (it_end - it_begin + it_step - 1) / it_step : 0;
         const int ip_shift = (IP == 4) ? 2 : (IP == 2 ? 1 : 0);       // IP is 1, 2 or 4
-        for (int c = wg; c < n_mine; c += kEpiGroups) {
+        // wide items: every warpgroup takes every item, and its 16-token
+        // chunks in turn; narrow items (one or a few chunks): warpgroups take
+        // the items in turn
+        const bool split_chunks = h.n_max > kNarrowMax;
+        const int c_first = split_chunks ? 0 : wg, c_step = split_chunks ? 1 : kEpiGroups;
+        const int n_first = split_chunks ? 16 * wg : 0, n_step = split_chunks ? 16 * kEpiGroups : 16;
+        for (int c = c_first; c < n_mine; c += c_step) {
             // item c: item lane c % IP, that lane's (c / IP)-th accumulator turn
             const int ip = c & (IP - 1);
             const uint32_t turn = static_cast<uint32_t>(c >> ip_shift);
@@ -505,7 +512,7 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
             E.sf_pitch = second ? E1.sf_pitch : E0.sf_pitch;
             E.sf_item = second ? E1.sf_item : E0.sf_item;
             const int rel_mt = w.mt - E.m_tile0;
-            for (int n0 = 0; n0 < nm; n0 += 16) {
+            for (int n0 = n_first; n0 < nm; n0 += n_step) {
                 // sum of the K-split partial accumulators, in group order
                 float v[16];
                 bool first = true;
@@ -522,28 +529,36 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                     first = false;
                 }
                 if (kOnlySilu || (kSilu && E.mode == EPI_SILU_QUANT)) {
-                    float* xb = xbuf + (wg * 2 + chunk_parity) * (2 * 32 * 16);
+                    // rows 0..63 of the tile are gate, 64..127 up: warp q < 2 holds
+                    // the gate of feature block q, warp q + 2 its up.  The pair
+                    // swaps halves of the chunk through shared memory, then warp
+                    // q < 2 finishes tokens 0..7 of block q and warp q + 2 tokens
+                    // 8..15: all four warps gate and quantise.
+                    float* xb = xbuf + (wg * 2 + chunk_parity) * (2 * 32 * 16);     // [block][token][lane]
                     chunk_parity ^= 1;
-                    if (q >= 2) {
+                    const int blk = q & 1;
+                    const bool gate_warp = q < 2;
+                    const int t0 = gate_warp ? 0 : 8;            // tokens this warp finishes
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) xb[(q - 2) * 512 + i * 32 + lane] = v[i];
-                    }
+                    for (int i = 0; i < 8; ++i)                  // hand over the other half
+                        xb[blk * 512 + ((gate_warp ? 8 : 0) + i) * 32 + lane] = gate_warp ? v[8 + i] : v[i];
                     named_bar_sync(bar_xchg, 128);
-                    if (q < 2) {
-                        const int64_t col = E.col0 + static_cast<int64_t>(rel_mt) * 64 + 32 * q + lane;
-                        const int nv = min(16, w.n - n0);
+                    const int64_t col = E.col0 + static_cast<int64_t>(rel_mt) * 64 + 32 * blk + lane;
+                    const int nv = min(8, w.n - n0 - t0);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            if (i >= nv) break;
-                            const float hv = silu_f(v[i]) * xb[q * 512 + i * 32 + lane];
-                            uint8_t sc;
-                            const uint8_t code = warp_mx8_quant(hv, &sc);
-                            const int64_t row = w.b_row0 + n0 + i;
-                            E.out_q[row * E.ld_q + col] = code;
-                            if (lane == 0)
-                                E.out_sf[E.sf_item ? sf_atom_offset(w.b_row0, n0 + i, col, E.sf_pitch)
-                                                   : sf_byte_offset(row, col, E.sf_pitch)] = sc;
-                        }
+                    for (int i = 0; i < 8; ++i) {
+                        if (i >= nv) break;
+                        const float mine = gate_warp ? v[i] : v[8 + i];
+                        const float other = xb[blk * 512 + (t0 + i) * 32 + lane];
+                        const float hv = gate_warp ? silu_f(mine) * other : silu_f(other) * mine;
+                        uint8_t sc;
+                        const uint8_t code = warp_mx8_quant(hv, &sc);
+                        const int n = n0 + t0 + i;
+                        const int64_t row = w.b_row0 + n;
+                        E.out_q[row * E.ld_q + col] = code;
+                        if (lane == 0)
+                            E.out_sf[E.sf_item ? sf_atom_offset(w.b_row0, n, col, E.sf_pitch)
+                                               : sf_byte_offset(row, col, E.sf_pitch)] = sc;
                     }
                 } else {
                     const int64_t col = E.col0 + static_cast<int64_t>(rel_mt) * 128 + 32 * q + lane;

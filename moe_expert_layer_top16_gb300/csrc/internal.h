@@ -19,6 +19,7 @@ constexpr int kBlockK = 128;
 constexpr int kNMax = 240;        // tokens per work item at most (TMEM: accumulators + scale columns <= 512)
 constexpr int kMaxGroups = 4;     // producer / MMA warp pairs per CTA
 constexpr int kEpiGroups = 2;       // epilogue warpgroups of the GEMM engine
+constexpr int kNarrowMax = 64;      // items of at most this many tokens are "narrow"
 constexpr int kGemmMaxThreads = (2 * kMaxGroups + 4 * kEpiGroups) * 32;
 constexpr int kSmemLimit = 227 * 1024;
 
