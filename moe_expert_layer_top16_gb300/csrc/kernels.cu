@@ -291,12 +291,11 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(TopkArgs a) {
     const bool need_cand = use_bias || approx;
     const float* zt = a.z + static_cast<int64_t>(t) * 2 * a.L;
     const int nper = (E + 31) / 32;
-    float lv[kTopkPerLane], key[kTopkPerLane];
+    float key[kTopkPerLane];                                  // selection-key estimates, expert lane + 32 i
 #pragma unroll
     for (int i = 0; i < kTopkPerLane; ++i) {
         const int e = lane + 32 * i;
-        lv[i] = (i < nper && e < E) ? l[e] : 0.0f;
-        float kv = lv[i];
+        float kv = (i < nper && e < E) ? l[e] : 0.0f;
         if (use_bias) kv = 1.0f / (1.0f + __expf(-kv)) + bias[e < E ? e : 0];
         if (kv != kv) kv = -INFINITY;                         // NaN ranks last
         key[i] = (i < nper && e < E) ? kv : -INFINITY;
@@ -371,40 +370,30 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(TopkArgs a) {
             if (lane < R) l[my_id] = my_l;                    // export the exact candidate logits
         }
         if (!safe) {
-            // rare: exact logits and keys of every expert, k rounds over all of them
+            // rare: exact logits (written back to the logits row) and keys of
+            // every expert, k rounds over all of them
             if (approx) {
-#pragma unroll
-                for (int i = 0; i < kTopkPerLane; ++i) {
-                    if (i < nper) {
-                        for (int c = 0; c < 32; ++c) {
-                            const int e = c + 32 * i;
-                            if (e >= E) break;
-                            const float v = exact_logit(zt, a.R, e, a.L, lane);
-                            if (c == lane) lv[i] = v;
-                        }
-                    }
+                for (int e = 0; e < E; ++e) {
+                    const float v = exact_logit(zt, a.R, e, a.L, lane);
+                    if (lane == 0) l[e] = v;
                 }
-#pragma unroll
-                for (int i = 0; i < kTopkPerLane; ++i) {
-                    const int e = lane + 32 * i;
-                    if (i < nper && e < E) l[e] = lv[i];
-                }
+                __syncwarp();
             }
             taken = 0;
             for (int j = 0; j < k; ++j) {
                 double bk = -INFINITY;
                 int bid = 0x7fffffff;
                 float bl = 0.0f;
-#pragma unroll
-                for (int i = 0; i < kTopkPerLane; ++i) {
+                for (int i = 0; i < nper; ++i) {
                     const int e = lane + 32 * i;
-                    if (i >= nper || e >= E || (taken & (1u << i))) continue;
-                    double kv = use_bias ? key64(lv[i], bias, e) : static_cast<double>(lv[i]);
+                    if (e >= E || (taken & (1u << i))) continue;
+                    const float le = l[e];
+                    double kv = use_bias ? key64(le, bias, e) : static_cast<double>(le);
                     if (kv != kv) kv = -INFINITY;
                     if (bid == 0x7fffffff || kv > bk || (kv == bk && e < bid)) {
                         bk = kv;
                         bid = e;
-                        bl = lv[i];
+                        bl = le;
                     }
                 }
 #pragma unroll
