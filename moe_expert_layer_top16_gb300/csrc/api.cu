@@ -265,6 +265,7 @@ int item_cap(int T) { return T <= 256 ? 48 : kNMax; }
 // items, so that successive items mostly belong to one expert.
 void shape_gemm(GemmParams& g, int E, int64_t est_items, int grid) {
     const bool narrow = g.n_max <= kNarrowMax;
+    const bool xbuf = gemm_needs_xbuf(g);     // the output modes must be set before shaping
     const int64_t per_cta = std::max<int64_t>(1, (est_items + grid - 1) / std::max(grid, 1));
     int ks_max = 1;
     while (ks_max < 4 && g.KT >= 8 * ks_max) ks_max *= 2;
@@ -273,8 +274,8 @@ void shape_gemm(GemmParams& g, int E, int64_t est_items, int grid) {
         KS = std::min(std::min(KS, ks_max), G);
         for (int NB = 2; NB >= 1; --NB) {
             if (!gemm_config_ok(g.n_max, G, KS, NB)) continue;
-            const int S = gemm_stages(g.n_max, G, E);
-            if (gemm_smem_bytes(g.n_max, G, S, E) > static_cast<size_t>(kSmemLimit)) continue;
+            const int S = gemm_stages(g.n_max, G, E, xbuf);
+            if (gemm_smem_bytes(g.n_max, S, E, xbuf) > static_cast<size_t>(kSmemLimit)) continue;
             g.groups = G;
             g.ksplit = KS;
             g.acc_bufs = NB;
@@ -287,7 +288,7 @@ void shape_gemm(GemmParams& g, int E, int64_t est_items, int grid) {
     g.ksplit = 1;
     g.contiguous = 0;
     g.acc_bufs = 1;
-    g.stages = gemm_stages(g.n_max, 1, E);
+    g.stages = gemm_stages(g.n_max, 1, E, xbuf);
 }
 
 moe_status validate(const moe_config* c) {
@@ -518,7 +519,10 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
     // dense GEMMs stream their weights once per token tile: a batch of up to
     // 64 tokens is one tile
     const int nmax_dense = (T <= 64) ? static_cast<int>(rup(T, 16)) : pick_n_max(T, item_cap(T));
-    const int nmax_grp = static_cast<int>(std::min<int64_t>(item_cap(T), rup(T, 16)));
+    // grouped token tile: about 3x the mean tokens per expert, 16..240
+    const int64_t per_expert = (static_cast<int64_t>(T) * k + E - 1) / E;
+    const int nmax_grp = static_cast<int>(std::min<int64_t>(std::min<int64_t>(std::max<int64_t>(rup(3 * per_expert, 16), 16), kNMax),
+                                                            rup(T, 16)));
     // experts expected to receive tokens (all of them once T * k >> E)
     const int64_t est_experts = std::min<int64_t>(E, static_cast<int64_t>(T) * k);
     // wide items load their token rows with one TMA box (height n_max)
@@ -670,8 +674,8 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
         g.E = E;
         g.mt_per_e = 2 * I / kBlockM;
         g.rows_per_e = 2 * I;
-        shape_gemm(g, E, est_experts * g.mt_per_e, p->num_sms);
         g.epi[0] = EpiParams{EPI_SILU_QUANT, 0, 0, 0, nullptr, 0, p->hq, Ip, p->hqsf, Rps, 1};
+        shape_gemm(g, E, est_experts * g.mt_per_e, p->num_sms);
         TRY(launch_gemm(g, p->num_sms, s));
     }
     // 9. routed down -> o
@@ -690,8 +694,8 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
         g.E = E;
         g.mt_per_e = L / kBlockM;
         g.rows_per_e = L;
-        shape_gemm(g, E, est_experts * g.mt_per_e, p->num_sms);
         g.epi[0] = EpiParams{EPI_F32, 0, 0, 0, p->o, L, nullptr, 0, nullptr, 0};
+        shape_gemm(g, E, est_experts * g.mt_per_e, p->num_sms);
         TRY(launch_gemm(g, p->num_sms, s));
     }
     // 10. weighted combine -> MXFP8 into columns [0, L) of the concatenated activation

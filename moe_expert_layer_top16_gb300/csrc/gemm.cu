@@ -232,12 +232,13 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
     const int G = pin(p.groups);
     const int KS = pin(p.ksplit);           // groups per item
     const int IP = G / KS;                  // item lanes
-    const int S = pin(p.stages);            // per group
+    const int S_all = pin(p.stages);        // stages of all groups; group g has S_all / G (+1 for g < S_all % G)
     const int NB = pin(p.acc_bufs);         // accumulator buffers per group
     const SmemLayout L = stage_layout(h.n_max);
-    uint8_t* tail = base + G * S * h.stage_bytes;
+    constexpr int kXbuf = kSilu ? kXbufBytes : 0;
+    uint8_t* tail = base + S_all * h.stage_bytes;
     float* xbuf = reinterpret_cast<float*>(tail);
-    uint64_t* full = reinterpret_cast<uint64_t*>(tail + kXbufBytes);      // [G][kMaxStagesPerGroup]
+    uint64_t* full = reinterpret_cast<uint64_t*>(tail + kXbuf);           // [G][kMaxStagesPerGroup]
     uint64_t* empty = full + kMaxGroups * kMaxStagesPerGroup;              // [G][kMaxStagesPerGroup]
     uint64_t* tfull = empty + kMaxGroups * kMaxStagesPerGroup;             // [G][2]
     uint64_t* tempty = tfull + kMaxGroups * 2;                             // [G][2]
@@ -246,7 +247,7 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     // item handed from each group's MMA warp to the epilogue with its accumulator
     Item* item_slot = reinterpret_cast<Item*>(reinterpret_cast<uint8_t*>(tmem_slot) + 16);    // [G][2]
-    int* ioff_s = reinterpret_cast<int*>(tail + kXbufBytes + kBarBytes);
+    int* ioff_s = reinterpret_cast<int*>(tail + kXbuf + kBarBytes);
     int* seg_s = ioff_s + (h.dense ? 0 : h.E + 1);
     int* cnt_s = seg_s + (h.dense ? 0 : h.E + 1);
 
@@ -255,6 +256,7 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
 
     if (threadIdx.x == 0) {
         for (int g = 0; g < G; ++g) {
+            const int S = S_all / G + (g < S_all % G ? 1 : 0);
             for (int s = 0; s < S; ++s) {
                 mbar_init(&full[g * kMaxStagesPerGroup + s], 1);
                 mbar_init(&empty[g * kMaxStagesPerGroup + s], 1);
@@ -308,7 +310,8 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
         group_range(h.KT, g % KS, KS, kb, ke);
         uint64_t* fullg = full + g * kMaxStagesPerGroup;
         uint64_t* emptyg = empty + g * kMaxStagesPerGroup;
-        uint8_t* ring = base + g * S * h.stage_bytes;
+        const int S = S_all / G + (g < S_all % G ? 1 : 0);
+        uint8_t* ring = base + (g * (S_all / G) + min(g, S_all % G)) * h.stage_bytes;
         uint32_t stage = 0, phase = 0;
         uint32_t issued = 0, issued_parity = 0;   // per-stage bits for the teardown drain
         bool ok = true;
@@ -372,7 +375,8 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
         group_range(h.KT, g % KS, KS, kb, ke);
         uint64_t* fullg = full + g * kMaxStagesPerGroup;
         uint64_t* emptyg = empty + g * kMaxStagesPerGroup;
-        uint8_t* ring = base + g * S * h.stage_bytes;
+        const int S = S_all / G + (g < S_all % G ? 1 : 0);
+        uint8_t* ring = base + (g * (S_all / G) + min(g, S_all % G)) * h.stage_bytes;
         const uint32_t gcol = tmem + static_cast<uint32_t>(g) * cols_per_group;
         const uint32_t sf_base = gcol + static_cast<uint32_t>(NB * h.n_max);
         uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
@@ -636,16 +640,17 @@ int gemm_stage_bytes(int n_max) {
     return (bytes + 1023) & ~1023;
 }
 
-size_t gemm_smem_bytes(int n_max, int groups, int stages, int E) {
-    return 1024 + static_cast<size_t>(groups) * stages * gemm_stage_bytes(n_max) + kXbufBytes + kBarBytes +
+size_t gemm_smem_bytes(int n_max, int stages, int E, bool xbuf) {
+    return 1024 + static_cast<size_t>(stages) * gemm_stage_bytes(n_max) + (xbuf ? kXbufBytes : 0) + kBarBytes +
            table_bytes(E);
 }
 
-int gemm_stages(int n_max, int groups, int E) {
-    int s = kMaxStagesPerGroup;
-    while (s > 2 && gemm_smem_bytes(n_max, groups, s, E) > static_cast<size_t>(kSmemLimit)) --s;
+int gemm_stages(int n_max, int groups, int E, bool xbuf) {
+    int s = kMaxStagesPerGroup * groups;
+    while (s > 2 * groups && gemm_smem_bytes(n_max, s, E, xbuf) > static_cast<size_t>(kSmemLimit)) --s;
     return s;
 }
+
 
 bool gemm_config_ok(int n_max, int groups, int ksplit, int acc_bufs) {
     if (groups < 1 || groups > kMaxGroups || acc_bufs < 1 || acc_bufs > 2) return false;
@@ -675,6 +680,11 @@ int epi_set(const GemmParams& p) {
 
 }  // namespace
 
+bool gemm_needs_xbuf(const GemmParams& p) {
+    const int set = epi_set(p);
+    return set == SET_SILU || set == SET_DUAL;
+}
+
 cudaError_t gemm_setup() {
     cudaError_t err = raise_smem<KIND_MX, SET_F32>();
     if (err == cudaSuccess) err = raise_smem<KIND_MX, SET_QUANT>();
@@ -686,8 +696,8 @@ cudaError_t gemm_setup() {
 
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s) {
     if (!gemm_config_ok(p.n_max, p.groups, p.ksplit, p.acc_bufs)) return cudaErrorInvalidValue;
-    if (p.stages < 2 || p.stages > kMaxStagesPerGroup) return cudaErrorInvalidValue;
-    const size_t smem = gemm_smem_bytes(p.n_max, p.groups, p.stages, p.dense ? 0 : p.E);
+    if (p.stages < 2 * p.groups || p.stages > kMaxStagesPerGroup * p.groups) return cudaErrorInvalidValue;
+    const size_t smem = gemm_smem_bytes(p.n_max, p.stages, p.dense ? 0 : p.E, gemm_needs_xbuf(p));
     if (smem > static_cast<size_t>(kSmemLimit)) return cudaErrorInvalidValue;
     if (p.kseg_tiles <= 0 || p.KT > 3 * p.kseg_tiles) return cudaErrorInvalidValue;
     if (!(p.b_box == 16 || p.b_box == p.n_max)) return cudaErrorInvalidValue;   // boxes must tile the B rows

@@ -63,7 +63,7 @@ struct GemmParams {
     int contiguous;         // 1: each CTA takes a contiguous range of items; 0: every gridDim.x-th item
     int b_box;              // token rows per TMA box of B (tmB's box height): 16, or n_max for wide items
     int acc_bufs;           // TMEM accumulator buffers per group (1 or 2)
-    int stages;             // shared-memory stages per group
+    int stages;             // shared-memory stages of all groups together
     int stage_bytes;
     int a_tx_bytes;         // bytes a 128x128 MXFP4 TMA box delivers to the mbarrier
     int dense;              // 1: items = m_tiles x ceil(n_tokens / n_max); 0: item list
@@ -90,8 +90,11 @@ struct GemmParams {
 };
 
 int gemm_stage_bytes(int n_max);
-int gemm_stages(int n_max, int groups, int E);          // E > 0: grouped items (per-expert tables in smem)
-size_t gemm_smem_bytes(int n_max, int groups, int stages, int E);
+// total shared-memory stages of a launch (all groups); E > 0: grouped items
+// (per-expert tables in shared memory); xbuf: the SiLU exchange buffer
+int gemm_stages(int n_max, int groups, int E, bool xbuf);
+size_t gemm_smem_bytes(int n_max, int stages, int E, bool xbuf);
+bool gemm_needs_xbuf(const GemmParams& p);
 bool gemm_config_ok(int n_max, int groups, int ksplit, int acc_bufs);
 cudaError_t gemm_setup();   // raise the dynamic shared memory limit once
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s);
