@@ -175,6 +175,7 @@ __device__ __forceinline__ void group_range(int KT, int g, int G, int& kb, int& 
 
 // Shared memory after the stages: epilogue exchange buffer (2 x 2 warps x
 // 32 lanes x 16 floats), then the barriers, then the grouped-item tables.
+constexpr int kSplitChunksMin = 32;   // items of this many tokens or more share their chunks among warpgroups
 constexpr int kXbufBytes = kEpiGroups * 2 * 2 * 32 * 16 * 4;    // per epilogue warpgroup: 2 chunks x 2 warps
 constexpr int kMaxStagesPerGroup = 16;
 // barriers, TMEM slot + abort flag (16 bytes), then the [G][2] item slots
@@ -264,7 +265,7 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
             for (int b = 0; b < 2; ++b) {
                 mbar_init(&tfull[g * 2 + b], 2);      // the MMAs' commit + the item slot
                 // released by every epilogue warp that works on the item
-                mbar_init(&tempty[g * 2 + b], h.n_max > kNarrowMax ? 4 * kEpiGroups : 4);
+                mbar_init(&tempty[g * 2 + b], h.n_max >= kSplitChunksMin ? 4 * kEpiGroups : 4);
             }
             mbar_init(&tdown[g], 1);
         }
@@ -475,10 +476,10 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
         int chunk_parity = 0;
         const int n_mine = (it_end > it_begin) ? (it_end - it_begin + it_step - 1) / it_step : 0;
         const int ip_shift = (IP == 4) ? 2 : (IP == 2 ? 1 : 0);       // IP is 1, 2 or 4
-        // wide items: every warpgroup takes every item, and its 16-token
-        // chunks in turn; narrow items (one or a few chunks): warpgroups take
-        // the items in turn
-        const bool split_chunks = h.n_max > kNarrowMax;
+        // items of several chunks: every warpgroup takes every item, and its
+        // 16-token chunks in turn; single-chunk items: warpgroups take the
+        // items in turn
+        const bool split_chunks = h.n_max >= kSplitChunksMin;
         const int c_first = split_chunks ? 0 : wg, c_step = split_chunks ? 1 : kEpiGroups;
         const int n_first = split_chunks ? 16 * wg : 0, n_step = split_chunks ? 16 * kEpiGroups : 16;
         for (int c = c_first; c < n_mine; c += c_step) {
