@@ -209,6 +209,7 @@ __global__ void __cluster_dims__(1, 1, kRouterSplit) __launch_bounds__(256)
 // Gates: sigmoid(l_j) / sum over the winners (fp32), or softmax over the
 // winners' logits.  Each selection sets bit t of the expert's token bitmap.
 constexpr int kTopkWarps = 4;
+constexpr int kTopkWideTokens = 512;  // batches up to this size use one CTA per token
 constexpr int kTopkPerLane = 32;     // E <= 1024
 constexpr int kMaxE = 32 * kTopkPerLane;
 constexpr float kKeyErr = 4.0e-6f;   // error bound of the fp32 sigmoid(l) + b estimate
@@ -279,10 +280,10 @@ __device__ __forceinline__ void exact_logit4(const float* __restrict__ zt, const
     out[3] = a3;
 }
 
-__global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(TopkArgs a) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * kTopkWarps + warp;
-    if (t >= a.T) return;
+// Second half of the top-k of token t, run by one warp: lane j < R holds the
+// j-th candidate id (on estimates); exact keys of the candidates, their
+// ranking (or the exact fallback on overflow), gates and token bitmaps.
+__device__ __noinline__ void topk_finish(const TopkArgs& a, int t, int lane, int R, bool overflow, int my_id) {
     const int E = a.E, k = a.k;
     float* l = a.logits + static_cast<int64_t>(t) * E;
     const float* bias = a.bias;
@@ -291,54 +292,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(TopkArgs a) {
     const bool need_cand = use_bias || approx;
     const float* zt = a.z + static_cast<int64_t>(t) * 2 * a.L;
     const int nper = (E + 31) / 32;
-    float key[kTopkPerLane];                                  // selection-key estimates, expert lane + 32 i
-#pragma unroll
-    for (int i = 0; i < kTopkPerLane; ++i) {
-        const int e = lane + 32 * i;
-        float kv = (i < nper && e < E) ? l[e] : 0.0f;
-        if (use_bias) kv = 1.0f / (1.0f + __expf(-kv)) + bias[e < E ? e : 0];
-        if (kv != kv) kv = -INFINITY;                         // NaN ranks last
-        key[i] = (i < nper && e < E) ? kv : -INFINITY;
-    }
-    uint32_t taken = 0;                                       // bit i: candidate lane + 32 i selected
-    // Candidates, in estimate order: the k best estimates, then every further
-    // expert whose estimate is within 2 * err of the k-th one.  An expert
-    // outside that band has a true key below k-th estimate - err, and each of
-    // the k best has a true key above it, so the exact top-k lies among the
-    // candidates.  More than 32 candidates (lane capacity): exact fallback.
-    const double err = approx ? (use_bias ? 0.25 * a.delta + kKeyErr : a.delta) : kKeyErr;
-    int R = 0;
-    bool overflow = false;
-    int my_id = 0;                                            // lane j < R holds the j-th pick
-    float kth_est = 0.0f;
-    for (int j = 0; j <= 32; ++j) {
-        if (j >= k && !need_cand) break;
-        KeyId b = {-INFINITY, 0x7fffffff};
-#pragma unroll
-        for (int i = 0; i < kTopkPerLane; ++i) {
-            const int e = lane + 32 * i;
-            if (i < nper && e < E && !(taken & (1u << i)) &&
-                (b.id == 0x7fffffff || key[i] > b.key || (key[i] == b.key && e < b.id))) {
-                b.key = key[i];
-                b.id = e;
-            }
-        }
-        b = warp_best(b);
-        if (j >= k) {
-            // band test in double: kth_est - 2 err is not rounded toward the candidate
-            if (b.id < 0 || b.id >= E || !(static_cast<double>(b.key) >= static_cast<double>(kth_est) - 2.0 * err))
-                break;
-            if (j == 32) {
-                overflow = true;
-                break;
-            }
-        }
-        if (b.id < 0 || b.id >= E) b.id = 0;                 // unreachable while k <= E
-        if (j == k - 1) kth_est = b.key;
-        if (lane == j) my_id = b.id;
-        if ((b.id & 31) == lane) taken |= 1u << (b.id >> 5);
-        R = j + 1;
-    }
+    uint32_t taken = 0;
     int slot = lane;                                          // final slot of this lane's pick
     float my_l = 0.0f;                                        // exact logit of this lane's pick
     if (need_cand) {
@@ -438,6 +392,166 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(TopkArgs a) {
         a.w[static_cast<int64_t>(t) * k + slot] = s / sum;
         atomicOr(&a.sel[static_cast<int64_t>(my_id) * a.W + (t >> 5)], 1u << (t & 31));
     }
+}
+
+__global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(TopkArgs a) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kTopkWarps + warp;
+    if (t >= a.T) return;
+    const int E = a.E, k = a.k;
+    float* l = a.logits + static_cast<int64_t>(t) * E;
+    const float* bias = a.bias;
+    const bool use_bias = (bias != nullptr) && !a.softmax;
+    const bool approx = a.refine != 0;
+    const bool need_cand = use_bias || approx;
+    const int nper = (E + 31) / 32;
+    float key[kTopkPerLane];                                  // selection-key estimates, expert lane + 32 i
+#pragma unroll
+    for (int i = 0; i < kTopkPerLane; ++i) {
+        const int e = lane + 32 * i;
+        float kv = (i < nper && e < E) ? l[e] : 0.0f;
+        if (use_bias) kv = 1.0f / (1.0f + __expf(-kv)) + bias[e < E ? e : 0];
+        if (kv != kv) kv = -INFINITY;                         // NaN ranks last
+        key[i] = (i < nper && e < E) ? kv : -INFINITY;
+    }
+    uint32_t taken = 0;                                       // bit i: candidate lane + 32 i selected
+    // Candidates, in estimate order: the k best estimates, then every further
+    // expert whose estimate is within 2 * err of the k-th one.  An expert
+    // outside that band has a true key below k-th estimate - err, and each of
+    // the k best has a true key above it, so the exact top-k lies among the
+    // candidates.  More than 32 candidates (lane capacity): exact fallback.
+    const double err = approx ? (use_bias ? 0.25 * a.delta + kKeyErr : a.delta) : kKeyErr;
+    int R = 0;
+    bool overflow = false;
+    int my_id = 0;                                            // lane j < R holds the j-th pick
+    float kth_est = 0.0f;
+    for (int j = 0; j <= 32; ++j) {
+        if (j >= k && !need_cand) break;
+        KeyId b = {-INFINITY, 0x7fffffff};
+#pragma unroll
+        for (int i = 0; i < kTopkPerLane; ++i) {
+            const int e = lane + 32 * i;
+            if (i < nper && e < E && !(taken & (1u << i)) &&
+                (b.id == 0x7fffffff || key[i] > b.key || (key[i] == b.key && e < b.id))) {
+                b.key = key[i];
+                b.id = e;
+            }
+        }
+        b = warp_best(b);
+        if (j >= k) {
+            // band test in double: kth_est - 2 err is not rounded toward the candidate
+            if (b.id < 0 || b.id >= E || !(static_cast<double>(b.key) >= static_cast<double>(kth_est) - 2.0 * err))
+                break;
+            if (j == 32) {
+                overflow = true;
+                break;
+            }
+        }
+        if (b.id < 0 || b.id >= E) b.id = 0;                 // unreachable while k <= E
+        if (j == k - 1) kth_est = b.key;
+        if (lane == j) my_id = b.id;
+        if ((b.id & 31) == lane) taken |= 1u << (b.id >> 5);
+        R = j + 1;
+    }
+    topk_finish(a, t, lane, R, overflow, my_id);
+}
+
+// Selection rounds over NPL (key, id) entries per lane (id < 0: empty): the k
+// best estimates, then every further entry within 2 * err of the k-th, at
+// most 32 (more: overflow).  Lane j < R receives the j-th pick.
+template <int NPL>
+__device__ __forceinline__ void pick_rounds(const float (&key)[NPL], const int (&eid)[NPL], int k, bool band,
+                                            double err, int lane, int& R, bool& overflow, int& my_id,
+                                            float& my_key) {
+    uint32_t taken = 0;
+    float kth = 0.0f;
+    R = 0;
+    overflow = false;
+    for (int j = 0; j <= 32; ++j) {
+        if (j >= k && !band) break;
+        KeyId b = {-INFINITY, 0x7fffffff};
+#pragma unroll
+        for (int i = 0; i < NPL; ++i)
+            if (eid[i] >= 0 && !(taken & (1u << i)) &&
+                (b.id == 0x7fffffff || key[i] > b.key || (key[i] == b.key && eid[i] < b.id))) {
+                b.key = key[i];
+                b.id = eid[i];
+            }
+        b = warp_best(b);
+        if (b.id == 0x7fffffff) break;                       // no entries left
+        if (j >= k) {
+            if (!(static_cast<double>(b.key) >= static_cast<double>(kth) - 2.0 * err)) break;
+            if (j == 32) {
+                overflow = true;
+                break;
+            }
+        }
+        if (j == k - 1) kth = b.key;
+        if (lane == j) {
+            my_id = b.id;
+            my_key = b.key;
+        }
+#pragma unroll
+        for (int i = 0; i < NPL; ++i)
+            if (eid[i] == b.id) taken |= 1u << i;
+        R = j + 1;
+    }
+}
+
+// Top-k of small batches: one CTA of 8 warps per token.  Warp w estimates the
+// keys of experts lane + 32 (w + 8 i) and picks its own top-k plus every
+// expert within 2 * err of its own k-th estimate -- a superset of the
+// token's candidates, since a warp's k-th estimate is never above the
+// token's.  Warp 0 merges the picks the same way and finishes as topk_kernel.
+constexpr int kTopkWideWarps = 8;
+constexpr int kTopkWidePerLane = kMaxE / (32 * kTopkWideWarps);      // 4
+__global__ void __launch_bounds__(kTopkWideWarps * 32) topk_wide_kernel(TopkArgs a) {
+    __shared__ float s_key[kTopkWideWarps][32];
+    __shared__ int s_id[kTopkWideWarps][32];
+    __shared__ int s_n[kTopkWideWarps];
+    __shared__ int s_over;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x;
+    const int E = a.E, k = a.k;
+    const float* l = a.logits + static_cast<int64_t>(t) * E;
+    const float* bias = a.bias;
+    const bool use_bias = (bias != nullptr) && !a.softmax;
+    const bool approx = a.refine != 0;
+    const bool band = use_bias || approx;
+    const double err = approx ? (use_bias ? 0.25 * a.delta + kKeyErr : a.delta) : kKeyErr;
+    if (threadIdx.x == 0) s_over = 0;
+    float key[kTopkWidePerLane];
+    int eid[kTopkWidePerLane];
+#pragma unroll
+    for (int i = 0; i < kTopkWidePerLane; ++i) {
+        const int e = lane + 32 * (warp + kTopkWideWarps * i);
+        float kv = (e < E) ? l[e] : 0.0f;
+        if (use_bias && e < E) kv = 1.0f / (1.0f + __expf(-kv)) + bias[e];
+        if (kv != kv) kv = -INFINITY;
+        key[i] = kv;
+        eid[i] = (e < E) ? e : -1;
+    }
+    int R, my_id = 0;
+    bool over;
+    float my_key = 0.0f;
+    pick_rounds(key, eid, k, band, err, lane, R, over, my_id, my_key);
+    s_key[warp][lane] = my_key;
+    s_id[warp][lane] = my_id;
+    if (lane == 0) {
+        s_n[warp] = R;
+        if (over) s_over = 1;
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    float mkey[kTopkWideWarps];
+    int mid[kTopkWideWarps];
+#pragma unroll
+    for (int i = 0; i < kTopkWideWarps; ++i) {       // entry lane of warp i's picks
+        mkey[i] = s_key[i][lane];
+        mid[i] = (lane < s_n[i]) ? s_id[i][lane] : -1;
+    }
+    pick_rounds(mkey, mid, k, band, err, lane, R, over, my_id, my_key);
+    topk_finish(a, t, lane, R, over || s_over != 0, my_id);
 }
 
 // ------------------------------------------------------------------ A5: per-expert scan
@@ -760,7 +874,10 @@ cudaError_t launch_router(const float* z, const float* R, float* logits, int T, 
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
     if (a.E > kMaxE || a.k > 32) return cudaErrorInvalidValue;
-    topk_kernel<<<(a.T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, s>>>(a);
+    if (a.T <= kTopkWideTokens)
+        topk_wide_kernel<<<a.T, kTopkWideWarps * 32, 0, s>>>(a);
+    else
+        topk_kernel<<<(a.T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, s>>>(a);
     return cudaGetLastError();
 }
 
