@@ -58,7 +58,7 @@ class _MX(C.Structure):
 
 
 class _Cfg(C.Structure):
-    _fields_ = [(n, C.c_int32) for n in ("D", "L", "E", "k", "I", "S", "Is", "softmax")]
+    _fields_ = [(n, C.c_int32) for n in ("D", "L", "E", "k", "I", "S", "Is", "softmax", "route_hidden")]
 
 
 class _Weights(C.Structure):
@@ -285,7 +285,7 @@ def moe_forward(wl, weights: LayerWeights, x_bf16_bits: np.ndarray, force_idx=No
         shp, dt = shapes[name]
         res[name] = np.zeros(shp, dt)
         setattr(out, name, res[name].ctypes.data)
-    cfg = _Cfg(D, L, E, k, I, S, Is, 1 if wl.score == "softmax" else 0)
+    cfg = _Cfg(D, L, E, k, I, S, Is, 1 if wl.score == "softmax" else 0, 1 if wl.route == "hidden" else 0)
     fi = None
     if force_idx is not None:
         fi = np.ascontiguousarray(force_idx, dtype=np.int32)

@@ -42,7 +42,11 @@
  *    activation is SiLU(g) = g / (1 + exp(-g)).
  *  - Every GEMM / activation output is rounded to fp32 before it is
  *    quantised or consumed; sums themselves run in fp64.
- *  - Router input is the fp32 latent z; logits are summed in fp64.
+ *  - Router input is the fp32 latent z ("Kimi K3: 2.8 Trillion Parameters,
+ *    Four Bits at a Time", section "The shape of the model": latent-space
+ *    routing); "What Kimi K3 asks of the hardware" leaves the latent part
+ *    unspecified, so routing on the hidden state x is kept as an option.
+ *    Logits are summed in fp64.
  *  - Slot order within a token: descending key, tie -> lower expert id.
  *  - Combine accumulates the k slots of a token in slot order.
  *
@@ -348,6 +352,7 @@ void orc_combine(const double *rows, const int32_t *order, const double *gates,
 typedef struct {
     int32_t D, L, E, k, I, S, Is;
     int32_t softmax;        /* 1: softmax over winners (toy); 0: sigmoid + bias */
+    int32_t route_hidden;   /* 1: the router reads the hidden state x ([E][D] weights); 0: the latent z */
 } orc_cfg;
 
 typedef struct {
@@ -359,7 +364,7 @@ typedef struct {
     const orc_mx *s_gate;   /* S x [Is][D] */
     const orc_mx *s_up;     /* S x [Is][D] */
     const orc_mx *s_down;   /* S x [D][Is] */
-    const float *router;    /* [E][L] fp32 */
+    const float *router;    /* [E][L] fp32 (latent routing) or [E][D] (hidden routing) */
     const float *bias;      /* [E] fp32 or NULL */
 } orc_weights;
 
@@ -441,12 +446,18 @@ int orc_moe_forward(const orc_cfg *cfg, const orc_weights *W, const uint16_t *x_
         if (out->hsq) memcpy(out->hsq + t * SIs, hsq, SIs);
         if (out->hss) memcpy(out->hss + t * (SIs / 32), hss, SIs / 32);
 
-        /* router logits on the latent, fp64 sum of fp32 products */
-        for (int64_t e = 0; e < E; ++e) {
-            double acc = 0.0;
-            for (int64_t l = 0; l < L; ++l)
-                acc += (double)z[l] * (double)W->router[e * L + l];
-            lg[e] = acc;
+        /* router logits, fp64 sum of fp32 products: on the latent z by
+         * default, on the hidden state x (exactly its bf16 value) when the
+         * router is configured to read the hidden state */
+        {
+            const float *rin = cfg->route_hidden ? xf : z;
+            const int64_t RK = cfg->route_hidden ? D : L;
+            for (int64_t e = 0; e < E; ++e) {
+                double acc = 0.0;
+                for (int64_t l = 0; l < RK; ++l)
+                    acc += (double)rin[l] * (double)W->router[e * RK + l];
+                lg[e] = acc;
+            }
         }
         if (out->logits) memcpy(out->logits + t * E, lg, sizeof(double) * E);
         orc_route(lg, W->bias, 1, (int)E, (int)k, cfg->softmax, sel, gate);

@@ -57,6 +57,8 @@ class Workload:
     score: str          # "sigmoid" (sigmoid + selection bias) or "softmax" (toy gates)
     bias: str           # "zero" or "zipf"
     seed: int = 0
+    route: str = "latent"   # router input: "latent" (z, [E][L] router) or "hidden" (x, [E][D] router)
+    out: str = "f32"        # output dtype of y: "f32" or "bf16"
 
     def with_tokens(self, t: int) -> "Workload":
         return replace(self, tokens=int(t), name=f"{self.name.split('@')[0]}@T{t}")
@@ -81,10 +83,24 @@ SWEEP_TOKENS = (1, 8, 64, 512, 4096, 32768)
 
 
 def workload(name: str) -> Workload:
-    if "@T" in name:
-        base, t = name.split("@T")
-        return WORKLOADS[base].with_tokens(int(t))
-    return WORKLOADS[name]
+    """A named workload; "name@T<n>" overrides the token count, "name+hidden"
+    routes on the hidden state, "name+bf16" writes a bf16 output."""
+    base, *opts = name.split("+")
+    if "@T" in base:
+        b, t = base.split("@T")
+        w = WORKLOADS[b].with_tokens(int(t))
+    else:
+        w = WORKLOADS[base]
+    for o in opts:
+        if o == "hidden":
+            w = replace(w, route="hidden")
+        elif o == "bf16":
+            w = replace(w, out="bf16")
+        else:
+            raise KeyError(name)
+    if opts:
+        w = replace(w, name=name)
+    return w
 
 
 def tensor_seed(master: int, name: str, index: int = 0) -> int:
@@ -109,7 +125,7 @@ def weight_shape(w: Workload, name: str):
         "p_down": (L, D), "p_up": (D, L),
         "w_gate": (I, L), "w_up": (I, L), "w_down": (L, I),
         "s_gate": (Is, D), "s_up": (Is, D), "s_down": (D, Is),
-        "router": (w.n_experts, L),
+        "router": (w.n_experts, L if w.route == "latent" else D),
     }[name]
 
 

@@ -141,3 +141,42 @@ def test_touched_expert_closed_form_matches_printed_simulation():
             counts, _, _ = oracle.permute(idx, E)
             t.append((counts > 0).sum())
         assert abs(np.mean(t) * 1.5 / B - rows[B]) <= 0.03 * rows[B]
+
+
+def _one_hot_router(E, K, stride=7, offset=3):
+    """Router rows that pick one input dimension each: row e = unit vector at
+    (stride * e + offset) % K."""
+    r = np.zeros((E, K), np.float32)
+    dims = (stride * np.arange(E) + offset) % K
+    r[np.arange(E), dims] = 1.0
+    return r, dims
+
+
+def _layer_with_router(wl, router):
+    import synth
+
+    def fetch(name, i):
+        if name == "router":
+            return router
+        if name == "bias":
+            return None
+        return synth.weight(wl, name, i).numpy()
+    return oracle.encode_layer(wl, fetch)
+
+
+def test_router_input_hidden_reads_x_and_latent_reads_z():
+    """With one-hot router rows each logit is one component of the router's
+    input: of x itself (its exact bf16 value) when routing on the hidden
+    state, of the oracle's own latent z otherwise."""
+    import synth
+    import torch
+    for route in ("hidden", "latent"):
+        wl = synth.workload("tiny" + ("+hidden" if route == "hidden" else "")).with_tokens(6)
+        K = wl.d_model if route == "hidden" else wl.d_latent
+        router, dims = _one_hot_router(wl.n_experts, K)
+        lw = _layer_with_router(wl, router)
+        x = synth.hidden_states(wl, 6)
+        xb = x.contiguous().view(torch.int16).numpy().view(np.uint16)
+        r = oracle.moe_forward(wl, lw, xb, route_only=True, want=("logits", "z"))
+        src = x.float().numpy() if route == "hidden" else r["z"]
+        assert np.array_equal(r["logits"], src[:, dims].astype(np.float64))
