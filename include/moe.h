@@ -70,6 +70,21 @@ typedef enum {
     MOE_SCORE_SOFTMAX = 1       /* top-k on the logit, softmax over the k winners */
 } moe_score_fn;
 
+/* What the router reads.  The pages route in the latent space ("Kimi K3: 2.8
+ * Trillion Parameters, Four Bits at a Time", "The shape of the model"); "What
+ * Kimi K3 asks of the hardware" leaves the latent part unspecified, so the
+ * hidden state can be routed on instead. */
+typedef enum {
+    MOE_ROUTE_ON_LATENT = 0,    /* logits = z R^T, R [E][L] */
+    MOE_ROUTE_ON_HIDDEN = 1     /* logits = x R^T (x exactly as given), R [E][D] */
+} moe_route_input;
+
+/* Element type of the output y. */
+typedef enum {
+    MOE_OUT_F32 = 0,            /* fp32 [T][D] */
+    MOE_OUT_BF16 = 1            /* bf16 [T][D], each value rounded to nearest even from fp32 */
+} moe_out_dtype;
+
 /* Layer shape.  Constraints (checked by moe_plan): d_model and d_latent
  * multiples of 128; expert_inter and shared_inter multiples of 64;
  * 1 <= top_k <= min(n_experts, 32); 1 <= n_experts <= 1024; n_shared >= 0;
@@ -84,6 +99,8 @@ typedef struct {
     int32_t shared_inter;  /* Is: shared expert inner width */
     int32_t max_tokens;    /* largest T a forward call may pass */
     int32_t score_fn;      /* moe_score_fn */
+    int32_t route_input;   /* moe_route_input */
+    int32_t out_dtype;     /* moe_out_dtype */
 } moe_config;
 
 typedef struct {
@@ -103,7 +120,7 @@ typedef struct {
     moe_mx4 s_gate;           /* [S][Is][D]   shared gate            */
     moe_mx4 s_up;             /* [S][Is][D]   shared up              */
     moe_mx4 s_down;           /* [S][D][Is]   shared down            */
-    const float *router_w;    /* [E][L] fp32 router on the latent    */
+    const float *router_w;    /* [E][L] fp32 router (latent routing), [E][D] (hidden routing) */
     const float *router_bias; /* [E] fp32 selection bias, or NULL (= 0) */
 } moe_weights;
 
@@ -144,19 +161,20 @@ typedef struct {
  * NULL.  Needs a compute capability 10.3 device. */
 MOE_API moe_status moe_plan(const moe_config *cfg, const moe_weights *w, int device, void **plan_out);
 
-/* Forward pass: x bf16 [T][D] (device, rows 16-byte aligned) -> y fp32
- * [T][D] (device).  Enqueued on `stream` (a cudaStream_t; NULL = legacy
+/* Forward pass: x bf16 [T][D] (device, rows 16-byte aligned) -> y [T][D]
+ * (device; fp32 or bf16 as cfg->out_dtype says).  Enqueued on `stream` (a cudaStream_t; NULL = legacy
  * default stream); no host synchronisation, no allocation.  1 <= T <=
  * max_tokens.  `dbg` may be NULL.  One plan serves one stream at a time:
  * calls on different streams that overlap race on the plan's workspace. */
-MOE_API moe_status moe_forward(void *plan, const void *x, int32_t T, float *y, void *stream,
+MOE_API moe_status moe_forward(void *plan, const void *x, int32_t T, void *y, void *stream,
                        const moe_debug *dbg);
 
 /* Same as moe_forward with HOST buffers: copies x (host, bf16 [T][D]) to the
- * device, runs the layer and copies y back to host memory y_host ([T][D]
- * fp32), all on `stream`, then synchronises the stream.  Page-locked host
+ * device, runs the layer and copies y back to host memory y_host ([T][D],
+ * fp32 or bf16 as cfg->out_dtype says), all on `stream`, then synchronises
+ * the stream.  Page-locked host
  * buffers make the copies asynchronous. */
-MOE_API moe_status moe_forward_host(void *plan, const uint16_t *x_host, int32_t T, float *y_host,
+MOE_API moe_status moe_forward_host(void *plan, const uint16_t *x_host, int32_t T, void *y_host,
                             void *stream);
 
 /* Sticky device-side status of the plan (call after synchronising the stream

@@ -26,6 +26,8 @@ _lock = threading.Lock()
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_OOM, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE = range(7)
 SCORE_SIGMOID_BIAS, SCORE_SOFTMAX = 0, 1
+ROUTE_ON_LATENT, ROUTE_ON_HIDDEN = 0, 1
+OUT_F32, OUT_BF16 = 0, 1
 
 # Entry points declared in include/moe.h.
 ENTRY_POINTS = ("moe_plan", "moe_forward", "moe_forward_host", "moe_get_device_status", "moe_workspace_bytes",
@@ -40,7 +42,8 @@ class MoeError(RuntimeError):
 
 class _Config(C.Structure):
     _fields_ = [(n, C.c_int32) for n in ("d_model", "d_latent", "n_experts", "top_k", "expert_inter",
-                                          "n_shared", "shared_inter", "max_tokens", "score_fn")]
+                                          "n_shared", "shared_inter", "max_tokens", "score_fn", "route_input",
+                                          "out_dtype")]
 
 
 class _MX4(C.Structure):
@@ -130,9 +133,13 @@ def config_struct(cfg) -> _Config:
     """`cfg` is any object with the synth.Workload fields (or a dict of them)."""
     g = (lambda k: cfg[k]) if isinstance(cfg, dict) else (lambda k: getattr(cfg, k))
     score = g("score")
+    route = g("route") if _has(cfg, "route") else "latent"
+    out = g("out") if _has(cfg, "out") else "f32"
     return _Config(g("d_model"), g("d_latent"), g("n_experts"), g("top_k"), g("expert_inter"), g("n_shared"),
                    g("shared_inter"), int(g("max_tokens")) if _has(cfg, "max_tokens") else g("tokens"),
-                   SCORE_SOFTMAX if score == "softmax" else SCORE_SIGMOID_BIAS)
+                   SCORE_SOFTMAX if score == "softmax" else SCORE_SIGMOID_BIAS,
+                   ROUTE_ON_HIDDEN if route == "hidden" else ROUTE_ON_LATENT,
+                   OUT_BF16 if out == "bf16" else OUT_F32)
 
 
 def _has(cfg, k):
@@ -201,6 +208,10 @@ class Plan:
     def handle(self):
         return self._h
 
+    @property
+    def out_dtype(self):
+        return torch.bfloat16 if self.cfg.out_dtype == OUT_BF16 else torch.float32
+
     def forward(self, x: torch.Tensor, out: Optional[torch.Tensor] = None, debug: Optional[dict] = None,
                 stream=None, stage_events=None) -> torch.Tensor:
         """y = layer(x); x bf16 [T][D] on the plan's device.  `debug` maps
@@ -211,7 +222,8 @@ class Plan:
         x = x.contiguous()
         T = x.shape[0]
         if out is None:
-            out = torch.empty(T, self.cfg.d_model, dtype=torch.float32, device=x.device)
+            out = torch.empty(T, self.cfg.d_model, dtype=self.out_dtype, device=x.device)
+        assert out.dtype == self.out_dtype and out.shape == (T, self.cfg.d_model)
         dbg = None
         if debug or stage_events:
             dbg = _Debug()
@@ -226,8 +238,8 @@ class Plan:
         return out
 
     def forward_host(self, x_host: torch.Tensor, y_host: torch.Tensor, stream=None):
-        """End-to-end call with host buffers (bf16 [T][D] in, fp32 [T][D] out)."""
-        assert x_host.dtype == torch.bfloat16 and not x_host.is_cuda and y_host.dtype == torch.float32
+        """End-to-end call with host buffers (bf16 [T][D] in, [T][D] out in the plan's output dtype)."""
+        assert x_host.dtype == torch.bfloat16 and not x_host.is_cuda and y_host.dtype == self.out_dtype
         T = x_host.shape[0]
         _check(lib().moe_forward_host(self._h, C.c_void_p(x_host.data_ptr()), T, C.c_void_p(y_host.data_ptr()),
                                       _stream_ptr(stream)), "moe_forward_host")

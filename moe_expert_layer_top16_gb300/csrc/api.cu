@@ -113,7 +113,10 @@ struct Plan {
     std::vector<void*> allocs;
     // weights
     uint8_t *a2c, *a2sf, *w13c, *w13sf, *w2c, *w2sf, *a10c, *a10sf;
-    float *router, *router2, *bias;   // router2: [E][2L] = TF32 high part | remainder
+    float *router, *router2, *bias;   // router [E][RK]; router2: [E][2 RK] = TF32 high part | remainder
+    int RK = 0;                       // router input width: L (latent routing) or D (hidden routing)
+    bool route_hidden = false, out_bf16 = false;
+    float* xr = nullptr;              // hidden routing: x as fp32 [T_pad][D]
     // workspace
     uint8_t *xq, *xsf, *zq, *zsf, *act, *actsf, *zqp, *zqpsf, *hq, *hqsf;
     float *z, *logits, *gw, *o;
@@ -301,6 +304,8 @@ moe_status validate(const moe_config* c) {
     if (c->top_k < 1 || c->top_k > 32 || c->top_k > c->n_experts) return MOE_ERR_INVALID_ARG;
     if (c->max_tokens < 1 || c->max_tokens > 65536) return MOE_ERR_INVALID_ARG;
     if (c->score_fn != MOE_SCORE_SIGMOID_BIAS && c->score_fn != MOE_SCORE_SOFTMAX) return MOE_ERR_INVALID_ARG;
+    if (c->route_input != MOE_ROUTE_ON_LATENT && c->route_input != MOE_ROUTE_ON_HIDDEN) return MOE_ERR_INVALID_ARG;
+    if (c->out_dtype != MOE_OUT_F32 && c->out_dtype != MOE_OUT_BF16) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
 }
 
@@ -444,10 +449,14 @@ moe_status moe_plan(const moe_config* cfg, const moe_weights* w, int device, voi
         }
         TRY(repack(p, segs, D, p->Kcat, &p->a10c, &p->a10sf));
     }
-    TRY(palloc(p, &p->router, sizeof(float) * E * L));
-    TRY(cudaMemcpy(p->router, w->router_w, sizeof(float) * E * L, cudaMemcpyDeviceToDevice));
-    TRY(palloc(p, &p->router2, sizeof(float) * E * 2 * L));
-    TRY(launch_tf32_split(p->router, E, L, p->router2, 0));
+    p->route_hidden = cfg->route_input == MOE_ROUTE_ON_HIDDEN;
+    p->out_bf16 = cfg->out_dtype == MOE_OUT_BF16;
+    p->RK = p->route_hidden ? D : L;
+    const int RK = p->RK;
+    TRY(palloc(p, &p->router, sizeof(float) * E * RK));
+    TRY(cudaMemcpy(p->router, w->router_w, sizeof(float) * E * RK, cudaMemcpyDeviceToDevice));
+    TRY(palloc(p, &p->router2, sizeof(float) * E * 2 * RK));
+    TRY(launch_tf32_split(p->router, E, RK, p->router2, 0));
     TRY(cudaDeviceSynchronize());
     p->bias = nullptr;
     if (w->router_bias) {
@@ -459,6 +468,7 @@ moe_status moe_plan(const moe_config* cfg, const moe_weights* w, int device, voi
     // token-operand scales of the GEMMs: item-atom planes with 32 spare slots
     TRY(palloc(p, &p->xsf, (D / 128) * (Tp + 32) * 16));
     TRY(palloc(p, &p->z, sizeof(float) * Tp * 2 * L));     // TF32 high part | remainder
+    if (p->route_hidden) TRY(palloc(p, &p->xr, sizeof(float) * Tp * D));
     TRY(palloc(p, &p->zq, Tp * L));
     TRY(palloc(p, &p->zsf, (L / 128) * Tp * 4));
     TRY(palloc(p, &p->act, Tp * p->Kcat));
@@ -495,8 +505,9 @@ moe_status moe_plan(const moe_config* cfg, const moe_weights* w, int device, voi
               map_mx4(&p->tA7, p->w13c, static_cast<int64_t>(E) * 2 * I, L) && map_mx8(&p->tB7, p->zqp, Rp, L) &&
               map_mx4(&p->tA8, p->w2c, static_cast<int64_t>(E) * L, Ip) && map_mx8(&p->tB8, p->hq, Rp, Ip) &&
               map_mx4(&p->tA10, p->a10c, D, p->Kcat) && map_mx8(&p->tB10, p->act, Tp, p->Kcat) &&
-              map_f32(&p->tAR, p->router2, E, 2 * L, 128) && map_f32(&p->tBR, p->z, Tp, 2 * L, 16);
-    p->tc_router = (E % 128 == 0) && (L % 32 == 0);
+              map_f32(&p->tAR, p->router2, E, 2 * p->RK, 128) &&
+              (p->route_hidden ? map_f32(&p->tBR, p->xr, Tp, D, 16) : map_f32(&p->tBR, p->z, Tp, 2 * L, 16));
+    p->tc_router = (E % 128 == 0) && (p->RK % 32 == 0);
     if (!ok) {
         plan_release(p);
         return MOE_ERR_CUDA;
@@ -505,11 +516,12 @@ moe_status moe_plan(const moe_config* cfg, const moe_weights* w, int device, voi
     return MOE_OK;
 }
 
-moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* stream, const moe_debug* dbg) {
+moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stream, const moe_debug* dbg) {
     Plan* p = static_cast<Plan*>(plan);
     if (!p || !x || !y) return MOE_ERR_INVALID_ARG;
     if (T < 1 || T > p->T_max) return MOE_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(y) & 3)) return MOE_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(y) & (p->out_bf16 ? 1 : 3)))
+        return MOE_ERR_INVALID_ARG;
     DevGuard guard(p->device);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int D = p->D, L = p->L, E = p->E, k = p->k, I = p->I, Ip = p->Ip;
@@ -551,7 +563,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
     TRY(cudaMemsetAsync(p->sel, 0, sizeof(uint32_t) * E * W, s));
     mark(0);
     // 1. x -> MXFP8
-    TRY(launch_quant_x(static_cast<const __nv_bfloat16*>(x), T, D, p->xq, p->xsf, Tps, nmax_dense, s));
+    TRY(launch_quant_x(static_cast<const __nv_bfloat16*>(x), T, D, p->xq, p->xsf, Tps, nmax_dense, p->xr, s));
     mark(1);
     // 2. latent down-projection + shared gate/up
     {
@@ -576,14 +588,22 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
     const bool tc_logits = p->tc_router && T > 128;
     if (tc_logits) {
         // logits = z R^T as three TF32 products, z_hi R_hi + z_lo R_hi + z_hi R_lo,
-        // K-concatenated through the maps' coordinates into one accumulator
-        GemmParams g = gemm_base(p->tAR, p->tBR, nullptr, nullptr, 0, 3 * L * 4, nmax_dense, E,
+        // K-concatenated through the maps' coordinates into one accumulator.
+        // Hidden routing: x is bf16, so x_hi = x and x_lo = 0: x R_hi + x R_lo.
+        const int RK = p->RK;
+        GemmParams g = gemm_base(p->tAR, p->tBR, nullptr, nullptr, 0, 3 * RK * 4, nmax_dense, E,
                                  static_cast<int>(Tp), p->status);
         g.kind = KIND_TF32;
-        g.KT = 3 * L / 32;
-        g.kseg_tiles = L / 32;
-        g.a_seg_x[0] = 0; g.a_seg_x[1] = 0; g.a_seg_x[2] = L;
-        g.b_seg_x[0] = 0; g.b_seg_x[1] = L; g.b_seg_x[2] = 0;
+        g.kseg_tiles = RK / 32;
+        if (p->route_hidden) {
+            g.KT = 2 * RK / 32;
+            g.a_seg_x[0] = 0; g.a_seg_x[1] = RK;
+            g.b_seg_x[0] = 0; g.b_seg_x[1] = 0;
+        } else {
+            g.KT = 3 * RK / 32;
+            g.a_seg_x[0] = 0; g.a_seg_x[1] = 0; g.a_seg_x[2] = RK;
+            g.b_seg_x[0] = 0; g.b_seg_x[1] = RK; g.b_seg_x[2] = 0;
+        }
         g.dense = 1;
         g.m_tiles = E / kBlockM;
         g.n_tokens = T;
@@ -593,7 +613,10 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
         shape_gemm(g, 0, items, std::min(items, p->num_sms));
         TRY(launch_gemm(g, std::min(items, p->num_sms), s));
     } else {
-        TRY(launch_router(p->z, p->router, p->logits, T, E, L, s));
+        if (p->route_hidden)
+            TRY(launch_router(p->xr, D, 0, p->router, p->logits, T, E, D, s));
+        else
+            TRY(launch_router(p->z, 2 * L, L, p->router, p->logits, T, E, L, s));
     }
     mark(3);
     {
@@ -606,9 +629,11 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
         a.softmax = p->cfg.score_fn == MOE_SCORE_SOFTMAX;
         a.refine = tc_logits ? 1 : 0;
         a.delta = kTcRouterDelta;
-        a.z = p->z;
+        a.z = p->route_hidden ? p->xr : p->z;
+        a.z_ld = p->route_hidden ? D : 2 * L;
+        a.z_lo = p->route_hidden ? 0 : L;
         a.R = p->router;
-        a.L = L;
+        a.L = p->RK;
         a.idx = p->idx;
         a.w = p->gw;
         a.sel = p->sel;
@@ -714,7 +739,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
         g.m_tiles = D / kBlockM;
         g.n_tokens = T;
         g.epi_split = 1 << 30;
-        g.epi[0] = EpiParams{EPI_F32, 0, 0, 0, y, D, nullptr, 0, nullptr, 0};
+        g.epi[0] = EpiParams{EPI_F32, 0, 0, 0, static_cast<float*>(y), D, nullptr, 0, nullptr, 0, 0, p->out_bf16 ? 1 : 0};
         const int items = g.m_tiles * ((T + g.n_max - 1) / g.n_max);
         shape_gemm(g, 0, items, std::min(items, p->num_sms));
         TRY(launch_gemm(g, std::min(items, p->num_sms), s));
@@ -755,7 +780,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, float* y, void* str
     return cuda_status(err);
 }
 
-moe_status moe_forward_host(void* plan, const uint16_t* x_host, int32_t T, float* y_host, void* stream) {
+moe_status moe_forward_host(void* plan, const uint16_t* x_host, int32_t T, void* y_host, void* stream) {
     Plan* p = static_cast<Plan*>(plan);
     if (!p || !x_host || !y_host) return MOE_ERR_INVALID_ARG;
     if (T < 1 || T > p->T_max) return MOE_ERR_INVALID_ARG;
@@ -765,7 +790,8 @@ moe_status moe_forward_host(void* plan, const uint16_t* x_host, int32_t T, float
     if (err != cudaSuccess) return cuda_status(err);
     moe_status st = moe_forward(plan, p->x_stage, T, p->y_stage, stream, nullptr);
     if (st != MOE_OK) return st;
-    err = cudaMemcpyAsync(y_host, p->y_stage, sizeof(float) * T * p->D, cudaMemcpyDeviceToHost, s);
+    err = cudaMemcpyAsync(y_host, p->y_stage, (p->out_bf16 ? 2 : 4) * static_cast<size_t>(T) * p->D,
+                          cudaMemcpyDeviceToHost, s);
     if (err == cudaSuccess) err = cudaStreamSynchronize(s);
     return cuda_status(err);
 }

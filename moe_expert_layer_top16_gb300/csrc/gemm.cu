@@ -108,6 +108,7 @@ __device__ __forceinline__ void pin_epi(EpiParams& e) {
     e.out_sf = pin(e.out_sf);
     e.sf_pitch = pin(e.sf_pitch);
     e.sf_item = pin(e.sf_item);
+    e.out_bf16 = pin(e.out_bf16);
 }
 
 // Item `it`.  Grouped items come from the per-expert tables staged in shared
@@ -516,6 +517,7 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
             E.out_sf = second ? E1.out_sf : E0.out_sf;
             E.sf_pitch = second ? E1.sf_pitch : E0.sf_pitch;
             E.sf_item = second ? E1.sf_item : E0.sf_item;
+            E.out_bf16 = second ? E1.out_bf16 : E0.out_bf16;
             const int rel_mt = w.mt - E.m_tile0;
             for (int n0 = n_first; n0 < nm; n0 += n_step) {
                 // sum of the K-split partial accumulators, in group order
@@ -570,9 +572,17 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                     const int nv = min(16, w.n - n0);                 // valid tokens of this chunk
                     const int64_t row0 = w.b_row0 + n0;
                     if (!kQuant || E.mode != EPI_QUANT) {
-                        // fp32 only: one store per valid token through a running pointer
+                        // fp32 (or bf16) only: one store per valid token through a running pointer
                         float* o = E.out_f32 + row0 * E.ld_f32 + col;
-                        if (E.f32_split) {
+                        if (E.out_bf16) {
+                            __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(E.out_f32) + row0 * E.ld_f32 + col;
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                if (i >= nv) break;
+                                ob[0] = __float2bfloat16_rn(v[i]);
+                                ob += E.ld_f32;
+                            }
+                        } else if (E.f32_split) {
 #pragma unroll
                             for (int i = 0; i < 16; ++i) {
                                 if (i >= nv) break;

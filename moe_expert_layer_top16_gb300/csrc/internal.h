@@ -43,6 +43,7 @@ struct EpiParams {
     uint8_t* out_sf;    // scale planes: uint32 word per (col/128, row), byte (col%128)/32
     int64_t sf_pitch;   // rows (raw planes) or 16-byte slots (item-atom planes) per plane
     int sf_item;        // 1: item-atom planes keyed by the output item's first row; 0: raw planes
+    int out_bf16;       // EPI_F32: out_f32 points at bf16 storage (ld_f32 in elements), values rounded to nearest
 };
 
 enum GemmKind : int {
@@ -101,13 +102,17 @@ cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s);
 
 // ------------------------------------------------------------------ other kernels
 // xsf: item-atom planes of a dense GEMM with token tiles of n_max
+// xf (optional): x as fp32 [T][D]
 cudaError_t launch_quant_x(const __nv_bfloat16* x, int T, int D, uint8_t* xq, uint8_t* xsf, int64_t pitch, int n_max,
-                           cudaStream_t s);
+                           float* xf, cudaStream_t s);
 // SIMT router on z = hi + lo ([T][2L]) writing logits [T][E]; batches of at
 // most kRouterSplitTokens tokens split K kRouterSplit ways over a cluster.
 constexpr int kRouterSplit = 8;
 constexpr int kRouterSplitTokens = 128;
-cudaError_t launch_router(const float* z, const float* R, float* logits, int T, int E, int L, cudaStream_t s);
+// z: router input rows of ld floats, K = L values, with their exact
+// remainders at offset lo (lo = 0: none); R [E][L]
+cudaError_t launch_router(const float* z, int ld, int lo, const float* R, float* logits, int T, int E, int L,
+                          cudaStream_t s);
 // top-k + gates (kernels.cu): with refine, the logits are
 // approximate within delta and the candidates' exact logits are recomputed
 // from z ([T][2L], hi | lo) and R ([E][L]).
@@ -117,8 +122,9 @@ struct TopkArgs {
     int T, E, k, softmax;
     int refine;
     float delta;
-    const float* z;
-    const float* R;
+    const float* z;         // router input rows (z_ld floats): K = L values, remainders at z_lo (0: none)
+    int z_ld, z_lo;
+    const float* R;         // [E][L]
     int L;
     int32_t* idx;
     float* w;

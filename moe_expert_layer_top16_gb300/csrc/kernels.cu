@@ -21,7 +21,7 @@ __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b -
 // 8 lanes form one 32-element block.  Scales go to the item-atom planes of
 // the GEMM that reads xq (token tiles of n_max rows; mx.cuh).
 __global__ void quant_x_kernel(const __nv_bfloat16* __restrict__ x, int T, int D, uint8_t* __restrict__ xq,
-                               uint8_t* __restrict__ xsf, int64_t pitch, int n_max) {
+                               uint8_t* __restrict__ xsf, int64_t pitch, int n_max, float* __restrict__ xf) {
     const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     const int tiles = D / 128;
@@ -35,6 +35,7 @@ __global__ void quant_x_kernel(const __nv_bfloat16* __restrict__ x, int T, int D
     v[1] = __uint_as_float(raw.x & 0xFFFF0000u);
     v[2] = __uint_as_float(raw.y << 16);
     v[3] = __uint_as_float(raw.y & 0xFFFF0000u);
+    if (xf) *reinterpret_cast<float4*>(xf + off) = make_float4(v[0], v[1], v[2], v[3]);   // x as fp32, exactly
     float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
     for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -61,8 +62,9 @@ __global__ void quant_x_kernel(const __nv_bfloat16* __restrict__ x, int T, int D
 // slices staged through shared memory, 4x4 outputs per thread.
 constexpr int RT = 64, RE = 64, RK = 16;
 __global__ void __launch_bounds__(256) router_kernel(const float* __restrict__ z, const float* __restrict__ R,
-                                                     float* __restrict__ logits, int T, int E, int L) {
-    // z: [T][2L] = TF32 high part | remainder; z = hi + lo exactly
+                                                     float* __restrict__ logits, int T, int E, int L, int ld, int lo) {
+    // z: rows of `ld` floats holding the router input (K = L) and, at offset
+    // lo > 0, its exact remainder (the input is hi + lo); lo = 0: no remainder
     __shared__ float zs[RK][RT + 4];
     __shared__ float rs[RK][RE + 4];
     const int t0 = blockIdx.y * RT, e0 = blockIdx.x * RE;
@@ -71,8 +73,8 @@ __global__ void __launch_bounds__(256) router_kernel(const float* __restrict__ z
     for (int k0 = 0; k0 < L; k0 += RK) {
         for (int i = threadIdx.x; i < RT * RK; i += 256) {
             const int r = i / RK, c = i % RK;
-            const float* zr = z + static_cast<int64_t>(t0 + r) * 2 * L + k0 + c;
-            zs[c][r] = (t0 + r < T) ? zr[0] + zr[L] : 0.0f;
+            const float* zr = z + static_cast<int64_t>(t0 + r) * ld + k0 + c;
+            zs[c][r] = (t0 + r < T) ? zr[0] + (lo ? zr[lo] : 0.0f) : 0.0f;
             rs[c][r] = (e0 + r < E) ? R[static_cast<int64_t>(e0 + r) * L + k0 + c] : 0.0f;
         }
         __syncthreads();
@@ -114,7 +116,7 @@ __global__ void __launch_bounds__(256) router_kernel(const float* __restrict__ z
 constexpr int RC_T = 64, RC_E = 32, RC_K = 32;
 __global__ void __cluster_dims__(1, 1, kRouterSplit) __launch_bounds__(256)
     router_cluster_kernel(const float* __restrict__ z, const float* __restrict__ R, float* __restrict__ logits, int T,
-                          int E, int L, int kper) {
+                          int E, int L, int ld, int lo, int kper) {
     __shared__ __align__(16) float zs[RC_K][RC_T + 4];     // [k][token]
     __shared__ __align__(16) float rs[RC_K][RC_E + 4];     // [k][expert]
     __shared__ float red[RC_T * RC_E];                     // this split's partial tile [token][expert]
@@ -131,10 +133,10 @@ __global__ void __cluster_dims__(1, 1, kRouterSplit) __launch_bounds__(256)
         for (int u = 0; u < 2; ++u) {
             const int i = threadIdx.x + 256 * u;
             const int r = i >> 3, c = (i & 7) * 4;
-            const float* zr = z + static_cast<int64_t>(t0 + r) * 2 * L + k0 + c;
+            const float* zr = z + static_cast<int64_t>(t0 + r) * ld + k0 + c;
             const bool tv = t0 + r < T;
             zh[u] = tv ? *reinterpret_cast<const float4*>(zr) : make_float4(0.f, 0.f, 0.f, 0.f);
-            zl[u] = tv ? *reinterpret_cast<const float4*>(zr + L) : make_float4(0.f, 0.f, 0.f, 0.f);
+            zl[u] = (tv && lo) ? *reinterpret_cast<const float4*>(zr + lo) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         const int r = threadIdx.x >> 3, c = (threadIdx.x & 7) * 4;
         rv = (e0 + r < E) ? *reinterpret_cast<const float4*>(R + static_cast<int64_t>(e0 + r) * L + k0 + c)
@@ -237,14 +239,15 @@ __device__ __forceinline__ double key64(float l, const float* bias, int e) {
     return 1.0 / (1.0 + exp(-static_cast<double>(l))) + static_cast<double>(bias[e]);
 }
 
-// Exact fp32 logit of expert `e` for the token whose latent is zt = [hi | lo]
-// (z = hi + lo): lane-strided FMA chains, then a fixed butterfly reduction.
-// Every lane returns the same value.
-__device__ __forceinline__ float exact_logit(const float* __restrict__ zt, const float* __restrict__ R, int e, int L,
-                                             int lane) {
+// Exact fp32 logit of expert `e` for the token whose router input row is zt
+// (K values, plus their exact remainders at offset lo when lo > 0):
+// lane-strided FMA chains, then a fixed butterfly reduction.  Every lane
+// returns the same value.
+__device__ __forceinline__ float exact_logit(const float* __restrict__ zt, int lo, const float* __restrict__ R, int e,
+                                             int L, int lane) {
     const float* r = R + static_cast<int64_t>(e) * L;
     float acc = 0.0f;
-    for (int i = lane; i < L; i += 32) acc = fmaf(zt[i] + zt[L + i], r[i], acc);
+    for (int i = lane; i < L; i += 32) acc = fmaf(zt[i] + (lo ? zt[lo + i] : 0.0f), r[i], acc);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     return acc;
@@ -252,7 +255,7 @@ __device__ __forceinline__ float exact_logit(const float* __restrict__ zt, const
 
 // The same for four experts at once (each chain identical to exact_logit's;
 // z is read once for the four).
-__device__ __forceinline__ void exact_logit4(const float* __restrict__ zt, const float* __restrict__ R,
+__device__ __forceinline__ void exact_logit4(const float* __restrict__ zt, int lo, const float* __restrict__ R,
                                              const int (&e)[4], int L, int lane, float (&out)[4]) {
     const float* r0 = R + static_cast<int64_t>(e[0]) * L;
     const float* r1 = R + static_cast<int64_t>(e[1]) * L;
@@ -261,7 +264,7 @@ __device__ __forceinline__ void exact_logit4(const float* __restrict__ zt, const
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll 4
     for (int i = lane; i < L; i += 32) {
-        const float zv = zt[i] + zt[L + i];
+        const float zv = zt[i] + (lo ? zt[lo + i] : 0.0f);
         a0 = fmaf(zv, r0[i], a0);
         a1 = fmaf(zv, r1[i], a1);
         a2 = fmaf(zv, r2[i], a2);
@@ -290,7 +293,7 @@ __device__ __noinline__ void topk_finish(const TopkArgs& a, int t, int lane, int
     const bool use_bias = (bias != nullptr) && !a.softmax;
     const bool approx = a.refine != 0;
     const bool need_cand = use_bias || approx;
-    const float* zt = a.z + static_cast<int64_t>(t) * 2 * a.L;
+    const float* zt = a.z + static_cast<int64_t>(t) * a.z_ld;
     const int nper = (E + 31) / 32;
     uint32_t taken = 0;
     int slot = lane;                                          // final slot of this lane's pick
@@ -302,7 +305,7 @@ __device__ __noinline__ void topk_finish(const TopkArgs& a, int t, int lane, int
 #pragma unroll
                 for (int u = 0; u < 4; ++u) ids[u] = __shfl_sync(0xffffffffu, my_id, min(c + u, R - 1));
                 float v[4];
-                exact_logit4(zt, a.R, ids, a.L, lane, v);
+                exact_logit4(zt, a.z_lo, a.R, ids, a.L, lane, v);
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
                     if (lane == c + u) my_l = v[u];
@@ -328,7 +331,7 @@ __device__ __noinline__ void topk_finish(const TopkArgs& a, int t, int lane, int
             // every expert, k rounds over all of them
             if (approx) {
                 for (int e = 0; e < E; ++e) {
-                    const float v = exact_logit(zt, a.R, e, a.L, lane);
+                    const float v = exact_logit(zt, a.z_lo, a.R, e, a.L, lane);
                     if (lane == 0) l[e] = v;
                 }
                 __syncwarp();
@@ -850,25 +853,26 @@ __global__ void gather_rows_kernel(const uint8_t* __restrict__ src, int64_t src_
 }  // namespace
 
 cudaError_t launch_quant_x(const __nv_bfloat16* x, int T, int D, uint8_t* xq, uint8_t* xsf, int64_t pitch, int n_max,
-                           cudaStream_t s) {
+                           float* xf, cudaStream_t s) {
     if (n_max <= 0) return cudaErrorInvalidValue;
     const int64_t warps = static_cast<int64_t>(T) * (D / 128);
     const int blocks = static_cast<int>((warps * 32 + 255) / 256);
-    quant_x_kernel<<<blocks, 256, 0, s>>>(x, T, D, xq, xsf, pitch, n_max);
+    quant_x_kernel<<<blocks, 256, 0, s>>>(x, T, D, xq, xsf, pitch, n_max, xf);
     return cudaGetLastError();
 }
 
-cudaError_t launch_router(const float* z, const float* R, float* logits, int T, int E, int L, cudaStream_t s) {
-    if (L % 4) return cudaErrorInvalidValue;
+cudaError_t launch_router(const float* z, int ld, int lo, const float* R, float* logits, int T, int E, int L,
+                          cudaStream_t s) {
+    if (L % 4 || ld % 4 || lo % 4) return cudaErrorInvalidValue;
     if (T <= kRouterSplitTokens && L % RC_K == 0) {
         static_assert(RC_T * RC_E == 256 * kRouterSplit, "one reduced output per thread");
         const int kper = ceil_div(L / RC_K, kRouterSplit) * RC_K;
         dim3 grid((E + RC_E - 1) / RC_E, (T + RC_T - 1) / RC_T, kRouterSplit);
-        router_cluster_kernel<<<grid, 256, 0, s>>>(z, R, logits, T, E, L, kper);
+        router_cluster_kernel<<<grid, 256, 0, s>>>(z, R, logits, T, E, L, ld, lo, kper);
         return cudaGetLastError();
     }
     dim3 grid((E + RE - 1) / RE, (T + RT - 1) / RT);
-    router_kernel<<<grid, 256, 0, s>>>(z, R, logits, T, E, L);
+    router_kernel<<<grid, 256, 0, s>>>(z, R, logits, T, E, L, ld, lo);
     return cudaGetLastError();
 }
 

@@ -48,13 +48,14 @@ def test_status_strings(L):
 
 def _cfg(**kw):
     base = dict(d_model=256, d_latent=128, n_experts=32, top_k=4, expert_inter=64, n_shared=1, shared_inter=128,
-                max_tokens=64, score_fn=1)
+                max_tokens=64, score_fn=1, route_input=0, out_dtype=0)
     base.update(kw)
     return moe._Config(*[base[f] for f, _ in moe._Config._fields_])
 
 
 @pytest.mark.parametrize("bad", [dict(d_model=200), dict(d_latent=96), dict(expert_inter=48), dict(top_k=0),
                                  dict(top_k=33), dict(top_k=40, n_experts=32), dict(n_experts=0), dict(n_experts=2048),
+                                 dict(route_input=2), dict(out_dtype=2), dict(route_input=-1),
                                  dict(max_tokens=0), dict(max_tokens=70000), dict(score_fn=7),
                                  dict(n_shared=1, shared_inter=0)])
 def test_plan_rejects_bad_config_without_a_device(L, bad):
