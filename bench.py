@@ -280,11 +280,20 @@ def run_cuda(args, wl, world, rank, local):
     counts_h = counts.cpu().numpy()
 
     K = args.steps
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(K)]
-    for evs in stage_ev:
-        for e in evs:
-            e.record()
+    # per-stage breakdown: a separate, untimed pass with events between the stages
+    n_stage = min(K, 20)
+    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(n_stage)]
+    for i in range(n_stage):
+        flush.fill_(float(i))
+        plan.forward(x, out=y, stage_events=stage_ev[i])
+    torch.cuda.synchronize()
+    stage_ms = np.array([[stage_ev[i][s].elapsed_time(stage_ev[i][s + 1]) for s in range(nst)]
+                         for i in range(n_stage)])
+
+    # timed region: exactly K forwards, each between two events on the forward's
+    # stream; the L2 flush sits between steps, outside the events
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     torch.cuda.synchronize()
     try:
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
@@ -297,8 +306,10 @@ def run_cuda(args, wl, world, rank, local):
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     for i in range(K):
-        flush.fill_(float(i))                       # L2 flush, outside the per-step events
-        plan.forward(x, out=y, stage_events=stage_ev[i])
+        flush.fill_(float(i))                       # L2 flush, outside the step events
+        ev0[i].record()
+        plan.forward(x, out=y)
+        ev1[i].record()
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - wall0
@@ -306,8 +317,7 @@ def run_cuda(args, wl, world, rank, local):
     if plan.device_status() != moe.MOE_OK:
         raise RuntimeError("device-side error in the timed region")
 
-    step_ms = [stage_ev[i][0].elapsed_time(stage_ev[i][nst]) for i in range(K)]
-    stage_ms = np.array([[stage_ev[i][s].elapsed_time(stage_ev[i][s + 1]) for s in range(nst)] for i in range(K)])
+    step_ms = [ev0[i].elapsed_time(ev1[i]) for i in range(K)]
     total_ms = max_over_ranks(world, float(np.sum(step_ms)))
     ms_per_step = total_ms / K
     value = world * T * K / (total_ms / 1e3)
@@ -357,6 +367,8 @@ def run_cuda(args, wl, world, rank, local):
     result = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "step_ms": {"median": float(np.median(step_ms)), "p10": float(np.percentile(step_ms, 10)),
+                    "p90": float(np.percentile(step_ms, 90))},
         "dtype": "mxfp4 weights x mxfp8 activations, fp32 accumulate", "data": "synthetic",
         "config": {"workload": wl.name, "tokens": T, "d_model": wl.d_model, "d_latent": wl.d_latent,
                    "experts": wl.n_experts, "top_k": wl.top_k, "expert_inter": wl.expert_inter,
@@ -369,6 +381,9 @@ def run_cuda(args, wl, world, rank, local):
                   "expert_weight_frac_hbm": expert_bytes / step_s / 1e9 / hbm,
                   "algorithmic_bytes": layer_bytes, "mx_tflops": layer_flops / step_s / 1e12,
                   "mx_frac_fp8_peak": layer_flops / step_s / 1e12 / (bf16 * 2.0),
+                  # the same against the FP4-only rate (kind::mxf4, nominally 6x bf16), which a
+                  # W4A8 product cannot reach: at most 1/3 of it
+                  "mx_frac_fp4_peak": layer_flops / step_s / 1e12 / (bf16 * 6.0),
                   "max_over_mean_load": float(counts_h.max() / max(counts_h.mean(), 1e-9)),
                   "stage_ms": {n: float(v) for n, v in zip(names, mean_stage)}},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": int(T * wl.d_model * 2),
@@ -401,6 +416,63 @@ def run_cuda(args, wl, world, rank, local):
     return 0
 
 
+def run_sweep(args, wl, rank, local):
+    """The layer at every batch size of the sweep (one plan), against both
+    rooflines: expert-weight bytes over HBM bandwidth, MX FLOPs over the
+    tensor peak.  The crossover is where the second overtakes the first."""
+    import torch
+    import synth
+    import moe_expert_layer_top16_gb300 as moe
+    from moe_expert_layer_top16_gb300 import build as mbuild
+    from moe_expert_layer_top16_gb300.weights import encode_layer
+
+    mbuild.build()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    Tmax = max(synth.SWEEP_TOKENS)
+
+    def fetch(name, i):
+        if name == "bias":
+            return synth.router_bias(wl, device=dev)
+        return synth.weight(wl, name, i, device=dev)
+
+    W = encode_layer(wl, fetch, dev)
+    plan = moe.Plan(wl, W, max_tokens=Tmax)
+    del W
+    torch.cuda.empty_cache()
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    hbm, bf16, _, _ = peaks()
+    for T in synth.SWEEP_TOKENS:
+        x = synth.hidden_states(wl, T, device=dev)
+        y = torch.empty(T, wl.d_model, dtype=plan.out_dtype, device=dev)
+        counts = torch.zeros(wl.n_experts, dtype=torch.int32, device=dev)
+        for i in range(args.warmup):
+            plan.forward(x, out=y, debug={"counts": counts} if i == 0 else None)
+        torch.cuda.synchronize()
+        steps = max(5, min(args.steps, (200 * 64) // T))
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(steps):
+            flush.fill_(float(i))
+            ev[i][0].record()
+            plan.forward(x, out=y)
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        if plan.device_status() != moe.MOE_OK:
+            raise RuntimeError(f"device-side error at T={T}")
+        ms = float(np.median([a.elapsed_time(b) for a, b in ev]))
+        work, touched, expert_bytes = algorithmic_work(wl, T, counts.cpu().numpy())
+        flops = sum(f for _, f in work.values())
+        line = {"impl": "sweep", "workload": wl.name, "tokens": T, "ms_median": ms, "tokens_per_s": T / (ms / 1e3),
+                "touched_experts": touched, "expert_weight_GBps": expert_bytes / (ms / 1e3) / 1e9,
+                "expert_weight_frac_hbm": expert_bytes / (ms / 1e3) / 1e9 / hbm,
+                "mx_tflops": flops / (ms / 1e3) / 1e12, "mx_frac_fp8_peak": flops / (ms / 1e3) / 1e12 / (bf16 * 2.0),
+                "steps": steps, "l2": "flushed between steps"}
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+    plan.close()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -411,6 +483,8 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=64)
     ap.add_argument("--reference-tokens", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="token-count sweep of the workload's layer: one JSON line per batch size")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -419,6 +493,8 @@ def main():
     world, rank, local = dist_setup()
     if args.impl == "reference":
         return run_reference(args, wl, world, rank)
+    if args.sweep:
+        return run_sweep(args, wl, rank, local)
     return run_cuda(args, wl, world, rank, local)
 
 
