@@ -283,6 +283,10 @@ def run_cuda(args, wl, world, rank, local):
     # per-stage breakdown: a separate, untimed pass with events between the stages
     n_stage = min(K, 20)
     stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(n_stage)]
+    for evs in stage_ev:                 # torch creates the CUDA events at their first record
+        for e in evs:
+            e.record()
+    torch.cuda.synchronize()
     for i in range(n_stage):
         flush.fill_(float(i))
         plan.forward(x, out=y, stage_events=stage_ev[i])

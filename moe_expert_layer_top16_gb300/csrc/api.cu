@@ -99,10 +99,12 @@ bool map_mx8(CUtensorMap* m, const void* codes, int64_t rows, int64_t K, int box
 inline int64_t rup(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
 
 // Bound on |tensor-core logit - fp32 logit| assumed by the top-k refinement.
-// The 3xTF32 product accumulated by the tensor core (which rounds its fp32
-// accumulator toward zero at every step) stays within ~5e-4 of the fp64
-// logit on the K3-shaped layer; the bound leaves a factor 8.
-constexpr float kTcRouterDelta = 4.0e-3f;
+// One TF32 product z_hi R_hi (both rounded to TF32, the fp32 accumulator of
+// the tensor core rounding toward zero at every step) stays within ~3e-3 of
+// the fp64 logit on the K3-shaped layer; the bound leaves a factor of 7.  The
+// refinement recomputes every candidate within 2 * delta of the k-th estimate
+// exactly, so delta sets how many candidates are recomputed, not the result.
+constexpr float kTcRouterDelta = 2.0e-2f;
 
 struct Plan {
     moe_config cfg;
@@ -587,23 +589,15 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
     mark(2);
     const bool tc_logits = p->tc_router && T > 128;
     if (tc_logits) {
-        // logits = z R^T as three TF32 products, z_hi R_hi + z_lo R_hi + z_hi R_lo,
-        // K-concatenated through the maps' coordinates into one accumulator.
-        // Hidden routing: x is bf16, so x_hi = x and x_lo = 0: x R_hi + x R_lo.
+        // estimated logits = z_hi R_hi, one TF32 product on the tensor cores
+        // (the high parts sit at the start of each row of z and router2; for
+        // hidden routing x is bf16, so its TF32 value is x itself)
         const int RK = p->RK;
-        GemmParams g = gemm_base(p->tAR, p->tBR, nullptr, nullptr, 0, 3 * RK * 4, nmax_dense, E,
+        GemmParams g = gemm_base(p->tAR, p->tBR, nullptr, nullptr, 0, RK * 4, nmax_dense, E,
                                  static_cast<int>(Tp), p->status);
         g.kind = KIND_TF32;
+        g.KT = RK / 32;
         g.kseg_tiles = RK / 32;
-        if (p->route_hidden) {
-            g.KT = 2 * RK / 32;
-            g.a_seg_x[0] = 0; g.a_seg_x[1] = RK;
-            g.b_seg_x[0] = 0; g.b_seg_x[1] = 0;
-        } else {
-            g.KT = 3 * RK / 32;
-            g.a_seg_x[0] = 0; g.a_seg_x[1] = 0; g.a_seg_x[2] = RK;
-            g.b_seg_x[0] = 0; g.b_seg_x[1] = RK; g.b_seg_x[2] = 0;
-        }
         g.dense = 1;
         g.m_tiles = E / kBlockM;
         g.n_tokens = T;

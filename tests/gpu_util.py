@@ -197,11 +197,12 @@ def run_sampled_parity(wl, plan, ol, T, sample, x=None):
     r0 = oracle.moe_forward(wl, ol.ensure([]), xb, route_only=True, want=("idx", "logits", "xq", "xs"))
     assert (r0["xq"] == g["xq"][sample]).all() and (r0["xs"] == g["xs"][sample]).all()
     # the selected experts' logits are fp32-accurate; above 128 tokens the
-    # others come from the tensor-core router (3xTF32, error well below 2e-3)
+    # others are tensor-core estimates (one TF32 product), within the bound
+    # the top-k refinement assumes (2e-2)
     sel = g["topk_idx"][sample].astype(np.int64)
     assert np.max(np.abs(np.take_along_axis(g["logits"][sample], sel, 1)
                          - np.take_along_axis(r0["logits"], sel, 1))) <= 1e-4
-    assert np.max(np.abs(g["logits"][sample] - r0["logits"])) <= 2e-3
+    assert np.max(np.abs(g["logits"][sample] - r0["logits"])) <= (2e-2 if T > 128 else 1e-4)
     accepted = certify_routing(ol, g["topk_idx"][sample], r0["idx"], g["logits"][sample], r0["logits"])
     lw = ol.ensure(np.concatenate([g["topk_idx"][sample].ravel(), r0["idx"].ravel()]))
     ref = oracle.moe_forward(wl, lw, xb, force_idx=g["topk_idx"][sample], want=("y",))
