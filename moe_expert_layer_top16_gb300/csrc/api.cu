@@ -106,6 +106,10 @@ inline int64_t rup(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
 // exactly, so delta sets how many candidates are recomputed, not the result.
 constexpr float kTcRouterDelta = 2.0e-2f;
 
+// Token-bitmap words per expert up to which the work-list kernel also does the
+// per-expert scan (batches of up to 2048 tokens).
+constexpr int kFusedScanWords = 64;
+
 struct Plan {
     moe_config cfg;
     int device = 0, num_sms = 0;
@@ -636,12 +640,17 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
     }
     // 5. per-expert prefix counts, 6. offsets + work lists
     mark(4);
-    TRY(launch_expert_scan(p->sel, E, W, p->wpre, p->counts, s));
+    const bool fused_scan = W <= kFusedScanWords;     // small batches: one launch for scan + work lists
+    if (!fused_scan) TRY(launch_expert_scan(p->sel, E, W, p->wpre, p->counts, s));
     mark(5);
     {
         WorkListArgs a;
         a.counts = p->counts;
         a.E = E;
+        a.sel = fused_scan ? p->sel : nullptr;
+        a.W = W;
+        a.wpre = p->wpre;
+        a.counts_out = p->counts;
         a.offsets = p->offsets;
         a.seg = p->seg;
         a.ioff1 = p->ioff7;

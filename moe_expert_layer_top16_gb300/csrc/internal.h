@@ -136,6 +136,12 @@ cudaError_t launch_expert_scan(const uint32_t* sel, int E, int W, int32_t* wpre,
 struct WorkListArgs {
     const int32_t* counts;
     int E;
+    // small batches: the per-expert scan of the token bitmaps happens here
+    // too (sel [E][W] words in, wpre [E][W] and counts out); null = done before
+    const uint32_t* sel;
+    int W;
+    int32_t* wpre;
+    int32_t* counts_out;
     int32_t* offsets;    // [E+1] exclusive scan of counts
     int32_t* seg;        // [E+1] exclusive scan of counts rounded up to 16 (row starts in permuted buffers)
     int32_t* ioff1; int n_max1; int mt1;   // [E+1] item offsets of the gate/up GEMM

@@ -589,7 +589,19 @@ __global__ void __launch_bounds__(1024) worklist_kernel(WorkListArgs a) {
     __shared__ int4 warp_tot[32];
     const int E = a.E;
     const int e = threadIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int n = (e < E) ? a.counts[e] : 0;
+    int n = 0;
+    if (a.sel) {
+        // expert e's prefix popcounts over its token bitmap (as expert_scan_kernel)
+        if (e < E) {
+            for (int w = 0; w < a.W; ++w) {
+                a.wpre[static_cast<int64_t>(e) * a.W + w] = n;
+                n += __popc(a.sel[static_cast<int64_t>(e) * a.W + w]);
+            }
+            a.counts_out[e] = n;
+        }
+    } else {
+        n = (e < E) ? a.counts[e] : 0;
+    }
     const int4 v = make_int4(n, (n + 15) & ~15, ceil_div(n, a.n_max1) * a.mt1, ceil_div(n, a.n_max2) * a.mt2);
     int4 inc = v;
 #pragma unroll
