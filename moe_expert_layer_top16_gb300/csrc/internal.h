@@ -130,6 +130,7 @@ struct TopkArgs {
     float* w;
     uint32_t* sel;
     int W;
+    float band_pad;         // set by launch_topk: twice the key-estimate error bound, rounded up
 };
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
 cudaError_t launch_expert_scan(const uint32_t* sel, int E, int W, int32_t* wpre, int32_t* counts, cudaStream_t s);

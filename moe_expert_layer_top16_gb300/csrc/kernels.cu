@@ -216,23 +216,25 @@ constexpr int kTopkPerLane = 32;     // E <= 1024
 constexpr int kMaxE = 32 * kTopkPerLane;
 constexpr float kKeyErr = 4.0e-6f;   // error bound of the fp32 sigmoid(l) + b estimate
 
-struct KeyId {
-    float key;
-    int id;
-};
+// Keys as unsigned integers that order like the floats (larger key, larger
+// integer; -inf above every "no entry" value 0), so that a selection round
+// is two warp reductions: the largest key, then the lowest expert id among
+// the lanes holding it.
+__device__ __forceinline__ uint32_t key_bits(float k) {
+    if (k == 0.0f) k = 0.0f;                  // -0 ties with +0, as the floats compare
+    const uint32_t u = __float_as_uint(k);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float bits_key(uint32_t b) {
+    return __uint_as_float((b & 0x80000000u) ? (b & 0x7fffffffu) : ~b);
+}
+constexpr uint32_t kNoKey = 0u;
 
-// warp-wide maximum of (key, id) ordered by key desc, id asc; id == INT_MAX = none
-__device__ __forceinline__ KeyId warp_best(KeyId v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float ok = __shfl_xor_sync(0xffffffffu, v.key, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, v.id, o);
-        if (oi != 0x7fffffff && (v.id == 0x7fffffff || ok > v.key || (ok == v.key && oi < v.id))) {
-            v.key = ok;
-            v.id = oi;
-        }
-    }
-    return v;
+// The warp's best (key bits, id) pair: key desc, id asc.  Returns id
+// 0x7fffffff when no lane holds an entry.
+__device__ __forceinline__ int warp_best_id(uint32_t kb, int id, uint32_t& best) {
+    best = __reduce_max_sync(0xffffffffu, kb);
+    return __reduce_min_sync(0xffffffffu, (kb == best && kb != kNoKey) ? id : 0x7fffffff);
 }
 
 __device__ __forceinline__ double key64(float l, const float* bias, int e) {
@@ -408,14 +410,14 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(TopkArgs a) {
     const bool approx = a.refine != 0;
     const bool need_cand = use_bias || approx;
     const int nper = (E + 31) / 32;
-    float key[kTopkPerLane];                                  // selection-key estimates, expert lane + 32 i
+    uint32_t key[kTopkPerLane];                               // selection-key estimates (key_bits), expert lane + 32 i
 #pragma unroll
     for (int i = 0; i < kTopkPerLane; ++i) {
         const int e = lane + 32 * i;
         float kv = (i < nper && e < E) ? l[e] : 0.0f;
         if (use_bias) kv = 1.0f / (1.0f + __expf(-kv)) + bias[e < E ? e : 0];
         if (kv != kv) kv = -INFINITY;                         // NaN ranks last
-        key[i] = (i < nper && e < E) ? kv : -INFINITY;
+        key[i] = (i < nper && e < E) ? key_bits(kv) : kNoKey;
     }
     uint32_t taken = 0;                                       // bit i: candidate lane + 32 i selected
     // Candidates, in estimate order: the k best estimates, then every further
@@ -430,131 +432,98 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(TopkArgs a) {
     float kth_est = 0.0f;
     for (int j = 0; j <= 32; ++j) {
         if (j >= k && !need_cand) break;
-        KeyId b = {-INFINITY, 0x7fffffff};
+        // this lane's best untaken entry (entries ascend in id, so the first
+        // of equal keys is the lowest id)
+        uint32_t lb = kNoKey;
+        int lid = 0x7fffffff;
 #pragma unroll
         for (int i = 0; i < kTopkPerLane; ++i) {
-            const int e = lane + 32 * i;
-            if (i < nper && e < E && !(taken & (1u << i)) &&
-                (b.id == 0x7fffffff || key[i] > b.key || (key[i] == b.key && e < b.id))) {
-                b.key = key[i];
-                b.id = e;
+            const uint32_t kv = (taken & (1u << i)) ? kNoKey : key[i];
+            if (kv > lb) {
+                lb = kv;
+                lid = lane + 32 * i;
             }
         }
-        b = warp_best(b);
+        uint32_t bb;
+        int bid = warp_best_id(lb, lid, bb);
+        const float bkey = bits_key(bb);
         if (j >= k) {
             // band test in double: kth_est - 2 err is not rounded toward the candidate
-            if (b.id < 0 || b.id >= E || !(static_cast<double>(b.key) >= static_cast<double>(kth_est) - 2.0 * err))
+            if (bid < 0 || bid >= E || !(static_cast<double>(bkey) >= static_cast<double>(kth_est) - 2.0 * err))
                 break;
             if (j == 32) {
                 overflow = true;
                 break;
             }
         }
-        if (b.id < 0 || b.id >= E) b.id = 0;                 // unreachable while k <= E
-        if (j == k - 1) kth_est = b.key;
-        if (lane == j) my_id = b.id;
-        if ((b.id & 31) == lane) taken |= 1u << (b.id >> 5);
+        if (bid < 0 || bid >= E) bid = 0;                    // unreachable while k <= E
+        if (j == k - 1) kth_est = bkey;
+        if (lane == j) my_id = bid;
+        if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
         R = j + 1;
     }
     topk_finish(a, t, lane, R, overflow, my_id);
 }
 
-// Selection rounds over NPL (key, id) entries per lane (id < 0: empty): the k
-// best estimates, then every further entry within 2 * err of the k-th, at
-// most 32 (more: overflow).  Lane j < R receives the j-th pick.
-template <int NPL>
-__device__ __forceinline__ void pick_rounds(const float (&key)[NPL], const int (&eid)[NPL], int k, bool band,
-                                            double err, int lane, int& R, bool& overflow, int& my_id,
-                                            float& my_key) {
-    uint32_t taken = 0;
-    float kth = 0.0f;
-    R = 0;
-    overflow = false;
-    for (int j = 0; j <= 32; ++j) {
-        if (j >= k && !band) break;
-        KeyId b = {-INFINITY, 0x7fffffff};
-#pragma unroll
-        for (int i = 0; i < NPL; ++i)
-            if (eid[i] >= 0 && !(taken & (1u << i)) &&
-                (b.id == 0x7fffffff || key[i] > b.key || (key[i] == b.key && eid[i] < b.id))) {
-                b.key = key[i];
-                b.id = eid[i];
-            }
-        b = warp_best(b);
-        if (b.id == 0x7fffffff) break;                       // no entries left
-        if (j >= k) {
-            if (!(static_cast<double>(b.key) >= static_cast<double>(kth) - 2.0 * err)) break;
-            if (j == 32) {
-                overflow = true;
-                break;
-            }
-        }
-        if (j == k - 1) kth = b.key;
-        if (lane == j) {
-            my_id = b.id;
-            my_key = b.key;
-        }
-#pragma unroll
-        for (int i = 0; i < NPL; ++i)
-            if (eid[i] == b.id) taken |= 1u << i;
-        R = j + 1;
-    }
-}
-
-// Top-k of small batches: one CTA of 8 warps per token.  Warp w estimates the
-// keys of experts lane + 32 (w + 8 i) and picks its own top-k plus every
-// expert within 2 * err of its own k-th estimate -- a superset of the
-// token's candidates, since a warp's k-th estimate is never above the
-// token's.  Warp 0 merges the picks the same way and finishes as topk_kernel.
-constexpr int kTopkWideWarps = 8;
-constexpr int kTopkWidePerLane = kMaxE / (32 * kTopkWideWarps);      // 4
-__global__ void __launch_bounds__(kTopkWideWarps * 32) topk_wide_kernel(TopkArgs a) {
-    __shared__ float s_key[kTopkWideWarps][32];
-    __shared__ int s_id[kTopkWideWarps][32];
-    __shared__ int s_n[kTopkWideWarps];
-    __shared__ int s_over;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// Top-k of small batches: one CTA per token, one thread per expert.  The
+// k-th largest key is found bit by bit with block-wide counts (the largest
+// v with at least k keys >= v); the candidates are the keys >= v, or, with
+// an error band, the keys >= the k-th estimate - 2 err (more than 32:
+// overflow).  Each candidate's rank among the candidates (larger key, or
+// equal key and lower id, first) orders them, and warp 0 finishes as
+// topk_kernel.  Every step is a short chain: this batch size is latency-bound.
+constexpr int kTopkWideThreads = kMaxE;
+constexpr int kRankCap = 33;
+__global__ void __launch_bounds__(kTopkWideThreads) topk_wide_kernel(TopkArgs a) {
+    __shared__ int s_cand[kMaxE];
+    __shared__ uint32_t s_ckb[kMaxE];
+    __shared__ int s_rank[kRankCap];
+    __shared__ int s_n;
+    const int lane = threadIdx.x & 31;
     const int t = blockIdx.x;
     const int E = a.E, k = a.k;
-    const float* l = a.logits + static_cast<int64_t>(t) * E;
-    const float* bias = a.bias;
-    const bool use_bias = (bias != nullptr) && !a.softmax;
-    const bool approx = a.refine != 0;
-    const bool band = use_bias || approx;
-    const double err = approx ? (use_bias ? 0.25 * a.delta + kKeyErr : a.delta) : kKeyErr;
-    if (threadIdx.x == 0) s_over = 0;
-    float key[kTopkWidePerLane];
-    int eid[kTopkWidePerLane];
-#pragma unroll
-    for (int i = 0; i < kTopkWidePerLane; ++i) {
-        const int e = lane + 32 * (warp + kTopkWideWarps * i);
-        float kv = (e < E) ? l[e] : 0.0f;
-        if (use_bias && e < E) kv = 1.0f / (1.0f + __expf(-kv)) + bias[e];
-        if (kv != kv) kv = -INFINITY;
-        key[i] = kv;
-        eid[i] = (e < E) ? e : -1;
+    const int e = threadIdx.x;
+    const bool use_bias = (a.bias != nullptr) && !a.softmax;
+    const bool band = use_bias || a.refine != 0;
+    uint32_t kb = kNoKey;
+    if (e < E) {
+        float kv = a.logits[static_cast<int64_t>(t) * E + e];
+        if (use_bias) kv = 1.0f / (1.0f + __expf(-kv)) + a.bias[e];
+        if (kv != kv) kv = -INFINITY;                         // NaN ranks last
+        kb = key_bits(kv);
     }
-    int R, my_id = 0;
-    bool over;
-    float my_key = 0.0f;
-    pick_rounds(key, eid, k, band, err, lane, R, over, my_id, my_key);
-    s_key[warp][lane] = my_key;
-    s_id[warp][lane] = my_id;
-    if (lane == 0) {
-        s_n[warp] = R;
-        if (over) s_over = 1;
+    if (threadIdx.x == 0) s_n = 0;
+    uint32_t v = 0;
+    for (int bit = 31; bit >= 0; --bit) {
+        const uint32_t tv = v | (1u << bit);
+        if (__syncthreads_count(kb >= tv) >= k) v = tv;
+    }
+    uint32_t lo = v;
+    if (band) lo = min(v, key_bits(__fsub_rd(bits_key(v), a.band_pad)));
+    if (e < E && kb >= lo) {
+        const int i = atomicAdd(&s_n, 1);
+        s_cand[i] = e;
+        s_ckb[i] = kb;
     }
     __syncthreads();
-    if (warp != 0) return;
-    float mkey[kTopkWideWarps];
-    int mid[kTopkWideWarps];
-#pragma unroll
-    for (int i = 0; i < kTopkWideWarps; ++i) {       // entry lane of warp i's picks
-        mkey[i] = s_key[i][lane];
-        mid[i] = (lane < s_n[i]) ? s_id[i][lane] : -1;
+    const int n = s_n;
+    for (int i = threadIdx.x; i < n; i += kTopkWideThreads) {
+        const uint32_t ki = s_ckb[i];
+        const int ei = s_cand[i];
+        int r = 0;
+        for (int j = 0; j < n; ++j) {
+            const uint32_t kj = s_ckb[j];
+            r += (kj > ki || (kj == ki && s_cand[j] < ei)) ? 1 : 0;
+        }
+        if (r < kRankCap) s_rank[r] = ei;
     }
-    pick_rounds(mkey, mid, k, band, err, lane, R, over, my_id, my_key);
-    topk_finish(a, t, lane, R, over || s_over != 0, my_id);
+    __syncthreads();
+    if (threadIdx.x >= 32) return;
+    int R = band ? n : k;
+    const bool over = R > 32;
+    if (over) R = 32;
+    const int my_id = (lane < R) ? s_rank[lane] : 0;
+    topk_finish(a, t, lane, R, over, my_id);
 }
 
 // ------------------------------------------------------------------ A5: per-expert scan
@@ -889,11 +858,17 @@ cudaError_t launch_router(const float* z, int ld, int lo, const float* R, float*
 }
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
-    if (a.E > kMaxE || a.k > 32) return cudaErrorInvalidValue;
+    if (a.E > kMaxE || a.k > 32 || a.k < 1 || a.k > a.E) return cudaErrorInvalidValue;
+    // the candidate band below the k-th estimate: twice the error bound, rounded up
+    TopkArgs b = a;
+    const bool use_bias = (a.bias != nullptr) && !a.softmax;
+    const double err = a.refine ? (use_bias ? 0.25 * a.delta + kKeyErr : a.delta) : kKeyErr;
+    b.band_pad = static_cast<float>(2.0 * err);
+    if (static_cast<double>(b.band_pad) < 2.0 * err) b.band_pad = nextafterf(b.band_pad, INFINITY);
     if (a.T <= kTopkWideTokens)
-        topk_wide_kernel<<<a.T, kTopkWideWarps * 32, 0, s>>>(a);
+        topk_wide_kernel<<<a.T, kTopkWideThreads, 0, s>>>(b);
     else
-        topk_kernel<<<(a.T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, s>>>(a);
+        topk_kernel<<<(a.T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, s>>>(b);
     return cudaGetLastError();
 }
 

@@ -12,15 +12,29 @@ from gpu_util import OracleLayer, gpu_plan, run_sampled_parity
 pytestmark = pytest.mark.gpu
 
 
-def test_zipf16384():
+@pytest.fixture(scope="module")
+def zipf():
     wl = synth.workload("zipf16384")
     plan, _ = gpu_plan(wl)
     ol = OracleLayer(wl)
-    try:
-        accepted, errs, counts = run_sampled_parity(wl, plan, ol, 16384, [0, 5000, 12345, 16383])
-    finally:
-        plan.close()
+    yield wl, plan, ol
+    plan.close()
+
+
+def test_zipf16384(zipf):
+    wl, plan, ol = zipf
+    accepted, errs, counts = run_sampled_parity(wl, plan, ol, 16384, [0, 5000, 12345, 16383])
     assert len(accepted) <= 1
     mean = 16384 * 16 / 896
     assert counts.max() > 10 * mean, f"hottest expert {counts.max()} vs mean {mean:.1f}"
     assert (counts == 0).sum() > 0
+
+
+@pytest.mark.parametrize("T", [1, 64, 300])
+def test_zipf_small_batches(zipf, T):
+    """Small batches take the one-CTA-per-token top-k; with the bias every
+    selection goes through the candidate band and the fp64 key ranking (and,
+    above 128 tokens, the tensor-core logit estimates' band as well)."""
+    wl, plan, ol = zipf
+    accepted, errs, counts = run_sampled_parity(wl, plan, ol, T, [0, T // 2, T - 1])
+    assert len(accepted) <= 1
