@@ -177,7 +177,9 @@ __device__ __forceinline__ void group_range(int KT, int g, int G, int& kb, int& 
 // Shared memory after the stages: epilogue exchange buffer (2 x 2 warps x
 // 32 lanes x 16 floats), then the barriers, then the grouped-item tables.
 constexpr int kSplitChunksMin = 32;   // items of this many tokens or more share their chunks among warpgroups
-constexpr int kXbufBytes = kEpiGroups * 2 * 2 * 32 * 16 * 4;    // per epilogue warpgroup: 2 chunks x 2 warps
+constexpr int kXchgBytes = kEpiGroups * 2 * 2 * 32 * 16 * 4;    // SiLU exchange, per warpgroup: 2 chunks x 2 warps
+constexpr int kQStageBytes = 4 * kEpiGroups * 512;              // per epilogue warp: 16 tokens x 32 codes
+constexpr int kXbufBytes = kXchgBytes + kQStageBytes;
 constexpr int kMaxStagesPerGroup = 16;
 // barriers, TMEM slot + abort flag (16 bytes), then the [G][2] item slots
 constexpr int kBarBytes = (kMaxGroups * (2 * kMaxStagesPerGroup + 2 * 2 + 1)) * 8 + 16 + kMaxGroups * 2 * 16;
@@ -237,9 +239,11 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
     const int S_all = pin(p.stages);        // stages of all groups; group g has S_all / G (+1 for g < S_all % G)
     const int NB = pin(p.acc_bufs);         // accumulator buffers per group
     const SmemLayout L = stage_layout(h.n_max);
-    constexpr int kXbuf = kSilu ? kXbufBytes : 0;
+    constexpr int kXbuf = (kSilu || kQuant) ? kXbufBytes : 0;
     uint8_t* tail = base + S_all * h.stage_bytes;
     float* xbuf = reinterpret_cast<float*>(tail);
+    // MXFP8 codes of a chunk are staged per warp, then stored as 16-byte rows
+    uint8_t* qstage = tail + kXchgBytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(tail + kXbuf);           // [G][kMaxStagesPerGroup]
     uint64_t* empty = full + kMaxGroups * kMaxStagesPerGroup;              // [G][kMaxStagesPerGroup]
     uint64_t* tfull = empty + kMaxGroups * kMaxStagesPerGroup;             // [G][2]
@@ -550,8 +554,10 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                     for (int i = 0; i < 8; ++i)                  // hand over the other half
                         xb[blk * 512 + ((gate_warp ? 8 : 0) + i) * 32 + lane] = gate_warp ? v[8 + i] : v[i];
                     named_bar_sync(bar_xchg, 128);
-                    const int64_t col = E.col0 + static_cast<int64_t>(rel_mt) * 64 + 32 * blk + lane;
+                    const int64_t col_blk = E.col0 + static_cast<int64_t>(rel_mt) * 64 + 32 * blk;
                     const int nv = min(8, w.n - n0 - t0);
+                    uint8_t* stg = qstage + (warp - 2 * G) * 512;            // [token][32 codes]
+                    uint8_t my_sc = 0;                                       // lane i: scale of token i
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         if (i >= nv) break;
@@ -559,14 +565,20 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                         const float other = xb[blk * 512 + (t0 + i) * 32 + lane];
                         const float hv = gate_warp ? silu_f(mine) * other : silu_f(other) * mine;
                         uint8_t sc;
-                        const uint8_t code = warp_mx8_quant(hv, &sc);
-                        const int n = n0 + t0 + i;
-                        const int64_t row = w.b_row0 + n;
-                        E.out_q[row * E.ld_q + col] = code;
-                        if (lane == 0)
-                            E.out_sf[E.sf_item ? sf_atom_offset(w.b_row0, n, col, E.sf_pitch)
-                                               : sf_byte_offset(row, col, E.sf_pitch)] = sc;
+                        stg[i * 32 + lane] = warp_mx8_quant(hv, &sc);
+                        if (lane == i) my_sc = sc;
                     }
+                    __syncwarp();
+                    const int64_t row0 = w.b_row0 + n0 + t0;
+                    if (lane < 2 * nv) {
+                        const int i = lane >> 1, hf = lane & 1;
+                        *reinterpret_cast<uint4*>(E.out_q + (row0 + i) * E.ld_q + col_blk + 16 * hf) =
+                            *reinterpret_cast<const uint4*>(stg + i * 32 + 16 * hf);
+                    }
+                    if (lane < nv)
+                        E.out_sf[E.sf_item ? sf_atom_offset(w.b_row0, n0 + t0 + lane, col_blk, E.sf_pitch)
+                                           : sf_byte_offset(row0 + lane, col_blk, E.sf_pitch)] = my_sc;
+                    __syncwarp();
                 } else {
                     const int64_t col = E.col0 + static_cast<int64_t>(rel_mt) * 128 + 32 * q + lane;
                     const int nv = min(16, w.n - n0);                 // valid tokens of this chunk
@@ -600,6 +612,8 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                             }
                         }
                     } else {
+                        uint8_t* stg = qstage + (warp - 2 * G) * 512;        // [token][32 codes]
+                        uint8_t my_sc = 0;                                   // lane i: scale of token i
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
                             if (i >= nv) break;
@@ -614,12 +628,20 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                                 }
                             }
                             uint8_t sc;
-                            const uint8_t code = warp_mx8_quant(v[i], &sc);
-                            E.out_q[row * E.ld_q + col] = code;
-                            if (lane == 0)
-                                E.out_sf[E.sf_item ? sf_atom_offset(w.b_row0, n0 + i, col, E.sf_pitch)
-                                                   : sf_byte_offset(row, col, E.sf_pitch)] = sc;
+                            stg[i * 32 + lane] = warp_mx8_quant(v[i], &sc);
+                            if (lane == i) my_sc = sc;
                         }
+                        __syncwarp();
+                        const int64_t col_blk = col - lane;
+                        if (lane < 2 * nv) {
+                            const int i = lane >> 1, hf = lane & 1;
+                            *reinterpret_cast<uint4*>(E.out_q + (row0 + i) * E.ld_q + col_blk + 16 * hf) =
+                                *reinterpret_cast<const uint4*>(stg + i * 32 + 16 * hf);
+                        }
+                        if (lane < nv)
+                            E.out_sf[E.sf_item ? sf_atom_offset(w.b_row0, n0 + lane, col_blk, E.sf_pitch)
+                                               : sf_byte_offset(row0 + lane, col_blk, E.sf_pitch)] = my_sc;
+                        __syncwarp();
                     }
                 }
             }
@@ -693,7 +715,7 @@ int epi_set(const GemmParams& p) {
 
 bool gemm_needs_xbuf(const GemmParams& p) {
     const int set = epi_set(p);
-    return set == SET_SILU || set == SET_DUAL;
+    return set == SET_SILU || set == SET_DUAL || set == SET_QUANT;
 }
 
 cudaError_t gemm_setup() {

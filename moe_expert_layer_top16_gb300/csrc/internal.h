@@ -92,7 +92,8 @@ struct GemmParams {
 
 int gemm_stage_bytes(int n_max);
 // total shared-memory stages of a launch (all groups); E > 0: grouped items
-// (per-expert tables in shared memory); xbuf: the SiLU exchange buffer
+// (per-expert tables in shared memory); xbuf: the SiLU exchange buffer and the
+// per-warp staging of MXFP8 output codes (quantising epilogues)
 int gemm_stages(int n_max, int groups, int E, bool xbuf);
 size_t gemm_smem_bytes(int n_max, int stages, int E, bool xbuf);
 bool gemm_needs_xbuf(const GemmParams& p);
