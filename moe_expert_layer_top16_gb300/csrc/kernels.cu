@@ -17,42 +17,54 @@ namespace {
 __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // ------------------------------------------------------------------ A1: x -> MXFP8
-// One warp per (row, 128-wide column tile); lane l owns elements 4l..4l+3, so
-// 8 lanes form one 32-element block.  Scales go to the item-atom planes of
-// the GEMM that reads xq (token tiles of n_max rows; mx.cuh).
+// One warp per (row, group of kQxTiles 128-wide column tiles): the group's
+// loads are issued together, then each tile is quantised; lane l owns
+// elements 4l..4l+3 of a tile, so 8 lanes form one 32-element block.  Scales
+// go to the item-atom planes of the GEMM that reads xq (token tiles of n_max
+// rows; mx.cuh).
+constexpr int kQxTiles = 4;
 __global__ void quant_x_kernel(const __nv_bfloat16* __restrict__ x, int T, int D, uint8_t* __restrict__ xq,
                                uint8_t* __restrict__ xsf, int64_t pitch, int n_max, float* __restrict__ xf) {
     const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     const int tiles = D / 128;
-    if (gw >= static_cast<int64_t>(T) * tiles) return;
-    const int64_t row = gw / tiles;
-    const int tile = static_cast<int>(gw % tiles);
-    const int64_t off = row * D + tile * 128 + lane * 4;
-    const uint2 raw = *reinterpret_cast<const uint2*>(x + off);
-    float v[4];
-    v[0] = __uint_as_float(raw.x << 16);
-    v[1] = __uint_as_float(raw.x & 0xFFFF0000u);
-    v[2] = __uint_as_float(raw.y << 16);
-    v[3] = __uint_as_float(raw.y & 0xFFFF0000u);
-    if (xf) *reinterpret_cast<float4*>(xf + off) = make_float4(v[0], v[1], v[2], v[3]);   // x as fp32, exactly
-    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+    const int groups = (tiles + kQxTiles - 1) / kQxTiles;
+    if (gw >= static_cast<int64_t>(T) * groups) return;
+    const int64_t row = gw / groups;
+    const int tile0 = static_cast<int>(gw % groups) * kQxTiles;
+    const int nt = min(kQxTiles, tiles - tile0);
+    uint2 raw[kQxTiles];
 #pragma unroll
-    for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const int e = mx8_exponent(amax);
-    const float inv = exp2i(-e);
-    uint32_t packed = 0;
+    for (int j = 0; j < kQxTiles; ++j)
+        if (j < nt) raw[j] = *reinterpret_cast<const uint2*>(x + row * D + (tile0 + j) * 128 + lane * 4);
+    const int64_t b0 = (row / n_max) * n_max;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) packed |= static_cast<uint32_t>(f32_to_e4m3(v[i] * inv)) << (8 * i);
-    *reinterpret_cast<uint32_t*>(xq + off) = packed;
-    // gather the 4 block scales (lanes 0, 8, 16, 24) into one word
-    const uint32_t sc = static_cast<uint32_t>(e + 127);
-    uint32_t word = 0;
+    for (int j = 0; j < kQxTiles; ++j) {
+        if (j >= nt) break;
+        const int tile = tile0 + j;
+        const int64_t off = row * D + tile * 128 + lane * 4;
+        float v[4];
+        v[0] = __uint_as_float(raw[j].x << 16);
+        v[1] = __uint_as_float(raw[j].x & 0xFFFF0000u);
+        v[2] = __uint_as_float(raw[j].y << 16);
+        v[3] = __uint_as_float(raw[j].y & 0xFFFF0000u);
+        if (xf) *reinterpret_cast<float4*>(xf + off) = make_float4(v[0], v[1], v[2], v[3]);   // x as fp32, exactly
+        float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
-    for (int b = 0; b < 4; ++b) word |= __shfl_sync(0xffffffffu, sc, b * 8) << (8 * b);
-    if (lane == 0) {
-        const int64_t b0 = (row / n_max) * n_max;
-        *reinterpret_cast<uint32_t*>(xsf + sf_atom_offset(b0, static_cast<int>(row - b0), tile * 128, pitch)) = word;
+        for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const int e = mx8_exponent(amax);
+        const float inv = exp2i(-e);
+        uint32_t packed = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) packed |= static_cast<uint32_t>(f32_to_e4m3(v[i] * inv)) << (8 * i);
+        *reinterpret_cast<uint32_t*>(xq + off) = packed;
+        // gather the 4 block scales (lanes 0, 8, 16, 24) into one word
+        const uint32_t sc = static_cast<uint32_t>(e + 127);
+        uint32_t word = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) word |= __shfl_sync(0xffffffffu, sc, b * 8) << (8 * b);
+        if (lane == 0)
+            *reinterpret_cast<uint32_t*>(xsf + sf_atom_offset(b0, static_cast<int>(row - b0), tile * 128, pitch)) = word;
     }
 }
 
@@ -629,6 +641,20 @@ __global__ void scatter_kernel(ScatterArgs a) {
     if (gw >= static_cast<int64_t>(a.T) * a.k) return;
     const int t = static_cast<int>(gw / a.k);
     const int e = a.idx[gw];
+    // the token's codes and scale words do not depend on where they go: their
+    // loads are issued before the rank's (up to 4096 codes a row from registers)
+    constexpr int kRowRegs = 8;
+    const int n16 = a.L / 16, n128 = a.L / 128;
+    const bool in_regs = n16 <= 32 * kRowRegs;
+    const uint4* src = reinterpret_cast<const uint4*>(a.zq + static_cast<int64_t>(t) * a.L);
+    uint4 buf[kRowRegs];
+    if (in_regs) {
+#pragma unroll
+        for (int j = 0; j < kRowRegs; ++j)
+            if (lane + 32 * j < n16) buf[j] = src[lane + 32 * j];
+    }
+    const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(a.zsf);
+    const uint32_t sw = (lane < n128) ? ssrc[lane * a.zsf_pitch + t] : 0u;
     const int w = t >> 5;
     const uint32_t bits = a.sel[static_cast<int64_t>(e) * a.W + w] & ((1u << (t & 31)) - 1u);
     const int rank = a.wpre[static_cast<int64_t>(e) * a.W + w] + __popc(bits);
@@ -639,14 +665,20 @@ __global__ void scatter_kernel(ScatterArgs a) {
         a.canon_to_pad[canon] = pos;
         a.sorted_token[canon] = t;
     }
-    const uint4* src = reinterpret_cast<const uint4*>(a.zq + static_cast<int64_t>(t) * a.L);
     uint4* dst = reinterpret_cast<uint4*>(a.zq_perm + static_cast<int64_t>(pos) * a.L);
-    for (int i = lane; i < a.L / 16; i += 32) dst[i] = src[i];
+    if (in_regs) {
+#pragma unroll
+        for (int j = 0; j < kRowRegs; ++j)
+            if (lane + 32 * j < n16) dst[lane + 32 * j] = buf[j];
+    } else {
+        for (int i = lane; i < n16; i += 32) dst[i] = src[i];
+    }
     // scales: raw planes in, item-atom planes of the grouped GEMM's token tile out
-    const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(a.zsf);
     const int64_t b0 = a.seg[e] + (rank / a.n_max) * a.n_max;
     const int l = rank % a.n_max;
-    for (int kt = lane; kt < a.L / 128; kt += 32)
+    if (lane < n128)
+        *reinterpret_cast<uint32_t*>(a.zq_perm_sf + sf_atom_offset(b0, l, static_cast<int64_t>(lane) * 128, a.perm_pitch)) = sw;
+    for (int kt = lane + 32; kt < n128; kt += 32)
         *reinterpret_cast<uint32_t*>(a.zq_perm_sf + sf_atom_offset(b0, l, static_cast<int64_t>(kt) * 128, a.perm_pitch)) =
             ssrc[kt * a.zsf_pitch + t];
 }
@@ -836,7 +868,7 @@ __global__ void gather_rows_kernel(const uint8_t* __restrict__ src, int64_t src_
 cudaError_t launch_quant_x(const __nv_bfloat16* x, int T, int D, uint8_t* xq, uint8_t* xsf, int64_t pitch, int n_max,
                            float* xf, cudaStream_t s) {
     if (n_max <= 0) return cudaErrorInvalidValue;
-    const int64_t warps = static_cast<int64_t>(T) * (D / 128);
+    const int64_t warps = static_cast<int64_t>(T) * ((D / 128 + kQxTiles - 1) / kQxTiles);
     const int blocks = static_cast<int>((warps * 32 + 255) / 256);
     quant_x_kernel<<<blocks, 256, 0, s>>>(x, T, D, xq, xsf, pitch, n_max, xf);
     return cudaGetLastError();
