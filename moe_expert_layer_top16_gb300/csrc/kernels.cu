@@ -253,48 +253,48 @@ __device__ __forceinline__ double key64(float l, const float* bias, int e) {
     return 1.0 / (1.0 + exp(-static_cast<double>(l))) + static_cast<double>(bias[e]);
 }
 
-// Exact fp32 logit of expert `e` for the token whose router input row is zt
-// (K values, plus their exact remainders at offset lo when lo > 0):
-// lane-strided FMA chains, then a fixed butterfly reduction.  Every lane
-// returns the same value.
-__device__ __forceinline__ float exact_logit(const float* __restrict__ zt, int lo, const float* __restrict__ R, int e,
-                                             int L, int lane) {
-    const float* r = R + static_cast<int64_t>(e) * L;
-    float acc = 0.0f;
-    for (int i = lane; i < L; i += 32) acc = fmaf(zt[i] + (lo ? zt[lo + i] : 0.0f), r[i], acc);
+// Exact fp32 logits of NE experts e[0..NE) for the token whose router input
+// row is zt (L values, plus their exact remainders at offset lo when lo > 0):
+// lane l runs one FMA chain per expert over elements 4l + 128j .. 4l + 128j
+// + 3, j = 0, 1, ... in order, then a fixed butterfly sums the lanes; every
+// lane returns the values.  The chain of an expert does not depend on NE or
+// on the other experts, so every path gives the same logit.  16-byte loads,
+// all NE rows of a step in flight together.  L % 128 == 0, 16-byte rows.
+template <int NE>
+__device__ __forceinline__ void exact_logits(const float* __restrict__ zt, int lo, const float* __restrict__ R,
+                                             const int* e, int L, int lane, float* out) {
+    const float* r[NE];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    return acc;
-}
-
-// The same for four experts at once (each chain identical to exact_logit's;
-// z is read once for the four).
-__device__ __forceinline__ void exact_logit4(const float* __restrict__ zt, int lo, const float* __restrict__ R,
-                                             const int (&e)[4], int L, int lane, float (&out)[4]) {
-    const float* r0 = R + static_cast<int64_t>(e[0]) * L;
-    const float* r1 = R + static_cast<int64_t>(e[1]) * L;
-    const float* r2 = R + static_cast<int64_t>(e[2]) * L;
-    const float* r3 = R + static_cast<int64_t>(e[3]) * L;
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll 4
-    for (int i = lane; i < L; i += 32) {
-        const float zv = zt[i] + (lo ? zt[lo + i] : 0.0f);
-        a0 = fmaf(zv, r0[i], a0);
-        a1 = fmaf(zv, r1[i], a1);
-        a2 = fmaf(zv, r2[i], a2);
-        a3 = fmaf(zv, r3[i], a3);
+    for (int u = 0; u < NE; ++u) r[u] = R + static_cast<int64_t>(e[u]) * L;
+    float acc[NE];
+#pragma unroll
+    for (int u = 0; u < NE; ++u) acc[u] = 0.0f;
+    for (int i = 4 * lane; i < L; i += 128) {
+        float4 z4 = __ldg(reinterpret_cast<const float4*>(zt + i));
+        if (lo) {
+            const float4 q = __ldg(reinterpret_cast<const float4*>(zt + lo + i));
+            z4.x += q.x;
+            z4.y += q.y;
+            z4.z += q.z;
+            z4.w += q.w;
+        }
+        float4 r4[NE];
+#pragma unroll
+        for (int u = 0; u < NE; ++u) r4[u] = __ldg(reinterpret_cast<const float4*>(r[u] + i));
+#pragma unroll
+        for (int u = 0; u < NE; ++u) {
+            acc[u] = fmaf(z4.x, r4[u].x, acc[u]);
+            acc[u] = fmaf(z4.y, r4[u].y, acc[u]);
+            acc[u] = fmaf(z4.z, r4[u].z, acc[u]);
+            acc[u] = fmaf(z4.w, r4[u].w, acc[u]);
+        }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        a0 += __shfl_xor_sync(0xffffffffu, a0, o);
-        a1 += __shfl_xor_sync(0xffffffffu, a1, o);
-        a2 += __shfl_xor_sync(0xffffffffu, a2, o);
-        a3 += __shfl_xor_sync(0xffffffffu, a3, o);
-    }
-    out[0] = a0;
-    out[1] = a1;
-    out[2] = a2;
-    out[3] = a3;
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int u = 0; u < NE; ++u) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], o);
+#pragma unroll
+    for (int u = 0; u < NE; ++u) out[u] = acc[u];
 }
 
 // Second half of the top-k of token t, run by one warp: lane j < R holds the
@@ -314,15 +314,24 @@ __device__ __noinline__ void topk_finish(const TopkArgs& a, int t, int lane, int
     float my_l = 0.0f;                                        // exact logit of this lane's pick
     if (need_cand) {
         if (approx) {
-            for (int c = 0; c < R; c += 4) {
-                int ids[4];
+            // candidates in groups of up to 8 (z is read once per group)
+            for (int c = 0; c < R; c += 8) {
+                const int m = min(8, R - c);
+                int ids[8];
+                float v[8];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) ids[u] = __shfl_sync(0xffffffffu, my_id, min(c + u, R - 1));
-                float v[4];
-                exact_logit4(zt, a.z_lo, a.R, ids, a.L, lane, v);
+                for (int u = 0; u < 8; ++u) ids[u] = __shfl_sync(0xffffffffu, my_id, min(c + u, R - 1));
+                if (m > 4)
+                    exact_logits<8>(zt, a.z_lo, a.R, ids, a.L, lane, v);
+                else if (m > 2)
+                    exact_logits<4>(zt, a.z_lo, a.R, ids, a.L, lane, v);
+                else if (m > 1)
+                    exact_logits<2>(zt, a.z_lo, a.R, ids, a.L, lane, v);
+                else
+                    exact_logits<1>(zt, a.z_lo, a.R, ids, a.L, lane, v);
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    if (lane == c + u) my_l = v[u];
+                for (int u = 0; u < 8; ++u)
+                    if (u < m && lane == c + u) my_l = v[u];
             }
         } else if (lane < R) {
             my_l = l[my_id];
@@ -345,7 +354,8 @@ __device__ __noinline__ void topk_finish(const TopkArgs& a, int t, int lane, int
             // every expert, k rounds over all of them
             if (approx) {
                 for (int e = 0; e < E; ++e) {
-                    const float v = exact_logit(zt, a.z_lo, a.R, e, a.L, lane);
+                    float v;
+                    exact_logits<1>(zt, a.z_lo, a.R, &e, a.L, lane, &v);
                     if (lane == 0) l[e] = v;
                 }
                 __syncwarp();
@@ -891,6 +901,8 @@ cudaError_t launch_router(const float* z, int ld, int lo, const float* R, float*
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
     if (a.E > kMaxE || a.k > 32 || a.k < 1 || a.k > a.E) return cudaErrorInvalidValue;
+    // refinement reads router rows as 16-byte vectors, 128 values per warp step
+    if (a.refine && (a.L <= 0 || a.L % 128 || a.z_ld % 4 || a.z_lo % 4)) return cudaErrorInvalidValue;
     // the candidate band below the k-th estimate: twice the error bound, rounded up
     TopkArgs b = a;
     const bool use_bias = (a.bias != nullptr) && !a.softmax;
