@@ -52,8 +52,8 @@ CPU_BASELINE_SECONDS = 10.0
 # capture, and the commit the capture was taken at; a capture stands only
 # until its kernel changes (summaries under profiles/).
 NCU_TRAFFIC = {
-    ("decode64", "gemm_gate_up"): (1.331786e9 + 3.80672e6, "9156dbd", "profiles/gate_up_decode64.md"),
-    ("prefill8192", "gemm_gate_up"): (2.266808e9 + 69.22368e6, "9156dbd", "profiles/gate_up_prefill8192.md"),
+    ("decode64", "gemm_gate_up"): (1.331121e9 + 3.783424e6, "60ceff4", "profiles/gate_up_decode64.md"),
+    ("prefill8192", "gemm_gate_up"): (2.266878e9 + 69.639424e6, "60ceff4", "profiles/gate_up_prefill8192.md"),
 }
 
 
