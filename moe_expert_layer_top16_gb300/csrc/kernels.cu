@@ -223,7 +223,7 @@ __global__ void __cluster_dims__(1, 1, kRouterSplit) __launch_bounds__(256)
 // Gates: sigmoid(l_j) / sum over the winners (fp32), or softmax over the
 // winners' logits.  Each selection sets bit t of the expert's token bitmap.
 constexpr int kTopkWarps = 4;
-constexpr int kTopkWideTokens = 512;  // batches up to this size use one CTA per token
+constexpr int kTopkWideTokens = 512;  // batches up to this size use one CTA per token (without refinement)
 constexpr int kTopkPerLane = 32;     // E <= 1024
 constexpr int kMaxE = 32 * kTopkPerLane;
 constexpr float kKeyErr = 4.0e-6f;   // error bound of the fp32 sigmoid(l) + b estimate
@@ -909,7 +909,10 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
     const double err = a.refine ? (use_bias ? 0.25 * a.delta + kKeyErr : a.delta) : kKeyErr;
     b.band_pad = static_cast<float>(2.0 * err);
     if (static_cast<double>(b.band_pad) < 2.0 * err) b.band_pad = nextafterf(b.band_pad, INFINITY);
-    if (a.T <= kTopkWideTokens)
+    // one CTA per token for small batches with exact logits; a batch whose
+    // candidates need the exact refinement (one warp's work per token) runs a
+    // warp per token, so that many tokens refine at once
+    if (a.T <= kTopkWideTokens && !a.refine)
         topk_wide_kernel<<<a.T, kTopkWideThreads, 0, s>>>(b);
     else
         topk_kernel<<<(a.T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, s>>>(b);
