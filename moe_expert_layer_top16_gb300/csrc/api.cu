@@ -135,8 +135,8 @@ struct Plan {
     CUtensorMap tA2, tB2, tA7, tB7, tA8, tB8, tA10, tB10, tAR, tBR;
     // B maps with one box per wide work item (box height = that n_max),
     // re-encoded when a forward needs another height
-    CUtensorMap tB2w, tB10w, tB7w, tB8w;
-    int wide_dense = 0, wide_grp = 0;
+    CUtensorMap tB2w, tB10w, tB7w, tB8w, tBRw;
+    int wide_dense = 0, wide_grp = 0, wide_router = 0;
     bool tc_router;    // router logits on the tensor cores (3xTF32) for batches above 128 tokens
 };
 
@@ -557,6 +557,16 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
             return MOE_ERR_CUDA;
         p->wide_grp = nmax_grp;
     }
+    // router estimate token tiles: 64 rows up to 1024 tokens (more work items
+    // for the few expert tiles), else the dense tile with one B box per item
+    const int nmax_router = (T <= 1024) ? 64 : nmax_dense;
+    if (p->tc_router && T > 128 && nmax_router > kNarrowMax && p->wide_router != nmax_router) {
+        p->wide_router = 0;
+        const bool ok = p->route_hidden ? map_f32(&p->tBRw, p->xr, Tp, D, nmax_router)
+                                        : map_f32(&p->tBRw, p->z, Tp, 2 * L, nmax_router);
+        if (!ok) return MOE_ERR_CUDA;
+        p->wide_router = nmax_router;
+    }
     cudaError_t err = cudaSuccess;
 #define TRY(x)                          \
     do {                                \
@@ -597,8 +607,12 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         // (the high parts sit at the start of each row of z and router2; for
         // hidden routing x is bf16, so its TF32 value is x itself)
         const int RK = p->RK;
-        GemmParams g = gemm_base(p->tAR, p->tBR, nullptr, nullptr, 0, RK * 4, nmax_dense, E,
+        GemmParams g = gemm_base(p->tAR, p->tBR, nullptr, nullptr, 0, RK * 4, nmax_router, E,
                                  static_cast<int>(Tp), p->status);
+        if (nmax_router > kNarrowMax) {
+            g.tmB = p->tBRw;
+            g.b_box = nmax_router;
+        }
         g.kind = KIND_TF32;
         g.KT = RK / 32;
         g.kseg_tiles = RK / 32;
