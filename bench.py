@@ -60,9 +60,9 @@ NCU_TRAFFIC = {
 def launches_per_forward(T):
     """Kernels of this library one forward of T tokens launches: quantiser, A2,
     router (or its tensor-core estimate), top-k, per-expert scan (batches over
-    2048 tokens; folded into the work-list kernel below that), work lists,
+    128 tokens; folded into the work-list kernel below that), work lists,
     dispatch, A7, A8, combine, A10."""
-    return 10 + (1 if (T + 31) // 32 > 64 else 0)
+    return 10 + (1 if (T + 31) // 32 > 4 else 0)
 
 
 def algorithmic_work(wl, T, counts):

@@ -107,8 +107,9 @@ inline int64_t rup(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
 constexpr float kTcRouterDelta = 2.0e-2f;
 
 // Token-bitmap words per expert up to which the work-list kernel also does the
-// per-expert scan (batches of up to 2048 tokens).
-constexpr int kFusedScanWords = 64;
+// per-expert scan (batches of up to 128 tokens; above that one CTA scanning
+// all experts costs more than the extra launch).
+constexpr int kFusedScanWords = 4;
 
 struct Plan {
     moe_config cfg;
