@@ -116,16 +116,16 @@ __global__ void __launch_bounds__(256) router_kernel(const float* __restrict__ z
     }
 }
 
-// Decode-sized batches (T <= 128): 32 experts x 64 tokens per output tile,
+// Decode-sized batches (T <= 128): 64 experts x 64 tokens per output tile,
 // its K range split over the kRouterSplit CTAs of a thread-block cluster, so
-// that ~E/32 x 8 CTAs stream R from HBM in parallel while z (L2-resident) is
-// re-read only E/32 times.  Each CTA accumulates its K range in registers
+// that ~E/64 x 8 CTAs (one per SM) stream R from HBM in parallel while z
+// (L2-resident) is re-read only E/64 times.  Each CTA accumulates its K range in registers
 // (one sequential FMA chain per output, the next 32-wide K slice prefetched
 // into registers during the current one), leaves its partial tile in shared
 // memory, and after a cluster barrier reduces 1/8 of the tile by adding the 8
 // partials, read through distributed shared memory, in split order -- a
 // fixed order, so the logits are deterministic.
-constexpr int RC_T = 64, RC_E = 32, RC_K = 32;
+constexpr int RC_T = 64, RC_E = 64, RC_K = 32;
 __global__ void __cluster_dims__(1, 1, kRouterSplit) __launch_bounds__(256)
     router_cluster_kernel(const float* __restrict__ z, const float* __restrict__ R, float* __restrict__ logits, int T,
                           int E, int L, int ld, int lo, int kper) {
@@ -136,10 +136,10 @@ __global__ void __cluster_dims__(1, 1, kRouterSplit) __launch_bounds__(256)
     const int t0 = blockIdx.y * RC_T, e0 = blockIdx.x * RC_E;
     const int ks = static_cast<int>(cluster.block_rank());
     const int kb = ks * kper, ke = min(L, kb + kper);
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;   // experts 2tx, 2tx+1; tokens 4ty..4ty+3
-    float acc[4][2] = {};
-    // one K slice: z rows t0..t0+63 (hi and lo, 2 float4 each per thread), R rows e0..e0+31 (1 float4)
-    float4 zh[2], zl[2], rv;
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;   // experts 4tx..4tx+3; tokens 4ty..4ty+3
+    float acc[4][4] = {};
+    // one K slice: z rows t0..t0+63 (hi and lo, 2 float4 each per thread), R rows e0..e0+63 (2 float4)
+    float4 zh[2], zl[2], rv[2];
     auto load = [&](int k0) {
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
@@ -150,9 +150,13 @@ __global__ void __cluster_dims__(1, 1, kRouterSplit) __launch_bounds__(256)
             zh[u] = tv ? *reinterpret_cast<const float4*>(zr) : make_float4(0.f, 0.f, 0.f, 0.f);
             zl[u] = (tv && lo) ? *reinterpret_cast<const float4*>(zr + lo) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        const int r = threadIdx.x >> 3, c = (threadIdx.x & 7) * 4;
-        rv = (e0 + r < E) ? *reinterpret_cast<const float4*>(R + static_cast<int64_t>(e0 + r) * L + k0 + c)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int i = threadIdx.x + 256 * u;
+            const int r = i >> 3, c = (i & 7) * 4;
+            rv[u] = (e0 + r < E) ? *reinterpret_cast<const float4*>(R + static_cast<int64_t>(e0 + r) * L + k0 + c)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     };
     if (kb < ke) load(kb);
     for (int k0 = kb; k0 < ke; k0 += RC_K) {
@@ -165,41 +169,45 @@ __global__ void __cluster_dims__(1, 1, kRouterSplit) __launch_bounds__(256)
             zs[c + 2][r] = zh[u].z + zl[u].z;
             zs[c + 3][r] = zh[u].w + zl[u].w;
         }
-        {
-            const int r = threadIdx.x >> 3, c = (threadIdx.x & 7) * 4;
-            rs[c][r] = rv.x;
-            rs[c + 1][r] = rv.y;
-            rs[c + 2][r] = rv.z;
-            rs[c + 3][r] = rv.w;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int i = threadIdx.x + 256 * u;
+            const int r = i >> 3, c = (i & 7) * 4;
+            rs[c][r] = rv[u].x;
+            rs[c + 1][r] = rv[u].y;
+            rs[c + 2][r] = rv[u].z;
+            rs[c + 3][r] = rv[u].w;
         }
         __syncthreads();
         if (k0 + RC_K < ke) load(k0 + RC_K);
 #pragma unroll 8
         for (int kk = 0; kk < RC_K; ++kk) {
             const float4 a4 = *reinterpret_cast<const float4*>(&zs[kk][ty * 4]);
-            const float2 b2 = *reinterpret_cast<const float2*>(&rs[kk][tx * 2]);
+            const float4 b4 = *reinterpret_cast<const float4*>(&rs[kk][tx * 4]);
             const float a[4] = {a4.x, a4.y, a4.z, a4.w};
+            const float b[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-            for (int i2 = 0; i2 < 4; ++i2) {
-                acc[i2][0] = fmaf(a[i2], b2.x, acc[i2][0]);
-                acc[i2][1] = fmaf(a[i2], b2.y, acc[i2][1]);
-            }
+            for (int i2 = 0; i2 < 4; ++i2)
+#pragma unroll
+                for (int j2 = 0; j2 < 4; ++j2) acc[i2][j2] = fmaf(a[i2], b[j2], acc[i2][j2]);
         }
         __syncthreads();
     }
 #pragma unroll
-    for (int i2 = 0; i2 < 4; ++i2) {
-        red[(ty * 4 + i2) * RC_E + tx * 2] = acc[i2][0];
-        red[(ty * 4 + i2) * RC_E + tx * 2 + 1] = acc[i2][1];
-    }
-    cluster.sync();
-    // this CTA's eighth of the tile: 256 outputs, one per thread
-    const int o = ks * 256 + threadIdx.x;
-    const int tt = o / RC_E, ee = o % RC_E;
-    float v = 0.0f;
+    for (int i2 = 0; i2 < 4; ++i2)
 #pragma unroll
-    for (int q = 0; q < kRouterSplit; ++q) v += cluster.map_shared_rank(red, q)[o];
-    if (t0 + tt < T && e0 + ee < E) logits[static_cast<int64_t>(t0 + tt) * E + e0 + ee] = v;
+        for (int j2 = 0; j2 < 4; ++j2) red[(ty * 4 + i2) * RC_E + tx * 4 + j2] = acc[i2][j2];
+    cluster.sync();
+    // this CTA's eighth of the tile: 512 outputs, two per thread
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int o = ks * 512 + h * 256 + threadIdx.x;
+        const int tt = o / RC_E, ee = o % RC_E;
+        float v = 0.0f;
+#pragma unroll
+        for (int q = 0; q < kRouterSplit; ++q) v += cluster.map_shared_rank(red, q)[o];
+        if (t0 + tt < T && e0 + ee < E) logits[static_cast<int64_t>(t0 + tt) * E + e0 + ee] = v;
+    }
     cluster.sync();     // no CTA leaves while another still reads its tile
 }
 
@@ -888,7 +896,7 @@ cudaError_t launch_router(const float* z, int ld, int lo, const float* R, float*
                           cudaStream_t s) {
     if (L % 4 || ld % 4 || lo % 4) return cudaErrorInvalidValue;
     if (T <= kRouterSplitTokens && L % RC_K == 0) {
-        static_assert(RC_T * RC_E == 256 * kRouterSplit, "one reduced output per thread");
+        static_assert(RC_T * RC_E == 512 * kRouterSplit, "two reduced outputs per thread");
         const int kper = ceil_div(L / RC_K, kRouterSplit) * RC_K;
         dim3 grid((E + RC_E - 1) / RC_E, (T + RC_T - 1) / RC_T, kRouterSplit);
         router_cluster_kernel<<<grid, 256, 0, s>>>(z, R, logits, T, E, L, ld, lo, kper);
