@@ -1,0 +1,54 @@
+"""The measurement arithmetic of bench.py, checked against figures derived by
+hand from the layer's shapes: MXFP4 costs 17/32 bytes per element (4-bit
+codes plus one 8-bit scale per 32), one K3 routed expert (gate, up, down of
+inner 512 on the 3584 latent) is 5,505,024 elements, and the MX work of one
+token is the four block-scaled GEMMs' multiply-adds."""
+import importlib.util
+import os
+
+import numpy as np
+
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_expert_weight_bytes():
+    b = _bench()
+    wl = synth.workload("decode64")
+    counts = np.zeros(wl.n_experts, np.int32)
+    counts[:1] = 1
+    _, touched, one = b.algorithmic_work(wl, 1, counts)
+    shared = 3 * 2 * 2048 * 7168 * 17 // 32              # 46,792,704 B
+    assert touched == 1
+    assert one == 2_924_544 + shared                      # 5,505,024 elements x 17/32
+    counts[:] = 3
+    _, touched, allb = b.algorithmic_work(wl, 168, counts)
+    assert touched == 896
+    assert allb == 896 * 2_924_544 + shared               # all routed experts: 2.620 GB
+
+
+def test_mx_flops_per_token():
+    b = _bench()
+    wl = synth.workload("decode64")
+    counts = np.ones(wl.n_experts, np.int32)
+    work, _, _ = b.algorithmic_work(wl, 64, counts)
+    mx = sum(work[s][1] for s in ("gemm_down_shared", "gemm_gate_up", "gemm_down", "gemm_up_shared"))
+    # projections + shared (2 x 11776 x 7168 + 2 x 7168 x 7680) and routed (16 x 2 x (1024 + 512) x 3584)
+    assert mx / 64 == 455_081_984
+
+
+def test_launches_per_forward():
+    b = _bench()
+    # the per-expert scan is its own kernel above 128 tokens (four bitmap words)
+    assert b.launches_per_forward(1) == 10
+    assert b.launches_per_forward(128) == 10
+    assert b.launches_per_forward(129) == 11
+    assert b.launches_per_forward(8192) == 11
