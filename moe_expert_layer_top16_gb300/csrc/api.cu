@@ -138,7 +138,7 @@ struct Plan {
     // re-encoded when a forward needs another height
     CUtensorMap tB2w, tB10w, tB7w, tB8w, tBRw;
     int wide_dense = 0, wide_grp = 0, wide_router = 0;
-    bool tc_router;    // router logits on the tensor cores (3xTF32) for batches above 128 tokens
+    bool tc_router;    // router logit estimates on the tensor cores (one TF32 product) above 128 tokens
 };
 
 template <typename T>
