@@ -133,7 +133,9 @@ typedef struct {
     float *z;                 /* [T][L]                      latent, fp32          */
     uint8_t *zq, *zs;         /* [T][L], [T][L/32]           MXFP8 of z            */
     uint8_t *hsq, *hss;       /* [T][S*Is], [T][S*Is/32]     MXFP8 shared activation */
-    float *logits;            /* [T][E]                      router logits         */
+    float *logits;            /* [T][E]  router logits: fp32 up to 128 tokens; above that (E % 128 == 0)
+                               * fp32 for each token's top-k candidates and a tensor-core
+                               * estimate (within 2e-2) for the other experts */
     int32_t *topk_idx;        /* [T][k]   slot order: descending key, tie -> lower id */
     float *topk_w;            /* [T][k]                      gates                 */
     int32_t *counts;          /* [E]                         tokens per expert     */
