@@ -497,7 +497,8 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(TopkArgs a) {
 
 // Top-k of small batches: one CTA per token, one thread per expert.  The
 // k-th largest key is found bit by bit with block-wide counts (the largest
-// v with at least k keys >= v); the candidates are the keys >= v, or, with
+// v with at least k keys >= v; without a band the search stops as soon as
+// exactly k keys are >= v); the candidates are the keys >= v, or, with
 // an error band, the keys >= the k-th estimate - 2 err (more than 32:
 // overflow).  Each candidate's rank among the candidates (larger key, or
 // equal key and lower id, first) orders them, and warp 0 finishes as
@@ -526,7 +527,13 @@ __global__ void __launch_bounds__(kTopkWideThreads) topk_wide_kernel(TopkArgs a)
     uint32_t v = 0;
     for (int bit = 31; bit >= 0; --bit) {
         const uint32_t tv = v | (1u << bit);
-        if (__syncthreads_count(kb >= tv) >= k) v = tv;
+        const int c = __syncthreads_count(kb >= tv);
+        if (c >= k) {
+            v = tv;
+            // exactly k keys >= v: they are the top k (without a band the
+            // remaining bits cannot change the candidates)
+            if (!band && c == k) break;
+        }
     }
     uint32_t lo = v;
     if (band) lo = min(v, key_bits(__fsub_rd(bits_key(v), a.band_pad)));
