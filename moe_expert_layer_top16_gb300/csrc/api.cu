@@ -568,6 +568,9 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         if (!ok) return MOE_ERR_CUDA;
         p->wide_router = nmax_router;
     }
+    // above 128 tokens the router logits are tensor-core estimates from z split
+    // into TF32 head + remainder; smaller batches keep z plain
+    const bool z_split = p->tc_router && T > 128;
     cudaError_t err = cudaSuccess;
 #define TRY(x)                          \
     do {                                \
@@ -594,7 +597,9 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         g.m_tiles = p->rowsA2 / kBlockM;
         g.n_tokens = T;
         g.epi_split = L / kBlockM;
-        g.epi[0] = EpiParams{EPI_QUANT, 0, 0, L, p->z, 2 * L, p->zq, L, p->zsf, Tp};
+        // z rows hold L values; the TF32 router estimate also wants them split
+        // into a TF32 head and its remainder (at column L), else they are plain
+        g.epi[0] = EpiParams{EPI_QUANT, 0, 0, z_split ? L : 0, p->z, 2 * L, p->zq, L, p->zsf, Tp};
         g.epi[1] = EpiParams{EPI_SILU_QUANT, L / kBlockM, L, 0, nullptr, 0, p->act, p->Kcat, p->actsf, Tps, 1};
         const int items = g.m_tiles * ((T + g.n_max - 1) / g.n_max);
         shape_gemm(g, 0, items, std::min(items, p->num_sms));
@@ -602,7 +607,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
     }
     // 3. router logits, 4. top-k + gates + bitmaps
     mark(2);
-    const bool tc_logits = p->tc_router && T > 128;
+    const bool tc_logits = z_split;
     if (tc_logits) {
         // estimated logits = z_hi R_hi, one TF32 product on the tensor cores
         // (the high parts sit at the start of each row of z and router2; for
@@ -629,7 +634,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         if (p->route_hidden)
             TRY(launch_router(p->xr, D, 0, p->router, p->logits, T, E, D, s));
         else
-            TRY(launch_router(p->z, 2 * L, L, p->router, p->logits, T, E, L, s));
+            TRY(launch_router(p->z, 2 * L, 0, p->router, p->logits, T, E, L, s));
     }
     mark(3);
     {
@@ -769,7 +774,13 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         const int64_t TK = static_cast<int64_t>(T) * k;
         if (dbg->xq) TRY(cudaMemcpyAsync(dbg->xq, p->xq, static_cast<size_t>(T) * D, cudaMemcpyDeviceToDevice, s));
         if (dbg->xs) TRY(launch_export_sf(p->xsf, Tps, nullptr, T, D / 32, 0, dbg->xs, nmax_dense, nullptr, 0, s));
-        if (dbg->z) TRY(launch_add_halves(p->z, T, L, dbg->z, s));
+        if (dbg->z) {
+            if (z_split)
+                TRY(launch_add_halves(p->z, T, L, dbg->z, s));
+            else
+                TRY(cudaMemcpy2DAsync(dbg->z, sizeof(float) * L, p->z, sizeof(float) * 2 * L, sizeof(float) * L, T,
+                                      cudaMemcpyDeviceToDevice, s));
+        }
         if (dbg->zq) TRY(cudaMemcpyAsync(dbg->zq, p->zq, static_cast<size_t>(T) * L, cudaMemcpyDeviceToDevice, s));
         if (dbg->zs) TRY(launch_export_sf(p->zsf, Tp, nullptr, T, L / 32, 0, dbg->zs, 0, nullptr, 0, s));
         if (S > 0 && dbg->hsq)
