@@ -241,8 +241,7 @@ constexpr float kKeyErr = 4.0e-6f;   // error bound of the fp32 sigmoid(l) + b e
 // is two warp reductions: the largest key, then the lowest expert id among
 // the lanes holding it.
 __device__ __forceinline__ uint32_t key_bits(float k) {
-    if (k == 0.0f) k = 0.0f;                  // -0 ties with +0, as the floats compare
-    const uint32_t u = __float_as_uint(k);
+    const uint32_t u = (k == 0.0f) ? 0u : __float_as_uint(k);     // -0 ties with +0, as the floats compare
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 __device__ __forceinline__ float bits_key(uint32_t b) {
