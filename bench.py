@@ -149,14 +149,19 @@ class ClockSampler:
 
 
 def dist_setup():
+    """Ranks from the launcher's environment; one process per GPU over NCCL
+    (gloo where no GPU is visible, for the host-side logic)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
         import torch
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+        else:
+            dist.init_process_group("gloo")
     return world, rank, local
 
 
@@ -166,12 +171,21 @@ def barrier(world):
         dist.barrier()
 
 
+def job_throughput(world, tokens_per_step, steps, slowest_ms):
+    """Whole-job tokens/s: each of `world` ranks runs `steps` steps of
+    `tokens_per_step` tokens (weak scaling); the job takes the slowest rank's
+    time."""
+    return world * tokens_per_step * steps / (slowest_ms / 1e3)
+
+
 def max_over_ranks(world, v: float) -> float:
+    """The largest of the ranks' values (every rank gets it)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -332,7 +346,7 @@ def run_cuda(args, wl, world, rank, local):
     step_ms = [ev0[i].elapsed_time(ev1[i]) for i in range(K)]
     total_ms = max_over_ranks(world, float(np.sum(step_ms)))
     ms_per_step = total_ms / K
-    value = world * T * K / (total_ms / 1e3)
+    value = job_throughput(world, T, K, total_ms)
 
     # end to end through the C ABI with host buffers (copies inside the timed region)
     xh = x.cpu().pin_memory()
