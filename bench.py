@@ -57,6 +57,13 @@ NCU_TRAFFIC = {
 }
 
 
+def workload_config(wl, T):
+    """The `config` keys both arms report for a workload of T tokens."""
+    return {"workload": wl.name, "tokens": T, "d_model": wl.d_model, "d_latent": wl.d_latent,
+            "experts": wl.n_experts, "top_k": wl.top_k, "expert_inter": wl.expert_inter,
+            "shared": wl.n_shared, "shared_inter": wl.shared_inter, "bias": wl.bias}
+
+
 def launches_per_forward(T):
     """Kernels of this library one forward of T tokens launches: quantiser, A2,
     router (or its tensor-core estimate), top-k, per-expert scan (batches over
@@ -255,7 +262,7 @@ def run_reference(args, wl, world, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "tokens_per_step": n_tok, "tokens_in_workload": wl.tokens},
+        "config": dict(workload_config(wl, wl.tokens), tokens_per_step=n_tok, parallelism="rank 0 only"),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
                          "sample": f"{n_tok} tokens of {wl.name} ({n_exp} experts) per step; fp64 C oracle, OpenMP, "
                                    f"{cpu_model()}"},
@@ -396,11 +403,9 @@ def run_cuda(args, wl, world, rank, local):
         "step_ms": {"median": float(np.median(step_ms)), "p10": float(np.percentile(step_ms, 10)),
                     "p90": float(np.percentile(step_ms, 90))},
         "dtype": "mxfp4 weights x mxfp8 activations, fp32 accumulate", "data": "synthetic",
-        "config": {"workload": wl.name, "tokens": T, "d_model": wl.d_model, "d_latent": wl.d_latent,
-                   "experts": wl.n_experts, "top_k": wl.top_k, "expert_inter": wl.expert_inter,
-                   "shared": wl.n_shared, "shared_inter": wl.shared_inter, "bias": wl.bias,
-                   "l2": "flushed by a 512 MB write between timed steps (outside the step events)",
-                   "parallelism": f"replicas x{world}"},
+        "config": dict(workload_config(wl, T),
+                       l2="flushed by a 512 MB write between timed steps (outside the step events)",
+                       parallelism=f"replicas x{world}"),
         "roofline": roof,
         "layer": {"touched_experts": touched, "expert_weight_bytes": expert_bytes,
                   "expert_weight_GBps": expert_bytes / step_s / 1e9,
