@@ -280,8 +280,11 @@ void orc_route(const double *logits, const float *bias, int64_t T, int E, int k,
     char *taken = (char *)malloc((size_t)E);
     for (int64_t t = 0; t < T; ++t) {
         const double *l = logits + t * E;
+        /* Without a bias the key sigmoid(l) orders exactly as l (sigmoid is
+         * strictly increasing); ranking l itself keeps that order where the
+         * fp64 sigmoid rounds to 1 (l above about 37). */
         for (int e = 0; e < E; ++e) {
-            key[e] = softmax ? l[e] : sigmoid(l[e]) + (bias ? (double)bias[e] : 0.0);
+            key[e] = (softmax || !bias) ? l[e] : sigmoid(l[e]) + (double)bias[e];
             taken[e] = 0;
         }
         /* k rounds of "largest remaining key, lower id on a tie". */

@@ -126,3 +126,45 @@ def test_output_scale(tiny):
     wl, W, x, out = tiny
     y = out["y"]
     assert np.isfinite(y).all() and y.std() > 0
+
+
+def test_forced_routing_sigmoid_gates_on_negated_router_rows():
+    """Forced selection in sigmoid mode ("How the router picks 16 of 896",
+    Fig. 2: the winners' raw sigmoid scores over their sum, the bias left
+    out).  The router's rows come in negated pairs, R[2i+1] = -R[2i], so the
+    logits of a pair are exactly l and -l, and sigmoid(l) + sigmoid(-l) = 1.
+    Forcing two whole pairs makes the normaliser exactly 2: every gate is
+    sigmoid(l_j) / 2 and each pair's gates add to 1/2 -- values a softmax
+    over the winners, a missing normalisation or a bias inside the gates
+    would all miss."""
+    from dataclasses import replace
+    wl = replace(synth.workload("tiny"), score="sigmoid")
+    base = synth.weight(wl, "router", 0).numpy()
+    router = base.copy()
+    router[1::2] = -base[0::2]
+    rng = np.random.default_rng(5)
+    bias = rng.normal(0, 0.5, size=wl.n_experts).astype(np.float32)
+    x = bf16_bits(synth.hidden_states(wl))
+    T = x.shape[0]
+    forced = np.tile(np.array([4, 5, 10, 11], np.int32), (T, 1))
+    outs = []
+    for b in (None, bias):
+        def fetch(name, i, b=b):
+            if name == "router":
+                return router
+            if name == "bias":
+                return b
+            return synth.weight(wl, name, i).numpy()
+        lw = oracle.encode_layer(wl, fetch)
+        outs.append(oracle.moe_forward(wl, lw, x, force_idx=forced, want=("gates", "logits", "idx")))
+    for r in outs:
+        lg = r["logits"]
+        assert np.array_equal(lg[:, 1::2], -lg[:, 0::2])
+        assert (r["idx"] == forced).all()
+        g = r["gates"]
+        np.testing.assert_allclose(g[:, 0] + g[:, 1], 0.5, rtol=0, atol=1e-15)
+        np.testing.assert_allclose(g[:, 2] + g[:, 3], 0.5, rtol=0, atol=1e-15)
+        sel = np.take_along_axis(lg, forced.astype(np.int64), 1)
+        np.testing.assert_allclose(g, 0.5 / (1.0 + np.exp(-sel)), rtol=1e-14, atol=0)
+    # the selection bias changes nothing in the forced gates
+    np.testing.assert_array_equal(outs[0]["gates"], outs[1]["gates"])

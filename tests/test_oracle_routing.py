@@ -180,3 +180,22 @@ def test_router_input_hidden_reads_x_and_latent_reads_z():
         r = oracle.moe_forward(wl, lw, xb, route_only=True, want=("logits", "z"))
         src = x.float().numpy() if route == "hidden" else r["z"]
         assert np.array_equal(r["logits"], src[:, dims].astype(np.float64))
+
+
+def test_sigmoid_keys_without_bias_keep_their_order_past_saturation():
+    """sigmoid is strictly increasing, so without a bias the selection key
+    sigmoid(l) orders the experts exactly as their logits do -- also where
+    sigmoid(l) rounds to 1.0 in fp64 (l above about 37), where a comparison
+    of the rounded keys would see ties and fall back to the expert id."""
+    E, k = 12, 4
+    logits = np.zeros((1, E))
+    logits[0, [2, 5, 7, 9, 11]] = [39.0, 41.0, 40.0, 38.5, 45.0]
+    assert 1.0 / (1.0 + np.exp(-39.0)) == 1.0 / (1.0 + np.exp(-41.0)) == 1.0   # the rounded keys tie
+    idx, gates = oracle.route(logits, k, softmax=False)
+    assert idx[0].tolist() == [11, 5, 7, 2]
+    np.testing.assert_allclose(gates, 0.25, rtol=0, atol=1e-15)
+    # with a bias the key is sigmoid(l) + b as written, evaluated in fp64
+    bias = np.zeros(E, np.float32)
+    bias[3] = 2.0
+    idx_b, _ = oracle.route(logits, k, softmax=False, bias=bias)
+    assert idx_b[0, 0] == 3
