@@ -135,7 +135,8 @@ typedef struct {
     uint8_t *hsq, *hss;       /* [T][S*Is], [T][S*Is/32]     MXFP8 shared activation */
     float *logits;            /* [T][E]  router logits: fp32 up to 128 tokens; above that (E % 128 == 0)
                                * fp32 for each token's top-k candidates and a tensor-core
-                               * estimate (within 2e-2) for the other experts */
+                               * estimate elsewhere, within a proven per-(token, expert)
+                               * bound of the fp32 value and below the k-th selected logit */
     int32_t *topk_idx;        /* [T][k]   slot order: descending key, tie -> lower id */
     float *topk_w;            /* [T][k]                      gates                 */
     int32_t *counts;          /* [E]                         tokens per expert     */
@@ -214,10 +215,26 @@ MOE_API moe_status moe_mxfp4_encode(const float *w, int64_t rows, int64_t K, uin
  * the engine's layouts in scratch memory that this call obtains with
  * cudaMallocAsync on `stream` and releases with cudaFreeAsync before it
  * returns.  dev_status (device int32, optional) receives a non-zero code if a
- * bounded wait inside the kernel ran out.  Asynchronous on `stream`. */
+ * bounded wait inside the kernel ran out; it is the only way to learn of such
+ * a time-out (out[] is then incomplete while the call still returns MOE_OK),
+ * so pass it wherever a time-out matters.  Asynchronous on `stream`. */
 MOE_API moe_status moe_mx_gemm(const uint8_t *a_codes, const uint8_t *a_scales, int32_t M, const uint8_t *b_codes,
                        const uint8_t *b_scales, int32_t N, int32_t K, float *out, int32_t *dev_status,
                        void *stream);
+
+/* Tensor-core rate probe (measurement, not part of the layer): enqueues on
+ * `stream` one CTA per SM of the current device, each issuing iters x 4
+ * back-to-back tcgen05.mma instructions of M = 128 x n on operand tiles held
+ * in shared memory (no global memory traffic), and stores the FLOPs of the
+ * launch in *flops_out (host).  Time it with events on `stream`.  kind:
+ *   0  kind::mxf8f6f4, E2M1 x E4M3 with E8M0 scales (the layer's MMA), n <= 240
+ *   1  kind::mxf8f6f4, E4M3 x E4M3 with E8M0 scales, n <= 240
+ *   2  kind::f16, bf16 x bf16, fp32 accumulate, n <= 256
+ * n a multiple of 16 (>= 16); 1 <= iters <= 2^22.  dev_status (device int32,
+ * required) becomes non-zero if the final bounded wait ran out.  Needs a
+ * compute capability 10.3 device (else MOE_ERR_UNSUPPORTED). */
+MOE_API moe_status moe_mma_probe(int32_t kind, int32_t n, int32_t iters, int32_t *dev_status, double *flops_out,
+                                 void *stream);
 
 /* moe_mx_gemm without any allocation (the paper has no counterpart: this is
  * an entry point for callers that cannot allocate device memory -- e.g. code
@@ -234,7 +251,8 @@ MOE_API moe_status moe_mx_gemm(const uint8_t *a_codes, const uint8_t *a_scales, 
  * the current device); make that first call before any stream capture.  All
  * calls share the one array and it keeps the previous call's contents: calls
  * whose executions overlap on the GPU (other streams, other host threads)
- * race on it.  Makes no cudaMalloc / cudaFree call. */
+ * race on it.  Makes no cudaMalloc / cudaFree call.  As with moe_mx_gemm, a
+ * device time-out is reported only through dev_status. */
 #define MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
 MOE_API moe_status moe_mx_gemm_noalloc(const uint8_t *a_codes, const uint8_t *a_scales, int32_t M,
                                        const uint8_t *b_codes, const uint8_t *b_scales, int32_t N, int32_t K,

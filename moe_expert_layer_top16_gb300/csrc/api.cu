@@ -19,6 +19,7 @@
 //                   up-projection and the shared experts' down-projection
 //                   summed in one accumulator
 #include <algorithm>
+#include <cmath>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -98,13 +99,26 @@ bool map_mx8(CUtensorMap* m, const void* codes, int64_t rows, int64_t K, int box
 
 inline int64_t rup(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
 
-// Bound on |tensor-core logit - fp32 logit| assumed by the top-k refinement.
-// One TF32 product z_hi R_hi (both rounded to TF32, the fp32 accumulator of
-// the tensor core rounding toward zero at every step) stays within ~3e-3 of
-// the fp64 logit on the K3-shaped layer; the bound leaves a factor of 7.  The
-// refinement recomputes every candidate within 2 * delta of the k-th estimate
-// exactly, so delta sets how many candidates are recomputed, not the result.
-constexpr float kTcRouterDelta = 2.0e-2f;
+// Coefficients of the proven error bound of a tensor-core router estimate
+// (TopkArgs in internal.h), for a router input of K values.
+//  * Tensor-core accumulation: the products of TF32 operands are exact in
+//    fp32; each one is added to the fp32 accumulator with an error of at most
+//    two units in the last place of the running sum (one for aligning it to
+//    the accumulator, one for rounding the sum, toward zero or to nearest),
+//    and the K-split partials of the engine add a few more additions:
+//    |est - sum z_hi R_hi| <= (K + 8) 2^-22 sum |z_hi| |R_hi|.
+//  * The exact path's fp32 FMA chain (K/32 FMAs per lane, a 5-level
+//    butterfly): at most (K/32 + 8) 2^-24 sum |z| |R|.
+//  * Norms of the input rows come from fp32 sums of K squares, each chain
+//    K/32 + 5 roundings long: the sums are scaled up by 2 (K/32 + 8) 2^-24.
+float round_up_f(double v) {
+    float f = static_cast<float>(v);
+    if (static_cast<double>(f) < v) f = nextafterf(f, INFINITY);
+    return f;
+}
+float tc_router_gamma(int K) { return round_up_f((K + 8) * 0x1p-22); }
+float exact_router_gamma(int K) { return round_up_f((K / 32 + 8) * 0x1p-24); }
+float router_norm_inflation(int K) { return round_up_f(1.0 + 2.0 * (K / 32 + 8) * 0x1p-24); }
 
 // Token-bitmap words per expert up to which the work-list kernel also does the
 // per-expert scan (batches of up to 128 tokens; above that one CTA scanning
@@ -121,6 +135,8 @@ struct Plan {
     // weights
     uint8_t *a2c, *a2sf, *w13c, *w13sf, *w2c, *w2sf, *a10c, *a10sf;
     float *router, *router2, *bias;   // router [E][RK]; router2: [E][2 RK] = TF32 high part | remainder
+    float* rnorm;                     // [2][E] upper bounds of |R_e| and of |R_lo_e| (router2's remainder)
+    float bias_absmax = 0.0f;
     int RK = 0;                       // router input width: L (latent routing) or D (hidden routing)
     bool route_hidden = false, out_bf16 = false;
     float* xr = nullptr;              // hidden routing: x as fp32 [T_pad][D]
@@ -464,11 +480,17 @@ moe_status moe_plan(const moe_config* cfg, const moe_weights* w, int device, voi
     TRY(cudaMemcpy(p->router, w->router_w, sizeof(float) * E * RK, cudaMemcpyDeviceToDevice));
     TRY(palloc(p, &p->router2, sizeof(float) * E * 2 * RK));
     TRY(launch_tf32_split(p->router, E, RK, p->router2, 0));
+    TRY(palloc(p, &p->rnorm, sizeof(float) * 2 * E));
+    TRY(launch_router_norms(p->router, p->router2, E, RK, p->rnorm, 0));
     TRY(cudaDeviceSynchronize());
     p->bias = nullptr;
     if (w->router_bias) {
         TRY(palloc(p, &p->bias, sizeof(float) * E));
         TRY(cudaMemcpy(p->bias, w->router_bias, sizeof(float) * E, cudaMemcpyDeviceToDevice));
+        std::vector<float> hb(E);
+        TRY(cudaMemcpy(hb.data(), w->router_bias, sizeof(float) * E, cudaMemcpyDeviceToHost));
+        if (err == cudaSuccess)
+            for (float b : hb) p->bias_absmax = std::max(p->bias_absmax, b == b ? std::fabs(b) : INFINITY);
     }
     // ---------------------------------------------------------------- workspace
     TRY(palloc(p, &p->xq, Tp * D));
@@ -638,7 +660,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
     }
     mark(3);
     {
-        TopkArgs a;
+        TopkArgs a{};
         a.logits = p->logits;
         a.bias = p->bias;
         a.T = T;
@@ -646,11 +668,16 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         a.k = k;
         a.softmax = p->cfg.score_fn == MOE_SCORE_SOFTMAX;
         a.refine = tc_logits ? 1 : 0;
-        a.delta = kTcRouterDelta;
+        // hidden routing reads x, which is bf16 and so exactly TF32: no remainder
         a.z = p->route_hidden ? p->xr : p->z;
         a.z_ld = p->route_hidden ? D : 2 * L;
         a.z_lo = p->route_hidden ? 0 : L;
         a.R = p->router;
+        a.rnorm = p->rnorm;
+        a.g_tc = tc_router_gamma(p->RK);
+        a.g_32 = exact_router_gamma(p->RK);
+        a.sq_infl = router_norm_inflation(p->RK);
+        a.bias_absmax = p->bias_absmax;
         a.L = p->RK;
         a.idx = p->idx;
         a.w = p->gw;
@@ -896,6 +923,21 @@ moe_status moe_mx_gemm(const uint8_t* a_codes, const uint8_t* a_scales, int32_t 
     cudaError_t ferr = cudaFreeAsync(scratch, s);
     if (err == cudaSuccess) err = ferr;
     return cuda_status(err);
+}
+
+moe_status moe_mma_probe(int32_t kind, int32_t n, int32_t iters, int32_t* dev_status, double* flops_out,
+                         void* stream) {
+    if (!dev_status || !flops_out || kind < PROBE_MX_E2M1_E4M3 || kind > PROBE_BF16) return MOE_ERR_INVALID_ARG;
+    if (n < 16 || n > (kind == PROBE_BF16 ? 256 : kNMax) || (n & 15) || iters < 1 || iters > (1 << 22))
+        return MOE_ERR_INVALID_ARG;
+    int dev = 0, sms = 0, major = 0, minor = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (err != cudaSuccess) return cuda_status(err);
+    if (major != 10 || minor != 3) return MOE_ERR_UNSUPPORTED;
+    return cuda_status(launch_mma_probe(kind, n, iters, sms, dev_status, flops_out, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

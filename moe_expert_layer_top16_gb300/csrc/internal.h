@@ -114,25 +114,38 @@ constexpr int kRouterSplitTokens = 128;
 // remainders at offset lo (lo = 0: none); R [E][L]
 cudaError_t launch_router(const float* z, int ld, int lo, const float* R, float* logits, int T, int E, int L,
                           cudaStream_t s);
-// top-k + gates (kernels.cu): with refine, the logits are
-// approximate within delta and the candidates' exact logits are recomputed
-// from z ([T][2L], hi | lo) and R ([E][L]).
+// top-k + gates (kernels.cu).  With refine, the logits are tensor-core
+// estimates z_hi R_hi (both rounded to TF32) and the candidates' exact fp32
+// logits are recomputed from z ([T][z_ld], hi | lo) and R ([E][L]).  The
+// estimate of expert e for token t is within
+//   delta_te = |z_hi_t| |R_lo_e| + (|z_lo_t| + g_tc (1 + 2^-11) |z_hi_t|
+//              + g_32 (|z_hi_t| + |z_lo_t|)) |R_e|        (2-norms)
+// of the exact logit: the first two terms bound the TF32 rounding of the
+// operands (Cauchy-Schwarz), g_tc the tensor core's fp32 accumulation and g_32
+// the exact path's FMA chain (both relative to sum |z| |R| <= |z| |R|).
 struct TopkArgs {
     float* logits;
     const float* bias;
     int T, E, k, softmax;
     int refine;
-    float delta;
     const float* z;         // router input rows (z_ld floats): K = L values, remainders at z_lo (0: none)
     int z_ld, z_lo;
     const float* R;         // [E][L]
+    const float* rnorm;     // refine: [2][E] upper bounds of |R_e| and |R_lo_e| (2-norms)
+    float g_tc, g_32;       // refine: accumulation error coefficients (see above), rounded up
+    float sq_infl;          // refine: factor covering the fp32 rounding of a sum of L squares
     int L;
     int32_t* idx;
     float* w;
     uint32_t* sel;
     int W;
-    float band_pad;         // set by launch_topk: twice the key-estimate error bound, rounded up
+    float bias_absmax;      // max |bias| (0 without a bias)
+    float key_err;          // set by launch_topk: error bound of an fp32 sigmoid(l) + b evaluation
+    float band_pad;         // set by launch_topk: twice key_err, rounded up
 };
+// upper bounds of the 2-norms of the rows of R [E][K] and of its TF32
+// remainders (Rs [E][2K], hi | lo): out [0, E) = |R_e|, [E, 2E) = |R_lo_e|
+cudaError_t launch_router_norms(const float* R, const float* Rs, int E, int K, float* out, cudaStream_t s);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
 cudaError_t launch_expert_scan(const uint32_t* sel, int E, int W, int32_t* wpre, int32_t* counts, cudaStream_t s);
 struct WorkListArgs {
@@ -187,5 +200,10 @@ cudaError_t launch_export_sf(const uint8_t* planes, int64_t pitch, const int32_t
                              cudaStream_t s);
 cudaError_t launch_gather_rows(const uint8_t* src, int64_t src_stride, const int32_t* row_map, int64_t rows,
                                int64_t row_bytes, uint8_t* dst, int64_t dst_stride, cudaStream_t s);
+
+// ------------------------------------------------------------------ tensor-core rate probe (peak.cu)
+enum ProbeKind : int { PROBE_MX_E2M1_E4M3 = 0, PROBE_MX_E4M3_E4M3 = 1, PROBE_BF16 = 2 };
+// grid CTAs each issue iters x 4 MMAs of M = 128 x n; *flops = their FLOPs
+cudaError_t launch_mma_probe(int kind, int n, int iters, int grid, int* status, double* flops, cudaStream_t s);
 
 }  // namespace moe

@@ -220,21 +220,31 @@ __global__ void __cluster_dims__(1, 1, kRouterSplit) __launch_bounds__(256)
 //    increasing, so ranking logits ranks sigmoid(l) exactly (ties only where
 //    the logits tie).
 //  * with a bias: sigmoid(l) + b, decided in fp64.
-// When the logits are approximate (tensor-core router, |error| <= delta) or
-// keys need fp64, candidates are picked on the estimates: the k best and
-// every expert within twice the estimate's error bound of the k-th (no expert
-// outside that band can be in the exact top-k).  Their exact fp32 logits
-// (recomputed from z and R when the logits were approximate) and keys give
-// the final ranking; with more than 32 candidates every expert's logit and key
-// are evaluated exactly instead.  Rounds take the largest remaining key, the
-// lower expert id on a tie.
+// When the logits are approximate (tensor-core router) or keys need fp64,
+// candidates are picked on the estimates.  Each key estimate k_e has a proven
+// error bound d_e (the per-(token, expert) bound of TopkArgs for estimated
+// logits, a quarter of it plus kKeyErr for sigmoid(l) + b, kKeyErr alone for
+// exact logits with a bias), so the exact key lies in [k_e - d_e, k_e + d_e].
+// With theta = the k-th largest lower end, k experts have an exact key >=
+// theta, and an expert whose upper end is below theta cannot be in the exact
+// top-k: the candidates are the experts with k_e + d_e >= theta.  Their exact
+// fp32 logits (recomputed from z and R when the logits were approximate) and
+// keys give the final ranking; with more than 32 candidates every expert's
+// logit and key are evaluated exactly instead.  Rounds take the largest
+// remaining key, the lower expert id on a tie.
 // Gates: sigmoid(l_j) / sum over the winners (fp32), or softmax over the
 // winners' logits.  Each selection sets bit t of the expert's token bitmap.
 constexpr int kTopkWarps = 4;
 constexpr int kTopkWideTokens = 512;  // batches up to this size use one CTA per token (without refinement)
 constexpr int kTopkPerLane = 32;     // E <= 1024
 constexpr int kMaxE = 32 * kTopkPerLane;
-constexpr float kKeyErr = 4.0e-6f;   // error bound of the fp32 sigmoid(l) + b estimate
+// Error bound of the fp32 estimate 1 / (1 + __expf(-l)) + b of sigmoid(l) + b
+// for |b| <= 1: __expf errs by at most 2 + floor(1.173 |x|) ulp (CUDA's
+// documented bound), which moves sigmoid by at most sigmoid (1 - sigmoid)
+// times that relative error (below 1e-7 for every l); the IEEE division and
+// the two additions add a few units of 2^-24.  Larger biases add |b| 2^-22
+// (TopkArgs::bias_absmax).
+constexpr float kKeyErr = 4.0e-6f;
 
 // Keys as unsigned integers that order like the floats (larger key, larger
 // integer; -inf above every "no entry" value 0), so that a selection round
@@ -320,7 +330,7 @@ __device__ __noinline__ void topk_finish(const TopkArgs& a, int t, int lane, int
     int slot = lane;                                          // final slot of this lane's pick
     float my_l = 0.0f;                                        // exact logit of this lane's pick
     if (need_cand) {
-        if (approx) {
+        if (approx && !overflow) {
             // candidates in groups of up to 8 (z is read once per group)
             for (int c = 0; c < R; c += 8) {
                 const int m = min(8, R - c);
@@ -340,7 +350,7 @@ __device__ __noinline__ void topk_finish(const TopkArgs& a, int t, int lane, int
                 for (int u = 0; u < 8; ++u)
                     if (u < m && lane == c + u) my_l = v[u];
             }
-        } else if (lane < R) {
+        } else if (lane < R && !overflow) {
             my_l = l[my_id];
         }
         // exact ranking of the R candidates
@@ -428,69 +438,172 @@ __device__ __noinline__ void topk_finish(const TopkArgs& a, int t, int lane, int
     }
 }
 
+// Key interval ends as key_bits values: lower end rounded down, upper end
+// rounded up; an end that is not a number widens to the infinity on its side.
+__device__ __forceinline__ uint32_t lo_bits(float kv, float d) {
+    const float v = __fsub_rd(kv, d);
+    return key_bits(v != v ? -INFINITY : v);
+}
+__device__ __forceinline__ uint32_t hi_bits(float kv, float d) {
+    const float v = __fadd_ru(kv, d);
+    return key_bits(v != v ? INFINITY : v);
+}
+
+// Upper bounds of the 2-norms of the TF32 head (the first L values) and of
+// the exact remainder (L values at offset lo; lo = 0: none, the row is then
+// exactly TF32) of one router input row, from fp32 sums of squares scaled by
+// `infl` (which covers their rounding).  Every lane returns both.
+__device__ __forceinline__ void input_norms(const float* __restrict__ zt, int lo, int L, float infl, int lane,
+                                            float& nhi, float& nlo) {
+    float sh = 0.0f, sl = 0.0f;
+    for (int i = 4 * lane; i < L; i += 128) {
+        const float4 h = __ldg(reinterpret_cast<const float4*>(zt + i));
+        sh = fmaf(h.x, h.x, sh);
+        sh = fmaf(h.y, h.y, sh);
+        sh = fmaf(h.z, h.z, sh);
+        sh = fmaf(h.w, h.w, sh);
+        if (lo) {
+            const float4 q = __ldg(reinterpret_cast<const float4*>(zt + lo + i));
+            sl = fmaf(q.x, q.x, sl);
+            sl = fmaf(q.y, q.y, sl);
+            sl = fmaf(q.z, q.z, sl);
+            sl = fmaf(q.w, q.w, sl);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        sh += __shfl_xor_sync(0xffffffffu, sh, o);
+        sl += __shfl_xor_sync(0xffffffffu, sl, o);
+    }
+    nhi = __fsqrt_ru(__fmul_ru(sh, infl));
+    nlo = lo ? __fsqrt_ru(__fmul_ru(sl, infl)) : 0.0f;
+}
+
 __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(TopkArgs a) {
+    __shared__ int s_cand[kTopkWarps][32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * kTopkWarps + warp;
     if (t >= a.T) return;
     const int E = a.E, k = a.k;
-    float* l = a.logits + static_cast<int64_t>(t) * E;
+    const float* l = a.logits + static_cast<int64_t>(t) * E;
     const float* bias = a.bias;
     const bool use_bias = (bias != nullptr) && !a.softmax;
     const bool approx = a.refine != 0;
-    const bool need_cand = use_bias || approx;
     const int nper = (E + 31) / 32;
-    uint32_t key[kTopkPerLane];                               // selection-key estimates (key_bits), expert lane + 32 i
+    if (!use_bias && !approx) {
+        // exact logits ranked as they are: k rounds give the selection in slot order
+        uint32_t key[kTopkPerLane];
+#pragma unroll
+        for (int i = 0; i < kTopkPerLane; ++i) {
+            const int e = lane + 32 * i;
+            float kv = (i < nper && e < E) ? l[e] : 0.0f;
+            if (kv != kv) kv = -INFINITY;                     // NaN ranks last
+            key[i] = (i < nper && e < E) ? key_bits(kv) : kNoKey;
+        }
+        uint32_t taken = 0;
+        int my_id = 0;
+        for (int j = 0; j < k; ++j) {
+            uint32_t lb = kNoKey;
+            int lid = 0x7fffffff;
+#pragma unroll
+            for (int i = 0; i < kTopkPerLane; ++i) {
+                const uint32_t kv = (taken & (1u << i)) ? kNoKey : key[i];
+                if (kv > lb) {
+                    lb = kv;
+                    lid = lane + 32 * i;
+                }
+            }
+            uint32_t bb;
+            int bid = warp_best_id(lb, lid, bb);
+            if (bid < 0 || bid >= E) bid = 0;                 // unreachable while k <= E
+            if (lane == j) my_id = bid;
+            if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
+        }
+        topk_finish(a, t, lane, k, false, my_id);
+        return;
+    }
+    // error bound of each key estimate: d_e = A |R_lo_e| + B |R_e| for
+    // tensor-core logit estimates (TopkArgs), a quarter of it through the
+    // sigmoid, plus kKeyErr for the fp32 evaluation of sigmoid(l) + b
+    float A = 0.0f, B = 0.0f;
+    if (approx) {
+        float nhi, nlo;
+        input_norms(a.z + static_cast<int64_t>(t) * a.z_ld, a.z_lo, a.L, a.sq_infl, lane, nhi, nlo);
+        A = nhi;
+        B = __fadd_ru(__fadd_ru(nlo, __fmul_ru(__fmul_ru(a.g_tc, 1.0f + 0x1p-11f), nhi)),
+                      __fmul_ru(a.g_32, __fadd_ru(nhi, nlo)));
+    }
+    auto estimate = [&](int e, float& kv, float& d) {
+        const float lv = l[e];
+        d = approx ? __fmaf_ru(A, a.rnorm[E + e], __fmul_ru(B, a.rnorm[e])) : 0.0f;
+        if (use_bias) {
+            kv = 1.0f / (1.0f + __expf(-lv)) + bias[e];
+            d = __fmaf_ru(0.25f, d, a.key_err);
+        } else {
+            kv = lv;
+        }
+        if (kv != kv) kv = -INFINITY;                         // NaN ranks last
+    };
+    // theta = the k-th largest lower end (k rounds over the lower ends)
+    uint32_t lbk[kTopkPerLane];
 #pragma unroll
     for (int i = 0; i < kTopkPerLane; ++i) {
         const int e = lane + 32 * i;
-        float kv = (i < nper && e < E) ? l[e] : 0.0f;
-        if (use_bias) kv = 1.0f / (1.0f + __expf(-kv)) + bias[e < E ? e : 0];
-        if (kv != kv) kv = -INFINITY;                         // NaN ranks last
-        key[i] = (i < nper && e < E) ? key_bits(kv) : kNoKey;
+        lbk[i] = kNoKey;
+        if (i < nper && e < E) {
+            float kv, d;
+            estimate(e, kv, d);
+            lbk[i] = lo_bits(kv, d);
+        }
     }
-    uint32_t taken = 0;                                       // bit i: candidate lane + 32 i selected
-    // Candidates, in estimate order: the k best estimates, then every further
-    // expert whose estimate is within 2 * err of the k-th one.  An expert
-    // outside that band has a true key below k-th estimate - err, and each of
-    // the k best has a true key above it, so the exact top-k lies among the
-    // candidates.  More than 32 candidates (lane capacity): exact fallback.
-    const double err = approx ? (use_bias ? 0.25 * a.delta + kKeyErr : a.delta) : kKeyErr;
-    int R = 0;
-    bool overflow = false;
-    int my_id = 0;                                            // lane j < R holds the j-th pick
-    float kth_est = 0.0f;
-    for (int j = 0; j <= 32; ++j) {
-        if (j >= k && !need_cand) break;
-        // this lane's best untaken entry (entries ascend in id, so the first
-        // of equal keys is the lowest id)
+    uint32_t taken = 0, theta = kNoKey;
+    for (int j = 0; j < k; ++j) {
         uint32_t lb = kNoKey;
         int lid = 0x7fffffff;
 #pragma unroll
         for (int i = 0; i < kTopkPerLane; ++i) {
-            const uint32_t kv = (taken & (1u << i)) ? kNoKey : key[i];
+            const uint32_t kv = (taken & (1u << i)) ? kNoKey : lbk[i];
             if (kv > lb) {
                 lb = kv;
                 lid = lane + 32 * i;
             }
         }
         uint32_t bb;
-        int bid = warp_best_id(lb, lid, bb);
-        const float bkey = bits_key(bb);
-        if (j >= k) {
-            // band test in double: kth_est - 2 err is not rounded toward the candidate
-            if (bid < 0 || bid >= E || !(static_cast<double>(bkey) >= static_cast<double>(kth_est) - 2.0 * err))
-                break;
-            if (j == 32) {
-                overflow = true;
-                break;
-            }
-        }
-        if (bid < 0 || bid >= E) bid = 0;                    // unreachable while k <= E
-        if (j == k - 1) kth_est = bkey;
-        if (lane == j) my_id = bid;
-        if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
-        R = j + 1;
+        const int bid = warp_best_id(lb, lid, bb);
+        theta = bb;
+        if (bid >= 0 && bid < E && (bid & 31) == lane) taken |= 1u << (bid >> 5);
     }
+    // candidates: every expert whose upper end reaches theta
+    uint32_t mask = 0;
+#pragma unroll
+    for (int i = 0; i < kTopkPerLane; ++i) {
+        const int e = lane + 32 * i;
+        if (i < nper && e < E) {
+            float kv, d;
+            estimate(e, kv, d);
+            if (hi_bits(kv, d) >= theta) mask |= 1u << i;
+        }
+    }
+    const int c = __popc(mask);
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    const bool overflow = total > 32;
+    if (!overflow) {
+        int pos = incl - c;
+        while (mask) {
+            const int i = __ffs(mask) - 1;
+            mask &= mask - 1;
+            s_cand[warp][pos++] = lane + 32 * i;
+        }
+    }
+    __syncwarp();
+    const int R = overflow ? 32 : total;
+    const int my_id = (!overflow && lane < R) ? s_cand[warp][lane] : 0;
     topk_finish(a, t, lane, R, overflow, my_id);
 }
 
@@ -851,6 +964,33 @@ __global__ void add_halves_kernel(const float* __restrict__ src, int64_t rows, i
     dst[i] = src[r * 2 * K + c] + src[r * 2 * K + K + c];
 }
 
+// Upper bounds of the 2-norms of router rows and of their TF32 remainders:
+// one warp per row, fp64 sums of squares (relative error below 2^-40 for rows
+// of up to 2^12 values per lane), square roots and the conversion to fp32
+// rounded up.
+__global__ void router_norms_kernel(const float* __restrict__ R, const float* __restrict__ Rs, int E, int K,
+                                    float* __restrict__ out) {
+    const int e = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (e >= E) return;
+    double s = 0.0, sl = 0.0;
+    for (int i = lane; i < K; i += 32) {
+        const double v = R[static_cast<int64_t>(e) * K + i];
+        const double q = Rs[static_cast<int64_t>(e) * 2 * K + K + i];
+        s = fma(v, v, s);
+        sl = fma(q, q, sl);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        s += __shfl_xor_sync(0xffffffffu, s, o);
+        sl += __shfl_xor_sync(0xffffffffu, sl, o);
+    }
+    if (lane == 0) {
+        out[e] = __double2float_ru(__dsqrt_ru(__dmul_ru(s, 1.0 + 0x1p-40)));
+        out[E + e] = __double2float_ru(__dsqrt_ru(__dmul_ru(sl, 1.0 + 0x1p-40)));
+    }
+}
+
 // ------------------------------------------------------------------ debug export
 __global__ void export_sf_kernel(const uint8_t* __restrict__ planes, int64_t pitch, const int32_t* __restrict__ row_map,
                                  int64_t rows, int64_t nblocks, int64_t col_block0, uint8_t* __restrict__ out,
@@ -917,12 +1057,18 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
     if (a.E > kMaxE || a.k > 32 || a.k < 1 || a.k > a.E) return cudaErrorInvalidValue;
     // refinement reads router rows as 16-byte vectors, 128 values per warp step
     if (a.refine && (a.L <= 0 || a.L % 128 || a.z_ld % 4 || a.z_lo % 4)) return cudaErrorInvalidValue;
-    // the candidate band below the k-th estimate: twice the error bound, rounded up
+    if (a.refine && (!a.rnorm || !(a.g_tc >= 0.0f) || !(a.g_32 >= 0.0f) || !(a.sq_infl >= 1.0f)))
+        return cudaErrorInvalidValue;
+    // exact logits with a bias: the candidate band below the k-th key
+    // estimate is twice the key's evaluation error, rounded up
     TopkArgs b = a;
-    const bool use_bias = (a.bias != nullptr) && !a.softmax;
-    const double err = a.refine ? (use_bias ? 0.25 * a.delta + kKeyErr : a.delta) : kKeyErr;
-    b.band_pad = static_cast<float>(2.0 * err);
-    if (static_cast<double>(b.band_pad) < 2.0 * err) b.band_pad = nextafterf(b.band_pad, INFINITY);
+    if (!(a.bias_absmax >= 0.0f)) return cudaErrorInvalidValue;
+    const double key_err = kKeyErr + static_cast<double>(a.bias_absmax) * 0x1p-22;
+    b.key_err = static_cast<float>(key_err);
+    if (static_cast<double>(b.key_err) < key_err) b.key_err = nextafterf(b.key_err, INFINITY);
+    b.band_pad = static_cast<float>(2.0 * static_cast<double>(b.key_err));
+    if (static_cast<double>(b.band_pad) < 2.0 * static_cast<double>(b.key_err))
+        b.band_pad = nextafterf(b.band_pad, INFINITY);
     // one CTA per token for small batches with exact logits; a batch whose
     // candidates need the exact refinement (one warp's work per token) runs a
     // warp per token, so that many tokens refine at once
@@ -930,6 +1076,12 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
         topk_wide_kernel<<<a.T, kTopkWideThreads, 0, s>>>(b);
     else
         topk_kernel<<<(a.T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, s>>>(b);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_router_norms(const float* R, const float* Rs, int E, int K, float* out, cudaStream_t s) {
+    if (E <= 0 || K <= 0 || K > (1 << 17)) return cudaErrorInvalidValue;
+    router_norms_kernel<<<(E * 32 + 255) / 256, 256, 0, s>>>(R, Rs, E, K, out);
     return cudaGetLastError();
 }
 

@@ -3,17 +3,21 @@
 2048, routed inner 512; sigmoid router, no bias) at every token count of the
 decode, prefill and sweep workloads.
 
-Whole batch, any size: top-k on the GPU's own logits and the dispatch
-(counts, offsets, stable permutation) are exact.  Sampled tokens (first,
-last, inside): x codes exact, logits within 1e-4, selections equal except at
-certified near-ties, and y within max |err| <= 2e-2 rms(y_ref),
-sum|err| / sum|y_ref| <= 2e-3.
+Whole batch, any size: top-k on the GPU's own exported logits and the
+dispatch (counts, offsets, stable permutation) are exact.  Sampled tokens:
+x codes exact, the selected experts' logits exact fp32, every tensor-core
+logit estimate within the layer's proven bound, selections equal to the
+oracle's (no near-tie on these uniform workloads), and y within
+max |err| <= 2e-2 rms(y_ref), sum|err| / sum|y_ref| <= 2e-3.  At 8192 and
+32768 tokens the grouped GEMMs are compared element by element on every row
+of the most loaded expert's first work item (all 240 rows of a full item at
+32768 tokens), and y on at least 256 tokens including that item's.
 """
 import numpy as np
 import pytest
 
 import synth
-from gpu_util import OracleLayer, gpu_plan, run_sampled_parity
+from gpu_util import OracleLayer, gpu_plan, run_item_parity, run_sampled_parity
 
 pytestmark = pytest.mark.gpu
 
@@ -29,28 +33,30 @@ def k3():
 
 def test_decode64(k3):
     wl, plan, ol = k3
-    accepted, errs, counts = run_sampled_parity(wl, plan, ol, 64, [0, 9, 17, 31, 40, 50, 58, 63])
-    assert len(accepted) <= 1
+    accepted, errs, counts = run_sampled_parity(wl, plan, ol, 64, range(64))
+    assert len(accepted) == 0
     touched = int((counts > 0).sum())
     assert 500 < touched <= 896          # about 613 expected under uniform routing
 
 
 def test_prefill8192(k3):
     wl, plan, ol = k3
-    accepted, errs, counts = run_sampled_parity(wl, plan, ol, 8192, [0, 239, 240, 4097, 8191])
-    assert len(accepted) <= 1
+    accepted, errs, counts, n_item = run_item_parity(wl, plan, ol, 8192)
+    assert len(accepted) == 0
     assert counts.sum() == 8192 * 16
+    assert n_item == counts.max() and n_item > 146          # the whole segment of the hottest expert
 
 
 @pytest.mark.parametrize("T", [1, 8, 77, 512, 4096])
 def test_sweep(k3, T):
     wl, plan, ol = k3
-    accepted, errs, counts = run_sampled_parity(wl, plan, ol, T, [0, T // 2, T - 1])
-    assert len(accepted) <= 1
+    accepted, errs, counts = run_sampled_parity(wl, plan, ol, T, np.linspace(0, T - 1, num=min(T, 24)).astype(int))
+    assert len(accepted) == 0
 
 
 def test_sweep_32768(k3):
     wl, plan, ol = k3
-    accepted, errs, counts = run_sampled_parity(wl, plan, ol, 32768, [0, 32767])
-    assert len(accepted) <= 1
+    accepted, errs, counts, n_item = run_item_parity(wl, plan, ol, 32768)
+    assert len(accepted) == 0
     assert counts.sum() == 32768 * 16
+    assert n_item == 240                                    # a full work item, positions 0..239

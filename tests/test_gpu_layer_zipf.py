@@ -2,12 +2,14 @@
 tokens: hot experts take many times the mean load, so the grouped GEMMs see
 very ragged segments (several full 240-token tiles for one expert, many
 empty experts).  Same parity contract as the uniform workloads; the bias
-enters the selection key only (sigmoid(l) + b, evaluated in fp64)."""
+enters the selection key only (sigmoid(l) + b, evaluated in fp64).  The
+hottest expert's first (full) work item is compared element by element, and
+y on at least 256 tokens including that item's."""
 import numpy as np
 import pytest
 
 import synth
-from gpu_util import OracleLayer, gpu_plan, run_sampled_parity
+from gpu_util import OracleLayer, gpu_plan, run_item_parity, run_sampled_parity
 
 pytestmark = pytest.mark.gpu
 
@@ -23,11 +25,12 @@ def zipf():
 
 def test_zipf16384(zipf):
     wl, plan, ol = zipf
-    accepted, errs, counts = run_sampled_parity(wl, plan, ol, 16384, [0, 5000, 12345, 16383])
+    accepted, errs, counts, n_item = run_item_parity(wl, plan, ol, 16384)
     assert len(accepted) <= 1
     mean = 16384 * 16 / 896
     assert counts.max() > 10 * mean, f"hottest expert {counts.max()} vs mean {mean:.1f}"
     assert (counts == 0).sum() > 0
+    assert n_item == 240
 
 
 @pytest.mark.parametrize("T", [1, 64, 300])
@@ -36,5 +39,5 @@ def test_zipf_small_batches(zipf, T):
     selection goes through the candidate band and the fp64 key ranking (and,
     above 128 tokens, the tensor-core logit estimates' band as well)."""
     wl, plan, ol = zipf
-    accepted, errs, counts = run_sampled_parity(wl, plan, ol, T, [0, T // 2, T - 1])
+    accepted, errs, counts = run_sampled_parity(wl, plan, ol, T, np.linspace(0, T - 1, num=min(T, 24)).astype(int))
     assert len(accepted) <= 1

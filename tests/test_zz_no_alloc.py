@@ -2,8 +2,10 @@
 allocate device memory (their memory belongs to another allocator with a
 fixed budget, or they cannot afford cudaFree's device-wide synchronisation).
 It keeps its scratch in a fixed device array inside the library instead of
-allocating; its results must equal those of moe_mx_gemm, call after call,
-although the shared array keeps whatever the previous call left in it."""
+allocating; its results must match those of moe_mx_gemm, call after call,
+although the shared array keeps whatever the previous call left in it, and
+both must match the oracle's exact block-scaled product within the tensor
+core's fp32 accumulation bound."""
 import ctypes as C
 
 import numpy as np
@@ -52,9 +54,15 @@ def test_noalloc_matches_allocating_gemm_on_consecutive_calls():
         ops = operands(seed, M, N, K)
         got = call(L.moe_mx_gemm_noalloc, ops, status)
         ref = call(L.moe_mx_gemm, ops, status)
+        exact = oracle.mx_matmul(*ops)
         mag = oracle.mx_matmul(ops[0] & 0x77, ops[1], ops[2] & 0x7F, ops[3])   # sum of |terms|
         assert np.isfinite(got).all()
         assert (np.abs(got - ref) <= mag * (K * 2.0 ** -23) + 1e-30).all()
+        # each product is added with at most two units in the last place of
+        # the running sum; the result is one more fp32 rounding
+        bound = mag * ((K + 8) * 2.0 ** -22) + np.abs(exact) * 2.0 ** -24 + 1e-30
+        assert (np.abs(got - exact) <= bound).all()
+        assert (np.abs(ref - exact) <= bound).all()
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
