@@ -238,6 +238,7 @@ constexpr int kTopkWarps = 4;
 constexpr int kTopkWideTokens = 512;  // batches up to this size use one CTA per token (without refinement)
 constexpr int kTopkPerLane = 32;     // E <= 1024
 constexpr int kMaxE = 32 * kTopkPerLane;
+constexpr int kMaxCand = 64;         // candidates ranked exactly per token (two per lane); more: exact pass over all
 // Error bound of the fp32 estimate 1 / (1 + __expf(-l)) + b of sigmoid(l) + b
 // for |b| <= 1: __expf errs by at most 2 + floor(1.173 |x|) ulp (CUDA's
 // documented bound), which moves sigmoid by at most sigmoid (1 - sigmoid)
@@ -314,10 +315,14 @@ __device__ __forceinline__ void exact_logits(const float* __restrict__ zt, int l
     for (int u = 0; u < NE; ++u) out[u] = acc[u];
 }
 
-// Second half of the top-k of token t, run by one warp: lane j < R holds the
-// j-th candidate id (on estimates); exact keys of the candidates, their
-// ranking (or the exact fallback on overflow), gates and token bitmaps.
-__device__ __noinline__ void topk_finish(const TopkArgs& a, int t, int lane, int R, bool overflow, int my_id) {
+// Second half of the top-k of token t, run by one warp.  cand[0..R) holds
+// the candidate ids (R <= kMaxCand; overflow: more than that): exact keys of
+// the candidates (their logits recomputed from z and R when the logits are
+// estimates), their ranking, gates and token bitmaps.  Lane j owns
+// candidates j and j + 32.  Without a band (exact logits, no bias) cand[0..k)
+// is already the selection in slot order.  On overflow every expert's logit
+// and key are evaluated exactly and k rounds select over all of them.
+__device__ __noinline__ void topk_finish(const TopkArgs& a, int t, int lane, const int* cand, int R, bool overflow) {
     const int E = a.E, k = a.k;
     float* l = a.logits + static_cast<int64_t>(t) * E;
     const float* bias = a.bias;
@@ -326,18 +331,26 @@ __device__ __noinline__ void topk_finish(const TopkArgs& a, int t, int lane, int
     const bool need_cand = use_bias || approx;
     const float* zt = a.z + static_cast<int64_t>(t) * a.z_ld;
     const int nper = (E + 31) / 32;
-    uint32_t taken = 0;
-    int slot = lane;                                          // final slot of this lane's pick
-    float my_l = 0.0f;                                        // exact logit of this lane's pick
-    if (need_cand) {
-        if (approx && !overflow) {
+    int id0 = 0x7fffffff, id1 = 0x7fffffff;                   // this lane's candidates (0x7fffffff: none)
+    float l0 = 0.0f, l1 = 0.0f;                               // their exact logits
+    int slot0 = 64, slot1 = 64;                               // their final slots (>= k: not selected)
+    if (!need_cand) {
+        if (lane < k) {
+            id0 = cand[lane];
+            l0 = l[id0];
+            slot0 = lane;
+        }
+    } else if (!overflow) {
+        if (lane < R) id0 = cand[lane];
+        if (lane + 32 < R) id1 = cand[lane + 32];
+        if (approx) {
             // candidates in groups of up to 8 (z is read once per group)
             for (int c = 0; c < R; c += 8) {
                 const int m = min(8, R - c);
                 int ids[8];
                 float v[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) ids[u] = __shfl_sync(0xffffffffu, my_id, min(c + u, R - 1));
+                for (int u = 0; u < 8; ++u) ids[u] = cand[min(c + u, R - 1)];
                 if (m > 4)
                     exact_logits<8>(zt, a.z_lo, a.R, ids, a.L, lane, v);
                 else if (m > 2)
@@ -347,94 +360,111 @@ __device__ __noinline__ void topk_finish(const TopkArgs& a, int t, int lane, int
                 else
                     exact_logits<1>(zt, a.z_lo, a.R, ids, a.L, lane, v);
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    if (u < m && lane == c + u) my_l = v[u];
+                for (int u = 0; u < 8; ++u) {
+                    if (u < m && c + u == lane) l0 = v[u];
+                    if (u < m && c + u == lane + 32) l1 = v[u];
+                }
             }
-        } else if (lane < R && !overflow) {
-            my_l = l[my_id];
+        } else {
+            if (id0 != 0x7fffffff) l0 = l[id0];
+            if (id1 != 0x7fffffff) l1 = l[id1];
         }
-        // exact ranking of the R candidates
-        const double kx = (lane < R) ? (use_bias ? key64(my_l, bias, my_id) : static_cast<double>(my_l)) : -INFINITY;
-        int rank = 0;
+        // exact ranking of the R candidates: larger key first, lower id on a tie
+        const double k0 = (id0 != 0x7fffffff) ? (use_bias ? key64(l0, bias, id0) : static_cast<double>(l0)) : -INFINITY;
+        const double k1 = (id1 != 0x7fffffff) ? (use_bias ? key64(l1, bias, id1) : static_cast<double>(l1)) : -INFINITY;
+        int r0 = 0, r1 = 0;
         for (int i = 0; i < R; ++i) {
-            const double oi = __shfl_sync(0xffffffffu, kx, i);
-            const int id = __shfl_sync(0xffffffffu, my_id, i);
-            if (i != lane && (oi > kx || (oi == kx && id < my_id))) ++rank;
+            const double a0 = __shfl_sync(0xffffffffu, k0, i & 31), a1 = __shfl_sync(0xffffffffu, k1, i & 31);
+            const int b0 = __shfl_sync(0xffffffffu, id0, i & 31), b1 = __shfl_sync(0xffffffffu, id1, i & 31);
+            const double ki = (i < 32) ? a0 : a1;
+            const int ii = (i < 32) ? b0 : b1;
+            if (ii != id0 && (ki > k0 || (ki == k0 && ii < id0))) ++r0;
+            if (ii != id1 && (ki > k1 || (ki == k1 && ii < id1))) ++r1;
         }
-        slot = (lane < R) ? rank : 32;
-        const bool safe = !overflow;
-        if (approx && safe) {
-            if (lane < R) l[my_id] = my_l;                    // export the exact candidate logits
-        }
-        if (!safe) {
-            // rare: exact logits (written back to the logits row) and keys of
-            // every expert, k rounds over all of them
-            if (approx) {
-                for (int e = 0; e < E; ++e) {
-                    float v;
-                    exact_logits<1>(zt, a.z_lo, a.R, &e, a.L, lane, &v);
-                    if (lane == 0) l[e] = v;
-                }
-                __syncwarp();
-            }
-            taken = 0;
-            for (int j = 0; j < k; ++j) {
-                double bk = -INFINITY;
-                int bid = 0x7fffffff;
-                float bl = 0.0f;
-                for (int i = 0; i < nper; ++i) {
-                    const int e = lane + 32 * i;
-                    if (e >= E || (taken & (1u << i))) continue;
-                    const float le = l[e];
-                    double kv = use_bias ? key64(le, bias, e) : static_cast<double>(le);
-                    if (kv != kv) kv = -INFINITY;
-                    if (bid == 0x7fffffff || kv > bk || (kv == bk && e < bid)) {
-                        bk = kv;
-                        bid = e;
-                        bl = le;
-                    }
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const double ob = __shfl_xor_sync(0xffffffffu, bk, o);
-                    const int oi = __shfl_xor_sync(0xffffffffu, bid, o);
-                    const float ol = __shfl_xor_sync(0xffffffffu, bl, o);
-                    if (oi != 0x7fffffff && (bid == 0x7fffffff || ob > bk || (ob == bk && oi < bid))) {
-                        bk = ob;
-                        bid = oi;
-                        bl = ol;
-                    }
-                }
-                if (bid < 0 || bid >= E) bid = 0;
-                if (lane == j) {
-                    my_id = bid;
-                    my_l = bl;
-                }
-                if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
-            }
-            slot = lane;
+        if (id0 != 0x7fffffff) slot0 = r0;
+        if (id1 != 0x7fffffff) slot1 = r1;
+        if (approx) {                                          // export the exact candidate logits
+            if (id0 != 0x7fffffff) l[id0] = l0;
+            if (id1 != 0x7fffffff) l[id1] = l1;
         }
     } else {
-        my_l = (lane < R) ? l[my_id] : 0.0f;
+        // rare: exact logits (written back to the logits row, eight experts
+        // at a time) and keys of every expert, k rounds over all of them
+        if (approx) {
+            for (int c = 0; c < E; c += 8) {
+                int ids[8];
+                float v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) ids[u] = min(c + u, E - 1);
+                exact_logits<8>(zt, a.z_lo, a.R, ids, a.L, lane, v);
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (c + u < E && lane == u) l[c + u] = v[u];
+            }
+            __syncwarp();
+        }
+        uint32_t taken = 0;
+        for (int j = 0; j < k; ++j) {
+            double bk = -INFINITY;
+            int bid = 0x7fffffff;
+            float bl = 0.0f;
+            for (int i = 0; i < nper; ++i) {
+                const int e = lane + 32 * i;
+                if (e >= E || (taken & (1u << i))) continue;
+                const float le = l[e];
+                double kv = use_bias ? key64(le, bias, e) : static_cast<double>(le);
+                if (kv != kv) kv = -INFINITY;
+                if (bid == 0x7fffffff || kv > bk || (kv == bk && e < bid)) {
+                    bk = kv;
+                    bid = e;
+                    bl = le;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const double ob = __shfl_xor_sync(0xffffffffu, bk, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bid, o);
+                const float ol = __shfl_xor_sync(0xffffffffu, bl, o);
+                if (oi != 0x7fffffff && (bid == 0x7fffffff || ob > bk || (ob == bk && oi < bid))) {
+                    bk = ob;
+                    bid = oi;
+                    bl = ol;
+                }
+            }
+            if (bid < 0 || bid >= E) bid = 0;
+            if (lane == j) {
+                id0 = bid;
+                l0 = bl;
+                slot0 = j;
+            }
+            if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
+        }
     }
-    // gates over the k winners (lanes whose slot < k), from exact logits
-    const bool winner = slot < k;
-    float s = winner ? my_l : 0.0f;
+    // gates over the k winners (candidates whose slot < k), from exact logits
+    const bool w0 = slot0 < k, w1 = slot1 < k;
+    float s0 = w0 ? l0 : 0.0f, s1 = w1 ? l1 : 0.0f;
     if (a.softmax) {
-        float lmax = winner ? s : -INFINITY;
+        float lmax = fmaxf(w0 ? s0 : -INFINITY, w1 ? s1 : -INFINITY);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
-        s = winner ? expf(s - lmax) : 0.0f;
+        s0 = w0 ? expf(s0 - lmax) : 0.0f;
+        s1 = w1 ? expf(s1 - lmax) : 0.0f;
     } else {
-        s = winner ? 1.0f / (1.0f + expf(-s)) : 0.0f;
+        s0 = w0 ? 1.0f / (1.0f + expf(-s0)) : 0.0f;
+        s1 = w1 ? 1.0f / (1.0f + expf(-s1)) : 0.0f;
     }
-    float sum = s;
+    float sum = s0 + s1;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (winner) {
-        a.idx[static_cast<int64_t>(t) * k + slot] = my_id;
-        a.w[static_cast<int64_t>(t) * k + slot] = s / sum;
-        atomicOr(&a.sel[static_cast<int64_t>(my_id) * a.W + (t >> 5)], 1u << (t & 31));
+    if (w0) {
+        a.idx[static_cast<int64_t>(t) * k + slot0] = id0;
+        a.w[static_cast<int64_t>(t) * k + slot0] = s0 / sum;
+        atomicOr(&a.sel[static_cast<int64_t>(id0) * a.W + (t >> 5)], 1u << (t & 31));
+    }
+    if (w1) {
+        a.idx[static_cast<int64_t>(t) * k + slot1] = id1;
+        a.w[static_cast<int64_t>(t) * k + slot1] = s1 / sum;
+        atomicOr(&a.sel[static_cast<int64_t>(id1) * a.W + (t >> 5)], 1u << (t & 31));
     }
 }
 
@@ -480,7 +510,7 @@ __device__ __forceinline__ void input_norms(const float* __restrict__ zt, int lo
 }
 
 __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(TopkArgs a) {
-    __shared__ int s_cand[kTopkWarps][32];
+    __shared__ int s_cand[kTopkWarps][kMaxCand];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * kTopkWarps + warp;
     if (t >= a.T) return;
@@ -501,7 +531,6 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(TopkArgs a) {
             key[i] = (i < nper && e < E) ? key_bits(kv) : kNoKey;
         }
         uint32_t taken = 0;
-        int my_id = 0;
         for (int j = 0; j < k; ++j) {
             uint32_t lb = kNoKey;
             int lid = 0x7fffffff;
@@ -516,10 +545,11 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(TopkArgs a) {
             uint32_t bb;
             int bid = warp_best_id(lb, lid, bb);
             if (bid < 0 || bid >= E) bid = 0;                 // unreachable while k <= E
-            if (lane == j) my_id = bid;
+            if (lane == 0) s_cand[warp][j] = bid;
             if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
         }
-        topk_finish(a, t, lane, k, false, my_id);
+        __syncwarp();
+        topk_finish(a, t, lane, s_cand[warp], k, false);
         return;
     }
     // error bound of each key estimate: d_e = A |R_lo_e| + B |R_e| for
@@ -592,7 +622,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(TopkArgs a) {
         if (lane >= o) incl += n;
     }
     const int total = __shfl_sync(0xffffffffu, incl, 31);
-    const bool overflow = total > 32;
+    const bool overflow = total > kMaxCand;
     if (!overflow) {
         int pos = incl - c;
         while (mask) {
@@ -602,9 +632,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(TopkArgs a) {
         }
     }
     __syncwarp();
-    const int R = overflow ? 32 : total;
-    const int my_id = (!overflow && lane < R) ? s_cand[warp][lane] : 0;
-    topk_finish(a, t, lane, R, overflow, my_id);
+    topk_finish(a, t, lane, s_cand[warp], overflow ? 0 : total, overflow);
 }
 
 // Top-k of small batches: one CTA per token, one thread per expert.  The
@@ -616,7 +644,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(TopkArgs a) {
 // equal key and lower id, first) orders them, and warp 0 finishes as
 // topk_kernel.  Every step is a short chain: this batch size is latency-bound.
 constexpr int kTopkWideThreads = kMaxE;
-constexpr int kRankCap = 33;
+constexpr int kRankCap = kMaxCand + 1;
 __global__ void __launch_bounds__(kTopkWideThreads) topk_wide_kernel(TopkArgs a) {
     __shared__ int s_cand[kMaxE];
     __shared__ uint32_t s_ckb[kMaxE];
@@ -668,11 +696,9 @@ __global__ void __launch_bounds__(kTopkWideThreads) topk_wide_kernel(TopkArgs a)
     }
     __syncthreads();
     if (threadIdx.x >= 32) return;
-    int R = band ? n : k;
-    const bool over = R > 32;
-    if (over) R = 32;
-    const int my_id = (lane < R) ? s_rank[lane] : 0;
-    topk_finish(a, t, lane, R, over, my_id);
+    const int R = band ? n : k;
+    const bool over = R > kMaxCand;
+    topk_finish(a, t, lane, s_rank, over ? 0 : R, over);
 }
 
 // ------------------------------------------------------------------ A5: per-expert scan
