@@ -48,13 +48,35 @@ def peaks():
 
 CPU_BASELINE_SECONDS = 10.0
 
-# DRAM bytes (read + write) per launch of a stage's kernel from one ncu
-# capture, and the commit the capture was taken at; a capture stands only
-# until its kernel changes (summaries under profiles/).
-NCU_TRAFFIC = {
-    ("decode64", "gemm_gate_up"): (1.331121e9 + 3.783424e6, "60ceff4", "profiles/gate_up_decode64.md"),
-    ("prefill8192", "gemm_gate_up"): (2.266878e9 + 69.639424e6, "60ceff4", "profiles/gate_up_prefill8192.md"),
-}
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the layer's
+# kernels from an ncu capture, stored with a hash of the kernel sources it
+# was taken on; a figure stands only while the sources are unchanged.
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+SOURCE_FILES = ("api.cu", "gemm.cu", "kernels.cu", "peak.cu", "router.cu", "internal.h", "mx.cuh", "ptx.cuh")
+
+
+def kernel_source_hash() -> str:
+    """sha256 (first 16 hex digits) of the library's CUDA sources and header."""
+    import hashlib
+    h = hashlib.sha256()
+    src = os.path.join(ROOT, "moe_expert_layer_top16_gb300", "csrc")
+    for f in SOURCE_FILES + ("../../include/moe.h",):
+        with open(os.path.join(src, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """(DRAM bytes of one forward, per-kernel dict) from the stored capture of
+    `workload`, or (None, None) when there is none or the sources changed."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f).get(workload)
+    except Exception:
+        return None, None
+    if not rec or rec.get("source_hash") != kernel_source_hash():
+        return None, None
+    return rec.get("layer_dram_bytes"), rec.get("kernels")
 
 
 def workload_config(wl, T):
@@ -273,6 +295,173 @@ def run_reference(args, wl, world, rank):
 
 
 # ---------------------------------------------------------------- CUDA path
+def measure_tensor_peaks(dev, reps=5):
+    """Issue rate of the tensor cores on this GPU (moe_mma_probe): the
+    layer's block-scaled kind::mxf8f6f4 MMA (E2M1 x E4M3, N = 240) and
+    kind::f16 (bf16, N = 256), best of `reps` timed launches, TFLOP/s."""
+    import torch
+    import moe_expert_layer_top16_gb300 as moe
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = {}
+    for name, kind, n, iters in (("mxf8f6f4_e2m1_e4m3", moe.PROBE_MX_E2M1_E4M3, 240, 20000),
+                                 ("f16_bf16", moe.PROBE_BF16, 256, 20000)):
+        rates = []
+        for i in range(reps + 2):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            flops = moe.mma_probe(kind, n, iters, status)
+            b.record()
+            torch.cuda.synchronize()
+            if i >= 2:
+                rates.append(flops / (a.elapsed_time(b) / 1e3) / 1e12)
+        if int(status.item()) != 0:
+            raise RuntimeError("device-side time-out in the tensor-core probe")
+        out[name] = max(rates)
+    return out
+
+
+def time_layer(plan, wl, T, x, y, flush, steps, warmup, world, with_stages=True):
+    """Warm-up, an untimed per-stage pass (events between the stages), then
+    exactly `steps` forwards each between two events on the forward's stream,
+    with the L2 flush outside the events.  Returns (step_ms list, mean stage
+    ms, realised counts, clocks, wall seconds of the timed region)."""
+    import torch
+    import moe_expert_layer_top16_gb300 as moe
+    dev = x.device
+    counts = torch.zeros(wl.n_experts, dtype=torch.int32, device=dev)
+    for i in range(max(warmup, 1)):
+        plan.forward(x, out=y, debug={"counts": counts} if i == 0 else None)
+    torch.cuda.synchronize()
+    if plan.device_status() != moe.MOE_OK:
+        raise RuntimeError("device-side error during warm-up")
+    counts_h = counts.cpu().numpy()
+    nst = moe.NUM_STAGES
+    stage_ms = None
+    if with_stages:
+        n_stage = min(steps, 20)
+        stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(n_stage)]
+        for evs in stage_ev:                 # torch creates the CUDA events at their first record
+            for e in evs:
+                e.record()
+        torch.cuda.synchronize()
+        for i in range(n_stage):
+            flush.fill_(float(i))
+            plan.forward(x, out=y, stage_events=stage_ev[i])
+        torch.cuda.synchronize()
+        stage_ms = np.array([[stage_ev[i][s].elapsed_time(stage_ev[i][s + 1]) for s in range(nst)]
+                             for i in range(n_stage)]).mean(axis=0)
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    torch.cuda.synchronize()
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(dev.index)
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(steps):
+        flush.fill_(float(i))                       # L2 flush, outside the step events
+        ev0[i].record()
+        plan.forward(x, out=y)
+        ev1[i].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    if plan.device_status() != moe.MOE_OK:
+        raise RuntimeError("device-side error in the timed region")
+    step_ms = [ev0[i].elapsed_time(ev1[i]) for i in range(steps)]
+    return step_ms, stage_ms, counts_h, clocks, wall
+
+
+def layer_roofline(wl, T, ms_per_step, stage_ms, counts_h, hbm, tensor_peak, peak_source):
+    """Roofline of the whole layer step and of its dominant kernel.  The
+    layer figure is the headline: decode-sized batches (below 4096 tokens)
+    on expert-weight bytes over the measured HBM copy bandwidth,
+    prefill-sized ones on MX FLOPs over the measured block-scaled MMA rate.
+    The dominant stage's own figure rides along under "kernel"."""
+    import moe_expert_layer_top16_gb300 as moe
+    work, touched, expert_bytes = algorithmic_work(wl, T, counts_h)
+    step_s = ms_per_step / 1e3
+    layer_flops = sum(f for _, f in work.values())
+    names = moe.STAGE_NAMES
+    dom = int(np.argmax(stage_ms))
+    dom_name = names[dom]
+    k_bytes, k_flops = work.get(dom_name, (0.0, 0.0))
+    k_s = stage_ms[dom] / 1e3
+    tensor_bound = T >= 4096
+    traffic, per_kernel = ncu_traffic(wl.name)
+    kernel = {"name": dom_name, "ms": float(stage_ms[dom]),
+              "hbm": {"achieved": k_bytes / k_s / 1e9, "frac": k_bytes / k_s / 1e9 / hbm, "algorithmic_bytes": k_bytes},
+              "tensor": {"achieved": k_flops / k_s / 1e12, "frac": k_flops / k_s / 1e12 / tensor_peak,
+                         "flops": k_flops},
+              "traffic": (per_kernel or {}).get(dom_name)}
+    if tensor_bound:
+        roof = {"bound": "tensor", "scope": "layer: MX FLOPs per step", "achieved": layer_flops / step_s / 1e12,
+                "peak": tensor_peak, "unit": "TFLOP/s", "frac": layer_flops / step_s / 1e12 / tensor_peak,
+                "peak_source": peak_source}
+    else:
+        roof = {"bound": "hbm", "scope": "layer: expert-weight bytes per step",
+                "achieved": expert_bytes / step_s / 1e9, "peak": hbm, "unit": "GB/s",
+                "frac": expert_bytes / step_s / 1e9 / hbm, "peak_source": "measured copy bandwidth"}
+    roof["traffic"] = traffic
+    roof["traffic_note"] = ("ncu dram__bytes_read.sum + dram__bytes_write.sum over one forward's kernels, "
+                            "taken on the current kernel sources" if traffic is not None
+                            else "no ncu capture of the current kernel sources")
+    roof["kernel"] = kernel
+    roof["kernel_frac"] = kernel["tensor" if tensor_bound else "hbm"]["frac"]
+    layer = {"touched_experts": touched, "expert_weight_bytes": expert_bytes,
+             "expert_weight_GBps": expert_bytes / step_s / 1e9,
+             "expert_weight_frac_hbm": expert_bytes / step_s / 1e9 / hbm,
+             "mx_tflops": layer_flops / step_s / 1e12, "mx_frac_tensor_peak": layer_flops / step_s / 1e12 / tensor_peak,
+             "max_over_mean_load": float(counts_h.max() / max(counts_h.mean(), 1e-9)),
+             "stage_ms": {n: float(v) for n, v in zip(names, stage_ms)}}
+    return roof, layer
+
+
+def routing_check(plan, wl, x, n_tok, dev):
+    """The GPU's selection for the first n_tok tokens against the oracle's
+    (on its own latent): tokens whose lists differ, and how many of those are
+    certified near-ties (key gap within twice the selected logits' error)."""
+    import torch
+    import oracle
+    import synth
+    import moe_expert_layer_top16_gb300 as moe
+
+    def fetch(name, i):
+        if name == "bias":
+            b = synth.router_bias(wl, device="cpu")
+            return None if b is None else b.numpy()
+        return synth.weight(wl, name, i, device=dev).cpu().numpy()
+
+    T = x.shape[0]
+    dbg = moe.debug_buffers(wl, T, dev, ("topk_idx", "logits"))
+    plan.forward(x, debug=dbg)
+    torch.cuda.synchronize()
+    idx = dbg["topk_idx"][:n_tok].cpu().numpy()
+    lg = dbg["logits"][:n_tok].cpu().numpy().astype(np.float64)
+    xb = x[:n_tok].contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+    r = oracle.moe_forward(wl, oracle.encode_layer(wl, fetch, experts=[]), xb, route_only=True,
+                           want=("idx", "logits"))
+    bias = synth.router_bias(wl, device="cpu")
+    b = 0.0 if bias is None else bias.numpy().astype(np.float64)
+    keys = r["logits"] if bias is None else 1.0 / (1.0 + np.exp(-r["logits"])) + b
+    differ, near = 0, 0
+    for t in range(n_tok):
+        if list(idx[t]) == list(r["idx"][t]):
+            continue
+        differ += 1
+        sel = idx[t].astype(np.int64)
+        delta = float(np.max(np.abs(lg[t, sel] - r["logits"][t, sel])))
+        if all(abs(keys[t, a] - keys[t, c]) <= 2 * delta + 1e-12 for a, c in zip(idx[t], r["idx"][t]) if a != c):
+            near += 1
+    return {"tokens": n_tok, "differing": differ, "certified_near_ties": near}
+
+
 def run_cuda(args, wl, world, rank, local):
     import torch
     import synth
@@ -284,6 +473,7 @@ def run_cuda(args, wl, world, rank, local):
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     T = wl.tokens
+    pre = None if args.no_prefill or T >= args.prefill_tokens else wl.with_tokens(args.prefill_tokens)
 
     def fetch(name, i):
         if name == "bias":
@@ -291,66 +481,19 @@ def run_cuda(args, wl, world, rank, local):
         return synth.weight(wl, name, i, device=dev)
 
     W = encode_layer(wl, fetch, dev)
-    plan = moe.Plan(wl, W, max_tokens=T)
+    plan = moe.Plan(wl, W, max_tokens=max(T, pre.tokens if pre else 0))
     del W
     torch.cuda.empty_cache()
+    hbm, bf16, bf16_sus, peak_kind = peaks()
+    tpk = measure_tensor_peaks(dev)
+    tensor_peak = tpk["mxf8f6f4_e2m1_e4m3"]
+    peak_source = "measured: tcgen05.mma kind::mxf8f6f4 E2M1 x E4M3 issue rate (moe_mma_probe), this GPU"
     x = synth.hidden_states(wl, T, device=dev, offset=rank * T)
     y = torch.empty(T, wl.d_model, dtype=torch.float32, device=dev)
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    counts = torch.zeros(wl.n_experts, dtype=torch.int32, device=dev)
-
-    nst = moe.NUM_STAGES
-    # warm-up (also captures the realised expert histogram)
-    for i in range(max(args.warmup, 1)):
-        plan.forward(x, out=y, debug={"counts": counts} if i == 0 else None)
-    torch.cuda.synchronize()
-    if plan.device_status() != moe.MOE_OK:
-        raise RuntimeError("device-side error during warm-up")
-    counts_h = counts.cpu().numpy()
 
     K = args.steps
-    # per-stage breakdown: a separate, untimed pass with events between the stages
-    n_stage = min(K, 20)
-    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(n_stage)]
-    for evs in stage_ev:                 # torch creates the CUDA events at their first record
-        for e in evs:
-            e.record()
-    torch.cuda.synchronize()
-    for i in range(n_stage):
-        flush.fill_(float(i))
-        plan.forward(x, out=y, stage_events=stage_ev[i])
-    torch.cuda.synchronize()
-    stage_ms = np.array([[stage_ev[i][s].elapsed_time(stage_ev[i][s + 1]) for s in range(nst)]
-                         for i in range(n_stage)])
-
-    # timed region: exactly K forwards, each between two events on the forward's
-    # stream; the L2 flush sits between steps, outside the events
-    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    torch.cuda.synchronize()
-    try:
-        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
-    except Exception:
-        gpu_id = str(local)
-    sampler = ClockSampler(gpu_id)
-    sampler.start()
-    time.sleep(0.3)
-    barrier(world)
-    torch.cuda.synchronize()
-    wall0 = time.perf_counter()
-    for i in range(K):
-        flush.fill_(float(i))                       # L2 flush, outside the step events
-        ev0[i].record()
-        plan.forward(x, out=y)
-        ev1[i].record()
-    torch.cuda.synchronize()
-    barrier(world)
-    wall = time.perf_counter() - wall0
-    clocks = sampler.stop()
-    if plan.device_status() != moe.MOE_OK:
-        raise RuntimeError("device-side error in the timed region")
-
-    step_ms = [ev0[i].elapsed_time(ev1[i]) for i in range(K)]
+    step_ms, stage_ms, counts_h, clocks, wall = time_layer(plan, wl, T, x, y, flush, K, args.warmup, world)
     total_ms = max_over_ranks(world, float(np.sum(step_ms)))
     ms_per_step = total_ms / K
     value = job_throughput(world, T, K, total_ms)
@@ -368,35 +511,7 @@ def run_cuda(args, wl, world, rank, local):
     e2e_s = max_over_ranks(world, time.perf_counter() - t0)
     e2e_value = world * T * n_e2e / e2e_s
 
-    hbm, bf16, bf16_sus, peak_kind = peaks()
-    work, touched, expert_bytes = algorithmic_work(wl, T, counts_h)
-    mean_stage = stage_ms.mean(axis=0)
-    names = moe.STAGE_NAMES
-    dom = int(np.argmax(mean_stage))
-    dom_name = names[dom]
-    bytes_, flops = work.get(dom_name, (0.0, 0.0))
-    stage_s = mean_stage[dom] / 1e3
-    key = (wl.name, dom_name)
-    traffic = NCU_TRAFFIC[key][0] if key in NCU_TRAFFIC else None
-    # decode-sized batches are judged on HBM bytes, prefill-sized ones (4096
-    # tokens and up) on the tensor pipe; the other roof's fraction rides along,
-    # since a grouped GEMM near 150 tokens per expert sits at the ridge of both
-    peak_t = bf16 * 2.0          # W4A8 block-scaled MMA: measured bf16 peak x nominal mxf8f6f4 / bf16 (4.5 / 2.25)
-    t_roof = {"bound": "tensor", "kernel": dom_name, "achieved": flops / stage_s / 1e12, "peak": peak_t,
-              "unit": "TFLOP/s", "frac": flops / stage_s / 1e12 / peak_t, "traffic": traffic,
-              "peak_source": f"{peak_kind} bf16 burst {bf16} TFLOP/s x 2 (nominal fp8/bf16 ratio)"}
-    h_roof = {"bound": "hbm", "kernel": dom_name, "achieved": bytes_ / stage_s / 1e9, "peak": hbm, "unit": "GB/s",
-              "frac": bytes_ / stage_s / 1e9 / hbm, "traffic": traffic, "peak_source": f"{peak_kind} copy bandwidth"}
-    tensor_bound = T >= 4096 and flops > 0
-    roof, other = (t_roof, h_roof) if tensor_bound else (h_roof, t_roof)
-    roof["other_roof"] = {"bound": other["bound"], "achieved": other["achieved"], "unit": other["unit"],
-                          "frac": other["frac"]}
-    if traffic is not None:
-        roof["traffic_source"] = f"ncu dram__bytes_read.sum + dram__bytes_write.sum, {NCU_TRAFFIC[key][2]}, " \
-                                 f"commit {NCU_TRAFFIC[key][1]}"
-    layer_bytes = sum(b for b, _ in work.values())
-    layer_flops = sum(f for _, f in work.values())
-    step_s = ms_per_step / 1e3
+    roof, layer = layer_roofline(wl, T, ms_per_step, stage_ms, counts_h, hbm, tensor_peak, peak_source)
     result = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -407,22 +522,36 @@ def run_cuda(args, wl, world, rank, local):
                        l2="flushed by a 512 MB write between timed steps (outside the step events)",
                        parallelism=f"replicas x{world}"),
         "roofline": roof,
-        "layer": {"touched_experts": touched, "expert_weight_bytes": expert_bytes,
-                  "expert_weight_GBps": expert_bytes / step_s / 1e9,
-                  "expert_weight_frac_hbm": expert_bytes / step_s / 1e9 / hbm,
-                  "algorithmic_bytes": layer_bytes, "mx_tflops": layer_flops / step_s / 1e12,
-                  "mx_frac_fp8_peak": layer_flops / step_s / 1e12 / (bf16 * 2.0),
-                  # the same against the FP4-only rate (kind::mxf4, nominally 6x bf16), which a
-                  # W4A8 product cannot reach: at most 1/3 of it
-                  "mx_frac_fp4_peak": layer_flops / step_s / 1e12 / (bf16 * 6.0),
-                  "max_over_mean_load": float(counts_h.max() / max(counts_h.mean(), 1e-9)),
-                  "stage_ms": {n: float(v) for n, v in zip(names, mean_stage)}},
+        "layer": layer,
+        "tensor_peaks_tflops": dict(tpk, note="issue rate of back-to-back MMAs on shared-memory operands, "
+                                              "one CTA per SM, best of 5 launches; kind::mxf4 is not probed: "
+                                              "a W4A8 product cannot use it"),
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": int(T * wl.d_model * 2),
                 "d2h_bytes_per_step": int(T * wl.d_model * 4)},
         "gpu_launches": launches_per_forward(T) * K,
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }
+    if pre is not None:
+        # the same layer at the prefill batch, timed the same way in the same run
+        Tp = pre.tokens
+        xp = synth.hidden_states(pre, Tp, device=dev, offset=rank * Tp)
+        yp = torch.empty(Tp, wl.d_model, dtype=torch.float32, device=dev)
+        Kp = max(5, min(K, 40))
+        p_ms, p_stage, p_counts, p_clocks, p_wall = time_layer(plan, pre, Tp, xp, yp, flush, Kp, args.warmup, world)
+        p_total = max_over_ranks(world, float(np.sum(p_ms)))
+        p_roof, p_layer = layer_roofline(pre, Tp, p_total / Kp, p_stage, p_counts, hbm, tensor_peak, peak_source)
+        result["prefill"] = {"workload": pre.name, "tokens": Tp, "steps": Kp, "ms_per_step": p_total / Kp,
+                             "value": job_throughput(world, Tp, Kp, p_total), "unit": "tokens/s",
+                             "step_ms": {"median": float(np.median(p_ms)), "p10": float(np.percentile(p_ms, 10)),
+                                         "p90": float(np.percentile(p_ms, 90))},
+                             "roofline": p_roof, "layer": p_layer, "gpu_launches": launches_per_forward(Tp) * Kp,
+                             "clocks": p_clocks, "wall_s_timed_region": p_wall}
+        result["gpu_launches"] += launches_per_forward(Tp) * Kp
+        del xp, yp
+    if rank == 0 and not args.no_cpu_baseline:
+        n_tok = min(args.cpu_tokens, T)
+        result["layer"]["routing_check"] = routing_check(plan, wl, x, n_tok, dev)
     plan.close()
     del flush
     if rank == 0 and not args.no_cpu_baseline:
@@ -473,6 +602,7 @@ def run_sweep(args, wl, rank, local):
     torch.cuda.empty_cache()
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     hbm, bf16, _, _ = peaks()
+    tensor_peak = measure_tensor_peaks(dev)["mxf8f6f4_e2m1_e4m3"]
     for T in synth.SWEEP_TOKENS:
         x = synth.hidden_states(wl, T, device=dev)
         y = torch.empty(T, wl.d_model, dtype=plan.out_dtype, device=dev)
@@ -496,7 +626,8 @@ def run_sweep(args, wl, rank, local):
         line = {"impl": "sweep", "workload": wl.name, "tokens": T, "ms_median": ms, "tokens_per_s": T / (ms / 1e3),
                 "touched_experts": touched, "expert_weight_GBps": expert_bytes / (ms / 1e3) / 1e9,
                 "expert_weight_frac_hbm": expert_bytes / (ms / 1e3) / 1e9 / hbm,
-                "mx_tflops": flops / (ms / 1e3) / 1e12, "mx_frac_fp8_peak": flops / (ms / 1e3) / 1e12 / (bf16 * 2.0),
+                "mx_tflops": flops / (ms / 1e3) / 1e12, "mx_frac_tensor_peak": flops / (ms / 1e3) / 1e12 / tensor_peak,
+                "tensor_peak_tflops": tensor_peak,
                 "steps": steps, "l2": "flushed between steps"}
         if rank == 0:
             print(json.dumps(line), flush=True)
@@ -514,6 +645,9 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=64)
     ap.add_argument("--reference-tokens", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="skip the prefill sub-record (the same layer at --prefill-tokens tokens)")
+    ap.add_argument("--prefill-tokens", type=int, default=8192)
     ap.add_argument("--sweep", action="store_true",
                     help="token-count sweep of the workload's layer: one JSON line per batch size")
     args = ap.parse_args()

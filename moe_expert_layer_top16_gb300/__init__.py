@@ -31,7 +31,8 @@ OUT_F32, OUT_BF16 = 0, 1
 
 # Entry points declared in include/moe.h.
 ENTRY_POINTS = ("moe_plan", "moe_forward", "moe_forward_host", "moe_get_device_status", "moe_workspace_bytes",
-                "moe_free", "moe_status_str", "moe_mxfp4_encode", "moe_mx_gemm", "moe_mx_gemm_noalloc")
+                "moe_free", "moe_status_str", "moe_mxfp4_encode", "moe_mx_gemm", "moe_mma_probe",
+                "moe_mx_gemm_noalloc")
 
 
 class MoeError(RuntimeError):
@@ -102,6 +103,8 @@ def lib(build_if_missing: bool = False):
             L.moe_mxfp4_encode.argtypes = [P, i64, i64, P, P, P]
             L.moe_mx_gemm.restype = C.c_int
             L.moe_mx_gemm.argtypes = [P, P, i32, P, P, i32, i32, P, P, P]
+            L.moe_mma_probe.restype = C.c_int
+            L.moe_mma_probe.argtypes = [i32, i32, i32, P, C.POINTER(C.c_double), P]
             L.moe_mx_gemm_noalloc.restype = C.c_int
             L.moe_mx_gemm_noalloc.argtypes = [P, P, i32, P, P, i32, i32, P, P, P]
             _lib = L
@@ -168,6 +171,18 @@ def mx_gemm(a_codes, a_scales, b_codes, b_scales, out=None, status=None, stream=
     _check(lib().moe_mx_gemm(_ptr(a_codes), _ptr(a_scales), M, _ptr(b_codes), _ptr(b_scales), N, K, _ptr(out),
                              _ptr(status), _stream_ptr(stream)), "moe_mx_gemm")
     return out
+
+
+PROBE_MX_E2M1_E4M3, PROBE_MX_E4M3_E4M3, PROBE_BF16 = 0, 1, 2
+
+
+def mma_probe(kind: int, n: int, iters: int, status: torch.Tensor, stream=None) -> float:
+    """Enqueue the tensor-core rate probe (see moe_mma_probe in include/moe.h);
+    returns the FLOPs of the launch."""
+    flops = C.c_double(0.0)
+    _check(lib().moe_mma_probe(int(kind), int(n), int(iters), _ptr(status), C.byref(flops), _stream_ptr(stream)),
+           "moe_mma_probe")
+    return flops.value
 
 
 class Plan:

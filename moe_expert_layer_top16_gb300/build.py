@@ -1,6 +1,6 @@
 """Build libmoe.so (the C-ABI library) in-tree with nvcc for sm_103a.
 
-The three translation units compile in parallel; the result lands in
+The translation units compile in parallel; the result lands in
 moe_expert_layer_top16_gb300/_build/libmoe.so.  The CUDA runtime is linked
 statically, so the library loads on machines without a GPU driver (it only
 needs one when a call reaches the device).
@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmoe.so")
-UNITS = ("gemm.cu", "kernels.cu", "api.cu")
+UNITS = ("gemm.cu", "kernels.cu", "api.cu", "peak.cu", "router.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]
 

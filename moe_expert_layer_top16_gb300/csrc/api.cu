@@ -84,6 +84,20 @@ bool map_f32(CUtensorMap* m, const void* base, int64_t rows, int64_t K, uint32_t
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 rows of `pitch` floats viewed as [rows][K], 32-wide (128-byte) x
+// box_rows boxes.
+bool map_f32_view(CUtensorMap* m, const void* base, int64_t rows, int64_t K, int64_t pitch, uint32_t box_rows) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch * 4)};
+    cuuint32_t box[2] = {32, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // MXFP8 activation codes [rows][K], 128-wide x 16-row boxes.
 bool map_mx8(CUtensorMap* m, const void* codes, int64_t rows, int64_t K, int box_rows = 16) {
     EncodeTiledFn f = encode_fn();
@@ -155,6 +169,10 @@ struct Plan {
     CUtensorMap tB2w, tB10w, tB7w, tB8w, tBRw;
     int wide_dense = 0, wide_grp = 0, wide_router = 0;
     bool tc_router;    // router logit estimates on the tensor cores (one TF32 product) above 128 tokens
+    // streaming exact router of up to 128 tokens: R and router input maps,
+    // and which cluster sizes this device schedules
+    CUtensorMap tRS, tZS;
+    bool rs16 = false, rs8 = false;
 };
 
 template <typename T>
@@ -537,6 +555,13 @@ moe_status moe_plan(const moe_config* cfg, const moe_weights* w, int device, voi
               map_f32(&p->tAR, p->router2, E, 2 * p->RK, 128) &&
               (p->route_hidden ? map_f32(&p->tBR, p->xr, Tp, D, 16) : map_f32(&p->tBR, p->z, Tp, 2 * L, 16));
     p->tc_router = (E % 128 == 0) && (p->RK % 32 == 0);
+    if (ok && router_stream_ok(p->RK) && router_stream_setup() == cudaSuccess) {
+        ok = map_f32_view(&p->tRS, p->router, E, p->RK, p->RK, 128) &&
+             (p->route_hidden ? map_f32_view(&p->tZS, p->xr, Tp, D, D, 64)
+                              : map_f32_view(&p->tZS, p->z, Tp, L, 2 * L, 64));
+        p->rs16 = router_stream_max_clusters(16) > 0;
+        p->rs8 = router_stream_max_clusters(8) > 0;
+    }
     if (!ok) {
         plan_release(p);
         return MOE_ERR_CUDA;
@@ -652,6 +677,8 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         const int items = g.m_tiles * ((T + g.n_max - 1) / g.n_max);
         shape_gemm(g, 0, items, std::min(items, p->num_sms));
         TRY(launch_gemm(g, std::min(items, p->num_sms), s));
+    } else if (T <= 128 && (T <= 64 ? p->rs16 : p->rs8)) {
+        TRY(launch_router_stream(p->tRS, p->tZS, p->logits, T, E, p->RK, T <= 64 ? 16 : 8, p->status, s));
     } else {
         if (p->route_hidden)
             TRY(launch_router(p->xr, D, 0, p->router, p->logits, T, E, D, s));

@@ -114,6 +114,15 @@ constexpr int kRouterSplitTokens = 128;
 // remainders at offset lo (lo = 0: none); R [E][L]
 cudaError_t launch_router(const float* z, int ld, int lo, const float* R, float* logits, int T, int E, int L,
                           cudaStream_t s);
+// Streaming exact fp32 router for up to 128 tokens (router.cu): tmR maps R
+// [E][K] fp32 (box {32, 128}), tmZ the router input rows [T_pad][K] (box
+// {32, 64}), both with the 128-byte swizzle; K split over clusters of c = 8
+// or 16 CTAs.
+bool router_stream_ok(int K);
+cudaError_t router_stream_setup();
+int router_stream_max_clusters(int c);
+cudaError_t launch_router_stream(const CUtensorMap& tmR, const CUtensorMap& tmZ, float* logits, int T, int E, int K,
+                                 int c, int* status, cudaStream_t s);
 // top-k + gates (kernels.cu).  With refine, the logits are tensor-core
 // estimates z_hi R_hi (both rounded to TF32) and the candidates' exact fp32
 // logits are recomputed from z ([T][z_ld], hi | lo) and R ([E][L]).  The
