@@ -24,6 +24,11 @@ Parity status per function (what pins it is in ``tests/test_oracle_*.py``):
                  the small layer, and by linearity of the combine; the pages
                  print no K3-shaped output, so end-to-end K3 values beyond
                  that are parity unpinned.
+  bf16_round     pinned: hand cases of round-to-nearest-even on the bf16 grid,
+                 and the library conversion (torch) on random fp32 values.
+  moe_forward, mixed scheme (BF16 projections and shared experts): pinned by
+                 a dense recomputation from numpy matmuls of the decoded bf16
+                 weights, and by one-hot projection rows that copy x into z.
 """
 from __future__ import annotations
 
@@ -58,14 +63,16 @@ class _MX(C.Structure):
 
 
 class _Cfg(C.Structure):
-    _fields_ = [(n, C.c_int32) for n in ("D", "L", "E", "k", "I", "S", "Is", "softmax", "route_hidden")]
+    _fields_ = [(n, C.c_int32) for n in ("D", "L", "E", "k", "I", "S", "Is", "softmax", "route_hidden", "mixed")]
 
 
 class _Weights(C.Structure):
     _fields_ = [("p_down", _MX), ("p_up", _MX),
                 ("w_gate", C.POINTER(_MX)), ("w_up", C.POINTER(_MX)), ("w_down", C.POINTER(_MX)),
                 ("s_gate", C.POINTER(_MX)), ("s_up", C.POINTER(_MX)), ("s_down", C.POINTER(_MX)),
-                ("router", C.c_void_p), ("bias", C.c_void_p)]
+                ("router", C.c_void_p), ("bias", C.c_void_p),
+                ("p_down_bf", C.c_void_p), ("p_up_bf", C.c_void_p), ("s_gate_bf", C.c_void_p),
+                ("s_up_bf", C.c_void_p), ("s_down_bf", C.c_void_p)]
 
 
 _OUT_FIELDS = ["y", "xq", "xs", "z", "zq", "zs", "hs", "hsq", "hss", "logits", "idx", "gates",
@@ -102,6 +109,8 @@ def lib():
             L.orc_permute.argtypes = [P, i64, C.c_int, C.c_int, P, P, P]
             L.orc_combine.restype = None
             L.orc_combine.argtypes = [P, P, P, i64, C.c_int, i64, P]
+            L.orc_bf16_round_array.restype = None
+            L.orc_bf16_round_array.argtypes = [P, i64, P]
             L.orc_moe_forward.restype = C.c_int
             L.orc_moe_forward.argtypes = [C.POINTER(_Cfg), C.POINTER(_Weights), P, i64, P, C.c_int,
                                           C.POINTER(_Out)]
@@ -171,6 +180,19 @@ def mxfp8_quantize(v: np.ndarray):
     scales = np.zeros((rows, K // 32), np.uint8)
     lib().orc_mxfp8_quantize(_p(v), rows, K, _p(codes), _p(scales))
     return codes, scales
+
+
+def bf16_round(v: np.ndarray) -> np.ndarray:
+    """fp32 values -> bf16 bit patterns (uint16), nearest with ties to even."""
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.zeros(v.shape, np.uint16)
+    lib().orc_bf16_round_array(_p(v), v.size, _p(out))
+    return out
+
+
+def bf16_decode(b: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> their exact values (fp64): the upper half of an fp32."""
+    return (np.asarray(b, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
 def mxfp8_decode(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
@@ -254,10 +276,20 @@ class LayerWeights:
         bias = enc.get("bias")
         bias = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
         self._keep += [router, bias]
-        self.cw = _Weights(mx(enc["p_down"]), mx(enc["p_up"]),
+
+        def bf(name):
+            a = enc.get(name + "_bf16")
+            if a is None:
+                return None
+            a = np.ascontiguousarray(a, dtype=np.uint16)
+            self._keep.append(a)
+            return a.ctypes.data
+
+        self.cw = _Weights(mx(enc.get("p_down")), mx(enc.get("p_up")),
                            arr("w_gate", E), arr("w_up", E), arr("w_down", E),
                            arr("s_gate", S), arr("s_up", S), arr("s_down", S),
-                           router.ctypes.data, None if bias is None else bias.ctypes.data)
+                           router.ctypes.data, None if bias is None else bias.ctypes.data,
+                           bf("p_down"), bf("p_up"), bf("s_gate"), bf("s_up"), bf("s_down"))
 
 
 def moe_forward(wl, weights: LayerWeights, x_bf16_bits: np.ndarray, force_idx=None,
@@ -285,7 +317,12 @@ def moe_forward(wl, weights: LayerWeights, x_bf16_bits: np.ndarray, force_idx=No
         shp, dt = shapes[name]
         res[name] = np.zeros(shp, dt)
         setattr(out, name, res[name].ctypes.data)
-    cfg = _Cfg(D, L, E, k, I, S, Is, 1 if wl.score == "softmax" else 0, 1 if wl.route == "hidden" else 0)
+    mixed = getattr(wl, "precision", "mx") == "mixed"
+    if mixed:
+        for name in ("p_down", "p_up") + (("s_gate", "s_up", "s_down") if S > 0 else ()):
+            assert weights.enc.get(name + "_bf16") is not None, f"mixed scheme needs bf16 {name}"
+    cfg = _Cfg(D, L, E, k, I, S, Is, 1 if wl.score == "softmax" else 0, 1 if wl.route == "hidden" else 0,
+               1 if mixed else 0)
     fi = None
     if force_idx is not None:
         fi = np.ascontiguousarray(force_idx, dtype=np.int32)
@@ -305,11 +342,19 @@ def encode_layer(wl, fetch, experts=None, device_hint=None) -> LayerWeights:
     limits which routed experts are encoded (None = all).
     """
     enc = {}
-    for name in ("p_down", "p_up"):
-        enc[name] = mxfp4_encode(fetch(name, 0))
-    for s in range(wl.n_shared):
-        for name in ("s_gate", "s_up", "s_down"):
-            enc[(name, s)] = mxfp4_encode(fetch(name, s))
+    if getattr(wl, "precision", "mx") == "mixed":
+        # the mixed scheme: bf16 latent projections and shared experts
+        for name in ("p_down", "p_up"):
+            enc[name + "_bf16"] = bf16_round(fetch(name, 0))
+        if wl.n_shared > 0:
+            for name in ("s_gate", "s_up", "s_down"):
+                enc[name + "_bf16"] = np.stack([bf16_round(fetch(name, s)) for s in range(wl.n_shared)])
+    else:
+        for name in ("p_down", "p_up"):
+            enc[name] = mxfp4_encode(fetch(name, 0))
+        for s in range(wl.n_shared):
+            for name in ("s_gate", "s_up", "s_down"):
+                enc[(name, s)] = mxfp4_encode(fetch(name, s))
     for e in (range(wl.n_experts) if experts is None else experts):
         for name in ("w_gate", "w_up", "w_down"):
             enc[(name, e)] = mxfp4_encode(fetch(name, e))

@@ -49,6 +49,15 @@
  *    Logits are summed in fp64.
  *  - Slot order within a token: descending key, tie -> lower expert id.
  *  - Combine accumulates the k slots of a token in slot order.
+ *  - Mixed precision (the scheme of "Precision and deployment", Fig. 6: only
+ *    the routed experts' weights are MXFP4 and their inputs MXFP8; the latent
+ *    projections, the shared experts and the router stay at higher
+ *    precision): "higher precision" is read as BF16 weights and BF16 inputs
+ *    for the latent projections and the shared experts (the hidden state x is
+ *    already bf16), fp32 for the router.  Values are rounded from fp32 to
+ *    bf16 to nearest, ties to even; the latent z stays fp32 for the router
+ *    and is MXFP8-quantised for the routed experts; the shared activation and
+ *    the combine output are rounded to bf16 before the up-projection.
  *
  * Byte layouts (this file's own): an MX matrix [rows][K] is `codes`
  * [rows][K/2] (element 2i in the low nibble of byte i) for MXFP4 or
@@ -103,6 +112,50 @@ static int floor_log2(double a)
 }
 
 static int clamp_e8m0(int e) { return e < -127 ? -127 : (e > 127 ? 127 : e); }
+
+/* ------------------------------------------------------------------ */
+/* BF16: 1 sign, 8 exponent, 7 mantissa bits -- the upper half of an    */
+/* fp32.                                                                */
+
+double orc_bf16_decode(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+/* fp32 -> nearest bf16, ties to even; NaN stays a quiet NaN, infinities
+ * and overflow to infinity follow from the rounding. */
+uint16_t orc_bf16_round(float v)
+{
+    uint32_t u;
+    memcpy(&u, &v, 4);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu))
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t keep = u >> 16, rest = u & 0xFFFFu;
+    if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u)))
+        keep += 1u;                         /* carries into the exponent as it should */
+    return (uint16_t)keep;
+}
+
+void orc_bf16_round_array(const float *v, int64_t n, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_bf16_round(v[i]);
+}
+
+/* y[m] = fp32(sum_k a[k] * bf16(W[m][k])) for W bf16 [M][K]. */
+static void bf16_gemv_f32(const double *a, const uint16_t *W, int64_t M, int64_t K, float *y)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m) {
+        double acc = 0.0;
+        for (int64_t k = 0; k < K; ++k)
+            acc += a[k] * orc_bf16_decode(W[m * K + k]);
+        y[m] = (float)acc;
+    }
+}
 
 /* ------------------------------------------------------------------ */
 /* MXFP4 encoder: the block algorithm of "Four bits from the start".   */
@@ -356,6 +409,7 @@ typedef struct {
     int32_t D, L, E, k, I, S, Is;
     int32_t softmax;        /* 1: softmax over winners (toy); 0: sigmoid + bias */
     int32_t route_hidden;   /* 1: the router reads the hidden state x ([E][D] weights); 0: the latent z */
+    int32_t mixed;          /* 1: BF16 latent projections and shared experts (mixed scheme); 0: all MXFP4 */
 } orc_cfg;
 
 typedef struct {
@@ -369,6 +423,13 @@ typedef struct {
     const orc_mx *s_down;   /* S x [D][Is] */
     const float *router;    /* [E][L] fp32 (latent routing) or [E][D] (hidden routing) */
     const float *bias;      /* [E] fp32 or NULL */
+    /* mixed scheme only: BF16 weights of the latent projections and the
+     * shared experts (the MXFP4 ones above are then unused) */
+    const uint16_t *p_down_bf;   /* [L][D] */
+    const uint16_t *p_up_bf;     /* [D][L] */
+    const uint16_t *s_gate_bf;   /* [S][Is][D] */
+    const uint16_t *s_up_bf;     /* [S][Is][D] */
+    const uint16_t *s_down_bf;   /* [S][D][Is] */
 } orc_weights;
 
 /* Optional outputs, one row per processed token (NULL = not wanted). */
@@ -424,14 +485,23 @@ int orc_moe_forward(const orc_cfg *cfg, const orc_weights *W, const uint16_t *x_
             uint32_t bits = (uint32_t)x_bf16[t * D + d] << 16;
             memcpy(&xf[d], &bits, 4);
         }
-        /* A1: activations enter the GEMMs as MXFP8 */
-        orc_mxfp8_quantize(xf, 1, D, q, qs);
-        if (out->xq) memcpy(out->xq + t * D, q, D);
-        if (out->xs) memcpy(out->xs + t * (D / 32), qs, D / 32);
-        dq_mxfp8(q, qs, D, a);
+        if (cfg->mixed) {
+            /* mixed scheme: the projections and shared experts read x in bf16 */
+            for (int64_t d = 0; d < D; ++d)
+                a[d] = (double)xf[d];
+        } else {
+            /* A1: activations enter the GEMMs as MXFP8 */
+            orc_mxfp8_quantize(xf, 1, D, q, qs);
+            if (out->xq) memcpy(out->xq + t * D, q, D);
+            if (out->xs) memcpy(out->xs + t * (D / 32), qs, D / 32);
+            dq_mxfp8(q, qs, D, a);
+        }
 
         /* latent down-projection z = x P_down^T */
-        mx4_gemv_f32(a, &W->p_down, L, D, z);
+        if (cfg->mixed)
+            bf16_gemv_f32(a, W->p_down_bf, L, D, z);
+        else
+            mx4_gemv_f32(a, &W->p_down, L, D, z);
         orc_mxfp8_quantize(z, 1, L, zq, zs);
         if (out->z) memcpy(out->z + t * L, z, sizeof(float) * L);
         if (out->zq) memcpy(out->zq + t * L, zq, L);
@@ -439,15 +509,22 @@ int orc_moe_forward(const orc_cfg *cfg, const orc_weights *W, const uint16_t *x_
 
         /* shared experts at full width: h_s = SiLU(x S_gate^T) * (x S_up^T) */
         for (int64_t s = 0; s < S; ++s) {
-            mx4_gemv_f32(a, &W->s_gate[s], Is, D, g);
-            mx4_gemv_f32(a, &W->s_up[s], Is, D, u);
+            if (cfg->mixed) {
+                bf16_gemv_f32(a, W->s_gate_bf + s * Is * D, Is, D, g);
+                bf16_gemv_f32(a, W->s_up_bf + s * Is * D, Is, D, u);
+            } else {
+                mx4_gemv_f32(a, &W->s_gate[s], Is, D, g);
+                mx4_gemv_f32(a, &W->s_up[s], Is, D, u);
+            }
             for (int64_t i = 0; i < Is; ++i)
                 hsh[s * Is + i] = (float)(silu((double)g[i]) * (double)u[i]);
         }
-        orc_mxfp8_quantize(hsh, 1, SIs, hsq, hss);
         if (out->hs) memcpy(out->hs + t * SIs, hsh, sizeof(float) * SIs);
-        if (out->hsq) memcpy(out->hsq + t * SIs, hsq, SIs);
-        if (out->hss) memcpy(out->hss + t * (SIs / 32), hss, SIs / 32);
+        if (!cfg->mixed) {
+            orc_mxfp8_quantize(hsh, 1, SIs, hsq, hss);
+            if (out->hsq) memcpy(out->hsq + t * SIs, hsq, SIs);
+            if (out->hss) memcpy(out->hss + t * (SIs / 32), hss, SIs / 32);
+        }
 
         /* router logits, fp64 sum of fp32 products: on the latent z by
          * default, on the hidden state x (exactly its bf16 value) when the
@@ -517,21 +594,38 @@ int orc_moe_forward(const orc_cfg *cfg, const orc_weights *W, const uint16_t *x_
                 acc += gate[j] * (double)o[j * L + l];
             c[l] = (float)acc;
         }
-        orc_mxfp8_quantize(c, 1, L, q, qs);
         if (out->c) memcpy(out->c + t * L, c, sizeof(float) * L);
-        if (out->cq) memcpy(out->cq + t * L, q, L);
-        if (out->cs) memcpy(out->cs + t * (L / 32), qs, L / 32);
+        double *ca = malloc(sizeof(double) * L), *ha = malloc(sizeof(double) * (SIs > 0 ? SIs : 1));
+        if (cfg->mixed) {
+            /* the up-projection's inputs are rounded to bf16 */
+            for (int64_t l = 0; l < L; ++l)
+                ca[l] = orc_bf16_decode(orc_bf16_round(c[l]));
+            for (int64_t i = 0; i < SIs; ++i)
+                ha[i] = orc_bf16_decode(orc_bf16_round(hsh[i]));
+        } else {
+            orc_mxfp8_quantize(c, 1, L, q, qs);
+            if (out->cq) memcpy(out->cq + t * L, q, L);
+            if (out->cs) memcpy(out->cs + t * (L / 32), qs, L / 32);
+            dq_mxfp8(q, qs, L, ca);
+            dq_mxfp8(hsq, hss, SIs, ha);
+        }
 
         /* y = c P_up^T + h_s S_down^T: routed branch up-projected, shared
          * branch summed, one fp64 sum per output */
-        double *ca = malloc(sizeof(double) * L), *ha = malloc(sizeof(double) * SIs);
-        dq_mxfp8(q, qs, L, ca);
-        dq_mxfp8(hsq, hss, SIs, ha);
 #pragma omp parallel for schedule(static)
         for (int64_t d = 0; d < D; ++d) {
-            double acc = mx4_row_dot(ca, &W->p_up, d, L);
-            for (int64_t s = 0; s < S; ++s)
-                acc += mx4_row_dot(ha + s * Is, &W->s_down[s], d, Is);
+            double acc = 0.0;
+            if (cfg->mixed) {
+                for (int64_t l = 0; l < L; ++l)
+                    acc += ca[l] * orc_bf16_decode(W->p_up_bf[d * L + l]);
+                for (int64_t s = 0; s < S; ++s)
+                    for (int64_t i = 0; i < Is; ++i)
+                        acc += ha[s * Is + i] * orc_bf16_decode(W->s_down_bf[(s * D + d) * Is + i]);
+            } else {
+                acc = mx4_row_dot(ca, &W->p_up, d, L);
+                for (int64_t s = 0; s < S; ++s)
+                    acc += mx4_row_dot(ha + s * Is, &W->s_down[s], d, Is);
+            }
             y[d] = (float)acc;
         }
         free(ca);

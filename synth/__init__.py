@@ -59,6 +59,7 @@ class Workload:
     seed: int = 0
     route: str = "latent"   # router input: "latent" (z, [E][L] router) or "hidden" (x, [E][D] router)
     out: str = "f32"        # output dtype of y: "f32" or "bf16"
+    precision: str = "mx"   # "mx": every weight MXFP4; "mixed": bf16 latent projections and shared experts
 
     def with_tokens(self, t: int) -> "Workload":
         return replace(self, tokens=int(t), name=f"{self.name.split('@')[0]}@T{t}")
@@ -84,7 +85,9 @@ SWEEP_TOKENS = (1, 8, 64, 512, 4096, 32768)
 
 def workload(name: str) -> Workload:
     """A named workload; "name@T<n>" overrides the token count, "name+hidden"
-    routes on the hidden state, "name+bf16" writes a bf16 output."""
+    routes on the hidden state, "name+bf16" writes a bf16 output, "name+mixed"
+    keeps the latent projections and shared experts in bf16 (only the routed
+    experts MXFP4)."""
     base, *opts = name.split("+")
     if "@T" in base:
         b, t = base.split("@T")
@@ -96,6 +99,8 @@ def workload(name: str) -> Workload:
             w = replace(w, route="hidden")
         elif o == "bf16":
             w = replace(w, out="bf16")
+        elif o == "mixed":
+            w = replace(w, precision="mixed")
         else:
             raise KeyError(name)
     if opts:
