@@ -83,15 +83,20 @@ def workload_config(wl, T):
     """The `config` keys both arms report for a workload of T tokens."""
     return {"workload": wl.name, "tokens": T, "d_model": wl.d_model, "d_latent": wl.d_latent,
             "experts": wl.n_experts, "top_k": wl.top_k, "expert_inter": wl.expert_inter,
-            "shared": wl.n_shared, "shared_inter": wl.shared_inter, "bias": wl.bias}
+            "shared": wl.n_shared, "shared_inter": wl.shared_inter, "bias": wl.bias,
+            "precision": getattr(wl, "precision", "mx")}
 
 
-def launches_per_forward(T):
-    """Kernels of this library one forward of T tokens launches: quantiser, A2,
-    router (or its tensor-core estimate), top-k, per-expert scan (batches over
-    128 tokens; folded into the work-list kernel below that), work lists,
-    dispatch, A7, A8, combine, A10."""
-    return 10 + (1 if (T + 31) // 32 > 4 else 0)
+def launches_per_forward(T, wl=None):
+    """Kernels of this library one forward of T tokens launches: quantiser
+    (not in the mixed scheme with latent routing), A2, router (or its
+    tensor-core estimate), top-k, per-expert scan (batches over 128 tokens;
+    folded into the work-list kernel below that), work lists, dispatch, A7,
+    A8, combine, A10."""
+    n = 10 + (1 if (T + 31) // 32 > 4 else 0)
+    if wl is not None and getattr(wl, "precision", "mx") == "mixed" and wl.route == "latent":
+        n -= 1
+    return n
 
 
 def algorithmic_work(wl, T, counts):
@@ -103,22 +108,27 @@ def algorithmic_work(wl, T, counts):
     TK = T * k
     rows_a2 = L + 2 * S * Is
     kcat = L + S * Is
+    # the mixed scheme keeps the projections and shared experts in bf16, and
+    # their inputs (x, h_s, c) too
+    mixed = getattr(wl, "precision", "mx") == "mixed"
+    wb = 2.0 if mixed else MX4_BYTES_PER_ELT          # bytes per weight element of A2 / A10
+    ab = 2.0 if mixed else MX8_BYTES_PER_ELT          # bytes per input element of A2 / A10
     w = {
-        "gemm_down_shared": (rows_a2 * D * MX4_BYTES_PER_ELT + T * D * MX8_BYTES_PER_ELT
-                             + T * L * (4 + MX8_BYTES_PER_ELT) + T * S * Is * MX8_BYTES_PER_ELT,
+        "gemm_down_shared": (rows_a2 * D * wb + T * D * ab
+                             + T * L * (4 + MX8_BYTES_PER_ELT) + T * S * Is * ab,
                              2.0 * T * rows_a2 * D),
         "router": (E * L * 4 + T * L * 4 + T * E * 4, 2.0 * T * E * L),
         "gemm_gate_up": (touched * 2 * I * L * MX4_BYTES_PER_ELT + TK * L * MX8_BYTES_PER_ELT
                          + TK * I * MX8_BYTES_PER_ELT, 2.0 * TK * 2 * I * L),
         "gemm_down": (touched * L * I * MX4_BYTES_PER_ELT + TK * I * MX8_BYTES_PER_ELT + TK * L * 4,
                       2.0 * TK * L * I),
-        "combine": (TK * L * 4 + T * L * MX8_BYTES_PER_ELT, 2.0 * TK * L),
-        "gemm_up_shared": (D * kcat * MX4_BYTES_PER_ELT + T * kcat * MX8_BYTES_PER_ELT + T * D * 4,
+        "combine": (TK * L * 4 + T * L * ab, 2.0 * TK * L),
+        "gemm_up_shared": (D * kcat * wb + T * kcat * ab + T * D * 4,
                            2.0 * T * D * kcat),
-        "quant_x": (T * D * (2 + MX8_BYTES_PER_ELT), 0.0),
+        "quant_x": (0.0 if mixed and wl.route == "latent" else T * D * (2 + MX8_BYTES_PER_ELT), 0.0),
         "dispatch": (TK * L * MX8_BYTES_PER_ELT * 2, 0.0),
     }
-    expert_weight_bytes = touched * 3 * I * L * MX4_BYTES_PER_ELT + 3 * S * Is * D * MX4_BYTES_PER_ELT
+    expert_weight_bytes = touched * 3 * I * L * MX4_BYTES_PER_ELT + 3 * S * Is * D * wb
     return w, touched, expert_weight_bytes
 
 
@@ -517,7 +527,9 @@ def run_cuda(args, wl, world, rank, local):
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "step_ms": {"median": float(np.median(step_ms)), "p10": float(np.percentile(step_ms, 10)),
                     "p90": float(np.percentile(step_ms, 90))},
-        "dtype": "mxfp4 weights x mxfp8 activations, fp32 accumulate", "data": "synthetic",
+        "dtype": ("mxfp4 x mxfp8 routed experts, bf16 projections and shared experts, fp32 accumulate"
+                  if getattr(wl, "precision", "mx") == "mixed" else "mxfp4 weights x mxfp8 activations, fp32 accumulate"),
+        "data": "synthetic",
         "config": dict(workload_config(wl, T),
                        l2="flushed by a 512 MB write between timed steps (outside the step events)",
                        parallelism=f"replicas x{world}"),
@@ -528,7 +540,7 @@ def run_cuda(args, wl, world, rank, local):
                                               "a W4A8 product cannot use it"),
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": int(T * wl.d_model * 2),
                 "d2h_bytes_per_step": int(T * wl.d_model * 4)},
-        "gpu_launches": launches_per_forward(T) * K,
+        "gpu_launches": launches_per_forward(T, wl) * K,
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }
@@ -545,9 +557,9 @@ def run_cuda(args, wl, world, rank, local):
                              "value": job_throughput(world, Tp, Kp, p_total), "unit": "tokens/s",
                              "step_ms": {"median": float(np.median(p_ms)), "p10": float(np.percentile(p_ms, 10)),
                                          "p90": float(np.percentile(p_ms, 90))},
-                             "roofline": p_roof, "layer": p_layer, "gpu_launches": launches_per_forward(Tp) * Kp,
+                             "roofline": p_roof, "layer": p_layer, "gpu_launches": launches_per_forward(Tp, pre) * Kp,
                              "clocks": p_clocks, "wall_s_timed_region": p_wall}
-        result["gpu_launches"] += launches_per_forward(Tp) * Kp
+        result["gpu_launches"] += launches_per_forward(Tp, pre) * Kp
         del xp, yp
     if rank == 0 and not args.no_cpu_baseline:
         n_tok = min(args.cpu_tokens, T)

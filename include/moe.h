@@ -26,6 +26,12 @@
  * it takes to serve it".  With score_fn = MOE_SCORE_SOFTMAX the gates are the
  * softmax of the winners' logits instead (that page's toy router).
  *
+ * With precision = MOE_PRECISION_MIXED the layer follows the scheme of
+ * "Precision and deployment", Fig. 6 instead: only the routed experts'
+ * weights are MXFP4 and their inputs MXFP8, while the latent projections and
+ * the shared experts keep BF16 weights and read BF16 inputs (x as given,
+ * h_s and c rounded to bf16, nearest even); z stays fp32 for the router.
+ *
  * Byte layouts.  An MXFP4 matrix W[rows][K] is `codes` uint8 [rows][K/2]
  * (element 2i in the low nibble of byte i, bit 3 of a nibble = sign) plus
  * `scales` uint8 [rows][K/32] (E8M0, value 2^(code-127)); rows are output
@@ -79,6 +85,12 @@ typedef enum {
     MOE_ROUTE_ON_HIDDEN = 1     /* logits = x R^T (x exactly as given), R [E][D] */
 } moe_route_input;
 
+/* Number formats of the non-routed GEMMs. */
+typedef enum {
+    MOE_PRECISION_MX = 0,       /* every weight MXFP4, every GEMM input MXFP8 */
+    MOE_PRECISION_MIXED = 1     /* bf16 latent projections and shared experts; MXFP4/MXFP8 routed experts */
+} moe_precision;
+
 /* Element type of the output y. */
 typedef enum {
     MOE_OUT_F32 = 0,            /* fp32 [T][D] */
@@ -101,6 +113,7 @@ typedef struct {
     int32_t score_fn;      /* moe_score_fn */
     int32_t route_input;   /* moe_route_input */
     int32_t out_dtype;     /* moe_out_dtype */
+    int32_t precision;     /* moe_precision */
 } moe_config;
 
 typedef struct {
@@ -122,6 +135,13 @@ typedef struct {
     moe_mx4 s_down;           /* [S][D][Is]   shared down            */
     const float *router_w;    /* [E][L] fp32 router (latent routing), [E][D] (hidden routing) */
     const float *router_bias; /* [E] fp32 selection bias, or NULL (= 0) */
+    /* MOE_PRECISION_MIXED only (the MXFP4 p_down, p_up and s_* above are then
+     * not read): bf16 bit patterns */
+    const uint16_t *p_down_bf16;  /* [L][D]     */
+    const uint16_t *p_up_bf16;    /* [D][L]     */
+    const uint16_t *s_gate_bf16;  /* [S][Is][D] */
+    const uint16_t *s_up_bf16;    /* [S][Is][D] */
+    const uint16_t *s_down_bf16;  /* [S][D][Is] */
 } moe_weights;
 
 /* Optional intermediate outputs of one forward call (device pointers; NULL
@@ -129,6 +149,7 @@ typedef struct {
  * stable sort of the flat (token, slot) pairs by expert: row p of a sorted
  * tensor belongs to token sorted_token[p]. */
 typedef struct {
+    /* xq/xs, hsq/hss and cq/cs exist in MOE_PRECISION_MX only */
     uint8_t *xq, *xs;         /* [T][D], [T][D/32]           MXFP8 of x            */
     float *z;                 /* [T][L]                      latent, fp32          */
     uint8_t *zq, *zs;         /* [T][L], [T][L/32]           MXFP8 of z            */

@@ -28,6 +28,7 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_OOM, MOE_ERR_CUDA, MOE
 SCORE_SIGMOID_BIAS, SCORE_SOFTMAX = 0, 1
 ROUTE_ON_LATENT, ROUTE_ON_HIDDEN = 0, 1
 OUT_F32, OUT_BF16 = 0, 1
+PRECISION_MX, PRECISION_MIXED = 0, 1
 
 # Entry points declared in include/moe.h.
 ENTRY_POINTS = ("moe_plan", "moe_forward", "moe_forward_host", "moe_get_device_status", "moe_workspace_bytes",
@@ -44,7 +45,7 @@ class MoeError(RuntimeError):
 class _Config(C.Structure):
     _fields_ = [(n, C.c_int32) for n in ("d_model", "d_latent", "n_experts", "top_k", "expert_inter",
                                           "n_shared", "shared_inter", "max_tokens", "score_fn", "route_input",
-                                          "out_dtype")]
+                                          "out_dtype", "precision")]
 
 
 class _MX4(C.Structure):
@@ -53,7 +54,8 @@ class _MX4(C.Structure):
 
 class _Weights(C.Structure):
     _fields_ = [(n, _MX4) for n in ("p_down", "p_up", "w_gate", "w_up", "w_down", "s_gate", "s_up", "s_down")] + \
-               [("router_w", C.c_void_p), ("router_bias", C.c_void_p)]
+               [("router_w", C.c_void_p), ("router_bias", C.c_void_p)] + \
+               [(n + "_bf16", C.c_void_p) for n in ("p_down", "p_up", "s_gate", "s_up", "s_down")]
 
 
 DEBUG_FIELDS = ("xq", "xs", "z", "zq", "zs", "hsq", "hss", "logits", "topk_idx", "topk_w", "counts", "offsets",
@@ -138,11 +140,13 @@ def config_struct(cfg) -> _Config:
     score = g("score")
     route = g("route") if _has(cfg, "route") else "latent"
     out = g("out") if _has(cfg, "out") else "f32"
+    precision = g("precision") if _has(cfg, "precision") else "mx"
     return _Config(g("d_model"), g("d_latent"), g("n_experts"), g("top_k"), g("expert_inter"), g("n_shared"),
                    g("shared_inter"), int(g("max_tokens")) if _has(cfg, "max_tokens") else g("tokens"),
                    SCORE_SOFTMAX if score == "softmax" else SCORE_SIGMOID_BIAS,
                    ROUTE_ON_HIDDEN if route == "hidden" else ROUTE_ON_LATENT,
-                   OUT_BF16 if out == "bf16" else OUT_F32)
+                   OUT_BF16 if out == "bf16" else OUT_F32,
+                   PRECISION_MIXED if precision == "mixed" else PRECISION_MX)
 
 
 def _has(cfg, k):
@@ -191,8 +195,10 @@ class Plan:
     weights: dict with MXFP4 pairs ``(codes, scales)`` for 'p_down' [L][D],
     'p_up' [D][L], 'w_gate'/'w_up' [E][I][L], 'w_down' [E][L][I],
     's_gate'/'s_up' [S][Is][D], 's_down' [S][D][Is]; 'router' fp32 [E][L];
-    optional 'bias' fp32 [E].  All CUDA tensors on one device; the plan copies
-    them, so they may be freed afterwards.
+    optional 'bias' fp32 [E].  With the mixed precision scheme, bf16 tensors
+    'p_down_bf16', 'p_up_bf16', 's_gate_bf16', 's_up_bf16', 's_down_bf16'
+    replace the MXFP4 projections and shared experts.  All CUDA tensors on
+    one device; the plan copies them, so they may be freed afterwards.
     """
 
     def __init__(self, cfg, weights: dict, max_tokens: Optional[int] = None):
@@ -210,8 +216,9 @@ class Plan:
             return _MX4(_ptr(pair[0]), _ptr(pair[1]))
 
         bias = weights.get("bias")
+        bf = [_ptr(weights.get(n + "_bf16")) for n in ("p_down", "p_up", "s_gate", "s_up", "s_down")]
         w = _Weights(mx("p_down"), mx("p_up"), mx("w_gate"), mx("w_up"), mx("w_down"), mx("s_gate"), mx("s_up"),
-                     mx("s_down"), _ptr(weights["router"]), _ptr(bias))
+                     mx("s_down"), _ptr(weights["router"]), _ptr(bias), *bf)
         h = C.c_void_p()
         with torch.cuda.device(dev):
             torch.cuda.synchronize()

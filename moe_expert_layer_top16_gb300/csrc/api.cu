@@ -98,6 +98,19 @@ bool map_f32_view(CUtensorMap* m, const void* base, int64_t rows, int64_t K, int
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 matrix [rows][K] (rows of K elements), 64-wide (128-byte) x box_rows boxes.
+bool map_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t K, uint32_t box_rows) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K * 2)};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // MXFP8 activation codes [rows][K], 128-wide x 16-row boxes.
 bool map_mx8(CUtensorMap* m, const void* codes, int64_t rows, int64_t K, int box_rows = 16) {
     EncodeTiledFn f = encode_fn();
@@ -153,6 +166,9 @@ struct Plan {
     float bias_absmax = 0.0f;
     int RK = 0;                       // router input width: L (latent routing) or D (hidden routing)
     bool route_hidden = false, out_bf16 = false;
+    bool mixed = false;               // bf16 latent projections and shared experts (MOE_PRECISION_MIXED)
+    uint16_t *a2b = nullptr, *a10b = nullptr;   // their bf16 operands, laid out as a2c / a10c
+    __nv_bfloat16* act_bf = nullptr;  // [T_pad][Kcat] bf16: c | h_s (mixed precision)
     float* xr = nullptr;              // hidden routing: x as fp32 [T_pad][D]
     // workspace
     uint8_t *xq, *xsf, *zq, *zsf, *act, *actsf, *zqp, *zqpsf, *hq, *hqsf;
@@ -258,6 +274,16 @@ cudaError_t repack(Plan* p, const std::vector<Segment>& segs, int64_t rows, int6
     return err;
 }
 
+// bf16 variant of repack: rows of 2-byte elements, no scales.
+cudaError_t repack_bf16(Plan* p, const std::vector<Segment>& segs, int64_t rows, int64_t Kp, uint16_t** out) {
+    cudaError_t err = palloc(p, out, static_cast<size_t>(rows * Kp * 2));
+    for (const Segment& s : segs) {
+        if (err != cudaSuccess) break;
+        err = copy_rows(reinterpret_cast<uint8_t*>(*out) + s.k_off * 2, Kp * 2, s.code_rows, s.k_len * 2);
+    }
+    return err;
+}
+
 moe_status cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return MOE_OK;
     if (e == cudaErrorMemoryAllocation) return MOE_ERR_OOM;
@@ -347,6 +373,7 @@ moe_status validate(const moe_config* c) {
     if (c->score_fn != MOE_SCORE_SIGMOID_BIAS && c->score_fn != MOE_SCORE_SOFTMAX) return MOE_ERR_INVALID_ARG;
     if (c->route_input != MOE_ROUTE_ON_LATENT && c->route_input != MOE_ROUTE_ON_HIDDEN) return MOE_ERR_INVALID_ARG;
     if (c->out_dtype != MOE_OUT_F32 && c->out_dtype != MOE_OUT_BF16) return MOE_ERR_INVALID_ARG;
+    if (c->precision != MOE_PRECISION_MX && c->precision != MOE_PRECISION_MIXED) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
 }
 
@@ -374,10 +401,12 @@ moe_status moe_plan(const moe_config* cfg, const moe_weights* w, int device, voi
     *plan_out = nullptr;
     moe_status st = validate(cfg);
     if (st != MOE_OK) return st;
-    if (!w || !mx_ok(w->p_down) || !mx_ok(w->p_up) || !mx_ok(w->w_gate) || !mx_ok(w->w_up) || !mx_ok(w->w_down) ||
-        !w->router_w)
+    const bool mixed = cfg->precision == MOE_PRECISION_MIXED;
+    if (!w || !mx_ok(w->w_gate) || !mx_ok(w->w_up) || !mx_ok(w->w_down) || !w->router_w) return MOE_ERR_INVALID_ARG;
+    if (mixed ? (!w->p_down_bf16 || !w->p_up_bf16) : (!mx_ok(w->p_down) || !mx_ok(w->p_up))) return MOE_ERR_INVALID_ARG;
+    if (cfg->n_shared > 0 && (mixed ? (!w->s_gate_bf16 || !w->s_up_bf16 || !w->s_down_bf16)
+                                    : (!mx_ok(w->s_gate) || !mx_ok(w->s_up) || !mx_ok(w->s_down))))
         return MOE_ERR_INVALID_ARG;
-    if (cfg->n_shared > 0 && (!mx_ok(w->s_gate) || !mx_ok(w->s_up) || !mx_ok(w->s_down))) return MOE_ERR_INVALID_ARG;
     int ndev = 0;
     if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return MOE_ERR_UNSUPPORTED;
     cudaDeviceProp prop;
@@ -416,7 +445,27 @@ moe_status moe_plan(const moe_config* cfg, const moe_weights* w, int device, voi
         if (err == cudaSuccess) err = (x); \
     } while (0)
     // ---------------------------------------------------------------- weights
-    {
+    p->mixed = mixed;
+    if (mixed) {
+        // the same row order in bf16: P_down, then per shared expert 128-row
+        // tiles of 64 gate rows and the 64 matching up rows
+        Segment s;
+        s.k_off = 0;
+        s.k_len = D;
+        for (int r = 0; r < p->rowsA2; ++r) {
+            const uint16_t* c;
+            if (r < L) {
+                c = w->p_down_bf16 + static_cast<int64_t>(r) * D;
+            } else {
+                const int rr = r - L, sh = rr / (2 * Is), within = rr % (2 * Is);
+                const int t = within / 128, h = within % 128;
+                const uint16_t* src = (h < 64) ? w->s_gate_bf16 : w->s_up_bf16;
+                c = src + (static_cast<int64_t>(sh) * Is + 64 * t + (h % 64)) * D;
+            }
+            s.code_rows.push_back(reinterpret_cast<const uint8_t*>(c));
+        }
+        TRY(repack_bf16(p, {s}, p->rowsA2, D, &p->a2b));
+    } else {
         // A2: rows [0, L) = P_down; then per shared expert, 128-row tiles of
         // 64 gate rows followed by the 64 matching up rows.
         Segment s;
@@ -469,7 +518,23 @@ moe_status moe_plan(const moe_config* cfg, const moe_weights* w, int device, voi
         }
         TRY(repack(p, {s}, rows, Ip, &p->w2c, &p->w2sf));
     }
-    {
+    if (mixed) {
+        // A10 in bf16: [D][Kcat] = [P_up | S_down[0] | S_down[1] | ...] along K
+        std::vector<Segment> segs(1 + S);
+        segs[0].k_off = 0;
+        segs[0].k_len = L;
+        for (int d = 0; d < D; ++d)
+            segs[0].code_rows.push_back(reinterpret_cast<const uint8_t*>(w->p_up_bf16 + static_cast<int64_t>(d) * L));
+        for (int sh = 0; sh < S; ++sh) {
+            Segment& g = segs[1 + sh];
+            g.k_off = L + static_cast<int64_t>(sh) * Is;
+            g.k_len = Is;
+            for (int d = 0; d < D; ++d)
+                g.code_rows.push_back(
+                    reinterpret_cast<const uint8_t*>(w->s_down_bf16 + (static_cast<int64_t>(sh) * D + d) * Is));
+        }
+        TRY(repack_bf16(p, segs, D, p->Kcat, &p->a10b));
+    } else {
         // A10: [D][Kcat] = [P_up | S_down[0] | S_down[1] | ...] along K.
         std::vector<Segment> segs(1 + S);
         segs[0].k_off = 0;
@@ -520,6 +585,7 @@ moe_status moe_plan(const moe_config* cfg, const moe_weights* w, int device, voi
     TRY(palloc(p, &p->zsf, (L / 128) * Tp * 4));
     TRY(palloc(p, &p->act, Tp * p->Kcat));
     TRY(palloc(p, &p->actsf, (p->Kcat / 128) * (Tp + 32) * 16));
+    if (mixed) TRY(palloc(p, &p->act_bf, Tp * p->Kcat * 2));
     TRY(palloc(p, &p->logits, sizeof(float) * p->T_max * E));
     TRY(palloc(p, &p->idx, sizeof(int32_t) * p->T_max * p->k));
     TRY(palloc(p, &p->gw, sizeof(float) * p->T_max * p->k));
@@ -548,10 +614,12 @@ moe_status moe_plan(const moe_config* cfg, const moe_weights* w, int device, voi
         return st;
     }
     // ---------------------------------------------------------------- TMA descriptors
-    bool ok = map_mx4(&p->tA2, p->a2c, p->rowsA2, D) && map_mx8(&p->tB2, p->xq, Tp, D) &&
+    bool ok = (mixed ? map_bf16(&p->tA2, p->a2b, p->rowsA2, D, 128)
+                     : (map_mx4(&p->tA2, p->a2c, p->rowsA2, D) && map_mx8(&p->tB2, p->xq, Tp, D))) &&
               map_mx4(&p->tA7, p->w13c, static_cast<int64_t>(E) * 2 * I, L) && map_mx8(&p->tB7, p->zqp, Rp, L) &&
               map_mx4(&p->tA8, p->w2c, static_cast<int64_t>(E) * L, Ip) && map_mx8(&p->tB8, p->hq, Rp, Ip) &&
-              map_mx4(&p->tA10, p->a10c, D, p->Kcat) && map_mx8(&p->tB10, p->act, Tp, p->Kcat) &&
+              (mixed ? (map_bf16(&p->tA10, p->a10b, D, p->Kcat, 128) && map_bf16(&p->tB10, p->act_bf, Tp, p->Kcat, 16))
+                     : (map_mx4(&p->tA10, p->a10c, D, p->Kcat) && map_mx8(&p->tB10, p->act, Tp, p->Kcat))) &&
               map_f32(&p->tAR, p->router2, E, 2 * p->RK, 128) &&
               (p->route_hidden ? map_f32(&p->tBR, p->xr, Tp, D, 16) : map_f32(&p->tBR, p->z, Tp, 2 * L, 16));
     p->tc_router = (E % 128 == 0) && (p->RK % 32 == 0);
@@ -595,10 +663,15 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
     const bool wide_d = nmax_dense > kNarrowMax, wide_g = nmax_grp > kNarrowMax;
     if (wide_d && p->wide_dense != nmax_dense) {
         p->wide_dense = 0;
-        if (!map_mx8(&p->tB2w, p->xq, Tp, D, nmax_dense) || !map_mx8(&p->tB10w, p->act, Tp, p->Kcat, nmax_dense))
-            return MOE_ERR_CUDA;
+        const bool ok = p->mixed ? map_bf16(&p->tB10w, p->act_bf, Tp, p->Kcat, nmax_dense)
+                                 : (map_mx8(&p->tB2w, p->xq, Tp, D, nmax_dense) &&
+                                    map_mx8(&p->tB10w, p->act, Tp, p->Kcat, nmax_dense));
+        if (!ok) return MOE_ERR_CUDA;
         p->wide_dense = nmax_dense;
     }
+    // mixed precision: the down-projection and shared gate/up read x itself (bf16)
+    CUtensorMap tx;
+    if (p->mixed && !map_bf16(&tx, x, T, D, wide_d ? nmax_dense : 16)) return MOE_ERR_CUDA;
     if (wide_g && p->wide_grp != nmax_grp) {
         p->wide_grp = 0;
         if (!map_mx8(&p->tB7w, p->zqp, Rp, L, nmax_grp) || !map_mx8(&p->tB8w, p->hq, Rp, Ip, nmax_grp))
@@ -629,8 +702,10 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
     };
     TRY(cudaMemsetAsync(p->sel, 0, sizeof(uint32_t) * E * W, s));
     mark(0);
-    // 1. x -> MXFP8
-    TRY(launch_quant_x(static_cast<const __nv_bfloat16*>(x), T, D, p->xq, p->xsf, Tps, nmax_dense, p->xr, s));
+    // 1. x -> MXFP8 (and x as fp32 for hidden routing); mixed precision reads
+    // x as it is, so only hidden routing needs this step
+    if (!p->mixed || p->route_hidden)
+        TRY(launch_quant_x(static_cast<const __nv_bfloat16*>(x), T, D, p->xq, p->xsf, Tps, nmax_dense, p->xr, s));
     mark(1);
     // 2. latent down-projection + shared gate/up
     {
@@ -640,6 +715,14 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
             g.tmB = p->tB2w;
             g.b_box = nmax_dense;
         }
+        if (p->mixed) {
+            g.tmB = tx;
+            g.kind = KIND_BF16;
+            g.KT = D / 64;
+            g.kseg_tiles = g.KT;
+            g.sfa = nullptr;
+            g.sfb = nullptr;
+        }
         g.dense = 1;
         g.m_tiles = p->rowsA2 / kBlockM;
         g.n_tokens = T;
@@ -647,7 +730,9 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         // z rows hold L values; the TF32 router estimate also wants them split
         // into a TF32 head and its remainder (at column L), else they are plain
         g.epi[0] = EpiParams{EPI_QUANT, 0, 0, z_split ? L : 0, p->z, 2 * L, p->zq, L, p->zsf, Tp};
-        g.epi[1] = EpiParams{EPI_SILU_QUANT, L / kBlockM, L, 0, nullptr, 0, p->act, p->Kcat, p->actsf, Tps, 1};
+        g.epi[1] = p->mixed ? EpiParams{EPI_SILU_BF16, L / kBlockM, L, 0, nullptr, 0,
+                                        reinterpret_cast<uint8_t*>(p->act_bf), p->Kcat, nullptr, 0, 0}
+                            : EpiParams{EPI_SILU_QUANT, L / kBlockM, L, 0, nullptr, 0, p->act, p->Kcat, p->actsf, Tps, 1};
         const int items = g.m_tiles * ((T + g.n_max - 1) / g.n_max);
         shape_gemm(g, 0, items, std::min(items, p->num_sms));
         TRY(launch_gemm(g, std::min(items, p->num_sms), s));
@@ -802,7 +887,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
     }
     // 10. weighted combine -> MXFP8 into columns [0, L) of the concatenated activation
     mark(9);
-    TRY(launch_combine(p->o, p->slot_pos, p->gw, T, k, L, p->act, p->Kcat, p->actsf, Tps, nmax_dense, s));
+    TRY(launch_combine(p->o, p->slot_pos, p->gw, T, k, L, p->act, p->Kcat, p->actsf, Tps, nmax_dense, p->act_bf, s));
     // 11. y = [cq | h_sq] [P_up | S_down]^T
     mark(10);
     {
@@ -811,6 +896,13 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         if (wide_d) {
             g.tmB = p->tB10w;
             g.b_box = nmax_dense;
+        }
+        if (p->mixed) {
+            g.kind = KIND_BF16;
+            g.KT = p->Kcat / 64;
+            g.kseg_tiles = g.KT;
+            g.sfa = nullptr;
+            g.sfb = nullptr;
         }
         g.dense = 1;
         g.m_tiles = D / kBlockM;

@@ -226,10 +226,11 @@ enum EpiSet : int {
 template <int KIND, int SET>
 __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __grid_constant__ GemmParams p) {
     constexpr bool kMX = (KIND == KIND_MX);
+    constexpr bool kBF16 = (KIND == KIND_BF16);
     constexpr bool kSilu = (SET == SET_SILU || SET == SET_DUAL);
     constexpr bool kQuant = (SET == SET_QUANT || SET == SET_DUAL);
     constexpr bool kOnlySilu = (SET == SET_SILU);
-    constexpr int kTileElems = kMX ? kBlockK : 32;      // K elements per 128-byte row of a stage
+    constexpr int kTileElems = kMX ? kBlockK : (kBF16 ? 64 : 32);   // K elements per 128-byte row of a stage
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const Hot h = load_hot(p);
@@ -408,7 +409,15 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                     const uint32_t accum_first = (kt == kb) ? 0u : 1u;
                     const uint64_t adesc = sdesc_sw128(smem_u32(sb));
                     const uint64_t bdesc = sdesc_sw128(smem_u32(sb + L.offB));
-                    if constexpr (!kMX) {
+                    if constexpr (kBF16) {
+                        const uint32_t idesc = idesc_bf16(kBlockM, nm);
+                        if (elect_one()) {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                mma_bf16(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, (accum_first | j) != 0 ? 1u : 0u);
+                            tc_commit(&emptyg[stage]);
+                        }
+                    } else if constexpr (!kMX) {
                         const uint32_t idesc = idesc_tf32(kBlockM, nm);
                         if (elect_one()) {
 #pragma unroll
@@ -539,7 +548,7 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                     for (int i = 0; i < 16; ++i) v[i] = first ? u[i] : v[i] + u[i];
                     first = false;
                 }
-                if (kOnlySilu || (kSilu && E.mode == EPI_SILU_QUANT)) {
+                if (kOnlySilu || (kSilu && (E.mode == EPI_SILU_QUANT || E.mode == EPI_SILU_BF16))) {
                     // rows 0..63 of the tile are gate, 64..127 up: warp q < 2 holds
                     // the gate of feature block q, warp q + 2 its up.  The pair
                     // swaps halves of the chunk through shared memory, then warp
@@ -556,6 +565,22 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                     named_bar_sync(bar_xchg, 128);
                     const int64_t col_blk = E.col0 + static_cast<int64_t>(rel_mt) * 64 + 32 * blk;
                     const int nv = min(8, w.n - n0 - t0);
+                    if (E.mode == EPI_SILU_BF16) {
+                        // bf16 activation (mixed precision): one value per lane and token
+                        __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(E.out_q) +
+                                            (w.b_row0 + n0 + t0) * E.ld_q + col_blk + lane;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            if (i >= nv) break;
+                            const float mine = gate_warp ? v[i] : v[8 + i];
+                            const float other = xb[blk * 512 + (t0 + i) * 32 + lane];
+                            const float hv = gate_warp ? silu_f(mine) * other : silu_f(other) * mine;
+                            ob[0] = __float2bfloat16_rn(hv);
+                            ob += E.ld_q;
+                        }
+                        __syncwarp();
+                        continue;
+                    }
                     uint8_t* stg = qstage + (warp - 2 * G) * 512;            // [token][32 codes]
                     uint8_t my_sc = 0;                                       // lane i: scale of token i
 #pragma unroll
@@ -704,7 +729,7 @@ int epi_set(const GemmParams& p) {
     const int m0 = p.epi[0].mode;
     const bool two = p.dense && p.epi_split < p.m_tiles;
     const int m1 = two ? p.epi[1].mode : m0;
-    const bool s0 = m0 == EPI_SILU_QUANT, s1 = m1 == EPI_SILU_QUANT;
+    const bool s0 = m0 == EPI_SILU_QUANT || m0 == EPI_SILU_BF16, s1 = m1 == EPI_SILU_QUANT || m1 == EPI_SILU_BF16;
     if (!s0 && !s1) return (m0 == EPI_QUANT || m1 == EPI_QUANT) ? SET_QUANT : SET_F32;
     if (s0 && s1) return SET_SILU;
     if (s1) return SET_DUAL;
@@ -724,6 +749,8 @@ cudaError_t gemm_setup() {
     if (err == cudaSuccess) err = raise_smem<KIND_MX, SET_SILU>();
     if (err == cudaSuccess) err = raise_smem<KIND_MX, SET_DUAL>();
     if (err == cudaSuccess) err = raise_smem<KIND_TF32, SET_F32>();
+    if (err == cudaSuccess) err = raise_smem<KIND_BF16, SET_F32>();
+    if (err == cudaSuccess) err = raise_smem<KIND_BF16, SET_DUAL>();
     return err;
 }
 
@@ -741,6 +768,13 @@ cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s) {
     if (p.kind == KIND_TF32) {
         if (set != SET_F32) return cudaErrorInvalidValue;
         mx_gemm_kernel<KIND_TF32, SET_F32><<<grid, threads, smem, s>>>(p);
+    } else if (p.kind == KIND_BF16) {
+        if (set == SET_F32)
+            mx_gemm_kernel<KIND_BF16, SET_F32><<<grid, threads, smem, s>>>(p);
+        else if (set == SET_DUAL)
+            mx_gemm_kernel<KIND_BF16, SET_DUAL><<<grid, threads, smem, s>>>(p);
+        else
+            return cudaErrorInvalidValue;
     } else if (set == SET_F32) {
         mx_gemm_kernel<KIND_MX, SET_F32><<<grid, threads, smem, s>>>(p);
     } else if (set == SET_QUANT) {

@@ -26,7 +26,8 @@ constexpr int kSmemLimit = 227 * 1024;
 enum EpiMode : int {
     EPI_F32 = 0,        // store fp32 accumulators
     EPI_QUANT = 1,      // optionally store fp32, and store MXFP8 of the row segment (blocks along M)
-    EPI_SILU_QUANT = 2  // rows 0..63 gate, 64..127 up: store MXFP8 of SiLU(gate) * up
+    EPI_SILU_QUANT = 2, // rows 0..63 gate, 64..127 up: store MXFP8 of SiLU(gate) * up
+    EPI_SILU_BF16 = 3   // rows 0..63 gate, 64..127 up: store SiLU(gate) * up rounded to bf16 (out_q holds bf16)
 };
 
 // Where an epilogue region writes.  Output row = item.b_row0 + token index;
@@ -48,7 +49,8 @@ struct EpiParams {
 
 enum GemmKind : int {
     KIND_MX = 0,        // MXFP4 A x MXFP8 B, block-scaled (kind::mxf8f6f4)
-    KIND_TF32 = 1       // fp32 A x fp32 B as TF32 (kind::tf32), no scales
+    KIND_TF32 = 1,      // fp32 A x fp32 B as TF32 (kind::tf32), no scales
+    KIND_BF16 = 2       // bf16 A x bf16 B (kind::f16), fp32 accumulate, no scales
 };
 
 struct GemmParams {
@@ -184,8 +186,10 @@ struct ScatterArgs {
 };
 cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s);
 // out_sf: item-atom planes of a dense GEMM with token tiles of n_max
+// out_bf (optional): write c rounded to bf16 at out_bf[t * ld_q + col] instead of MXFP8
 cudaError_t launch_combine(const float* o, const int32_t* slot_pos, const float* w, int T, int k, int L,
-                           uint8_t* out_q, int64_t ld_q, uint8_t* out_sf, int64_t sf_pitch, int n_max, cudaStream_t s);
+                           uint8_t* out_q, int64_t ld_q, uint8_t* out_sf, int64_t sf_pitch, int n_max,
+                           __nv_bfloat16* out_bf, cudaStream_t s);
 cudaError_t launch_mxfp4_encode(const float* w, int64_t rows, int64_t K, uint8_t* codes, uint8_t* scales,
                                 cudaStream_t s);
 cudaError_t kernels_setup();   // per-device kernel attributes

@@ -853,7 +853,8 @@ __global__ void scatter_kernel(ScatterArgs a) {
 constexpr int kCombineWarps = 8;
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(
     const float* __restrict__ o, const int32_t* __restrict__ slot_pos, const float* __restrict__ w, int T, int k,
-    int L, uint8_t* __restrict__ out_q, int64_t ld_q, uint8_t* __restrict__ out_sf, int64_t sf_pitch, int n_max) {
+    int L, uint8_t* __restrict__ out_q, int64_t ld_q, uint8_t* __restrict__ out_sf, int64_t sf_pitch, int n_max,
+    __nv_bfloat16* __restrict__ out_bf) {
     const int t = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __shared__ int pos_s[32];
@@ -868,6 +869,10 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(
     const int col = blk * 32 + lane;
     float acc = 0.0f;
     for (int j = 0; j < k; ++j) acc = fmaf(w_s[j], o[static_cast<int64_t>(pos_s[j]) * L + col], acc);
+    if (out_bf) {                     // mixed precision: the up-projection reads c in bf16
+        out_bf[static_cast<int64_t>(t) * ld_q + col] = __float2bfloat16_rn(acc);
+        return;
+    }
     uint8_t sc;
     const uint8_t code = warp_mx8_quant(acc, &sc);
     out_q[static_cast<int64_t>(t) * ld_q + col] = code;
@@ -1129,10 +1134,12 @@ cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_combine(const float* o, const int32_t* slot_pos, const float* w, int T, int k, int L,
-                           uint8_t* out_q, int64_t ld_q, uint8_t* out_sf, int64_t sf_pitch, int n_max, cudaStream_t s) {
+                           uint8_t* out_q, int64_t ld_q, uint8_t* out_sf, int64_t sf_pitch, int n_max,
+                           __nv_bfloat16* out_bf, cudaStream_t s) {
     if (n_max <= 0) return cudaErrorInvalidValue;
     dim3 grid(T, (L / 32 + kCombineWarps - 1) / kCombineWarps);
-    combine_kernel<<<grid, kCombineWarps * 32, 0, s>>>(o, slot_pos, w, T, k, L, out_q, ld_q, out_sf, sf_pitch, n_max);
+    combine_kernel<<<grid, kCombineWarps * 32, 0, s>>>(o, slot_pos, w, T, k, L, out_q, ld_q, out_sf, sf_pitch, n_max,
+                                                       out_bf);
     return cudaGetLastError();
 }
 

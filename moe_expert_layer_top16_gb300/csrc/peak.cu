@@ -21,28 +21,6 @@ namespace {
 constexpr int kProbeThreads = 128;
 constexpr int kProbeSmem = 160 * 1024;    // keeps one CTA per SM (one TMEM allocation each)
 
-// Instruction descriptor for kind::f16: fp32 accumulator, bf16 A and B, both
-// K-major.
-__host__ __device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
-    uint32_t d = 0;
-    d |= 1u << 4;                                           // accumulator format F32
-    d |= 1u << 7;                                           // A: BF16
-    d |= 1u << 10;                                          // B: BF16
-    d |= static_cast<uint32_t>((N >> 3) & 63) << 17;
-    d |= static_cast<uint32_t>((M >> 4) & 31) << 24;
-    return d;
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 template <int KIND>
 __global__ void __launch_bounds__(kProbeThreads, 1) mma_probe_kernel(int iters, int n, int* status) {
     extern __shared__ uint8_t smem_raw[];

@@ -241,6 +241,29 @@ __host__ __device__ __forceinline__ uint32_t idesc_tf32(int M, int N) {
     return d;
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 operands, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor for kind::f16 with bf16 A and B (both K-major) and
+// an fp32 accumulator.
+__host__ __device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
+    uint32_t d = 0;
+    d |= 1u << 4;                                           // accumulator format F32
+    d |= 1u << 7;                                           // A: BF16
+    d |= 1u << 10;                                          // B: BF16
+    d |= static_cast<uint32_t>((N >> 3) & 63) << 17;
+    d |= static_cast<uint32_t>((M >> 4) & 31) << 24;
+    return d;
+}
+
 // fp32 -> nearest TF32 value (10 mantissa bits, ties away from zero), as fp32.
 __device__ __forceinline__ float tf32_round(float v) {
     uint32_t r;

@@ -16,10 +16,21 @@ from . import mxfp4_encode
 
 def encode_layer(cfg, fetch, device) -> dict:
     E, S = cfg.n_experts, cfg.n_shared
+    mixed = getattr(cfg, "precision", "mx") == "mixed"
     out = {}
-    for name in ("p_down", "p_up"):
-        out[name] = mxfp4_encode(fetch(name, 0))
-    for name, count in (("w_gate", E), ("w_up", E), ("w_down", E), ("s_gate", S), ("s_up", S), ("s_down", S)):
+    if mixed:
+        # the mixed scheme keeps the projections and shared experts in bf16
+        # (fp32 rounded to nearest even)
+        for name in ("p_down", "p_up"):
+            out[name + "_bf16"] = fetch(name, 0).to(torch.bfloat16).contiguous()
+        if S > 0:
+            for name in ("s_gate", "s_up", "s_down"):
+                out[name + "_bf16"] = torch.stack([fetch(name, i).to(torch.bfloat16) for i in range(S)]).contiguous()
+    else:
+        for name in ("p_down", "p_up"):
+            out[name] = mxfp4_encode(fetch(name, 0))
+    shared = () if mixed else (("s_gate", S), ("s_up", S), ("s_down", S))
+    for name, count in (("w_gate", E), ("w_up", E), ("w_down", E)) + shared:
         if count == 0:
             continue
         first = fetch(name, 0)

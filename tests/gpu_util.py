@@ -117,11 +117,20 @@ class OracleLayer:
             return synth.weight(wl, name, i, device=DEV).cpu().numpy()
 
         self._fetch = fetch
-        for name in ("p_down", "p_up"):
-            self.enc[name] = oracle.mxfp4_encode(fetch(name, 0))
-        for s in range(wl.n_shared):
-            for name in ("s_gate", "s_up", "s_down"):
-                self.enc[(name, s)] = oracle.mxfp4_encode(fetch(name, s))
+        if getattr(wl, "precision", "mx") == "mixed":
+            # bf16 projections and shared experts, rounded by the oracle's own conversion
+            for name in ("p_down", "p_up"):
+                self.enc[name + "_bf16"] = oracle.bf16_round(fetch(name, 0))
+            if wl.n_shared > 0:
+                for name in ("s_gate", "s_up", "s_down"):
+                    self.enc[name + "_bf16"] = np.stack([oracle.bf16_round(fetch(name, s))
+                                                         for s in range(wl.n_shared)])
+        else:
+            for name in ("p_down", "p_up"):
+                self.enc[name] = oracle.mxfp4_encode(fetch(name, 0))
+            for s in range(wl.n_shared):
+                for name in ("s_gate", "s_up", "s_down"):
+                    self.enc[(name, s)] = oracle.mxfp4_encode(fetch(name, s))
         self.enc["router"] = fetch("router", 0)
         b = synth.router_bias(wl, device="cpu")
         self.enc["bias"] = None if b is None else b.numpy()
@@ -276,7 +285,8 @@ def sampled_y(wl, ol, T, x, g, y, sample):
     sample = np.asarray(sorted(set(int(s) for s in sample if 0 <= s < T)))
     xb = bf16_bits(x[torch.as_tensor(sample, device=DEV)])
     r0 = oracle.moe_forward(wl, ol.ensure([]), xb, route_only=True, want=("idx", "logits", "xq", "xs", "z"))
-    assert (r0["xq"] == g["xq"][sample]).all() and (r0["xs"] == g["xs"][sample]).all()
+    if getattr(wl, "precision", "mx") != "mixed":        # the mixed scheme reads x as it is
+        assert (r0["xq"] == g["xq"][sample]).all() and (r0["xs"] == g["xs"][sample]).all()
     if wl.route == "latent":
         z_gpu, z_ref = g["z"][sample], r0["z"]
     else:

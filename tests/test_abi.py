@@ -48,7 +48,7 @@ def test_status_strings(L):
 
 def _cfg(**kw):
     base = dict(d_model=256, d_latent=128, n_experts=32, top_k=4, expert_inter=64, n_shared=1, shared_inter=128,
-                max_tokens=64, score_fn=1, route_input=0, out_dtype=0)
+                max_tokens=64, score_fn=1, route_input=0, out_dtype=0, precision=0)
     base.update(kw)
     return moe._Config(*[base[f] for f, _ in moe._Config._fields_])
 
@@ -57,7 +57,7 @@ def _cfg(**kw):
                                  dict(top_k=33), dict(top_k=40, n_experts=32), dict(n_experts=0), dict(n_experts=2048),
                                  dict(route_input=2), dict(out_dtype=2), dict(route_input=-1),
                                  dict(max_tokens=0), dict(max_tokens=70000), dict(score_fn=7),
-                                 dict(n_shared=1, shared_inter=0)])
+                                 dict(n_shared=1, shared_inter=0), dict(precision=2), dict(precision=-1)])
 def test_plan_rejects_bad_config_without_a_device(L, bad):
     w = moe._Weights()
     h = C.c_void_p(123)
@@ -69,6 +69,13 @@ def test_plan_rejects_bad_config_without_a_device(L, bad):
 def test_plan_rejects_missing_weights(L):
     h = C.c_void_p()
     assert L.moe_plan(C.byref(_cfg()), C.byref(moe._Weights()), 0, C.byref(h)) == moe.MOE_ERR_INVALID_ARG
+    # the mixed scheme needs the bf16 projections and shared experts, the MXFP4 ones do not stand in
+    p = C.c_void_p(256)
+    w = moe._Weights()
+    for n in ("p_down", "p_up", "w_gate", "w_up", "w_down", "s_gate", "s_up", "s_down"):
+        setattr(w, n, moe._MX4(p, p))
+    w.router_w = p
+    assert L.moe_plan(C.byref(_cfg(precision=1)), C.byref(w), 0, C.byref(h)) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_plan(C.byref(_cfg()), None, 0, C.byref(h)) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_plan(None, None, 0, C.byref(h)) == moe.MOE_ERR_INVALID_ARG
 
