@@ -56,15 +56,16 @@ def test_launches_per_forward():
 
 def test_mixed_scheme_bytes():
     """In the mixed scheme the projections and shared experts move 2 bytes per
-    weight element: the shared experts' 3 x 2 x 2048 x 7168 elements are
-    88,080,384 bytes instead of 46,792,704, and one quantiser launch fewer."""
+    weight element: the shared experts' 3 x 2 x 2048 x 7168 = 88,080,384
+    elements are 176,160,768 bytes instead of 46,792,704, and one quantiser
+    launch fewer."""
     b = _bench()
     wl = synth.workload("decode64+mixed")
     counts = np.zeros(wl.n_experts, np.int32)
     counts[0] = 1
     _, touched, b1 = b.algorithmic_work(wl, 1, counts)
     assert touched == 1
-    assert b1 == 2_924_544 + 88_080_384
+    assert b1 == 2_924_544 + 176_160_768
     work, _, _ = b.algorithmic_work(wl, 64, counts)
     assert work["gemm_down_shared"][0] >= (3584 + 2 * 2 * 2048) * 7168 * 2
     assert b.launches_per_forward(64, wl) == 9 and b.launches_per_forward(64, synth.workload("decode64")) == 10
