@@ -243,6 +243,36 @@ MOE_API moe_status moe_mx_gemm(const uint8_t *a_codes, const uint8_t *a_scales, 
                        const uint8_t *b_scales, int32_t N, int32_t K, float *out, int32_t *dev_status,
                        void *stream);
 
+/* Expert-parallel dispatch, emulated on one GPU ("Kimi K3: 2.8 Trillion
+ * Parameters, Four Bits at a Time", section "What it takes to serve it": each
+ * token's vector ships to the devices owning its k experts and the k partial
+ * outputs ship back; "What Kimi K3 asks of the hardware", section "Width: 896
+ * experts and the interconnect").  The layer's routed experts read the MXFP8
+ * latent, so that is the payload.  The E experts are split into `ranks`
+ * contiguous slices (rank r owns experts [floor(E r / ranks),
+ * floor(E (r + 1) / ranks))).  For the state of the last moe_forward call on
+ * this plan (T must be its token count; enqueue on the same stream after
+ * it), writes one wire row of moe_ep_row_bytes(plan) bytes per (token, slot)
+ * into `wire` (device, T * k rows, 16-byte aligned): a 16-byte header of four
+ * 32-bit fields {token, expert, slot, gate (fp32 bits)}, the token's L E4M3
+ * codes of the latent, its L / 32 E8M0 scales, zero-padded to 16 bytes.  Rows
+ * follow the layer's dispatch order, the stable sort of the (token, slot)
+ * pairs by expert, so each rank's rows are contiguous: rank r sends rows
+ * [rank_offsets[r], rank_offsets[r + 1]) (device int64 [ranks + 1]).
+ * 1 <= ranks <= E.  Asynchronous on `stream`. */
+MOE_API int64_t moe_ep_row_bytes(const void *plan);
+MOE_API moe_status moe_ep_dispatch(void *plan, int32_t T, int32_t ranks, uint8_t *wire, int64_t *rank_offsets,
+                                   void *stream);
+
+/* The matching combine: expert_out (device fp32 [T * k][L]) holds the expert
+ * outputs in wire-row order, as the owning ranks would return them; writes
+ * c[t] = sum over the token's slots j, in slot order, of gate_j times its
+ * row (device fp32 [T][L]) -- the layer's combine before its MXFP8
+ * quantisation.  `wire` is the dispatch's output for the same T.
+ * Asynchronous on `stream`. */
+MOE_API moe_status moe_ep_combine(void *plan, int32_t T, const uint8_t *wire, const float *expert_out, float *c,
+                                  void *stream);
+
 /* Tensor-core rate probe (measurement, not part of the layer): enqueues on
  * `stream` one CTA per SM of the current device, each issuing iters x 4
  * back-to-back tcgen05.mma instructions of M = 128 x n on operand tiles held

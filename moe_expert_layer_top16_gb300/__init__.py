@@ -33,7 +33,7 @@ PRECISION_MX, PRECISION_MIXED = 0, 1
 # Entry points declared in include/moe.h.
 ENTRY_POINTS = ("moe_plan", "moe_forward", "moe_forward_host", "moe_get_device_status", "moe_workspace_bytes",
                 "moe_free", "moe_status_str", "moe_mxfp4_encode", "moe_mx_gemm", "moe_mma_probe",
-                "moe_mx_gemm_noalloc")
+                "moe_ep_row_bytes", "moe_ep_dispatch", "moe_ep_combine", "moe_mx_gemm_noalloc")
 
 
 class MoeError(RuntimeError):
@@ -105,6 +105,12 @@ def lib(build_if_missing: bool = False):
             L.moe_mxfp4_encode.argtypes = [P, i64, i64, P, P, P]
             L.moe_mx_gemm.restype = C.c_int
             L.moe_mx_gemm.argtypes = [P, P, i32, P, P, i32, i32, P, P, P]
+            L.moe_ep_row_bytes.restype = C.c_int64
+            L.moe_ep_row_bytes.argtypes = [P]
+            L.moe_ep_dispatch.restype = C.c_int
+            L.moe_ep_dispatch.argtypes = [P, i32, i32, P, P, P]
+            L.moe_ep_combine.restype = C.c_int
+            L.moe_ep_combine.argtypes = [P, i32, P, P, P, P]
             L.moe_mma_probe.restype = C.c_int
             L.moe_mma_probe.argtypes = [i32, i32, i32, P, C.POINTER(C.c_double), P]
             L.moe_mx_gemm_noalloc.restype = C.c_int
@@ -266,6 +272,27 @@ class Plan:
         _check(lib().moe_forward_host(self._h, C.c_void_p(x_host.data_ptr()), T, C.c_void_p(y_host.data_ptr()),
                                       _stream_ptr(stream)), "moe_forward_host")
         return y_host
+
+    def ep_row_bytes(self) -> int:
+        """Bytes of one expert-parallel wire row (header, latent codes, scales, padding)."""
+        return int(lib().moe_ep_row_bytes(self._h))
+
+    def ep_dispatch(self, T: int, ranks: int, stream=None):
+        """Expert-parallel dispatch of the last forward's T tokens over `ranks`
+        virtual ranks: (wire uint8 [T*k][row_bytes], rank_offsets int64 [ranks+1])."""
+        k = self.cfg.top_k
+        wire = torch.empty(T * k, self.ep_row_bytes(), dtype=torch.uint8, device=self.device)
+        offs = torch.empty(ranks + 1, dtype=torch.int64, device=self.device)
+        _check(lib().moe_ep_dispatch(self._h, int(T), int(ranks), _ptr(wire), _ptr(offs), _stream_ptr(stream)),
+               "moe_ep_dispatch")
+        return wire, offs
+
+    def ep_combine(self, T: int, wire: torch.Tensor, expert_out: torch.Tensor, stream=None) -> torch.Tensor:
+        """c [T][L] fp32 from expert outputs in wire-row order (the matching combine)."""
+        c = torch.empty(T, self.cfg.d_latent, dtype=torch.float32, device=self.device)
+        _check(lib().moe_ep_combine(self._h, int(T), _ptr(wire), _ptr(expert_out.contiguous()), _ptr(c),
+                                    _stream_ptr(stream)), "moe_ep_combine")
+        return c
 
     def device_status(self) -> int:
         return lib().moe_get_device_status(self._h)

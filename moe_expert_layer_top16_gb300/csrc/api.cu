@@ -179,6 +179,8 @@ struct Plan {
     int* status;
     void* x_stage;
     float* y_stage;
+    int32_t* ep_inv;          // [T_max * k] wire row of each (token, slot) for the expert-parallel combine
+    int last_T = 0;           // tokens of the last forward call (the expert-parallel dispatch reads its state)
     CUtensorMap tA2, tB2, tA7, tB7, tA8, tB8, tA10, tB10, tAR, tBR;
     // B maps with one box per wide work item (box height = that n_max),
     // re-encoded when a forward needs another height
@@ -605,6 +607,7 @@ moe_status moe_plan(const moe_config* cfg, const moe_weights* w, int device, voi
     TRY(palloc(p, &p->ioff7, sizeof(int32_t) * (E + 1)));
     TRY(palloc(p, &p->ioff8, sizeof(int32_t) * (E + 1)));
     TRY(palloc(p, &p->status, sizeof(int) * 4));
+    TRY(palloc(p, &p->ep_inv, sizeof(int32_t) * p->T_max * p->k));
     TRY(palloc(p, &p->x_stage, sizeof(uint16_t) * p->T_max * D));
     TRY(palloc(p, &p->y_stage, sizeof(float) * p->T_max * D));
 #undef TRY
@@ -914,6 +917,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         TRY(launch_gemm(g, std::min(items, p->num_sms), s));
     }
     mark(MOE_NUM_STAGES);
+    if (err == cudaSuccess) p->last_T = T;
     // intermediate outputs on request
     if (dbg && err == cudaSuccess) {
         const int S = p->S, SIs = p->SIs;
@@ -969,6 +973,32 @@ moe_status moe_forward_host(void* plan, const uint16_t* x_host, int32_t T, void*
                           cudaMemcpyDeviceToHost, s);
     if (err == cudaSuccess) err = cudaStreamSynchronize(s);
     return cuda_status(err);
+}
+
+int64_t moe_ep_row_bytes(const void* plan) {
+    const Plan* p = static_cast<const Plan*>(plan);
+    return p ? ep_row_bytes(p->L) : 0;
+}
+
+moe_status moe_ep_dispatch(void* plan, int32_t T, int32_t ranks, uint8_t* wire, int64_t* rank_offsets, void* stream) {
+    Plan* p = static_cast<Plan*>(plan);
+    if (!p || !wire || !rank_offsets || T < 1 || T != p->last_T || ranks < 1 || ranks > p->E)
+        return MOE_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(wire) & 15 || reinterpret_cast<uintptr_t>(rank_offsets) & 7) return MOE_ERR_INVALID_ARG;
+    DevGuard guard(p->device);
+    return cuda_status(launch_ep_pack(p->sorted_token, p->offsets, p->idx, p->gw, p->zq,
+                                      reinterpret_cast<const uint32_t*>(p->zsf), p->T_pad, T, p->k, p->E, p->L, ranks,
+                                      wire, rank_offsets, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_ep_combine(void* plan, int32_t T, const uint8_t* wire, const float* expert_out, float* c, void* stream) {
+    Plan* p = static_cast<Plan*>(plan);
+    if (!p || !wire || !expert_out || !c || T < 1 || T > p->T_max) return MOE_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(wire) & 15 || reinterpret_cast<uintptr_t>(expert_out) & 3 ||
+        reinterpret_cast<uintptr_t>(c) & 3)
+        return MOE_ERR_INVALID_ARG;
+    DevGuard guard(p->device);
+    return cuda_status(launch_ep_combine(wire, expert_out, T, p->k, p->L, p->ep_inv, c, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_get_device_status(void* plan) {

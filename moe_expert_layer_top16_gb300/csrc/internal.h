@@ -214,6 +214,14 @@ cudaError_t launch_export_sf(const uint8_t* planes, int64_t pitch, const int32_t
 cudaError_t launch_gather_rows(const uint8_t* src, int64_t src_stride, const int32_t* row_map, int64_t rows,
                                int64_t row_bytes, uint8_t* dst, int64_t dst_stride, cudaStream_t s);
 
+// ------------------------------------------------------------------ expert-parallel emulation (ep.cu)
+int64_t ep_row_bytes(int L);
+cudaError_t launch_ep_pack(const int32_t* sorted_token, const int32_t* offsets, const int32_t* idx, const float* gw,
+                           const uint8_t* zq, const uint32_t* zsf, int64_t zsf_pitch, int T, int k, int E, int L,
+                           int R, uint8_t* wire, int64_t* rank_offsets, cudaStream_t s);
+cudaError_t launch_ep_combine(const uint8_t* wire, const float* out, int T, int k, int L, int32_t* inv, float* c,
+                              cudaStream_t s);
+
 // ------------------------------------------------------------------ tensor-core rate probe (peak.cu)
 enum ProbeKind : int { PROBE_MX_E2M1_E4M3 = 0, PROBE_MX_E4M3_E4M3 = 1, PROBE_BF16 = 2 };
 // grid CTAs each issue iters x 4 MMAs of M = 128 x n; *flops = their FLOPs

@@ -80,6 +80,13 @@ def test_plan_rejects_missing_weights(L):
     assert L.moe_plan(None, None, 0, C.byref(h)) == moe.MOE_ERR_INVALID_ARG
 
 
+def test_expert_parallel_calls_reject_bad_arguments(L):
+    p = C.c_void_p(256)
+    assert L.moe_ep_row_bytes(None) == 0
+    assert L.moe_ep_dispatch(None, 1, 8, p, p, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_ep_combine(None, 1, p, p, p, None) == moe.MOE_ERR_INVALID_ARG
+
+
 def test_null_plan_calls(L):
     assert L.moe_forward(None, None, 1, None, None, None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_forward_host(None, None, 1, None, None) == moe.MOE_ERR_INVALID_ARG
