@@ -26,6 +26,11 @@ Parity status per function (what pins it is in ``tests/test_oracle_*.py``):
                  that are parity unpinned.
   bf16_round     pinned: hand cases of round-to-nearest-even on the bf16 grid,
                  and the library conversion (torch) on random fp32 values.
+  quantile_balance  pinned: with a step of 1, an expert updated alone gets
+                 exactly the target load (brute force over the batch); the
+                 update is unchanged when every bias shifts by a constant;
+                 repeated damped updates drive a Zipf-skewed load toward the
+                 mean.
   moe_forward, mixed scheme (BF16 projections and shared experts): pinned by
                  a dense recomputation from numpy matmuls of the decoded bf16
                  weights, and by one-hot projection rows that copy x into z.
@@ -109,6 +114,8 @@ def lib():
             L.orc_permute.argtypes = [P, i64, C.c_int, C.c_int, P, P, P]
             L.orc_combine.restype = None
             L.orc_combine.argtypes = [P, P, P, i64, C.c_int, i64, P]
+            L.orc_quantile_balance.restype = None
+            L.orc_quantile_balance.argtypes = [P, P, i64, C.c_int, C.c_int, i64, C.c_double, P]
             L.orc_bf16_round_array.restype = None
             L.orc_bf16_round_array.argtypes = [P, i64, P]
             L.orc_moe_forward.restype = C.c_int
@@ -222,6 +229,17 @@ def route(logits: np.ndarray, k: int, softmax: bool, bias=None):
     b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
     lib().orc_route(_p(lg), None if b is None else _p(b), T, E, k, int(bool(softmax)), _p(idx), _p(gates))
     return idx, gates
+
+
+def quantile_balance(logits: np.ndarray, bias, k: int, target: int, alpha: float) -> np.ndarray:
+    """Quantile Balancing update of the selection bias from logits [T][E]
+    (the reading in moe_oracle.c); returns the new bias (fp64 [E])."""
+    lg = np.ascontiguousarray(logits, dtype=np.float64)
+    T, E = lg.shape
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    out = np.zeros(E, np.float64)
+    lib().orc_quantile_balance(_p(lg), None if b is None else _p(b), T, E, k, int(target), float(alpha), _p(out))
+    return out
 
 
 def permute(idx: np.ndarray, E: int):

@@ -369,6 +369,63 @@ void orc_route(const double *logits, const float *bias, int64_t T, int E, int k,
     free(taken);
 }
 
+/* ------------------------------------------------------------------ */
+/* Quantile Balancing ("Kimi K3 and the New Open-Weights Moat", section  */
+/* "How the router picks 16 of 896", Fig. 2: each expert's selection     */
+/* bias is updated from the distribution of its score margins so that    */
+/* its routed token count approaches the target load; "What Kimi K3 asks */
+/* of the hardware": allocation derived from quantiles of the router     */
+/* scores).  The pages give no formula; the reading used here:           */
+/*  - key_te = sigmoid(l_te) + b_e;                                      */
+/*  - the margin of expert e for token t is key_te minus the key e must  */
+/*    beat: the k-th largest key among the other experts (the (k+1)-th   */
+/*    largest key of the token when e is among its top k, else the k-th) */
+/*    -- e is selected exactly when its margin is positive (ties aside); */
+/*  - with m_(1) >= m_(2) >= ... e's margins in descending order and n   */
+/*    the target count (clamped to [1, T-1]), q_e = (m_(n) + m_(n+1))/2  */
+/*    is the shift of e's bias that leaves exactly n positive margins    */
+/*    when the other biases stay as they are;                            */
+/*  - b_e <- b_e - alpha q_e (alpha in (0, 1]: the drift toward the      */
+/*    target).                                                           */
+
+static int cmp_desc(const void *a, const void *b)
+{
+    double x = *(const double *)a, y = *(const double *)b;
+    return (x < y) - (x > y);
+}
+
+void orc_quantile_balance(const double *logits, const float *bias, int64_t T, int E, int k, int64_t target,
+                          double alpha, double *bias_out)
+{
+    double *key = (double *)malloc(sizeof(double) * (size_t)E);
+    double *srt = (double *)malloc(sizeof(double) * (size_t)E);
+    double *marg = (double *)malloc(sizeof(double) * (size_t)(T * E));   /* [E][T] */
+    for (int64_t t = 0; t < T; ++t) {
+        for (int e = 0; e < E; ++e) {
+            key[e] = sigmoid(logits[t * E + e]) + (bias ? (double)bias[e] : 0.0);
+            srt[e] = key[e];
+        }
+        qsort(srt, (size_t)E, sizeof(double), cmp_desc);
+        double kth = srt[k - 1], next = (k < E) ? srt[k] : -INFINITY;
+        for (int e = 0; e < E; ++e) {
+            /* e beats the k-th largest of the others: next when e is at or
+             * above the k-th key, kth otherwise */
+            double thr = (key[e] >= kth) ? next : kth;
+            marg[(int64_t)e * T + t] = key[e] - thr;
+        }
+    }
+    int64_t n = target < 1 ? 1 : (target > T - 1 ? T - 1 : target);
+    for (int e = 0; e < E; ++e) {
+        double *m = marg + (int64_t)e * T;
+        qsort(m, (size_t)T, sizeof(double), cmp_desc);
+        double q = 0.5 * (m[n - 1] + m[n]);
+        bias_out[e] = (bias ? (double)bias[e] : 0.0) - alpha * q;
+    }
+    free(key);
+    free(srt);
+    free(marg);
+}
+
 /* Dispatch of the one-page data path: per-expert counts, exclusive offsets,
  * and the stable sort of flat indices f = t*k + j by expert. */
 void orc_permute(const int32_t *idx, int64_t T, int k, int E,
