@@ -243,6 +243,32 @@ MOE_API moe_status moe_mx_gemm(const uint8_t *a_codes, const uint8_t *a_scales, 
                        const uint8_t *b_scales, int32_t N, int32_t K, float *out, int32_t *dev_status,
                        void *stream);
 
+/* Quantile Balancing of the selection bias ("Kimi K3 and the New
+ * Open-Weights Moat", section "How the router picks 16 of 896", Fig. 2: each
+ * expert's bias is updated from the distribution of its score margins so
+ * that its routed token count approaches the target load).  The pages give
+ * no formula; this computes, from the logits of the last moe_forward call
+ * (T must be its token count; enqueue on its stream after it) and the
+ * plan's current bias b:
+ *   key_te = sigmoid(l_te) + b_e (fp64);  m_te = key_te - the k-th largest
+ *   key of token t among the other experts (positive exactly when e is
+ *   selected, ties aside);  q_e = (m_(n) + m_(n+1)) / 2 over e's margins in
+ *   descending order, n = target clamped to [1, T - 1] (target <= 0: the mean
+ *   load round(T k / E));  bias_out[e] = b_e - alpha q_e  (0 < alpha <= 1).
+ * With alpha = 1 an expert updated alone would get exactly n tokens.
+ * bias_out: device fp32 [E].  Sigmoid scoring only.  The first call on a
+ * plan allocates an [E][max_tokens] fp64 workspace (host-synchronous); later
+ * calls are asynchronous and allocate nothing.  Above 128 tokens the logits
+ * of experts outside a token's candidates are tensor-core estimates (see
+ * moe_debug.logits), and the update reads them as they are. */
+MOE_API moe_status moe_quantile_balance(void *plan, int32_t T, int32_t target, double alpha, float *bias_out,
+                                        void *stream);
+
+/* Replace the plan's selection bias with bias (device fp32 [E], finite);
+ * later forward calls select on sigmoid(l) + bias.  Host-synchronous
+ * (synchronises the device).  Sigmoid scoring only. */
+MOE_API moe_status moe_set_bias(void *plan, const float *bias);
+
 /* Expert-parallel dispatch, emulated on one GPU ("Kimi K3: 2.8 Trillion
  * Parameters, Four Bits at a Time", section "What it takes to serve it": each
  * token's vector ships to the devices owning its k experts and the k partial

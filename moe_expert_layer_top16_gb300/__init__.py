@@ -33,7 +33,8 @@ PRECISION_MX, PRECISION_MIXED = 0, 1
 # Entry points declared in include/moe.h.
 ENTRY_POINTS = ("moe_plan", "moe_forward", "moe_forward_host", "moe_get_device_status", "moe_workspace_bytes",
                 "moe_free", "moe_status_str", "moe_mxfp4_encode", "moe_mx_gemm", "moe_mma_probe",
-                "moe_ep_row_bytes", "moe_ep_dispatch", "moe_ep_combine", "moe_mx_gemm_noalloc")
+                "moe_ep_row_bytes", "moe_ep_dispatch", "moe_ep_combine", "moe_quantile_balance", "moe_set_bias",
+                "moe_mx_gemm_noalloc")
 
 
 class MoeError(RuntimeError):
@@ -111,6 +112,10 @@ def lib(build_if_missing: bool = False):
             L.moe_ep_dispatch.argtypes = [P, i32, i32, P, P, P]
             L.moe_ep_combine.restype = C.c_int
             L.moe_ep_combine.argtypes = [P, i32, P, P, P, P]
+            L.moe_quantile_balance.restype = C.c_int
+            L.moe_quantile_balance.argtypes = [P, i32, i32, C.c_double, P, P]
+            L.moe_set_bias.restype = C.c_int
+            L.moe_set_bias.argtypes = [P, P]
             L.moe_mma_probe.restype = C.c_int
             L.moe_mma_probe.argtypes = [i32, i32, i32, P, C.POINTER(C.c_double), P]
             L.moe_mx_gemm_noalloc.restype = C.c_int
@@ -272,6 +277,19 @@ class Plan:
         _check(lib().moe_forward_host(self._h, C.c_void_p(x_host.data_ptr()), T, C.c_void_p(y_host.data_ptr()),
                                       _stream_ptr(stream)), "moe_forward_host")
         return y_host
+
+    def quantile_balance(self, T: int, alpha: float = 1.0, target: int = 0, stream=None) -> torch.Tensor:
+        """Quantile Balancing update of the selection bias from the last
+        forward's T tokens (see moe_quantile_balance): the new bias, fp32 [E]."""
+        out = torch.empty(self.cfg.n_experts, dtype=torch.float32, device=self.device)
+        _check(lib().moe_quantile_balance(self._h, int(T), int(target), float(alpha), _ptr(out), _stream_ptr(stream)),
+               "moe_quantile_balance")
+        return out
+
+    def set_bias(self, bias: torch.Tensor):
+        """Install a new selection bias (fp32 [E] on the plan's device)."""
+        assert bias.dtype == torch.float32 and bias.numel() == self.cfg.n_experts
+        _check(lib().moe_set_bias(self._h, _ptr(bias.contiguous())), "moe_set_bias")
 
     def ep_row_bytes(self) -> int:
         """Bytes of one expert-parallel wire row (header, latent codes, scales, padding)."""

@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmoe.so")
-UNITS = ("gemm.cu", "kernels.cu", "api.cu", "peak.cu", "router.cu", "ep.cu")
+UNITS = ("gemm.cu", "kernels.cu", "api.cu", "peak.cu", "router.cu", "ep.cu", "balance.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]
 

@@ -164,6 +164,8 @@ struct Plan {
     float *router, *router2, *bias;   // router [E][RK]; router2: [E][2 RK] = TF32 high part | remainder
     float* rnorm;                     // [2][E] upper bounds of |R_e| and of |R_lo_e| (router2's remainder)
     float bias_absmax = 0.0f;
+    bool has_bias = false;            // the selection bias is in use (bias holds E floats either way)
+    double* qb_marg = nullptr;        // [E][T_max] margins of the Quantile Balancing update, made on first use
     int RK = 0;                       // router input width: L (latent routing) or D (hidden routing)
     bool route_hidden = false, out_bf16 = false;
     bool mixed = false;               // bf16 latent projections and shared experts (MOE_PRECISION_MIXED)
@@ -568,9 +570,9 @@ moe_status moe_plan(const moe_config* cfg, const moe_weights* w, int device, voi
     TRY(palloc(p, &p->rnorm, sizeof(float) * 2 * E));
     TRY(launch_router_norms(p->router, p->router2, E, RK, p->rnorm, 0));
     TRY(cudaDeviceSynchronize());
-    p->bias = nullptr;
+    TRY(palloc(p, &p->bias, sizeof(float) * E));
     if (w->router_bias) {
-        TRY(palloc(p, &p->bias, sizeof(float) * E));
+        p->has_bias = true;
         TRY(cudaMemcpy(p->bias, w->router_bias, sizeof(float) * E, cudaMemcpyDeviceToDevice));
         std::vector<float> hb(E);
         TRY(cudaMemcpy(hb.data(), w->router_bias, sizeof(float) * E, cudaMemcpyDeviceToHost));
@@ -777,7 +779,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
     {
         TopkArgs a{};
         a.logits = p->logits;
-        a.bias = p->bias;
+        a.bias = p->has_bias ? p->bias : nullptr;
         a.T = T;
         a.E = E;
         a.k = k;
@@ -973,6 +975,42 @@ moe_status moe_forward_host(void* plan, const uint16_t* x_host, int32_t T, void*
                           cudaMemcpyDeviceToHost, s);
     if (err == cudaSuccess) err = cudaStreamSynchronize(s);
     return cuda_status(err);
+}
+
+moe_status moe_quantile_balance(void* plan, int32_t T, int32_t target, double alpha, float* bias_out, void* stream) {
+    Plan* p = static_cast<Plan*>(plan);
+    if (!p || !bias_out || T < 2 || T != p->last_T || p->cfg.score_fn != MOE_SCORE_SIGMOID_BIAS || p->k >= p->E ||
+        !(alpha > 0.0 && alpha <= 1.0))
+        return MOE_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(bias_out) & 3) return MOE_ERR_INVALID_ARG;
+    DevGuard guard(p->device);
+    if (!p->qb_marg) {
+        cudaError_t err = palloc(p, &p->qb_marg, sizeof(double) * p->E * p->T_max);
+        if (err != cudaSuccess) return cuda_status(err);
+    }
+    if (target <= 0) target = static_cast<int32_t>((static_cast<int64_t>(T) * p->k + p->E / 2) / p->E);
+    return cuda_status(launch_quantile_balance(p->logits, p->has_bias ? p->bias : nullptr, T, p->E, p->k, target, alpha,
+                                               p->qb_marg, bias_out, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_set_bias(void* plan, const float* bias) {
+    Plan* p = static_cast<Plan*>(plan);
+    if (!p || !bias || p->cfg.score_fn != MOE_SCORE_SIGMOID_BIAS) return MOE_ERR_INVALID_ARG;
+    DevGuard guard(p->device);
+    std::vector<float> hb(p->E);
+    cudaError_t err = cudaDeviceSynchronize();
+    if (err == cudaSuccess) err = cudaMemcpy(hb.data(), bias, sizeof(float) * p->E, cudaMemcpyDeviceToHost);
+    if (err != cudaSuccess) return cuda_status(err);
+    float absmax = 0.0f;
+    for (float b : hb) {
+        if (!(b == b) || std::fabs(b) == INFINITY) return MOE_ERR_INVALID_ARG;
+        absmax = std::max(absmax, std::fabs(b));
+    }
+    err = cudaMemcpy(p->bias, bias, sizeof(float) * p->E, cudaMemcpyDeviceToDevice);
+    if (err != cudaSuccess) return cuda_status(err);
+    p->bias_absmax = absmax;
+    p->has_bias = true;
+    return MOE_OK;
 }
 
 int64_t moe_ep_row_bytes(const void* plan) {

@@ -222,6 +222,11 @@ cudaError_t launch_ep_pack(const int32_t* sorted_token, const int32_t* offsets, 
 cudaError_t launch_ep_combine(const uint8_t* wire, const float* out, int T, int k, int L, int32_t* inv, float* c,
                               cudaStream_t s);
 
+// ------------------------------------------------------------------ Quantile Balancing (balance.cu)
+// new bias [E] from logits [T][E] and the current bias (null: 0); marg: [E][T] fp64 workspace
+cudaError_t launch_quantile_balance(const float* logits, const float* bias, int T, int E, int k, int target,
+                                    double alpha, double* marg, float* bias_out, cudaStream_t s);
+
 // ------------------------------------------------------------------ tensor-core rate probe (peak.cu)
 enum ProbeKind : int { PROBE_MX_E2M1_E4M3 = 0, PROBE_MX_E4M3_E4M3 = 1, PROBE_BF16 = 2 };
 // grid CTAs each issue iters x 4 MMAs of M = 128 x n; *flops = their FLOPs

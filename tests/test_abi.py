@@ -82,6 +82,8 @@ def test_plan_rejects_missing_weights(L):
 
 def test_expert_parallel_calls_reject_bad_arguments(L):
     p = C.c_void_p(256)
+    assert L.moe_quantile_balance(None, 64, 0, 1.0, p, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_set_bias(None, p) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_ep_row_bytes(None) == 0
     assert L.moe_ep_dispatch(None, 1, 8, p, p, None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_ep_combine(None, 1, p, p, p, None) == moe.MOE_ERR_INVALID_ARG
