@@ -52,7 +52,7 @@ CPU_BASELINE_SECONDS = 10.0
 # kernels from an ncu capture, stored with a hash of the kernel sources it
 # was taken on; a figure stands only while the sources are unchanged.
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
-SOURCE_FILES = ("api.cu", "gemm.cu", "kernels.cu", "peak.cu", "router.cu", "internal.h", "mx.cuh", "ptx.cuh")
+SOURCE_FILES = ("api.cu", "gemm.cu", "kernels.cu", "peak.cu", "router.cu", "ep.cu", "balance.cu", "internal.h", "mx.cuh", "ptx.cuh")
 
 
 def kernel_source_hash() -> str:
@@ -544,6 +544,33 @@ def run_cuda(args, wl, world, rank, local):
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }
+    if args.ep_ranks > 0:
+        # expert-parallel dispatch and combine of this batch over virtual ranks
+        R = min(args.ep_ranks, wl.n_experts)
+        plan.forward(x, out=y)
+        wire, offs = plan.ep_dispatch(T, R)
+        o = torch.zeros(T * wl.top_k, wl.d_latent, dtype=torch.float32, device=dev)
+        plan.ep_combine(T, wire, o)
+        torch.cuda.synchronize()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(10)]
+        for e3 in evs:
+            e3[0].record()
+            plan.ep_dispatch(T, R)
+            e3[1].record()
+            plan.ep_combine(T, wire, o)
+            e3[2].record()
+        torch.cuda.synchronize()
+        rows = np.diff(offs.cpu().numpy())
+        rb = plan.ep_row_bytes()
+        result["ep"] = {"ranks": R, "tokens": T,
+                        "payload_bytes_per_token": wl.top_k * (wl.d_latent + wl.d_latent // 32),
+                        "wire_bytes_per_token": wl.top_k * rb,
+                        "combine_bytes_per_token_fp32": wl.top_k * wl.d_latent * 4,
+                        "pages_2kd_fp8_bytes_per_token": 2 * wl.top_k * wl.d_model,
+                        "rows_per_rank_min_max": [int(rows.min()), int(rows.max())],
+                        "dispatch_ms": float(np.median([a.elapsed_time(b) for a, b, _ in evs])),
+                        "combine_ms": float(np.median([b.elapsed_time(c) for _, b, c in evs]))}
+        del wire, offs, o
     if pre is not None:
         # the same layer at the prefill batch, timed the same way in the same run
         Tp = pre.tokens
@@ -647,6 +674,121 @@ def run_sweep(args, wl, rank, local):
     return 0
 
 
+PAGES_BATCHES = (1, 8, 64, 256, 1024, 4096)
+
+
+def pages_uniform_gb_per_token():
+    """The pages' uniform-routing column (GB per token by batch), from the
+    stored copy of their printed table."""
+    out = {}
+    with open(os.path.join(ROOT, "tests", "golden", "expert_amortisation.txt")) as f:
+        for ln in f:
+            ln = ln.strip()
+            if ln and not ln.startswith("#"):
+                parts = ln.split()
+                out[int(parts[0])] = float(parts[1])
+    return out
+
+
+def run_multilayer(args, wl, rank, local):
+    """A decode step through N layers of the K3-shaped MoE: layer l has its
+    own weights (seed 1000 + l) and its own seeded hidden states.  Between two
+    MoE layers a model runs attention, a residual add and a norm, which this
+    library does not implement; feeding one layer's raw output into the next
+    would correlate the tokens and skew the routing, while the pages'
+    amortisation table assumes uniform routing.  For every batch size the N
+    forwards are captured once in a CUDA graph and the graph is replayed; one
+    JSON line per batch size reports the step time, the experts each layer
+    touched, the expert-weight bytes streamed per token, and the achieved
+    bandwidth.  The pages' uniform column (GB per token at an assumed 1.5 GB
+    per expert for the whole model) rides along, rescaled to this stack's
+    bytes per expert, so that the two curves can be compared by shape."""
+    import dataclasses
+    import torch
+    import synth
+    import moe_expert_layer_top16_gb300 as moe
+    from moe_expert_layer_top16_gb300 import build as mbuild
+    from moe_expert_layer_top16_gb300.weights import encode_layer
+
+    mbuild.build()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    batches = [int(b) for b in args.batches.split(",")]
+    N = args.layers
+    layers = [dataclasses.replace(wl, seed=1000 + l) for l in range(N)]
+    plans = []
+    for lw in layers:
+        def fetch(name, i, lw=lw):
+            if name == "bias":
+                return synth.router_bias(lw, device=dev)
+            return synth.weight(lw, name, i, device=dev)
+        W = encode_layer(lw, fetch, dev)
+        plans.append(moe.Plan(lw, W, max_tokens=max(batches)))
+        del W
+        torch.cuda.empty_cache()
+    hbm, _, _, _ = peaks()
+    pages = pages_uniform_gb_per_token()
+    D, L, I, S, Is = wl.d_model, wl.d_latent, wl.expert_inter, wl.n_shared, wl.shared_inter
+    per_expert = 3 * I * L * MX4_BYTES_PER_ELT                  # bytes of one routed expert in one layer
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    for B in batches:
+        xs = [synth.hidden_states(lw, B, device=dev) for lw in layers]
+        bufs = [torch.empty(B, D, dtype=torch.float32, device=dev) for _ in range(2)]
+        # one eager pass: the experts each layer touches (the graph exports nothing)
+        touched = []
+        for l, plan in enumerate(plans):
+            counts = torch.zeros(wl.n_experts, dtype=torch.int32, device=dev)
+            plan.forward(xs[l], out=bufs[l % 2], debug={"counts": counts})
+            touched.append(int((counts > 0).sum().item()))
+        torch.cuda.synchronize()
+        for plan in plans:
+            if plan.device_status() != moe.MOE_OK:
+                raise RuntimeError(f"device-side error at batch {B}")
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            plans[0].forward(xs[0], out=bufs[0])               # warm-up on the capture stream
+            stream.synchronize()
+            with torch.cuda.graph(graph, stream=stream):
+                for l, plan in enumerate(plans):
+                    plan.forward(xs[l], out=bufs[l % 2])
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        steps = max(3, min(args.steps, 20))
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        with torch.cuda.stream(stream):
+            for i in range(steps):
+                flush.fill_(float(i))
+                evs[i][0].record()
+                graph.replay()
+                evs[i][1].record()
+        torch.cuda.synchronize()
+        for plan in plans:
+            if plan.device_status() != moe.MOE_OK:
+                raise RuntimeError(f"device-side error at batch {B}")
+        ms = float(np.median([a.elapsed_time(b) for a, b in evs]))
+        routed = sum(touched) * per_expert
+        dense = N * ((L + 2 * S * Is) * D + D * (L + S * Is)) * MX4_BYTES_PER_ELT
+        line = {"impl": "multilayer", "workload": wl.name, "layers": N, "tokens": B, "ms_per_step": ms,
+                "ms_per_layer": ms / N, "tokens_per_s": B / (ms / 1e3),
+                "touched_per_layer": float(np.mean(touched)),
+                "routed_weight_GB_per_token": routed / B / 1e9,
+                "all_weight_GB_per_token": (routed + dense) / B / 1e9,
+                "weight_GBps": (routed + dense) / (ms / 1e3) / 1e9,
+                "weight_frac_hbm": (routed + dense) / (ms / 1e3) / 1e9 / hbm,
+                "pages_uniform_GB_per_token": pages.get(B),
+                "pages_uniform_rescaled_GB_per_token": (pages[B] / 1.5e9 * per_expert * N) if B in pages else None,
+                "steps": steps, "graph": "one CUDA graph of the N forwards, replayed",
+                "l2": "flushed between steps"}
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        del graph
+    for plan in plans:
+        plan.close()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -660,8 +802,13 @@ def main():
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip the prefill sub-record (the same layer at --prefill-tokens tokens)")
     ap.add_argument("--prefill-tokens", type=int, default=8192)
+    ap.add_argument("--ep-ranks", type=int, default=64,
+                    help="virtual ranks of the expert-parallel dispatch/combine record (0: skip)")
     ap.add_argument("--sweep", action="store_true",
                     help="token-count sweep of the workload's layer: one JSON line per batch size")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="multi-layer decode step: N layers with their own weights, one CUDA graph per batch size")
+    ap.add_argument("--batches", default=",".join(str(b) for b in PAGES_BATCHES))
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -672,6 +819,8 @@ def main():
         return run_reference(args, wl, world, rank)
     if args.sweep:
         return run_sweep(args, wl, rank, local)
+    if args.layers > 0:
+        return run_multilayer(args, wl, rank, local)
     return run_cuda(args, wl, world, rank, local)
 
 
