@@ -4,9 +4,12 @@
 
 A step is one forward pass of the whole layer (every stage of moe_forward)
 over one batch of synthetic tokens of the workload (default: the K3-shaped
-decode batch, 64 tokens).  Inputs and weights are resident in HBM before the
-timed region; L2 is flushed (a 512 MB write) between timed steps, outside the
-per-step CUDA events.  Prints one JSON line (rank 0).
+decode batch, 64 tokens).  The forward is captured once in a CUDA graph and
+each step replays it (--eager: plain launches; the eager time is reported
+either way).  Inputs and weights are resident in HBM before the timed region;
+L2 is flushed (a 512 MB write) between timed steps, outside the per-step CUDA
+events.  Prints one JSON line (rank 0), with a sub-record of the same layer at
+8192 tokens (prefill) timed the same way in the same run.
 
 --impl reference times the CPU oracle instead (the reference arm): each step
 is the oracle's forward over a bounded sample of the same workload's tokens on
@@ -330,11 +333,15 @@ def measure_tensor_peaks(dev, reps=5):
     return out
 
 
-def time_layer(plan, wl, T, x, y, flush, steps, warmup, world, with_stages=True):
+def time_layer(plan, wl, T, x, y, flush, steps, warmup, world, with_stages=True, graph=True):
     """Warm-up, an untimed per-stage pass (events between the stages), then
     exactly `steps` forwards each between two events on the forward's stream,
-    with the L2 flush outside the events.  Returns (step_ms list, mean stage
-    ms, realised counts, clocks, wall seconds of the timed region)."""
+    with the L2 flush outside the events.  With `graph` the forward (all its
+    kernels, unchanged) is captured once in a CUDA graph and each timed step
+    replays it, as a serving loop runs a batch bucket; the eager time of the
+    same forward is measured too.  Returns (step_ms list, mean stage ms,
+    realised counts, clocks, wall seconds of the timed region, eager ms per
+    step or None)."""
     import torch
     import moe_expert_layer_top16_gb300 as moe
     dev = x.device
@@ -360,6 +367,30 @@ def time_layer(plan, wl, T, x, y, flush, steps, warmup, world, with_stages=True)
         torch.cuda.synchronize()
         stage_ms = np.array([[stage_ev[i][s].elapsed_time(stage_ev[i][s + 1]) for s in range(nst)]
                              for i in range(n_stage)]).mean(axis=0)
+    eager_ms = None
+    g = None
+    if graph:
+        # eager reference of the same forward, then the capture
+        ea = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(min(steps, 20))]
+        for i, (a, b) in enumerate(ea):
+            flush.fill_(float(i))
+            a.record()
+            plan.forward(x, out=y)
+            b.record()
+        torch.cuda.synchronize()
+        eager_ms = float(np.median([a.elapsed_time(b) for a, b in ea]))
+        g = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream(device=dev)
+        cs.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(cs):
+            plan.forward(x, out=y)
+            cs.synchronize()
+            with torch.cuda.graph(g, stream=cs):
+                plan.forward(x, out=y)
+        torch.cuda.current_stream().wait_stream(cs)
+        for _ in range(max(warmup, 1)):
+            g.replay()
+        torch.cuda.synchronize()
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     torch.cuda.synchronize()
@@ -376,7 +407,10 @@ def time_layer(plan, wl, T, x, y, flush, steps, warmup, world, with_stages=True)
     for i in range(steps):
         flush.fill_(float(i))                       # L2 flush, outside the step events
         ev0[i].record()
-        plan.forward(x, out=y)
+        if g is not None:
+            g.replay()
+        else:
+            plan.forward(x, out=y)
         ev1[i].record()
     torch.cuda.synchronize()
     barrier(world)
@@ -385,7 +419,8 @@ def time_layer(plan, wl, T, x, y, flush, steps, warmup, world, with_stages=True)
     if plan.device_status() != moe.MOE_OK:
         raise RuntimeError("device-side error in the timed region")
     step_ms = [ev0[i].elapsed_time(ev1[i]) for i in range(steps)]
-    return step_ms, stage_ms, counts_h, clocks, wall
+    del g
+    return step_ms, stage_ms, counts_h, clocks, wall, eager_ms
 
 
 def layer_roofline(wl, T, ms_per_step, stage_ms, counts_h, hbm, tensor_peak, peak_source):
@@ -503,7 +538,8 @@ def run_cuda(args, wl, world, rank, local):
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
 
     K = args.steps
-    step_ms, stage_ms, counts_h, clocks, wall = time_layer(plan, wl, T, x, y, flush, K, args.warmup, world)
+    step_ms, stage_ms, counts_h, clocks, wall, eager_ms = time_layer(plan, wl, T, x, y, flush, K, args.warmup, world,
+                                                                     graph=not args.eager)
     total_ms = max_over_ranks(world, float(np.sum(step_ms)))
     ms_per_step = total_ms / K
     value = job_throughput(world, T, K, total_ms)
@@ -527,6 +563,9 @@ def run_cuda(args, wl, world, rank, local):
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "step_ms": {"median": float(np.median(step_ms)), "p10": float(np.percentile(step_ms, 10)),
                     "p90": float(np.percentile(step_ms, 90))},
+        "launch": ("each step replays one CUDA graph of the whole forward (its kernels unchanged)"
+                   if eager_ms is not None else "eager launches"),
+        "eager_ms_per_step": eager_ms,
         "dtype": ("mxfp4 x mxfp8 routed experts, bf16 projections and shared experts, fp32 accumulate"
                   if getattr(wl, "precision", "mx") == "mixed" else "mxfp4 weights x mxfp8 activations, fp32 accumulate"),
         "data": "synthetic",
@@ -577,10 +616,12 @@ def run_cuda(args, wl, world, rank, local):
         xp = synth.hidden_states(pre, Tp, device=dev, offset=rank * Tp)
         yp = torch.empty(Tp, wl.d_model, dtype=torch.float32, device=dev)
         Kp = max(5, min(K, 40))
-        p_ms, p_stage, p_counts, p_clocks, p_wall = time_layer(plan, pre, Tp, xp, yp, flush, Kp, args.warmup, world)
+        p_ms, p_stage, p_counts, p_clocks, p_wall, p_eager = time_layer(plan, pre, Tp, xp, yp, flush, Kp, args.warmup,
+                                                                        world, graph=not args.eager)
         p_total = max_over_ranks(world, float(np.sum(p_ms)))
         p_roof, p_layer = layer_roofline(pre, Tp, p_total / Kp, p_stage, p_counts, hbm, tensor_peak, peak_source)
         result["prefill"] = {"workload": pre.name, "tokens": Tp, "steps": Kp, "ms_per_step": p_total / Kp,
+                             "eager_ms_per_step": p_eager,
                              "value": job_throughput(world, Tp, Kp, p_total), "unit": "tokens/s",
                              "step_ms": {"median": float(np.median(p_ms)), "p10": float(np.percentile(p_ms, 10)),
                                          "p90": float(np.percentile(p_ms, 90))},
@@ -802,6 +843,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip the prefill sub-record (the same layer at --prefill-tokens tokens)")
     ap.add_argument("--prefill-tokens", type=int, default=8192)
+    ap.add_argument("--eager", action="store_true",
+                    help="time eager launches of the forward instead of replays of its CUDA graph")
     ap.add_argument("--ep-ranks", type=int, default=64,
                     help="virtual ranks of the expert-parallel dispatch/combine record (0: skip)")
     ap.add_argument("--sweep", action="store_true",

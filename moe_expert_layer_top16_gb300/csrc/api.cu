@@ -187,6 +187,8 @@ struct Plan {
     // B maps with one box per wide work item (box height = that n_max),
     // re-encoded when a forward needs another height
     CUtensorMap tB2w, tB10w, tB7w, tB8w, tBRw;
+    // the same MXFP8 token operands with one-row boxes (items of fewer than 16 tokens)
+    CUtensorMap tB2r, tB7r, tB8r, tB10r;
     int wide_dense = 0, wide_grp = 0, wide_router = 0;
     bool tc_router;    // router logit estimates on the tensor cores (one TF32 product) above 128 tokens
     // streaming exact router of up to 128 tokens: R and router input maps,
@@ -625,6 +627,8 @@ moe_status moe_plan(const moe_config* cfg, const moe_weights* w, int device, voi
               map_mx4(&p->tA8, p->w2c, static_cast<int64_t>(E) * L, Ip) && map_mx8(&p->tB8, p->hq, Rp, Ip) &&
               (mixed ? (map_bf16(&p->tA10, p->a10b, D, p->Kcat, 128) && map_bf16(&p->tB10, p->act_bf, Tp, p->Kcat, 16))
                      : (map_mx4(&p->tA10, p->a10c, D, p->Kcat) && map_mx8(&p->tB10, p->act, Tp, p->Kcat))) &&
+              map_mx8(&p->tB2r, p->xq, Tp, D, 1) && map_mx8(&p->tB7r, p->zqp, Rp, L, 1) &&
+              map_mx8(&p->tB8r, p->hq, Rp, Ip, 1) && map_mx8(&p->tB10r, p->act, Tp, p->Kcat, 1) &&
               map_f32(&p->tAR, p->router2, E, 2 * p->RK, 128) &&
               (p->route_hidden ? map_f32(&p->tBR, p->xr, Tp, D, 16) : map_f32(&p->tBR, p->z, Tp, 2 * L, 16));
     p->tc_router = (E % 128 == 0) && (p->RK % 32 == 0);
@@ -720,7 +724,12 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
             g.tmB = p->tB2w;
             g.b_box = nmax_dense;
         }
+        if (!wide_d) {
+            g.tmB1 = p->tB2r;
+            g.b_row1 = 1;
+        }
         if (p->mixed) {
+            g.b_row1 = 0;
             g.tmB = tx;
             g.kind = KIND_BF16;
             g.KT = D / 64;
@@ -858,6 +867,9 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         if (wide_g) {
             g.tmB = p->tB7w;
             g.b_box = nmax_grp;
+        } else {
+            g.tmB1 = p->tB7r;
+            g.b_row1 = 1;
         }
         g.dense = 0;
         g.ioff = p->ioff7;
@@ -878,6 +890,9 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         if (wide_g) {
             g.tmB = p->tB8w;
             g.b_box = nmax_grp;
+        } else {
+            g.tmB1 = p->tB8r;
+            g.b_row1 = 1;
         }
         g.dense = 0;
         g.ioff = p->ioff8;
@@ -901,6 +916,10 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         if (wide_d) {
             g.tmB = p->tB10w;
             g.b_box = nmax_dense;
+        }
+        if (!wide_d && !p->mixed) {
+            g.tmB1 = p->tB10r;
+            g.b_row1 = 1;
         }
         if (p->mixed) {
             g.kind = KIND_BF16;
@@ -1082,9 +1101,10 @@ moe_status moe_mx_gemm(const uint8_t* a_codes, const uint8_t* a_scales, int32_t 
     const int64_t Np = rup(N, 16);
     const size_t atom_bytes = static_cast<size_t>(M) * K / 32;
     const size_t plane_bytes = static_cast<size_t>(K / 128) * (Np + 32) * 16;    // item-atom planes
-    CUtensorMap tA, tB;
+    CUtensorMap tA, tB, tB1;
     const int box_rows = pick_n_max(N, item_cap(N)) > kNarrowMax ? pick_n_max(N, item_cap(N)) : 16;
-    if (!map_mx4(&tA, a_codes, M, K) || !map_mx8(&tB, b_codes, N, K, box_rows)) return MOE_ERR_INVALID_ARG;
+    if (!map_mx4(&tA, a_codes, M, K) || !map_mx8(&tB, b_codes, N, K, box_rows) || !map_mx8(&tB1, b_codes, N, K, 1))
+        return MOE_ERR_INVALID_ARG;
     uint8_t* scratch = nullptr;
     err = cudaMallocAsync(reinterpret_cast<void**>(&scratch), atom_bytes + plane_bytes + 256, s);
     if (err != cudaSuccess) return cuda_status(err);
@@ -1097,7 +1117,12 @@ moe_status moe_mx_gemm(const uint8_t* a_codes, const uint8_t* a_scales, int32_t 
     if (err == cudaSuccess) err = launch_sf_item_planes(b_scales, N, K / 32, planes, Np + 32, nmax, s);
     if (err == cudaSuccess) {
         GemmParams g = gemm_base(tA, tB, atoms, planes, Np + 32, K, nmax, M, static_cast<int>(Np), st);
-        if (nmax > kNarrowMax) g.b_box = nmax;      // tB was encoded with one box per item
+        if (nmax > kNarrowMax) {
+            g.b_box = nmax;      // tB was encoded with one box per item
+        } else {
+            g.tmB1 = tB1;        // items of fewer than 16 tokens load their rows one by one
+            g.b_row1 = 1;
+        }
         g.dense = 1;
         g.m_tiles = M / kBlockM;
         g.n_tokens = N;

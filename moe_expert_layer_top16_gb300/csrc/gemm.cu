@@ -57,7 +57,7 @@ struct Item {
 // them from the parameter space would repeat after every asm statement that
 // clobbers memory).
 struct Hot {
-    int KT, n_max, stage_bytes, a_tx_bytes, kseg_tiles, b_box;
+    int KT, n_max, stage_bytes, a_tx_bytes, kseg_tiles, b_box, b_row1;
     int dense, m_tiles, n_tokens, a_rows, b_rows, E, mt_per_e, rows_per_e, epi_split;
     int ax0, ax1, ax2, bx0, bx1, bx2;
     int64_t sfb_pitch;
@@ -74,6 +74,7 @@ __device__ __forceinline__ Hot load_hot(const GemmParams& p) {
     h.a_tx_bytes = pin(p.a_tx_bytes);
     h.kseg_tiles = pin(p.kseg_tiles);
     h.b_box = pin(p.b_box);
+    h.b_row1 = pin(p.b_row1);
     h.dense = pin(p.dense);
     h.m_tiles = pin(p.m_tiles);
     h.n_tokens = pin(p.n_tokens);
@@ -279,6 +280,7 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
         fence_mbar_init();
         prefetch_tmap(&p.tmA);
         prefetch_tmap(&p.tmB);
+        if (h.b_row1) prefetch_tmap(&p.tmB1);
     }
     if (warp == G) {
         tmem_alloc(tmem_slot, kTmemCols);
@@ -332,8 +334,15 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
             const int nm = (w.n + 15) & ~15;
             const int natoms = (nm + 127) / 128;
             const int nbox = (nm + h.b_box - 1) / h.b_box;           // B boxes of b_box rows
-            const uint32_t b_bytes = static_cast<uint32_t>(nbox * h.b_box * kBlockK);
-            const uint32_t tx = kMX ? static_cast<uint32_t>(h.a_tx_bytes) + b_bytes + 512u + natoms * 512u
+            // an item of fewer than 16 tokens loads only its own token rows
+            // (one-row boxes) and, up to 32 tokens, only its own scale slots:
+            // the MMA still reads 16 rows, and the accumulator columns of the
+            // rows left as they were are never stored
+            const bool row_loads = kMX && h.b_row1 && w.n < 16;
+            const uint32_t b_bytes = row_loads ? static_cast<uint32_t>(w.n * kBlockK)
+                                               : static_cast<uint32_t>(nbox * h.b_box * kBlockK);
+            const uint32_t sfb_bytes = (w.n <= 32) ? static_cast<uint32_t>(w.n * 16) : static_cast<uint32_t>(natoms * 512);
+            const uint32_t tx = kMX ? static_cast<uint32_t>(h.a_tx_bytes) + b_bytes + 512u + sfb_bytes
                                     : static_cast<uint32_t>(kBlockM * 128) + b_bytes;
             const uint8_t* sfa_tile = kMX ? h.sfa + static_cast<size_t>(w.a_row0 / kBlockM) * h.KT * 512 : nullptr;
             for (int kt = kb; kt < ke; ++kt) {
@@ -350,13 +359,18 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                 if (elect_one()) {
                     mbar_arrive_expect_tx(&fullg[stage], tx);
                     tma_load_2d(sb, &p.tmA, &fullg[stage], ax, w.a_row0);
-                    for (int c = 0; c < nbox; ++c)
-                        tma_load_2d(sb + L.offB + c * h.b_box * kBlockK, &p.tmB, &fullg[stage], bx,
-                                    w.b_row0 + c * h.b_box);
+                    if (row_loads) {
+                        for (int r = 0; r < w.n; ++r)
+                            tma_load_2d(sb + L.offB + r * kBlockK, &p.tmB1, &fullg[stage], bx, w.b_row0 + r);
+                    } else {
+                        for (int c = 0; c < nbox; ++c)
+                            tma_load_2d(sb + L.offB + c * h.b_box * kBlockK, &p.tmB, &fullg[stage], bx,
+                                        w.b_row0 + c * h.b_box);
+                    }
                     if constexpr (kMX) {
                         bulk_load(sb + L.offSFA, sfa_tile + static_cast<size_t>(kt) * 512, 512, &fullg[stage]);
                         bulk_load(sb + L.offSFB, h.sfb + (static_cast<size_t>(kt) * h.sfb_pitch + w.b_row0) * 16,
-                                  static_cast<uint32_t>(natoms * 512), &fullg[stage]);
+                                  sfb_bytes, &fullg[stage]);
                     }
                 }
                 __syncwarp();

@@ -56,6 +56,8 @@ enum GemmKind : int {
 struct GemmParams {
     CUtensorMap tmA;        // MX: MXFP4 weights, 16U4_ALIGN16B, box {128, 128}; TF32: fp32, box {32, 128}
     CUtensorMap tmB;        // MX: MXFP8 activations, UINT8, box {128, 16}; TF32: fp32, box {32, 16}
+    CUtensorMap tmB1;       // MX, b_row1 != 0: the same activations with a one-row box {128, 1}
+    int b_row1;             // items of fewer than 16 tokens load only their own rows (tmB1) and scale slots
     const uint8_t* sfa;     // weight scales, pre-arranged: [rows/128][KT][512]
     const uint8_t* sfb;     // activation scales, item-atom planes: [KT][sfb_pitch] 16-byte slots
     int64_t sfb_pitch;
