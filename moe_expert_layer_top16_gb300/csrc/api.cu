@@ -710,11 +710,25 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         if (ev && err == cudaSuccess) err = cudaEventRecord(ev[i], s);
     };
     TRY(cudaMemsetAsync(p->sel, 0, sizeof(uint32_t) * E * W, s));
+    // Kernels after the first are launched with programmatic serialization:
+    // each may start while its predecessor drains and waits for it on the
+    // device (pdl_wait).  Measured on GB300: every kernel gains up to 128
+    // tokens; above that only the GEMMs do (their prologue is long and their
+    // CTAs cannot share an SM with a running GEMM), while the small
+    // many-CTA kernels launched early slowed the GEMMs they wait behind.  The
+    // first kernel follows the memset with a plain launch; with per-stage
+    // events every launch is plain.
+    bool first_kernel = true;
+    auto pdl = [&](bool gemm) {
+        const bool r = !first_kernel && ev == nullptr && (gemm || T <= 128);
+        first_kernel = false;
+        return r;
+    };
     mark(0);
     // 1. x -> MXFP8 (and x as fp32 for hidden routing); mixed precision reads
     // x as it is, so only hidden routing needs this step
     if (!p->mixed || p->route_hidden)
-        TRY(launch_quant_x(static_cast<const __nv_bfloat16*>(x), T, D, p->xq, p->xsf, Tps, nmax_dense, p->xr, s));
+        TRY(launch_quant_x(static_cast<const __nv_bfloat16*>(x), T, D, p->xq, p->xsf, Tps, nmax_dense, p->xr, s, pdl(false)));
     mark(1);
     // 2. latent down-projection + shared gate/up
     {
@@ -749,7 +763,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
                             : EpiParams{EPI_SILU_QUANT, L / kBlockM, L, 0, nullptr, 0, p->act, p->Kcat, p->actsf, Tps, 1};
         const int items = g.m_tiles * ((T + g.n_max - 1) / g.n_max);
         shape_gemm(g, 0, items, std::min(items, p->num_sms));
-        TRY(launch_gemm(g, std::min(items, p->num_sms), s));
+        TRY(launch_gemm(g, std::min(items, p->num_sms), s, pdl(true)));
     }
     // 3. router logits, 4. top-k + gates + bitmaps
     mark(2);
@@ -775,14 +789,14 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         g.epi[0] = EpiParams{EPI_F32, 0, 0, 0, p->logits, E, nullptr, 0, nullptr, 0};
         const int items = g.m_tiles * ((T + g.n_max - 1) / g.n_max);
         shape_gemm(g, 0, items, std::min(items, p->num_sms));
-        TRY(launch_gemm(g, std::min(items, p->num_sms), s));
+        TRY(launch_gemm(g, std::min(items, p->num_sms), s, pdl(true)));
     } else if (T <= 128 && (T <= 64 ? p->rs16 : p->rs8)) {
-        TRY(launch_router_stream(p->tRS, p->tZS, p->logits, T, E, p->RK, T <= 64 ? 16 : 8, p->status, s));
+        TRY(launch_router_stream(p->tRS, p->tZS, p->logits, T, E, p->RK, T <= 64 ? 16 : 8, p->status, s, pdl(false)));
     } else {
         if (p->route_hidden)
-            TRY(launch_router(p->xr, D, 0, p->router, p->logits, T, E, D, s));
+            TRY(launch_router(p->xr, D, 0, p->router, p->logits, T, E, D, s, pdl(false)));
         else
-            TRY(launch_router(p->z, 2 * L, 0, p->router, p->logits, T, E, L, s));
+            TRY(launch_router(p->z, 2 * L, 0, p->router, p->logits, T, E, L, s, pdl(false)));
     }
     mark(3);
     {
@@ -809,12 +823,12 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         a.w = p->gw;
         a.sel = p->sel;
         a.W = W;
-        TRY(launch_topk(a, s));
+        TRY(launch_topk(a, s, pdl(false)));
     }
     // 5. per-expert prefix counts, 6. offsets + work lists
     mark(4);
     const bool fused_scan = W <= kFusedScanWords;     // small batches: one launch for scan + work lists
-    if (!fused_scan) TRY(launch_expert_scan(p->sel, E, W, p->wpre, p->counts, s));
+    if (!fused_scan) TRY(launch_expert_scan(p->sel, E, W, p->wpre, p->counts, s, pdl(false)));
     mark(5);
     {
         WorkListArgs a;
@@ -832,7 +846,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         a.ioff2 = p->ioff8;
         a.n_max2 = nmax_grp;
         a.mt2 = L / kBlockM;
-        TRY(launch_worklist(a, s));
+        TRY(launch_worklist(a, s, pdl(false)));
     }
     // 7. stable ranks, permuted rows, gather of zq
     mark(6);
@@ -857,7 +871,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         a.zq_perm_sf = p->zqpsf;
         a.perm_pitch = Rps;
         a.n_max = nmax_grp;
-        TRY(launch_scatter(a, s));
+        TRY(launch_scatter(a, s, pdl(false)));
     }
     // 8. routed gate/up + SiLU -> MXFP8
     mark(7);
@@ -880,7 +894,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         g.rows_per_e = 2 * I;
         g.epi[0] = EpiParams{EPI_SILU_QUANT, 0, 0, 0, nullptr, 0, p->hq, Ip, p->hqsf, Rps, 1};
         shape_gemm(g, E, est_experts * g.mt_per_e, p->num_sms);
-        TRY(launch_gemm(g, p->num_sms, s));
+        TRY(launch_gemm(g, p->num_sms, s, pdl(true)));
     }
     // 9. routed down -> o
     mark(8);
@@ -903,11 +917,12 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         g.rows_per_e = L;
         g.epi[0] = EpiParams{EPI_F32, 0, 0, 0, p->o, L, nullptr, 0, nullptr, 0};
         shape_gemm(g, E, est_experts * g.mt_per_e, p->num_sms);
-        TRY(launch_gemm(g, p->num_sms, s));
+        TRY(launch_gemm(g, p->num_sms, s, pdl(true)));
     }
     // 10. weighted combine -> MXFP8 into columns [0, L) of the concatenated activation
     mark(9);
-    TRY(launch_combine(p->o, p->slot_pos, p->gw, T, k, L, p->act, p->Kcat, p->actsf, Tps, nmax_dense, p->act_bf, s));
+    TRY(launch_combine(p->o, p->slot_pos, p->gw, T, k, L, p->act, p->Kcat, p->actsf, Tps, nmax_dense, p->act_bf, s,
+                       pdl(false)));
     // 11. y = [cq | h_sq] [P_up | S_down]^T
     mark(10);
     {
@@ -935,7 +950,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         g.epi[0] = EpiParams{EPI_F32, 0, 0, 0, static_cast<float*>(y), D, nullptr, 0, nullptr, 0, 0, p->out_bf16 ? 1 : 0};
         const int items = g.m_tiles * ((T + g.n_max - 1) / g.n_max);
         shape_gemm(g, 0, items, std::min(items, p->num_sms));
-        TRY(launch_gemm(g, std::min(items, p->num_sms), s));
+        TRY(launch_gemm(g, std::min(items, p->num_sms), s, pdl(true)));
     }
     mark(MOE_NUM_STAGES);
     if (err == cudaSuccess) p->last_T = T;

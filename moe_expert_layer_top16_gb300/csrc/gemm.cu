@@ -261,6 +261,7 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    pdl_trigger();
 
     if (threadIdx.x == 0) {
         for (int g = 0; g < G; ++g) {
@@ -286,6 +287,9 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
+    // everything above touches only this CTA's resources; from here on the
+    // kernel reads and writes buffers of earlier kernels
+    pdl_wait();
     if (!h.dense) {
         for (int i = threadIdx.x; i <= h.E; i += blockDim.x) {
             ioff_s[i] = p.ioff[i];
@@ -768,7 +772,7 @@ cudaError_t gemm_setup() {
     return err;
 }
 
-cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s) {
+cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s, bool pdl) {
     if (!gemm_config_ok(p.n_max, p.groups, p.ksplit, p.acc_bufs)) return cudaErrorInvalidValue;
     if (p.stages < 2 * p.groups || p.stages > kMaxStagesPerGroup * p.groups) return cudaErrorInvalidValue;
     const size_t smem = gemm_smem_bytes(p.n_max, p.stages, p.dense ? 0 : p.E, gemm_needs_xbuf(p));
@@ -778,27 +782,20 @@ cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s) {
     if (!p.dense && (p.E <= 0 || p.E > 1024)) return cudaErrorInvalidValue;
     const int set = epi_set(p);
     if (set < 0) return cudaErrorInvalidValue;
-    const int threads = (2 * p.groups + 4 * kEpiGroups) * 32;
+    const dim3 g(grid), b((2 * p.groups + 4 * kEpiGroups) * 32);
     if (p.kind == KIND_TF32) {
         if (set != SET_F32) return cudaErrorInvalidValue;
-        mx_gemm_kernel<KIND_TF32, SET_F32><<<grid, threads, smem, s>>>(p);
-    } else if (p.kind == KIND_BF16) {
-        if (set == SET_F32)
-            mx_gemm_kernel<KIND_BF16, SET_F32><<<grid, threads, smem, s>>>(p);
-        else if (set == SET_DUAL)
-            mx_gemm_kernel<KIND_BF16, SET_DUAL><<<grid, threads, smem, s>>>(p);
-        else
-            return cudaErrorInvalidValue;
-    } else if (set == SET_F32) {
-        mx_gemm_kernel<KIND_MX, SET_F32><<<grid, threads, smem, s>>>(p);
-    } else if (set == SET_QUANT) {
-        mx_gemm_kernel<KIND_MX, SET_QUANT><<<grid, threads, smem, s>>>(p);
-    } else if (set == SET_SILU) {
-        mx_gemm_kernel<KIND_MX, SET_SILU><<<grid, threads, smem, s>>>(p);
-    } else {
-        mx_gemm_kernel<KIND_MX, SET_DUAL><<<grid, threads, smem, s>>>(p);
+        return launch_ex(mx_gemm_kernel<KIND_TF32, SET_F32>, g, b, smem, s, pdl, p);
     }
-    return cudaGetLastError();
+    if (p.kind == KIND_BF16) {
+        if (set == SET_F32) return launch_ex(mx_gemm_kernel<KIND_BF16, SET_F32>, g, b, smem, s, pdl, p);
+        if (set == SET_DUAL) return launch_ex(mx_gemm_kernel<KIND_BF16, SET_DUAL>, g, b, smem, s, pdl, p);
+        return cudaErrorInvalidValue;
+    }
+    if (set == SET_F32) return launch_ex(mx_gemm_kernel<KIND_MX, SET_F32>, g, b, smem, s, pdl, p);
+    if (set == SET_QUANT) return launch_ex(mx_gemm_kernel<KIND_MX, SET_QUANT>, g, b, smem, s, pdl, p);
+    if (set == SET_SILU) return launch_ex(mx_gemm_kernel<KIND_MX, SET_SILU>, g, b, smem, s, pdl, p);
+    return launch_ex(mx_gemm_kernel<KIND_MX, SET_DUAL>, g, b, smem, s, pdl, p);
 }
 
 }  // namespace moe

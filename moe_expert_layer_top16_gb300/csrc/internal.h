@@ -7,6 +7,34 @@
 
 namespace moe {
 
+// Programmatic dependent launch.  The forward's kernels after the first are
+// launched with programmatic stream serialization (launch_ex with pdl): such
+// a kernel may start while its predecessor in the stream drains, runs its
+// prologue (barriers, TMEM allocation, descriptor prefetch), then waits in
+// pdl_wait() until the predecessor has completed and its writes are visible,
+// before it reads or writes any buffer.  Each of these kernels calls
+// pdl_trigger() when it starts, so that its successor can launch as soon as
+// every CTA of this grid is running.  Both are no-ops in a kernel launched
+// without programmatic serialization.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                             Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Device status codes (sticky; read by moe_get_device_status).
 enum : int { DEV_OK = 0, DEV_TIMEOUT_PRODUCER = 1, DEV_TIMEOUT_MMA = 2, DEV_TIMEOUT_EPILOGUE = 3,
              DEV_TIMEOUT_TEARDOWN = 4, DEV_BAD_WORK = 5 };
@@ -103,13 +131,13 @@ size_t gemm_smem_bytes(int n_max, int stages, int E, bool xbuf);
 bool gemm_needs_xbuf(const GemmParams& p);
 bool gemm_config_ok(int n_max, int groups, int ksplit, int acc_bufs);
 cudaError_t gemm_setup();   // raise the dynamic shared memory limit once
-cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s);
+cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s, bool pdl = false);
 
 // ------------------------------------------------------------------ other kernels
 // xsf: item-atom planes of a dense GEMM with token tiles of n_max
 // xf (optional): x as fp32 [T][D]
 cudaError_t launch_quant_x(const __nv_bfloat16* x, int T, int D, uint8_t* xq, uint8_t* xsf, int64_t pitch, int n_max,
-                           float* xf, cudaStream_t s);
+                           float* xf, cudaStream_t s, bool pdl = false);
 // SIMT router on z = hi + lo ([T][2L]) writing logits [T][E]; batches of at
 // most kRouterSplitTokens tokens split K kRouterSplit ways over a cluster.
 constexpr int kRouterSplit = 8;
@@ -117,7 +145,7 @@ constexpr int kRouterSplitTokens = 128;
 // z: router input rows of ld floats, K = L values, with their exact
 // remainders at offset lo (lo = 0: none); R [E][L]
 cudaError_t launch_router(const float* z, int ld, int lo, const float* R, float* logits, int T, int E, int L,
-                          cudaStream_t s);
+                          cudaStream_t s, bool pdl = false);
 // Streaming exact fp32 router for up to 128 tokens (router.cu): tmR maps R
 // [E][K] fp32 (box {32, 128}), tmZ the router input rows [T_pad][K] (box
 // {32, 64}), both with the 128-byte swizzle; K split over clusters of c = 8
@@ -126,7 +154,7 @@ bool router_stream_ok(int K);
 cudaError_t router_stream_setup();
 int router_stream_max_clusters(int c);
 cudaError_t launch_router_stream(const CUtensorMap& tmR, const CUtensorMap& tmZ, float* logits, int T, int E, int K,
-                                 int c, int* status, cudaStream_t s);
+                                 int c, int* status, cudaStream_t s, bool pdl = false);
 // top-k + gates (kernels.cu).  With refine, the logits are tensor-core
 // estimates z_hi R_hi (both rounded to TF32) and the candidates' exact fp32
 // logits are recomputed from z ([T][z_ld], hi | lo) and R ([E][L]).  The
@@ -159,8 +187,9 @@ struct TopkArgs {
 // upper bounds of the 2-norms of the rows of R [E][K] and of its TF32
 // remainders (Rs [E][2K], hi | lo): out [0, E) = |R_e|, [E, 2E) = |R_lo_e|
 cudaError_t launch_router_norms(const float* R, const float* Rs, int E, int K, float* out, cudaStream_t s);
-cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
-cudaError_t launch_expert_scan(const uint32_t* sel, int E, int W, int32_t* wpre, int32_t* counts, cudaStream_t s);
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s, bool pdl = false);
+cudaError_t launch_expert_scan(const uint32_t* sel, int E, int W, int32_t* wpre, int32_t* counts, cudaStream_t s,
+                               bool pdl = false);
 struct WorkListArgs {
     const int32_t* counts;
     int E;
@@ -175,7 +204,7 @@ struct WorkListArgs {
     int32_t* ioff1; int n_max1; int mt1;   // [E+1] item offsets of the gate/up GEMM
     int32_t* ioff2; int n_max2; int mt2;   // [E+1] item offsets of the down GEMM
 };
-cudaError_t launch_worklist(const WorkListArgs& a, cudaStream_t s);
+cudaError_t launch_worklist(const WorkListArgs& a, cudaStream_t s, bool pdl = false);
 struct ScatterArgs {
     const int32_t* idx; int T; int k; int W;
     const uint32_t* sel; const int32_t* wpre; const int32_t* offsets; const int32_t* seg;
@@ -186,12 +215,12 @@ struct ScatterArgs {
     uint8_t* zq_perm; uint8_t* zq_perm_sf; int64_t perm_pitch;   // zq_perm_sf: item-atom planes
     int n_max;                // token tile of the grouped GEMM that reads zq_perm
 };
-cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s);
+cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s, bool pdl = false);
 // out_sf: item-atom planes of a dense GEMM with token tiles of n_max
 // out_bf (optional): write c rounded to bf16 at out_bf[t * ld_q + col] instead of MXFP8
 cudaError_t launch_combine(const float* o, const int32_t* slot_pos, const float* w, int T, int k, int L,
                            uint8_t* out_q, int64_t ld_q, uint8_t* out_sf, int64_t sf_pitch, int n_max,
-                           __nv_bfloat16* out_bf, cudaStream_t s);
+                           __nv_bfloat16* out_bf, cudaStream_t s, bool pdl = false);
 cudaError_t launch_mxfp4_encode(const float* w, int64_t rows, int64_t K, uint8_t* codes, uint8_t* scales,
                                 cudaStream_t s);
 cudaError_t kernels_setup();   // per-device kernel attributes

@@ -25,6 +25,8 @@ __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b -
 constexpr int kQxTiles = 4;
 __global__ void quant_x_kernel(const __nv_bfloat16* __restrict__ x, int T, int D, uint8_t* __restrict__ xq,
                                uint8_t* __restrict__ xsf, int64_t pitch, int n_max, float* __restrict__ xf) {
+    pdl_trigger();
+    pdl_wait();
     const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     const int tiles = D / 128;
@@ -75,6 +77,8 @@ __global__ void quant_x_kernel(const __nv_bfloat16* __restrict__ x, int T, int D
 constexpr int RT = 64, RE = 64, RK = 16;
 __global__ void __launch_bounds__(256) router_kernel(const float* __restrict__ z, const float* __restrict__ R,
                                                      float* __restrict__ logits, int T, int E, int L, int ld, int lo) {
+    pdl_trigger();
+    pdl_wait();
     // z: rows of `ld` floats holding the router input (K = L) and, at offset
     // lo > 0, its exact remainder (the input is hi + lo); lo = 0: no remainder
     __shared__ float zs[RK][RT + 4];
@@ -129,6 +133,8 @@ constexpr int RC_T = 64, RC_E = 64, RC_K = 32;
 __global__ void __cluster_dims__(1, 1, kRouterSplit) __launch_bounds__(256)
     router_cluster_kernel(const float* __restrict__ z, const float* __restrict__ R, float* __restrict__ logits, int T,
                           int E, int L, int ld, int lo, int kper) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ __align__(16) float zs[RC_K][RC_T + 4];     // [k][token]
     __shared__ __align__(16) float rs[RC_K][RC_E + 4];     // [k][expert]
     __shared__ float red[RC_T * RC_E];                     // this split's partial tile [token][expert]
@@ -510,6 +516,8 @@ __device__ __forceinline__ void input_norms(const float* __restrict__ zt, int lo
 }
 
 __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(TopkArgs a) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ int s_cand[kTopkWarps][kMaxCand];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * kTopkWarps + warp;
@@ -646,6 +654,8 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(TopkArgs a) {
 constexpr int kTopkWideThreads = kMaxE;
 constexpr int kRankCap = kMaxCand + 1;
 __global__ void __launch_bounds__(kTopkWideThreads) topk_wide_kernel(TopkArgs a) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ int s_cand[kMaxE];
     __shared__ uint32_t s_ckb[kMaxE];
     __shared__ int s_rank[kRankCap];
@@ -706,6 +716,8 @@ __global__ void __launch_bounds__(kTopkWideThreads) topk_wide_kernel(TopkArgs a)
 // number of tokens < 32w that selected e; counts[e] = total.
 __global__ void expert_scan_kernel(const uint32_t* __restrict__ sel, int E, int W, int32_t* __restrict__ wpre,
                                    int32_t* __restrict__ counts) {
+    pdl_trigger();
+    pdl_wait();
     const int e = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (e >= E) return;
@@ -730,6 +742,8 @@ __global__ void expert_scan_kernel(const uint32_t* __restrict__ sel, int E, int 
 // thread e owns expert e).  Expert e contributes ceil(n_e / n_max) token tiles
 // x mt weight tiles to a GEMM; the GEMM derives each item from these tables.
 __global__ void __launch_bounds__(1024) worklist_kernel(WorkListArgs a) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ int4 warp_tot[32];
     const int E = a.E;
     const int e = threadIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -799,6 +813,8 @@ __global__ void __launch_bounds__(1024) worklist_kernel(WorkListArgs a) {
 // is the number of tokens < t that selected e (bitmap prefix + popcount), so
 // the resulting order is the stable sort of (token, slot) pairs by expert.
 __global__ void scatter_kernel(ScatterArgs a) {
+    pdl_trigger();
+    pdl_wait();
     const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (gw >= static_cast<int64_t>(a.T) * a.k) return;
@@ -855,6 +871,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(
     const float* __restrict__ o, const int32_t* __restrict__ slot_pos, const float* __restrict__ w, int T, int k,
     int L, uint8_t* __restrict__ out_q, int64_t ld_q, uint8_t* __restrict__ out_sf, int64_t sf_pitch, int n_max,
     __nv_bfloat16* __restrict__ out_bf) {
+    pdl_trigger();
+    pdl_wait();
     const int t = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __shared__ int pos_s[32];
@@ -1061,30 +1079,27 @@ __global__ void gather_rows_kernel(const uint8_t* __restrict__ src, int64_t src_
 }  // namespace
 
 cudaError_t launch_quant_x(const __nv_bfloat16* x, int T, int D, uint8_t* xq, uint8_t* xsf, int64_t pitch, int n_max,
-                           float* xf, cudaStream_t s) {
+                           float* xf, cudaStream_t s, bool pdl) {
     if (n_max <= 0) return cudaErrorInvalidValue;
     const int64_t warps = static_cast<int64_t>(T) * ((D / 128 + kQxTiles - 1) / kQxTiles);
     const int blocks = static_cast<int>((warps * 32 + 255) / 256);
-    quant_x_kernel<<<blocks, 256, 0, s>>>(x, T, D, xq, xsf, pitch, n_max, xf);
-    return cudaGetLastError();
+    return launch_ex(quant_x_kernel, dim3(blocks), dim3(256), 0, s, pdl, x, T, D, xq, xsf, pitch, n_max, xf);
 }
 
 cudaError_t launch_router(const float* z, int ld, int lo, const float* R, float* logits, int T, int E, int L,
-                          cudaStream_t s) {
+                          cudaStream_t s, bool pdl) {
     if (L % 4 || ld % 4 || lo % 4) return cudaErrorInvalidValue;
     if (T <= kRouterSplitTokens && L % RC_K == 0) {
         static_assert(RC_T * RC_E == 512 * kRouterSplit, "two reduced outputs per thread");
         const int kper = ceil_div(L / RC_K, kRouterSplit) * RC_K;
         dim3 grid((E + RC_E - 1) / RC_E, (T + RC_T - 1) / RC_T, kRouterSplit);
-        router_cluster_kernel<<<grid, 256, 0, s>>>(z, R, logits, T, E, L, ld, lo, kper);
-        return cudaGetLastError();
+        return launch_ex(router_cluster_kernel, grid, dim3(256), 0, s, pdl, z, R, logits, T, E, L, ld, lo, kper);
     }
     dim3 grid((E + RE - 1) / RE, (T + RT - 1) / RT);
-    router_kernel<<<grid, 256, 0, s>>>(z, R, logits, T, E, L, ld, lo);
-    return cudaGetLastError();
+    return launch_ex(router_kernel, grid, dim3(256), 0, s, pdl, z, R, logits, T, E, L, ld, lo);
 }
 
-cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s, bool pdl) {
     if (a.E > kMaxE || a.k > 32 || a.k < 1 || a.k > a.E) return cudaErrorInvalidValue;
     // refinement reads router rows as 16-byte vectors, 128 values per warp step
     if (a.refine && (a.L <= 0 || a.L % 128 || a.z_ld % 4 || a.z_lo % 4)) return cudaErrorInvalidValue;
@@ -1104,10 +1119,8 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
     // candidates need the exact refinement (one warp's work per token) runs a
     // warp per token, so that many tokens refine at once
     if (a.T <= kTopkWideTokens && !a.refine)
-        topk_wide_kernel<<<a.T, kTopkWideThreads, 0, s>>>(b);
-    else
-        topk_kernel<<<(a.T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, s>>>(b);
-    return cudaGetLastError();
+        return launch_ex(topk_wide_kernel, dim3(a.T), dim3(kTopkWideThreads), 0, s, pdl, b);
+    return launch_ex(topk_kernel, dim3((a.T + kTopkWarps - 1) / kTopkWarps), dim3(kTopkWarps * 32), 0, s, pdl, b);
 }
 
 cudaError_t launch_router_norms(const float* R, const float* Rs, int E, int K, float* out, cudaStream_t s) {
@@ -1116,31 +1129,28 @@ cudaError_t launch_router_norms(const float* R, const float* Rs, int E, int K, f
     return cudaGetLastError();
 }
 
-cudaError_t launch_expert_scan(const uint32_t* sel, int E, int W, int32_t* wpre, int32_t* counts, cudaStream_t s) {
-    expert_scan_kernel<<<(E * 32 + 255) / 256, 256, 0, s>>>(sel, E, W, wpre, counts);
-    return cudaGetLastError();
+cudaError_t launch_expert_scan(const uint32_t* sel, int E, int W, int32_t* wpre, int32_t* counts, cudaStream_t s,
+                               bool pdl) {
+    return launch_ex(expert_scan_kernel, dim3((E * 32 + 255) / 256), dim3(256), 0, s, pdl, sel, E, W, wpre, counts);
 }
 
-cudaError_t launch_worklist(const WorkListArgs& a, cudaStream_t s) {
+cudaError_t launch_worklist(const WorkListArgs& a, cudaStream_t s, bool pdl) {
     if (a.E > 1024) return cudaErrorInvalidValue;
-    worklist_kernel<<<1, 1024, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_ex(worklist_kernel, dim3(1), dim3(1024), 0, s, pdl, a);
 }
 
-cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s) {
+cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s, bool pdl) {
     const int64_t warps = static_cast<int64_t>(a.T) * a.k;
-    scatter_kernel<<<static_cast<int>((warps * 32 + 255) / 256), 256, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_ex(scatter_kernel, dim3(static_cast<int>((warps * 32 + 255) / 256)), dim3(256), 0, s, pdl, a);
 }
 
 cudaError_t launch_combine(const float* o, const int32_t* slot_pos, const float* w, int T, int k, int L,
                            uint8_t* out_q, int64_t ld_q, uint8_t* out_sf, int64_t sf_pitch, int n_max,
-                           __nv_bfloat16* out_bf, cudaStream_t s) {
+                           __nv_bfloat16* out_bf, cudaStream_t s, bool pdl) {
     if (n_max <= 0) return cudaErrorInvalidValue;
     dim3 grid(T, (L / 32 + kCombineWarps - 1) / kCombineWarps);
-    combine_kernel<<<grid, kCombineWarps * 32, 0, s>>>(o, slot_pos, w, T, k, L, out_q, ld_q, out_sf, sf_pitch, n_max,
-                                                       out_bf);
-    return cudaGetLastError();
+    return launch_ex(combine_kernel, grid, dim3(kCombineWarps * 32), 0, s, pdl, o, slot_pos, w, T, k, L, out_q, ld_q,
+                     out_sf, sf_pitch, n_max, out_bf);
 }
 
 cudaError_t launch_mxfp4_encode(const float* w, int64_t rows, int64_t K, uint8_t* codes, uint8_t* scales,

@@ -122,6 +122,7 @@ __global__ void __launch_bounds__((kRsWarps + 1) * 32, 1) router_stream_kernel(c
     const int cb = chunks * rank / c, ce = chunks * (rank + 1) / c;
     const int n = ce - cb;
     const int S = n < kRsStages ? n : kRsStages;
+    pdl_trigger();
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRsStages; ++s) {
             mbar_init(&full[s], 1);
@@ -134,6 +135,7 @@ __global__ void __launch_bounds__((kRsWarps + 1) * 32, 1) router_stream_kernel(c
         prefetch_tmap(&p.tmZ);
     }
     __syncthreads();
+    pdl_wait();         // the router input and the logits belong to the kernels around this one
     // peers may copy into this CTA only once its barriers exist: arrive now,
     // wait just before the copies
     cluster_arrive();
@@ -267,7 +269,7 @@ int router_stream_max_clusters(int c) {
 }
 
 cudaError_t launch_router_stream(const CUtensorMap& tmR, const CUtensorMap& tmZ, float* logits, int T, int E, int K,
-                                 int c, int* status, cudaStream_t s) {
+                                 int c, int* status, cudaStream_t s, bool pdl) {
     if (T < 1 || T > 2 * kRsT || E < 1 || (c != 8 && c != 16) || !router_stream_ok(K)) return cudaErrorInvalidValue;
     RouterStreamParams prm;
     prm.tmR = tmR;
@@ -282,13 +284,15 @@ cudaError_t launch_router_stream(const CUtensorMap& tmR, const CUtensorMap& tmZ,
     cfg.blockDim = dim3((kRsWarps + 1) * 32, 1, 1);
     cfg.dynamicSmemBytes = kRsSmem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = c;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, router_stream_kernel, prm);
 }
 
