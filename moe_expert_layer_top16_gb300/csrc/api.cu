@@ -37,6 +37,11 @@ namespace {
 // mbarrier transaction: the packed size (128 rows x 64 B).  In shared memory
 // the box occupies 16 KB -- each 16-byte chunk holds 8 bytes of packed
 // elements and an 8-byte gap that the copy leaves unwritten.
+// A single-group GEMM (wide items) issues its token-side copies from a warp
+// of their own.
+#ifndef MOE_B_PRODUCER
+#define MOE_B_PRODUCER 1
+#endif
 #ifndef MOE_A_TX_BYTES
 #define MOE_A_TX_BYTES 8192
 #endif
@@ -357,6 +362,7 @@ void shape_gemm(GemmParams& g, int E, int64_t est_items, int grid) {
             g.acc_bufs = NB;
             g.stages = S;
             g.contiguous = narrow ? 1 : 0;
+            g.b_producer = (G == 1 && MOE_B_PRODUCER) ? 1 : 0;
             return;
         }
     }

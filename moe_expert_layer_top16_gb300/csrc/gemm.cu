@@ -57,7 +57,7 @@ struct Item {
 // them from the parameter space would repeat after every asm statement that
 // clobbers memory).
 struct Hot {
-    int KT, n_max, stage_bytes, a_tx_bytes, kseg_tiles, b_box, b_row1;
+    int KT, n_max, stage_bytes, a_tx_bytes, kseg_tiles, b_box, b_row1, b_producer;
     int dense, m_tiles, n_tokens, a_rows, b_rows, E, mt_per_e, rows_per_e, epi_split;
     int ax0, ax1, ax2, bx0, bx1, bx2;
     int64_t sfb_pitch;
@@ -75,6 +75,7 @@ __device__ __forceinline__ Hot load_hot(const GemmParams& p) {
     h.kseg_tiles = pin(p.kseg_tiles);
     h.b_box = pin(p.b_box);
     h.b_row1 = pin(p.b_row1);
+    h.b_producer = pin(p.b_producer);
     h.dense = pin(p.dense);
     h.m_tiles = pin(p.m_tiles);
     h.n_tokens = pin(p.n_tokens);
@@ -363,18 +364,21 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                 if (elect_one()) {
                     mbar_arrive_expect_tx(&fullg[stage], tx);
                     tma_load_2d(sb, &p.tmA, &fullg[stage], ax, w.a_row0);
-                    if (row_loads) {
-                        for (int r = 0; r < w.n; ++r)
-                            tma_load_2d(sb + L.offB + r * kBlockK, &p.tmB1, &fullg[stage], bx, w.b_row0 + r);
-                    } else {
-                        for (int c = 0; c < nbox; ++c)
-                            tma_load_2d(sb + L.offB + c * h.b_box * kBlockK, &p.tmB, &fullg[stage], bx,
-                                        w.b_row0 + c * h.b_box);
+                    if (!h.b_producer) {
+                        if (row_loads) {
+                            for (int r = 0; r < w.n; ++r)
+                                tma_load_2d(sb + L.offB + r * kBlockK, &p.tmB1, &fullg[stage], bx, w.b_row0 + r);
+                        } else {
+                            for (int c = 0; c < nbox; ++c)
+                                tma_load_2d(sb + L.offB + c * h.b_box * kBlockK, &p.tmB, &fullg[stage], bx,
+                                            w.b_row0 + c * h.b_box);
+                        }
                     }
                     if constexpr (kMX) {
                         bulk_load(sb + L.offSFA, sfa_tile + static_cast<size_t>(kt) * 512, 512, &fullg[stage]);
-                        bulk_load(sb + L.offSFB, h.sfb + (static_cast<size_t>(kt) * h.sfb_pitch + w.b_row0) * 16,
-                                  sfb_bytes, &fullg[stage]);
+                        if (!h.b_producer)
+                            bulk_load(sb + L.offSFB, h.sfb + (static_cast<size_t>(kt) * h.sfb_pitch + w.b_row0) * 16,
+                                      sfb_bytes, &fullg[stage]);
                     }
                 }
                 __syncwarp();
@@ -698,6 +702,63 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                 }
             }
         }
+    } else if (h.b_producer && warp == 2 * G + 4 * kEpiGroups) {
+        // ------------------------------------------------------------ token-side producer (groups == 1)
+        // Follows producer 0 stage by stage: the same items and K tiles, the
+        // same free stages; it issues the token rows and their scales, whose
+        // bytes producer 0 has counted on the stage barrier (or is about to:
+        // a barrier's byte count may dip below zero meanwhile, and the phase
+        // cannot complete before producer 0 has arrived).
+        const int S = S_all;
+        uint32_t stage = 0, phase = 0;
+        uint32_t issued = 0, issued_parity = 0;
+        bool ok = true;
+        int ecur = -1;
+        for (int it = it_begin; ok && it < it_end; it += it_step) {
+            const Item w = get_item(h, it, ioff_s, seg_s, cnt_s, ecur);
+            if (w.n <= 0) continue;
+            const int nm = (w.n + 15) & ~15;
+            const int natoms = (nm + 127) / 128;
+            const int nbox = (nm + h.b_box - 1) / h.b_box;
+            const bool row_loads = kMX && h.b_row1 && w.n < 16;
+            const uint32_t sfb_bytes = (w.n <= 32) ? static_cast<uint32_t>(w.n * 16) : static_cast<uint32_t>(natoms * 512);
+            for (int kt = 0; kt < h.KT; ++kt) {
+                ok = mbar_wait(&empty[stage], phase ^ 1, abort_flag, h.status, DEV_TIMEOUT_PRODUCER);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
+                const int sg = kt / h.kseg_tiles;
+                const int kin = (kt - sg * h.kseg_tiles) * kTileElems;
+                const int bx = (sg == 0 ? h.bx0 : (sg == 1 ? h.bx1 : h.bx2)) + kin;
+                uint8_t* sb = base + stage * h.stage_bytes;
+                if (elect_one()) {
+                    if (row_loads) {
+                        for (int r = 0; r < w.n; ++r)
+                            tma_load_2d(sb + L.offB + r * kBlockK, &p.tmB1, &full[stage], bx, w.b_row0 + r);
+                    } else {
+                        for (int c = 0; c < nbox; ++c)
+                            tma_load_2d(sb + L.offB + c * h.b_box * kBlockK, &p.tmB, &full[stage], bx,
+                                        w.b_row0 + c * h.b_box);
+                    }
+                    if constexpr (kMX)
+                        bulk_load(sb + L.offSFB, h.sfb + (static_cast<size_t>(kt) * h.sfb_pitch + w.b_row0) * 16,
+                                  sfb_bytes, &full[stage]);
+                }
+                __syncwarp();
+                issued |= 1u << stage;
+                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == static_cast<uint32_t>(S)) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        if (*abort_flag && lane == 0) {
+            for (int s = 0; s < S; ++s)
+                if (issued & (1u << s)) mbar_wait_teardown(&full[s], (issued_parity >> s) & 1u, h.status);
+        }
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -782,7 +843,8 @@ cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s, bool pdl)
     if (!p.dense && (p.E <= 0 || p.E > 1024)) return cudaErrorInvalidValue;
     const int set = epi_set(p);
     if (set < 0) return cudaErrorInvalidValue;
-    const dim3 g(grid), b((2 * p.groups + 4 * kEpiGroups) * 32);
+    if (p.b_producer && p.groups != 1) return cudaErrorInvalidValue;
+    const dim3 g(grid), b((2 * p.groups + 4 * kEpiGroups + (p.b_producer ? 1 : 0)) * 32);
     if (p.kind == KIND_TF32) {
         if (set != SET_F32) return cudaErrorInvalidValue;
         return launch_ex(mx_gemm_kernel<KIND_TF32, SET_F32>, g, b, smem, s, pdl, p);

@@ -86,6 +86,7 @@ struct GemmParams {
     CUtensorMap tmB;        // MX: MXFP8 activations, UINT8, box {128, 16}; TF32: fp32, box {32, 16}
     CUtensorMap tmB1;       // MX, b_row1 != 0: the same activations with a one-row box {128, 1}
     int b_row1;             // items of fewer than 16 tokens load only their own rows (tmB1) and scale slots
+    int b_producer;         // groups == 1: a warp of its own issues the token-side copies (B rows, their scales)
     const uint8_t* sfa;     // weight scales, pre-arranged: [rows/128][KT][512]
     const uint8_t* sfb;     // activation scales, item-atom planes: [KT][sfb_pitch] 16-byte slots
     int64_t sfb_pitch;

@@ -240,8 +240,14 @@ __global__ void __cluster_dims__(1, 1, kRouterSplit) __launch_bounds__(256)
 // remaining key, the lower expert id on a tie.
 // Gates: sigmoid(l_j) / sum over the winners (fp32), or softmax over the
 // winners' logits.  Each selection sets bit t of the expert's token bitmap.
-constexpr int kTopkWarps = 4;
-constexpr int kTopkWideTokens = 512;  // batches up to this size use one CTA per token (without refinement)
+#ifndef MOE_TOPK_WARPS
+#define MOE_TOPK_WARPS 4
+#endif
+#ifndef MOE_TOPK_WIDE_TOKENS
+#define MOE_TOPK_WIDE_TOKENS 512
+#endif
+constexpr int kTopkWarps = MOE_TOPK_WARPS;            // tokens (one warp each) per CTA of topk_kernel
+constexpr int kTopkWideTokens = MOE_TOPK_WIDE_TOKENS;  // batches up to this size use one CTA per token (without refinement)
 constexpr int kTopkPerLane = 32;     // E <= 1024
 constexpr int kMaxE = 32 * kTopkPerLane;
 constexpr int kMaxCand = 64;         // candidates ranked exactly per token (two per lane); more: exact pass over all
