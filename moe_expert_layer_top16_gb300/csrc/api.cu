@@ -42,6 +42,10 @@ namespace {
 #ifndef MOE_B_PRODUCER
 #define MOE_B_PRODUCER 1
 #endif
+// K-splits of the grouped GEMMs' narrow items (0: chosen from the items per CTA).
+#ifndef MOE_GROUPED_NARROW_KS
+#define MOE_GROUPED_NARROW_KS 0
+#endif
 #ifndef MOE_A_TX_BYTES
 #define MOE_A_TX_BYTES 8192
 #endif
@@ -341,9 +345,11 @@ int item_cap(int T) { return T <= 256 ? 48 : kNMax; }
 // Wide items (prefill) run one group with two accumulators: the tensor pipe
 // is busy for a whole item and the epilogue overlaps the next one.  Narrow
 // items are issue-bound, so four groups run side by side: as four item lanes
-// when each CTA has enough items, else as K-splits of fewer items (each
-// split keeping at least 4 K tiles); a CTA then takes a contiguous range of
-// items, so that successive items mostly belong to one expert.
+// when each CTA has 16 items or more, else as K-splits of fewer items (each
+// split keeping at least 4 K tiles; two splits with 2..15 items per CTA
+// measured faster than four lanes at 8 tokens); a CTA then takes a
+// contiguous range of items, so that successive items mostly belong to one
+// expert.
 void shape_gemm(GemmParams& g, int E, int64_t est_items, int grid) {
     const bool narrow = g.n_max <= kNarrowMax;
     const bool xbuf = gemm_needs_xbuf(g);     // the output modes must be set before shaping
@@ -351,7 +357,8 @@ void shape_gemm(GemmParams& g, int E, int64_t est_items, int grid) {
     int ks_max = 1;
     while (ks_max < 4 && g.KT >= 8 * ks_max) ks_max *= 2;
     for (int G = narrow ? 4 : 1; G >= 1; G >>= 1) {
-        int KS = per_cta >= 4 ? 1 : (per_cta >= 2 ? 2 : 4);
+        int KS = per_cta >= 16 ? 1 : (per_cta >= 2 ? 2 : 4);
+        if (E > 0 && narrow && MOE_GROUPED_NARROW_KS > 0) KS = MOE_GROUPED_NARROW_KS;
         KS = std::min(std::min(KS, ks_max), G);
         for (int NB = 2; NB >= 1; --NB) {
             if (!gemm_config_ok(g.n_max, G, KS, NB)) continue;

@@ -554,7 +554,40 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
             E.sf_item = second ? E1.sf_item : E0.sf_item;
             E.out_bf16 = second ? E1.out_bf16 : E0.out_bf16;
             const int rel_mt = w.mt - E.m_tile0;
-            for (int n0 = n_first; n0 < nm; n0 += n_step) {
+            bool stored = false;
+            if constexpr (SET == SET_F32) {
+              if (KS == 1 && !E.out_bf16 && E.f32_split == 0) {
+                stored = true;
+                // fp32 output of one accumulator: the next chunk's TMEM load is
+                // in flight while this chunk is stored
+                const uint32_t a0 = tmem + t_lane + static_cast<uint32_t>(g0) * cols_per_group +
+                                    acc * static_cast<uint32_t>(h.n_max);
+                const int64_t col = E.col0 + static_cast<int64_t>(rel_mt) * 128 + 32 * q + lane;
+                uint32_t cur[16], nxt[16];
+                if (n_first < nm) {
+                    tmem_ld16_async(a0 + static_cast<uint32_t>(n_first), cur);
+                    tmem_wait16(cur);
+                }
+                for (int n0 = n_first; n0 < nm; n0 += n_step) {
+                    const bool more = n0 + n_step < nm;
+                    if (more) tmem_ld16_async(a0 + static_cast<uint32_t>(n0 + n_step), nxt);
+                    const int nv = min(16, w.n - n0);
+                    float* o = E.out_f32 + (w.b_row0 + n0) * E.ld_f32 + col;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        if (i >= nv) break;
+                        o[0] = __uint_as_float(cur[i]);
+                        o += E.ld_f32;
+                    }
+                    if (more) {
+                        tmem_wait16(nxt);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) cur[i] = nxt[i];
+                    }
+                }
+              }
+            }
+            for (int n0 = n_first; n0 < (stored ? n_first : nm); n0 += n_step) {
                 // sum of the K-split partial accumulators, in group order
                 float v[16];
                 bool first = true;
