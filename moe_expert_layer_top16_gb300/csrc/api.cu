@@ -46,6 +46,16 @@ namespace {
 #ifndef MOE_GROUPED_NARROW_KS
 #define MOE_GROUPED_NARROW_KS 0
 #endif
+// From this many tokens on, the shared experts' gate/up (the weight tiles of
+// step 2 after the latent projection) runs on a stream of its own beside the
+// routing steps, which leave the tensor cores idle; SMs kept free of it for
+// the routing kernels.
+#ifndef MOE_SPLIT_A2_TOKENS
+#define MOE_SPLIT_A2_TOKENS 2048
+#endif
+#ifndef MOE_SPLIT_A2_FREE_SMS
+#define MOE_SPLIT_A2_FREE_SMS 8
+#endif
 #ifndef MOE_A_TX_BYTES
 #define MOE_A_TX_BYTES 8192
 #endif
@@ -204,6 +214,10 @@ struct Plan {
     // and which cluster sizes this device schedules
     CUtensorMap tRS, tZS;
     bool rs16 = false, rs8 = false;
+    // large batches: the shared experts' part of step 2 runs on a stream of
+    // the plan's own, beside the routing steps (fork / join events)
+    cudaStream_t side = nullptr;
+    cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
 };
 
 template <typename T>
@@ -231,6 +245,9 @@ void plan_release(Plan* p) {
     cudaSetDevice(p->device);
     cudaDeviceSynchronize();
     for (void* a : p->allocs) cudaFree(a);
+    if (p->ev_fork) cudaEventDestroy(p->ev_fork);
+    if (p->ev_join) cudaEventDestroy(p->ev_join);
+    if (p->side) cudaStreamDestroy(p->side);
     cudaSetDevice(cur);
     delete p;
 }
@@ -652,6 +669,10 @@ moe_status moe_plan(const moe_config* cfg, const moe_weights* w, int device, voi
         p->rs16 = router_stream_max_clusters(16) > 0;
         p->rs8 = router_stream_max_clusters(8) > 0;
     }
+    if (ok && p->T_max >= MOE_SPLIT_A2_TOKENS && !mixed)
+        ok = cudaStreamCreateWithFlags(&p->side, cudaStreamNonBlocking) == cudaSuccess &&
+             cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming) == cudaSuccess;
     if (!ok) {
         plan_release(p);
         return MOE_ERR_CUDA;
@@ -713,6 +734,12 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
     // above 128 tokens the router logits are tensor-core estimates from z split
     // into TF32 head + remainder; smaller batches keep z plain
     const bool z_split = p->tc_router && T > 128;
+    // large batches run the shared experts' gate/up (the tiles of step 2 after
+    // the latent projection) on the side stream, beside the routing steps --
+    // not while per-stage events are recorded, which time the steps one by one
+    const bool split_a2 = p->side != nullptr && T >= MOE_SPLIT_A2_TOKENS && !(dbg && dbg->stage_events);
+    GemmParams a2s;
+    int a2s_grid = 0;
     cudaError_t err = cudaSuccess;
 #define TRY(x)                          \
     do {                                \
@@ -765,7 +792,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
             g.sfb = nullptr;
         }
         g.dense = 1;
-        g.m_tiles = p->rowsA2 / kBlockM;
+        g.m_tiles = split_a2 ? L / kBlockM : p->rowsA2 / kBlockM;
         g.n_tokens = T;
         g.epi_split = L / kBlockM;
         // z rows hold L values; the TF32 router estimate also wants them split
@@ -774,6 +801,15 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         g.epi[1] = p->mixed ? EpiParams{EPI_SILU_BF16, L / kBlockM, L, 0, nullptr, 0,
                                         reinterpret_cast<uint8_t*>(p->act_bf), p->Kcat, nullptr, 0, 0}
                             : EpiParams{EPI_SILU_QUANT, L / kBlockM, L, 0, nullptr, 0, p->act, p->Kcat, p->actsf, Tps, 1};
+        if (split_a2) {
+            // the shared experts' tiles, launched on the side stream after the router
+            a2s = g;
+            a2s.mt_base = L / kBlockM;
+            a2s.m_tiles = p->rowsA2 / kBlockM - L / kBlockM;
+            const int items_s = a2s.m_tiles * ((T + a2s.n_max - 1) / a2s.n_max);
+            a2s_grid = std::max(1, std::min(items_s, p->num_sms - MOE_SPLIT_A2_FREE_SMS));
+            shape_gemm(a2s, 0, items_s, a2s_grid);
+        }
         const int items = g.m_tiles * ((T + g.n_max - 1) / g.n_max);
         shape_gemm(g, 0, items, std::min(items, p->num_sms));
         TRY(launch_gemm(g, std::min(items, p->num_sms), s, pdl(true)));
@@ -810,6 +846,12 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
             TRY(launch_router(p->xr, D, 0, p->router, p->logits, T, E, D, s, pdl(false)));
         else
             TRY(launch_router(p->z, 2 * L, 0, p->router, p->logits, T, E, L, s, pdl(false)));
+    }
+    if (split_a2) {
+        TRY(cudaEventRecord(p->ev_fork, s));
+        TRY(cudaStreamWaitEvent(p->side, p->ev_fork, 0));
+        TRY(launch_gemm(a2s, a2s_grid, p->side, false));
+        TRY(cudaEventRecord(p->ev_join, p->side));
     }
     mark(3);
     {
@@ -938,6 +980,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
                        pdl(false)));
     // 11. y = [cq | h_sq] [P_up | S_down]^T
     mark(10);
+    if (split_a2) TRY(cudaStreamWaitEvent(s, p->ev_join, 0));
     {
         GemmParams g = gemm_base(p->tA10, p->tB10, p->a10sf, p->actsf, Tps, p->Kcat, nmax_dense, D,
                                  static_cast<int>(Tp), p->status);
@@ -963,7 +1006,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         g.epi[0] = EpiParams{EPI_F32, 0, 0, 0, static_cast<float*>(y), D, nullptr, 0, nullptr, 0, 0, p->out_bf16 ? 1 : 0};
         const int items = g.m_tiles * ((T + g.n_max - 1) / g.n_max);
         shape_gemm(g, 0, items, std::min(items, p->num_sms));
-        TRY(launch_gemm(g, std::min(items, p->num_sms), s, pdl(true)));
+        TRY(launch_gemm(g, std::min(items, p->num_sms), s, split_a2 ? false : pdl(true)));
     }
     mark(MOE_NUM_STAGES);
     if (err == cudaSuccess) p->last_T = T;

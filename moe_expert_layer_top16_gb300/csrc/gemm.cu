@@ -58,7 +58,7 @@ struct Item {
 // clobbers memory).
 struct Hot {
     int KT, n_max, stage_bytes, a_tx_bytes, kseg_tiles, b_box, b_row1, b_producer;
-    int dense, m_tiles, n_tokens, a_rows, b_rows, E, mt_per_e, rows_per_e, epi_split;
+    int dense, m_tiles, mt_base, n_tokens, a_rows, b_rows, E, mt_per_e, rows_per_e, epi_split;
     int ax0, ax1, ax2, bx0, bx1, bx2;
     int64_t sfb_pitch;
     const uint8_t* sfa;
@@ -78,6 +78,7 @@ __device__ __forceinline__ Hot load_hot(const GemmParams& p) {
     h.b_producer = pin(p.b_producer);
     h.dense = pin(p.dense);
     h.m_tiles = pin(p.m_tiles);
+    h.mt_base = pin(p.mt_base);
     h.n_tokens = pin(p.n_tokens);
     h.a_rows = pin(p.a_rows);
     h.b_rows = pin(p.b_rows);
@@ -122,7 +123,7 @@ __device__ __forceinline__ Item get_item(const Hot& h, int it, const int* ioff, 
                                          int& e) {
     Item w;
     if (h.dense) {
-        const int mt = it % h.m_tiles;
+        const int mt = h.mt_base + it % h.m_tiles;
         const int nt = it / h.m_tiles;
         w.a_row0 = mt * kBlockM;
         w.b_row0 = nt * h.n_max;
@@ -836,15 +837,19 @@ cudaError_t raise_smem() {
     return cudaFuncSetAttribute(mx_gemm_kernel<KIND, SET>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
 }
 
-// The kernel instance whose epilogue covers the launch's output modes.
+// The kernel instance whose epilogue covers the launch's output modes: those
+// of epi[0] (weight tiles below epi_split) and epi[1] (from epi_split on)
+// that the launch's tiles use.
 int epi_set(const GemmParams& p) {
-    const int m0 = p.epi[0].mode;
-    const bool two = p.dense && p.epi_split < p.m_tiles;
-    const int m1 = two ? p.epi[1].mode : m0;
-    const bool s0 = m0 == EPI_SILU_QUANT || m0 == EPI_SILU_BF16, s1 = m1 == EPI_SILU_QUANT || m1 == EPI_SILU_BF16;
-    if (!s0 && !s1) return (m0 == EPI_QUANT || m1 == EPI_QUANT) ? SET_QUANT : SET_F32;
-    if (s0 && s1) return SET_SILU;
-    if (s1) return SET_DUAL;
+    const bool use0 = !p.dense || p.epi_split > p.mt_base;
+    const bool use1 = p.dense && p.epi_split < p.mt_base + p.m_tiles;
+    const int m0 = p.epi[0].mode, m1 = p.epi[1].mode;
+    const bool silu0 = m0 == EPI_SILU_QUANT || m0 == EPI_SILU_BF16, silu1 = m1 == EPI_SILU_QUANT || m1 == EPI_SILU_BF16;
+    const bool s0 = use0 && silu0, s1 = use1 && silu1;          // SiLU outputs in use
+    const bool n0 = use0 && !silu0, n1 = use1 && !silu1;        // other outputs in use
+    if (!s0 && !s1) return ((n0 && m0 == EPI_QUANT) || (n1 && m1 == EPI_QUANT)) ? SET_QUANT : SET_F32;
+    if (!n0 && !n1) return SET_SILU;
+    if (s1 && n0 && !s0 && !n1) return SET_DUAL;
     return -1;
 }
 
@@ -877,6 +882,7 @@ cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s, bool pdl)
     const int set = epi_set(p);
     if (set < 0) return cudaErrorInvalidValue;
     if (p.b_producer && p.groups != 1) return cudaErrorInvalidValue;
+    if (p.dense && (p.mt_base < 0 || (p.mt_base + p.m_tiles) * kBlockM > p.a_rows)) return cudaErrorInvalidValue;
     const dim3 g(grid), b((2 * p.groups + 4 * kEpiGroups + (p.b_producer ? 1 : 0)) * 32);
     if (p.kind == KIND_TF32) {
         if (set != SET_F32) return cudaErrorInvalidValue;

@@ -102,6 +102,7 @@ struct GemmParams {
     int a_tx_bytes;         // bytes a 128x128 MXFP4 TMA box delivers to the mbarrier
     int dense;              // 1: items = m_tiles x ceil(n_tokens / n_max); 0: item list
     int m_tiles;
+    int mt_base;            // dense: the first of the m_tiles weight tiles (row block mt_base + i)
     int n_tokens;
     int a_rows;             // rows of A (bounds check of list items)
     int b_rows;             // rows of B / scale planes (bounds check)
