@@ -686,24 +686,15 @@ def run_sweep(args, wl, rank, local):
     for T in synth.SWEEP_TOKENS:
         x = synth.hidden_states(wl, T, device=dev)
         y = torch.empty(T, wl.d_model, dtype=plan.out_dtype, device=dev)
-        counts = torch.zeros(wl.n_experts, dtype=torch.int32, device=dev)
-        for i in range(args.warmup):
-            plan.forward(x, out=y, debug={"counts": counts} if i == 0 else None)
-        torch.cuda.synchronize()
         steps = max(5, min(args.steps, (200 * 64) // T))
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-        for i in range(steps):
-            flush.fill_(float(i))
-            ev[i][0].record()
-            plan.forward(x, out=y)
-            ev[i][1].record()
-        torch.cuda.synchronize()
-        if plan.device_status() != moe.MOE_OK:
-            raise RuntimeError(f"device-side error at T={T}")
-        ms = float(np.median([a.elapsed_time(b) for a, b in ev]))
-        work, touched, expert_bytes = algorithmic_work(wl, T, counts.cpu().numpy())
+        # the same timing as the headline: graph replay, L2 flushed between steps
+        step_ms, _, counts_h, _, _, eager_ms = time_layer(plan, wl, T, x, y, flush, steps, max(args.warmup, 3), 1,
+                                                          with_stages=False, graph=not args.eager)
+        ms = float(np.median(step_ms))
+        work, touched, expert_bytes = algorithmic_work(wl, T, counts_h)
         flops = sum(f for _, f in work.values())
-        line = {"impl": "sweep", "workload": wl.name, "tokens": T, "ms_median": ms, "tokens_per_s": T / (ms / 1e3),
+        line = {"impl": "sweep", "workload": wl.name, "tokens": T, "ms_median": ms, "eager_ms_median": eager_ms,
+                "tokens_per_s": T / (ms / 1e3),
                 "touched_experts": touched, "expert_weight_GBps": expert_bytes / (ms / 1e3) / 1e9,
                 "expert_weight_frac_hbm": expert_bytes / (ms / 1e3) / 1e9 / hbm,
                 "mx_tflops": flops / (ms / 1e3) / 1e12, "mx_frac_tensor_peak": flops / (ms / 1e3) / 1e12 / tensor_peak,
