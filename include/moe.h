@@ -189,7 +189,11 @@ MOE_API moe_status moe_plan(const moe_config *cfg, const moe_weights *w, int dev
  * (device; fp32 or bf16 as cfg->out_dtype says).  Enqueued on `stream` (a cudaStream_t; NULL = legacy
  * default stream); no host synchronisation, no allocation.  1 <= T <=
  * max_tokens.  `dbg` may be NULL.  One plan serves one stream at a time:
- * calls on different streams that overlap race on the plan's workspace. */
+ * calls on different streams that overlap race on the plan's workspace.
+ * From 2048 tokens on, the shared experts' first GEMM runs on a stream the
+ * plan owns, forked from `stream` by an event and joined back into it
+ * before the last step, so the call stays one unit of work on `stream`
+ * (and can be captured in a CUDA graph). */
 MOE_API moe_status moe_forward(void *plan, const void *x, int32_t T, void *y, void *stream,
                        const moe_debug *dbg);
 

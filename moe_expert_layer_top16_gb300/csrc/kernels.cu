@@ -229,13 +229,14 @@ __global__ void __cluster_dims__(1, 1, kRouterSplit) __launch_bounds__(256)
 // When the logits are approximate (tensor-core router) or keys need fp64,
 // candidates are picked on the estimates.  Each key estimate k_e has a proven
 // error bound d_e (the per-(token, expert) bound of TopkArgs for estimated
-// logits, a quarter of it plus kKeyErr for sigmoid(l) + b, kKeyErr alone for
-// exact logits with a bias), so the exact key lies in [k_e - d_e, k_e + d_e].
+// logits; for sigmoid(l) + b that bound times the largest slope of sigmoid
+// over the logit's interval, plus kKeyErr; kKeyErr alone for exact logits
+// with a bias), so the exact key lies in [k_e - d_e, k_e + d_e].
 // With theta = the k-th largest lower end, k experts have an exact key >=
 // theta, and an expert whose upper end is below theta cannot be in the exact
 // top-k: the candidates are the experts with k_e + d_e >= theta.  Their exact
 // fp32 logits (recomputed from z and R when the logits were approximate) and
-// keys give the final ranking; with more than 32 candidates every expert's
+// keys give the final ranking; with more than 64 candidates every expert's
 // logit and key are evaluated exactly instead.  Rounds take the largest
 // remaining key, the lower expert id on a tie.
 // Gates: sigmoid(l_j) / sum over the winners (fp32), or softmax over the
@@ -258,6 +259,23 @@ constexpr int kMaxCand = 64;         // candidates ranked exactly per token (two
 // the two additions add a few units of 2^-24.  Larger biases add |b| 2^-22
 // (TopkArgs::bias_absmax).
 constexpr float kKeyErr = 4.0e-6f;
+
+// An upper bound of the slope sigmoid'(x) = sigmoid(x) (1 - sigmoid(x)) over
+// [l - d, l + d], so that |sigmoid(l) - sigmoid(l')| <= bound * d for every l'
+// in the interval (mean value theorem): 1/4 when the interval holds 0, else
+// sigmoid'(m) <= 1 - sigmoid(m) = 1 / (1 + e^m) at the distance m of the
+// interval from 0 (sigmoid' falls with |x|).  e^m comes from __expf, lowered
+// by its documented error (2 + floor(1.173 m) units in the last place); every
+// step rounds toward the safe side.
+__device__ __forceinline__ float sigmoid_slope_ub(float l, float d) {
+    const float lo = __fsub_rd(l, d), hi = __fadd_ru(l, d);
+    if (!(lo > 0.0f || hi < 0.0f)) return 0.25f;          // holds 0 (or NaN)
+    const float m = lo > 0.0f ? lo : -hi;                 // > 0
+    const float rel = __fmul_ru(__fadd_ru(3.0f, __fmul_ru(1.174f, m)), 0x1p-23f);
+    const float e_lo = __fmul_rd(__expf(m), __fsub_rd(1.0f, rel));
+    const float s = __frcp_ru(__fadd_rd(1.0f, fmaxf(e_lo, 0.0f)));
+    return fminf(fmaxf(s, 0x1p-126f), 0.25f);
+}
 
 // Keys as unsigned integers that order like the floats (larger key, larger
 // integer; -inf above every "no entry" value 0), so that a selection round
@@ -567,8 +585,9 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(TopkArgs a) {
         return;
     }
     // error bound of each key estimate: d_e = A |R_lo_e| + B |R_e| for
-    // tensor-core logit estimates (TopkArgs), a quarter of it through the
-    // sigmoid, plus kKeyErr for the fp32 evaluation of sigmoid(l) + b
+    // tensor-core logit estimates (TopkArgs), times the largest slope of the
+    // sigmoid over [l - d_e, l + d_e] (sigmoid_slope_ub), plus kKeyErr for
+    // the fp32 evaluation of sigmoid(l) + b
     float A = 0.0f, B = 0.0f;
     if (approx) {
         float nhi, nlo;
@@ -582,7 +601,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(TopkArgs a) {
         d = approx ? __fmaf_ru(A, a.rnorm[E + e], __fmul_ru(B, a.rnorm[e])) : 0.0f;
         if (use_bias) {
             kv = 1.0f / (1.0f + __expf(-lv)) + bias[e];
-            d = __fmaf_ru(0.25f, d, a.key_err);
+            d = __fmaf_ru(sigmoid_slope_ub(lv, d), d, a.key_err);
         } else {
             kv = lv;
         }
