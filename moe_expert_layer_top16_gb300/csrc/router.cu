@@ -33,7 +33,14 @@ namespace {
 constexpr int kRsE = 128;                  // experts per tile
 constexpr int kRsT = 64;                   // tokens per tile
 constexpr int kRsKC = 32;                  // K per chunk (one 128-byte row of fp32)
-constexpr int kRsWarps = 8;                // compute warps; warp kRsWarps produces
+#ifndef MOE_RS_WARPS
+#define MOE_RS_WARPS 16
+#endif
+#ifndef MOE_RS_UNROLL
+#define MOE_RS_UNROLL 8
+#endif
+constexpr int kRsWarps = MOE_RS_WARPS;     // compute warps; warp kRsWarps produces
+constexpr int kRsUnroll = MOE_RS_UNROLL;   // K steps of 4 unrolled in the compute loop
 constexpr int kRsEpw = 128 / kRsWarps;     // experts per compute warp
 constexpr int kRsStages = 8;
 constexpr int kRsRBytes = kRsE * kRsKC * 4;             // 16 KB
@@ -174,7 +181,7 @@ __global__ void __launch_bounds__((kRsWarps + 1) * 32, 1) router_stream_kernel(c
             if (!__all_sync(0xffffffffu, ok)) break;
             const uint32_t Rt = opaque(smem_u32(base + s * kRsStageBytes));
             const uint32_t Zt = Rt + kRsRBytes;
-#pragma unroll 2
+#pragma unroll kRsUnroll
             for (int c4 = 0; c4 < kRsKC / 4; ++c4) {
                 const F2x2 z0 = lds128(Zt + swz(lane, c4));
                 const F2x2 z1 = lds128(Zt + swz(lane + 32, c4));
