@@ -53,6 +53,11 @@ namespace {
 #ifndef MOE_SPLIT_A2_TOKENS
 #define MOE_SPLIT_A2_TOKENS 2048
 #endif
+// Where the side stream forks: 0 after the router estimate (beside top-k
+// and the dispatch), 1 after the routed down-projection (beside the combine).
+#ifndef MOE_SPLIT_A2_AT
+#define MOE_SPLIT_A2_AT 0
+#endif
 #ifndef MOE_SPLIT_A2_FREE_SMS
 #define MOE_SPLIT_A2_FREE_SMS 8
 #endif
@@ -749,7 +754,10 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
     auto mark = [&](int i) {
         if (ev && err == cudaSuccess) err = cudaEventRecord(ev[i], s);
     };
-    TRY(cudaMemsetAsync(p->sel, 0, sizeof(uint32_t) * E * W, s));
+    // the selection bitmaps are cleared by the quantiser, the first kernel of
+    // the forward; without it (bf16 projections, latent routing) by a memset
+    const bool run_quant_x = !p->mixed || p->route_hidden;
+    if (!run_quant_x) TRY(cudaMemsetAsync(p->sel, 0, sizeof(uint32_t) * E * W, s));
     // Kernels after the first are launched with programmatic serialization:
     // each may start while its predecessor drains and waits for it on the
     // device (pdl_wait).  Measured on GB300: every kernel gains up to 128
@@ -767,8 +775,9 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
     mark(0);
     // 1. x -> MXFP8 (and x as fp32 for hidden routing); mixed precision reads
     // x as it is, so only hidden routing needs this step
-    if (!p->mixed || p->route_hidden)
-        TRY(launch_quant_x(static_cast<const __nv_bfloat16*>(x), T, D, p->xq, p->xsf, Tps, nmax_dense, p->xr, s, pdl(false)));
+    if (run_quant_x)
+        TRY(launch_quant_x(static_cast<const __nv_bfloat16*>(x), T, D, p->xq, p->xsf, Tps, nmax_dense, p->xr, p->sel,
+                           static_cast<int64_t>(E) * W, s, pdl(false)));
     mark(1);
     // 2. latent down-projection + shared gate/up
     {
@@ -847,12 +856,13 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         else
             TRY(launch_router(p->z, 2 * L, 0, p->router, p->logits, T, E, L, s, pdl(false)));
     }
-    if (split_a2) {
+    auto fork_a2s = [&]() {
         TRY(cudaEventRecord(p->ev_fork, s));
         TRY(cudaStreamWaitEvent(p->side, p->ev_fork, 0));
         TRY(launch_gemm(a2s, a2s_grid, p->side, false));
         TRY(cudaEventRecord(p->ev_join, p->side));
-    }
+    };
+    if (split_a2 && MOE_SPLIT_A2_AT == 0) fork_a2s();
     mark(3);
     {
         TopkArgs a{};
@@ -974,6 +984,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         shape_gemm(g, E, est_experts * g.mt_per_e, p->num_sms);
         TRY(launch_gemm(g, p->num_sms, s, pdl(true)));
     }
+    if (split_a2 && MOE_SPLIT_A2_AT == 1) fork_a2s();
     // 10. weighted combine -> MXFP8 into columns [0, L) of the concatenated activation
     mark(9);
     TRY(launch_combine(p->o, p->slot_pos, p->gw, T, k, L, p->act, p->Kcat, p->actsf, Tps, nmax_dense, p->act_bf, s,

@@ -138,8 +138,11 @@ cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s, bool pdl 
 // ------------------------------------------------------------------ other kernels
 // xsf: item-atom planes of a dense GEMM with token tiles of n_max
 // xf (optional): x as fp32 [T][D]
+// x -> MXFP8 codes and item-atom scales (and x as fp32 when xf is set);
+// also clears zero[0, n_zero) (the forward's selection bitmaps)
 cudaError_t launch_quant_x(const __nv_bfloat16* x, int T, int D, uint8_t* xq, uint8_t* xsf, int64_t pitch, int n_max,
-                           float* xf, cudaStream_t s, bool pdl = false);
+                           float* xf, uint32_t* zero, int64_t n_zero,
+                           cudaStream_t s, bool pdl = false);
 // SIMT router on z = hi + lo ([T][2L]) writing logits [T][E]; batches of at
 // most kRouterSplitTokens tokens split K kRouterSplit ways over a cluster.
 constexpr int kRouterSplit = 8;

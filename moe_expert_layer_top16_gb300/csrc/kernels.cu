@@ -24,9 +24,15 @@ __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b -
 // rows; mx.cuh).
 constexpr int kQxTiles = 4;
 __global__ void quant_x_kernel(const __nv_bfloat16* __restrict__ x, int T, int D, uint8_t* __restrict__ xq,
-                               uint8_t* __restrict__ xsf, int64_t pitch, int n_max, float* __restrict__ xf) {
+                               uint8_t* __restrict__ xsf, int64_t pitch, int n_max, float* __restrict__ xf,
+                               uint32_t* __restrict__ zero, int64_t n_zero) {
     pdl_trigger();
     pdl_wait();
+    // the forward's selection bitmaps start cleared (the first kernel of the
+    // forward clears them, instead of a memset of its own)
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_zero;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        zero[i] = 0u;
     const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     const int tiles = D / 128;
@@ -1104,11 +1110,11 @@ __global__ void gather_rows_kernel(const uint8_t* __restrict__ src, int64_t src_
 }  // namespace
 
 cudaError_t launch_quant_x(const __nv_bfloat16* x, int T, int D, uint8_t* xq, uint8_t* xsf, int64_t pitch, int n_max,
-                           float* xf, cudaStream_t s, bool pdl) {
-    if (n_max <= 0) return cudaErrorInvalidValue;
+                           float* xf, uint32_t* zero, int64_t n_zero, cudaStream_t s, bool pdl) {
+    if (n_max <= 0 || n_zero < 0 || (n_zero > 0 && !zero)) return cudaErrorInvalidValue;
     const int64_t warps = static_cast<int64_t>(T) * ((D / 128 + kQxTiles - 1) / kQxTiles);
     const int blocks = static_cast<int>((warps * 32 + 255) / 256);
-    return launch_ex(quant_x_kernel, dim3(blocks), dim3(256), 0, s, pdl, x, T, D, xq, xsf, pitch, n_max, xf);
+    return launch_ex(quant_x_kernel, dim3(blocks), dim3(256), 0, s, pdl, x, T, D, xq, xsf, pitch, n_max, xf, zero, n_zero);
 }
 
 cudaError_t launch_router(const float* z, int ld, int lo, const float* R, float* logits, int T, int E, int L,
