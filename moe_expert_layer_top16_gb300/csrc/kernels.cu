@@ -678,7 +678,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(TopkArgs a) {
 // k-th largest key is found bit by bit with block-wide counts (the largest
 // v with at least k keys >= v; without a band the search stops as soon as
 // exactly k keys are >= v); the candidates are the keys >= v, or, with
-// an error band, the keys >= the k-th estimate - 2 err (more than 32:
+// an error band, the keys >= the k-th estimate - 2 err (more than kMaxCand:
 // overflow).  Each candidate's rank among the candidates (larger key, or
 // equal key and lower id, first) orders them, and warp 0 finishes as
 // topk_kernel.  Every step is a short chain: this batch size is latency-bound.

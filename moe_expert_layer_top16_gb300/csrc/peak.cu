@@ -1,4 +1,4 @@
-// Tensor-core issue-rate probe: the peak that the layer's GEMMs are judged
+// Tensor-core issue-rate probe: the peak that the layer's GEMMs are measured
 // against, measured on the GPU at hand instead of taken from a data sheet.
 //
 // One CTA per SM issues back-to-back tcgen05.mma instructions of one kind on

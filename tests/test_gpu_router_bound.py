@@ -6,7 +6,7 @@ tensor cores and recomputes in exact fp32 only the candidates whose key
 interval (estimate +- the per-(token, expert) bound) reaches the k-th largest
 lower end.  The bound scales with |z_t| |R_e|, so it holds for any input
 scale.  Two adversarial variants of the K3-shaped layer push the estimate
-error far beyond the 2e-2 band an earlier build assumed:
+error far beyond a fixed band of 2e-2:
   * hidden states scaled by 64 (every logit and every estimate error 64x);
   * eight router rows scaled by 64 (their experts' logits and errors 64x).
 The selection must still be exact: on the exported logits for the whole
