@@ -64,6 +64,10 @@ namespace {
 #ifndef MOE_A_TX_BYTES
 #define MOE_A_TX_BYTES 8192
 #endif
+// wide GEMMs of batches of at least this many tokens run on CTA pairs (0: never)
+#ifndef MOE_PAIR_TOKENS
+#define MOE_PAIR_TOKENS 1024
+#endif
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -148,6 +152,21 @@ bool map_mx8(CUtensorMap* m, const void* codes, int64_t rows, int64_t K, int box
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Scale atoms or item-atom planes as rows of 16 bytes, boxes of box_rows
+// rows (32 rows: one 512-byte atom): the paired GEMMs load their scales
+// through these.
+bool map_rows16(CUtensorMap* m, const void* base, int64_t rows, uint32_t box_rows = 32) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    cuuint64_t dims[2] = {16, static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {16};
+    cuuint32_t box[2] = {16, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 inline int64_t rup(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
 
 // Coefficients of the proven error bound of a tensor-core router estimate
@@ -223,6 +242,15 @@ struct Plan {
     // the plan's own, beside the routing steps (fork / join events)
     cudaStream_t side = nullptr;
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+    // CTA pairs of the wide GEMMs: resident two-CTA clusters (0: pairs off)
+    // and the scale maps of their paired copies (weights: atoms; tokens:
+    // item-atom planes)
+    int pair_clusters = 0;
+    CUtensorMap tSA2, tSA7, tSA8, tSA10;
+    // per token tile size (re-encoded when a forward needs another): each
+    // CTA's half of an item's token rows, and all of the item's scale atoms
+    CUtensorMap tPB2, tPB10, tPB7, tPB8, tPS2, tPS10, tPS7, tPS8;
+    int pair_dense = 0, pair_grp = 0;
 };
 
 template <typename T>
@@ -400,6 +428,64 @@ void shape_gemm(GemmParams& g, int E, int64_t est_items, int grid) {
     g.contiguous = 0;
     g.acc_bufs = 1;
     g.stages = gemm_stages(g.n_max, 1, E, xbuf);
+}
+
+// CTA pairs: an MX launch of wide items (one group, whole items, both
+// producers) on two-CTA clusters whose CTAs share M = 256 MMAs, which halves
+// the token rows each SM loads per weight tile.  g must carry the 16-row B map
+// and its scale maps; E > 0 for grouped items.  Returns the grid (an even
+// number of CTAs, at most max_grid), or 0 when the launch stays unpaired
+// (g unchanged).
+int shape_gemm_pair(GemmParams& g, int E, int64_t n_pairs, int max_grid, int clusters) {
+    if (clusters <= 0 || g.kind != KIND_MX || g.n_max <= kNarrowMax) return 0;
+    if (g.dense ? ((g.m_tiles & 1) || (g.mt_base & 1)) : (g.mt_per_e & 1)) return 0;
+    if (!gemm_config_ok(g.n_max, 1, 1, 2)) return 0;
+    const int64_t cl = std::min<int64_t>(std::min<int64_t>(clusters, max_grid / 2), std::max<int64_t>(n_pairs, 1));
+    if (cl < 1) return 0;
+    GemmParams t = g;
+    t.pair = 1;
+    t.groups = 1;
+    t.ksplit = 1;
+    t.acc_bufs = 2;
+    t.b_producer = 1;
+    t.b_box = pair_b_rows(t.n_max);
+    t.b_row1 = 0;
+    t.contiguous = 0;
+    t.stage_bytes = gemm_stage_bytes(t.n_max, true);
+    const bool xbuf = gemm_needs_xbuf(t);
+    t.stages = gemm_stages(t.n_max, 1, E, xbuf, true);
+    if (gemm_smem_bytes(t.n_max, t.stages, E, xbuf, true) > static_cast<size_t>(kSmemLimit)) return 0;
+    g = t;
+    return static_cast<int>(2 * cl);
+}
+
+// The dense GEMM of the standalone entry points (moe_mx_gemm and its
+// no-allocation form): items of nmax tokens, wide ones on CTA pairs where
+// that applies.  The caller encodes B with dense_box_rows() rows per box and
+// fills g's output description.
+int dense_pair_clusters(int M, int nmax) {
+    return (MOE_PAIR_TOKENS > 0 && nmax > kNarrowMax && (M / kBlockM) % 2 == 0) ? gemm_pair_clusters() : 0;
+}
+int dense_box_rows(int nmax, int pair_cl) {
+    return nmax <= kNarrowMax ? 16 : (pair_cl > 0 ? pair_b_rows(nmax) : nmax);
+}
+cudaError_t launch_dense_mx(GemmParams& g, int M, int N, int K, int64_t Np, int nmax, int pair_cl,
+                            const uint8_t* atoms, const uint8_t* planes, int sms, cudaStream_t s) {
+    if (nmax > kNarrowMax) g.b_box = dense_box_rows(nmax, pair_cl);
+    g.dense = 1;
+    g.m_tiles = M / kBlockM;
+    g.n_tokens = N;
+    g.epi_split = 1 << 30;
+    const int items = g.m_tiles * ((N + nmax - 1) / nmax);
+    int grid = 0;
+    if (pair_cl > 0 && map_rows16(&g.tmSFA, atoms, static_cast<int64_t>(M) * K / 512) &&
+        map_rows16(&g.tmSFB, planes, static_cast<int64_t>(K / 128) * (Np + 32), 32 * ((nmax + 127) / 128)))
+        grid = shape_gemm_pair(g, 0, items / 2, sms, pair_cl);
+    if (!grid) {
+        grid = std::min(items, sms);
+        shape_gemm(g, 0, items, grid);
+    }
+    return launch_gemm(g, grid, s);
 }
 
 moe_status validate(const moe_config* c) {
@@ -667,6 +753,14 @@ moe_status moe_plan(const moe_config* cfg, const moe_weights* w, int device, voi
               map_f32(&p->tAR, p->router2, E, 2 * p->RK, 128) &&
               (p->route_hidden ? map_f32(&p->tBR, p->xr, Tp, D, 16) : map_f32(&p->tBR, p->z, Tp, 2 * L, 16));
     p->tc_router = (E % 128 == 0) && (p->RK % 32 == 0);
+    if (ok && !mixed && MOE_PAIR_TOKENS > 0 && p->T_max >= MOE_PAIR_TOKENS) {
+        p->pair_clusters = gemm_pair_clusters();
+        if (p->pair_clusters > 0)
+            ok = map_rows16(&p->tSA2, p->a2sf, static_cast<int64_t>(p->rowsA2 / 128) * (D / 128) * 32) &&
+                 map_rows16(&p->tSA7, p->w13sf, static_cast<int64_t>(E) * (2 * I / 128) * (L / 128) * 32) &&
+                 map_rows16(&p->tSA8, p->w2sf, static_cast<int64_t>(E) * (L / 128) * (Ip / 128) * 32) &&
+                 map_rows16(&p->tSA10, p->a10sf, static_cast<int64_t>(D / 128) * (p->Kcat / 128) * 32);
+    }
     if (ok && router_stream_ok(p->RK) && router_stream_setup() == cudaSuccess) {
         ok = map_f32_view(&p->tRS, p->router, E, p->RK, p->RK, 128) &&
              (p->route_hidden ? map_f32_view(&p->tZS, p->xr, Tp, D, D, 64)
@@ -767,6 +861,40 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
     // first kernel follows the memset with a plain launch; with per-stage
     // events every launch is plain.
     bool first_kernel = true;
+    // wide GEMMs on CTA pairs: the copy of g with the pair's token and scale
+    // maps, if it pairs; returns its grid or 0
+    const bool pair_on = p->pair_clusters > 0 && T >= MOE_PAIR_TOKENS;
+    if (pair_on && wide_d && p->pair_dense != nmax_dense) {
+        p->pair_dense = 0;
+        const uint32_t sb = 32 * ((nmax_dense + 127) / 128);
+        if (!map_mx8(&p->tPB2, p->xq, Tp, D, pair_b_rows(nmax_dense)) ||
+            !map_mx8(&p->tPB10, p->act, Tp, p->Kcat, pair_b_rows(nmax_dense)) ||
+            !map_rows16(&p->tPS2, p->xsf, static_cast<int64_t>(D / 128) * Tps, sb) ||
+            !map_rows16(&p->tPS10, p->actsf, static_cast<int64_t>(p->Kcat / 128) * Tps, sb))
+            return MOE_ERR_CUDA;
+        p->pair_dense = nmax_dense;
+    }
+    if (pair_on && wide_g && p->pair_grp != nmax_grp) {
+        p->pair_grp = 0;
+        const uint32_t sb = 32 * ((nmax_grp + 127) / 128);
+        if (!map_mx8(&p->tPB7, p->zqp, Rp, L, pair_b_rows(nmax_grp)) ||
+            !map_mx8(&p->tPB8, p->hq, Rp, Ip, pair_b_rows(nmax_grp)) ||
+            !map_rows16(&p->tPS7, p->zqpsf, static_cast<int64_t>(L / 128) * Rps, sb) ||
+            !map_rows16(&p->tPS8, p->hqsf, static_cast<int64_t>(Ip / 128) * Rps, sb))
+            return MOE_ERR_CUDA;
+        p->pair_grp = nmax_grp;
+    }
+    auto try_pair = [&](GemmParams& g, const CUtensorMap& b16, const CUtensorMap& msfa, const CUtensorMap& msfb,
+                        int E_tab, int64_t n_pairs, int max_grid) -> int {
+        if (!pair_on) return 0;
+        GemmParams t = g;
+        t.tmB = b16;
+        t.tmSFA = msfa;
+        t.tmSFB = msfb;
+        const int grid = shape_gemm_pair(t, E_tab, n_pairs, max_grid, p->pair_clusters);
+        if (grid) g = t;
+        return grid;
+    };
     auto pdl = [&](bool gemm) {
         const bool r = !first_kernel && ev == nullptr && (gemm || T <= 128);
         first_kernel = false;
@@ -817,11 +945,19 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
             a2s.m_tiles = p->rowsA2 / kBlockM - L / kBlockM;
             const int items_s = a2s.m_tiles * ((T + a2s.n_max - 1) / a2s.n_max);
             a2s_grid = std::max(1, std::min(items_s, p->num_sms - MOE_SPLIT_A2_FREE_SMS));
-            shape_gemm(a2s, 0, items_s, a2s_grid);
+            const int pg = try_pair(a2s, p->tPB2, p->tSA2, p->tPS2, 0, items_s / 2, a2s_grid);
+            if (pg)
+                a2s_grid = pg;
+            else
+                shape_gemm(a2s, 0, items_s, a2s_grid);
         }
         const int items = g.m_tiles * ((T + g.n_max - 1) / g.n_max);
-        shape_gemm(g, 0, items, std::min(items, p->num_sms));
-        TRY(launch_gemm(g, std::min(items, p->num_sms), s, pdl(true)));
+        int grid = split_a2 ? try_pair(g, p->tPB2, p->tSA2, p->tPS2, 0, items / 2, p->num_sms) : 0;
+        if (!grid) {
+            grid = std::min(items, p->num_sms);
+            shape_gemm(g, 0, items, grid);
+        }
+        TRY(launch_gemm(g, grid, s, pdl(true)));
     }
     // 3. router logits, 4. top-k + gates + bitmaps
     mark(2);
@@ -958,8 +1094,12 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         g.mt_per_e = 2 * I / kBlockM;
         g.rows_per_e = 2 * I;
         g.epi[0] = EpiParams{EPI_SILU_QUANT, 0, 0, 0, nullptr, 0, p->hq, Ip, p->hqsf, Rps, 1};
-        shape_gemm(g, E, est_experts * g.mt_per_e, p->num_sms);
-        TRY(launch_gemm(g, p->num_sms, s, pdl(true)));
+        int grid = try_pair(g, p->tPB7, p->tSA7, p->tPS7, E, est_experts * g.mt_per_e / 2, p->num_sms);
+        if (!grid) {
+            grid = p->num_sms;
+            shape_gemm(g, E, est_experts * g.mt_per_e, grid);
+        }
+        TRY(launch_gemm(g, grid, s, pdl(true)));
     }
     // 9. routed down -> o
     mark(8);
@@ -981,8 +1121,12 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         g.mt_per_e = L / kBlockM;
         g.rows_per_e = L;
         g.epi[0] = EpiParams{EPI_F32, 0, 0, 0, p->o, L, nullptr, 0, nullptr, 0};
-        shape_gemm(g, E, est_experts * g.mt_per_e, p->num_sms);
-        TRY(launch_gemm(g, p->num_sms, s, pdl(true)));
+        int grid = try_pair(g, p->tPB8, p->tSA8, p->tPS8, E, est_experts * g.mt_per_e / 2, p->num_sms);
+        if (!grid) {
+            grid = p->num_sms;
+            shape_gemm(g, E, est_experts * g.mt_per_e, grid);
+        }
+        TRY(launch_gemm(g, grid, s, pdl(true)));
     }
     if (split_a2 && MOE_SPLIT_A2_AT == 1) fork_a2s();
     // 10. weighted combine -> MXFP8 into columns [0, L) of the concatenated activation
@@ -1016,8 +1160,12 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         g.epi_split = 1 << 30;
         g.epi[0] = EpiParams{EPI_F32, 0, 0, 0, static_cast<float*>(y), D, nullptr, 0, nullptr, 0, 0, p->out_bf16 ? 1 : 0};
         const int items = g.m_tiles * ((T + g.n_max - 1) / g.n_max);
-        shape_gemm(g, 0, items, std::min(items, p->num_sms));
-        TRY(launch_gemm(g, std::min(items, p->num_sms), s, split_a2 ? false : pdl(true)));
+        int grid = try_pair(g, p->tPB10, p->tSA10, p->tPS10, 0, items / 2, p->num_sms);
+        if (!grid) {
+            grid = std::min(items, p->num_sms);
+            shape_gemm(g, 0, items, grid);
+        }
+        TRY(launch_gemm(g, grid, s, split_a2 ? false : pdl(true)));
     }
     mark(MOE_NUM_STAGES);
     if (err == cudaSuccess) p->last_T = T;
@@ -1184,8 +1332,10 @@ moe_status moe_mx_gemm(const uint8_t* a_codes, const uint8_t* a_scales, int32_t 
     const size_t atom_bytes = static_cast<size_t>(M) * K / 32;
     const size_t plane_bytes = static_cast<size_t>(K / 128) * (Np + 32) * 16;    // item-atom planes
     CUtensorMap tA, tB, tB1;
-    const int box_rows = pick_n_max(N, item_cap(N)) > kNarrowMax ? pick_n_max(N, item_cap(N)) : 16;
-    if (!map_mx4(&tA, a_codes, M, K) || !map_mx8(&tB, b_codes, N, K, box_rows) || !map_mx8(&tB1, b_codes, N, K, 1))
+    const int nmax = pick_n_max(N, item_cap(N));
+    const int pair_cl = dense_pair_clusters(M, nmax);
+    if (!map_mx4(&tA, a_codes, M, K) || !map_mx8(&tB, b_codes, N, K, dense_box_rows(nmax, pair_cl)) ||
+        !map_mx8(&tB1, b_codes, N, K, 1))
         return MOE_ERR_INVALID_ARG;
     uint8_t* scratch = nullptr;
     err = cudaMallocAsync(reinterpret_cast<void**>(&scratch), atom_bytes + plane_bytes + 256, s);
@@ -1195,24 +1345,15 @@ moe_status moe_mx_gemm(const uint8_t* a_codes, const uint8_t* a_scales, int32_t 
     int32_t* st = dev_status ? dev_status : reinterpret_cast<int32_t*>(scratch + atom_bytes + plane_bytes);
     err = cudaMemsetAsync(planes, 0, plane_bytes + 256, s);
     if (err == cudaSuccess) err = launch_sf_atoms(a_scales, M, K / 32, atoms, s);
-    const int nmax = pick_n_max(N, item_cap(N));
     if (err == cudaSuccess) err = launch_sf_item_planes(b_scales, N, K / 32, planes, Np + 32, nmax, s);
     if (err == cudaSuccess) {
         GemmParams g = gemm_base(tA, tB, atoms, planes, Np + 32, K, nmax, M, static_cast<int>(Np), st);
-        if (nmax > kNarrowMax) {
-            g.b_box = nmax;      // tB was encoded with one box per item
-        } else {
+        if (nmax <= kNarrowMax) {
             g.tmB1 = tB1;        // items of fewer than 16 tokens load their rows one by one
             g.b_row1 = 1;
         }
-        g.dense = 1;
-        g.m_tiles = M / kBlockM;
-        g.n_tokens = N;
-        g.epi_split = 1 << 30;
         g.epi[0] = EpiParams{EPI_F32, 0, 0, 0, out, M, nullptr, 0, nullptr, 0};
-        const int items = g.m_tiles * ((N + nmax - 1) / nmax);
-        shape_gemm(g, 0, items, std::min(items, sms));
-        err = launch_gemm(g, std::min(items, sms), s);
+        err = launch_dense_mx(g, M, N, K, Np, nmax, pair_cl, atoms, planes, sms, s);
     }
     cudaError_t ferr = cudaFreeAsync(scratch, s);
     if (err == cudaSuccess) err = ferr;
@@ -1287,8 +1428,10 @@ extern "C" moe_status moe_mx_gemm_noalloc(const uint8_t* a_codes, const uint8_t*
     if (err == cudaSuccess) err = noalloc_scratch(dev, &scratch);
     if (err != cudaSuccess) return cuda_status(err);
     CUtensorMap tA, tB;
-    const int box_rows = pick_n_max(N, item_cap(N)) > kNarrowMax ? pick_n_max(N, item_cap(N)) : 16;
-    if (!map_mx4(&tA, a_codes, M, K) || !map_mx8(&tB, b_codes, N, K, box_rows)) return MOE_ERR_INVALID_ARG;
+    const int nmax = pick_n_max(N, item_cap(N));
+    const int pair_cl = dense_pair_clusters(M, nmax);
+    if (!map_mx4(&tA, a_codes, M, K) || !map_mx8(&tB, b_codes, N, K, dense_box_rows(nmax, pair_cl)))
+        return MOE_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* atoms = scratch;
     uint8_t* planes = scratch + atom_bytes;
@@ -1297,19 +1440,11 @@ extern "C" moe_status moe_mx_gemm_noalloc(const uint8_t* a_codes, const uint8_t*
     // (their padding rows) and the internal status word
     err = cudaMemsetAsync(planes, 0, plane_bytes + 256, s);
     if (err == cudaSuccess) err = launch_sf_atoms(a_scales, M, K / 32, atoms, s);
-    const int nmax = pick_n_max(N, item_cap(N));
     if (err == cudaSuccess) err = launch_sf_item_planes(b_scales, N, K / 32, planes, Np + 32, nmax, s);
     if (err == cudaSuccess) {
         GemmParams g = gemm_base(tA, tB, atoms, planes, Np + 32, K, nmax, M, static_cast<int>(Np), st);
-        if (nmax > kNarrowMax) g.b_box = nmax;      // tB was encoded with one box per item
-        g.dense = 1;
-        g.m_tiles = M / kBlockM;
-        g.n_tokens = N;
-        g.epi_split = 1 << 30;
         g.epi[0] = EpiParams{EPI_F32, 0, 0, 0, out, M, nullptr, 0, nullptr, 0};
-        const int items = g.m_tiles * ((N + nmax - 1) / nmax);
-        shape_gemm(g, 0, items, std::min(items, sms));
-        err = launch_gemm(g, std::min(items, sms), s);
+        err = launch_dense_mx(g, M, N, K, Np, nmax, pair_cl, atoms, planes, sms, s);
     }
     return cuda_status(err);
 }

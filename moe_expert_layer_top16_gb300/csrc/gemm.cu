@@ -163,10 +163,11 @@ struct SmemLayout {
 
 // One stage: A tile, B rows, then the scale atoms of A (512 B) and of B
 // (512 B per started 128 tokens), both copied as they sit in global memory.
-__host__ __device__ __forceinline__ SmemLayout stage_layout(int n_max) {
+// A CTA of a pair holds half of the token rows (pair_b_rows).
+__host__ __device__ __forceinline__ SmemLayout stage_layout(int n_max, bool pair = false) {
     SmemLayout l;
     l.offB = kABytes;
-    l.offSFA = l.offB + n_max * kBlockK;
+    l.offSFA = l.offB + (pair ? pair_b_rows(n_max) : n_max) * kBlockK;
     l.offSFB = l.offSFA + 512;
     return l;
 }
@@ -226,7 +227,7 @@ enum EpiSet : int {
     SET_DUAL = 3        // EPI_F32 / EPI_QUANT (epi[0]) and EPI_SILU_QUANT (epi[1])
 };
 
-template <int KIND, int SET>
+template <int KIND, int SET, bool PAIR = false>
 __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __grid_constant__ GemmParams p) {
     constexpr bool kMX = (KIND == KIND_MX);
     constexpr bool kBF16 = (KIND == KIND_BF16);
@@ -242,7 +243,9 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
     const int IP = G / KS;                  // item lanes
     const int S_all = pin(p.stages);        // stages of all groups; group g has S_all / G (+1 for g < S_all % G)
     const int NB = pin(p.acc_bufs);         // accumulator buffers per group
-    const SmemLayout L = stage_layout(h.n_max);
+    const SmemLayout L = stage_layout(h.n_max, PAIR);
+    // CTA pairs: this CTA's rank in the pair; the even CTA issues the MMAs
+    const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
     constexpr int kXbuf = (kSilu || kQuant) ? kXbufBytes : 0;
     uint8_t* tail = base + S_all * h.stage_bytes;
     float* xbuf = reinterpret_cast<float*>(tail);
@@ -274,8 +277,10 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
             }
             for (int b = 0; b < 2; ++b) {
                 mbar_init(&tfull[g * 2 + b], 2);      // the MMAs' commit + the item slot
-                // released by every epilogue warp that works on the item
-                mbar_init(&tempty[g * 2 + b], h.n_max >= kSplitChunksMin ? 4 * kEpiGroups : 4);
+                // released by every epilogue warp that works on the item (in
+                // a pair: the even CTA's by the epilogue warps of both CTAs)
+                mbar_init(&tempty[g * 2 + b],
+                          (PAIR && rank == 0 ? 2 : 1) * (h.n_max >= kSplitChunksMin ? 4 * kEpiGroups : 4));
             }
             mbar_init(&tdown[g], 1);
         }
@@ -284,10 +289,19 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
         prefetch_tmap(&p.tmA);
         prefetch_tmap(&p.tmB);
         if (h.b_row1) prefetch_tmap(&p.tmB1);
+        if (PAIR) {
+            prefetch_tmap(&p.tmSFA);
+            prefetch_tmap(&p.tmSFB);
+        }
     }
     if (warp == G) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(tmem_slot, kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, kTmemCols);
+            tmem_relinquish();
+        }
     }
     // everything above touches only this CTA's resources; from here on the
     // kernel reads and writes buffers of earlier kernels
@@ -301,19 +315,23 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
     }
     tc_fence_before();
     __syncthreads();
+    // a pair's barriers are initialised before either CTA signals the other's
+    if constexpr (PAIR) cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const int n_items = h.dense ? h.m_tiles * ((h.n_tokens + h.n_max - 1) / h.n_max) : ioff_s[h.E];
+    // pairs: item i of the launch is engine item 2i + rank of this CTA
+    const int n_items_all = h.dense ? h.m_tiles * ((h.n_tokens + h.n_max - 1) / h.n_max) : ioff_s[h.E];
+    const int n_items = PAIR ? (n_items_all >> 1) : n_items_all;
+    const int cta = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int n_cta = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
     // this CTA's items: it_begin + c * it_step for c = 0, 1, ... while below
     // it_end -- a contiguous range (narrow items: consecutive items mostly
-    // share an expert), or every gridDim.x-th item
+    // share an expert), or every n_cta-th item
     const bool contiguous = p.contiguous != 0;
-    const int it_begin = contiguous ? static_cast<int>(static_cast<int64_t>(n_items) * blockIdx.x / gridDim.x)
-                                    : static_cast<int>(blockIdx.x);
-    const int it_end = contiguous ? static_cast<int>(static_cast<int64_t>(n_items) * (blockIdx.x + 1) / gridDim.x)
-                                  : n_items;
-    const int it_step = contiguous ? 1 : static_cast<int>(gridDim.x);
+    const int it_begin = contiguous ? static_cast<int>(static_cast<int64_t>(n_items) * cta / n_cta) : cta;
+    const int it_end = contiguous ? static_cast<int>(static_cast<int64_t>(n_items) * (cta + 1) / n_cta) : n_items;
+    const int it_step = contiguous ? 1 : n_cta;
     const uint32_t cols_per_group = static_cast<uint32_t>(NB * h.n_max + 24);
 
     if (warp < G) {
@@ -332,7 +350,7 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
         bool ok = true;
         int ecur = -1;
         for (int it = it_begin + ip * it_step; ok && it < it_end && ke > kb; it += IP * it_step) {
-            const Item w = get_item(h, it, ioff_s, seg_s, cnt_s, ecur);
+            const Item w = get_item(h, PAIR ? 2 * it + rank : it, ioff_s, seg_s, cnt_s, ecur);
             if (w.n <= 0) {
                 if (w.n < 0 && g == 0 && lane == 0) atomicCAS(h.status, 0, DEV_BAD_WORK);
                 continue;
@@ -348,7 +366,12 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
             const uint32_t b_bytes = row_loads ? static_cast<uint32_t>(w.n * kBlockK)
                                                : static_cast<uint32_t>(nbox * h.b_box * kBlockK);
             const uint32_t sfb_bytes = (w.n <= 32) ? static_cast<uint32_t>(w.n * 16) : static_cast<uint32_t>(natoms * 512);
-            const uint32_t tx = kMX ? static_cast<uint32_t>(h.a_tx_bytes) + b_bytes + 512u + sfb_bytes
+            // a pair's stage: both CTAs' weight tiles and scale atoms, and
+            // one box of token rows and one of token scales per CTA (the even
+            // CTA counts them all on its barrier)
+            const uint32_t tx = PAIR ? 2u * (static_cast<uint32_t>(h.a_tx_bytes) + 512u +
+                                             static_cast<uint32_t>(((h.n_max + 127) / 128) * 512 + h.b_box * kBlockK))
+                              : kMX ? static_cast<uint32_t>(h.a_tx_bytes) + b_bytes + 512u + sfb_bytes
                                     : static_cast<uint32_t>(kBlockM * 128) + b_bytes;
             const uint8_t* sfa_tile = kMX ? h.sfa + static_cast<size_t>(w.a_row0 / kBlockM) * h.KT * 512 : nullptr;
             for (int kt = kb; kt < ke; ++kt) {
@@ -362,7 +385,17 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                 const int ax = (sg == 0 ? h.ax0 : (sg == 1 ? h.ax1 : h.ax2)) + kin;
                 const int bx = (sg == 0 ? h.bx0 : (sg == 1 ? h.bx1 : h.bx2)) + kin;
                 uint8_t* sb = ring + stage * h.stage_bytes;
-                if (elect_one()) {
+                if constexpr (PAIR) {
+                    if (elect_one()) {
+                        const uint32_t fb = mapa_shared(smem_u32(&fullg[stage]), 0);
+                        // the even CTA counts the pair's bytes on its own barrier
+                        // (a CTA-local arrive: the cluster-scope form costs about a
+                        // microsecond per stage)
+                        if (rank == 0) mbar_arrive_expect_tx(&fullg[stage], tx);
+                        tma_load_2d_pair(sb, &p.tmA, fb, ax, w.a_row0);
+                        tma_load_2d_pair(sb + L.offSFA, &p.tmSFA, fb, 0, ((w.a_row0 / kBlockM) * h.KT + kt) * 32);
+                    }
+                } else if (elect_one()) {
                     mbar_arrive_expect_tx(&fullg[stage], tx);
                     tma_load_2d(sb, &p.tmA, &fullg[stage], ax, w.a_row0);
                     if (!h.b_producer) {
@@ -391,8 +424,22 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                 }
             }
         }
-        if (*abort_flag && lane == 0) {
-            // drain: every issued stage's copies must land before exit
+        if constexpr (PAIR) {
+            // the even CTA's MMAs read this CTA's stages and their commits
+            // arrive on its barriers: before this CTA may exit, every stage
+            // must have been released
+            for (int i = 0; ok && i < S; ++i) {
+                ok = mbar_wait(&emptyg[stage], phase ^ 1, abort_flag, h.status, DEV_TIMEOUT_PRODUCER);
+                ok = __all_sync(0xffffffffu, ok);
+                if (++stage == static_cast<uint32_t>(S)) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        if (*abort_flag && lane == 0 && rank == 0) {
+            // drain: every issued stage's copies must land before exit (a
+            // pair's copies all count on the even CTA's barriers)
             for (int s = 0; s < S; ++s)
                 if (issued & (1u << s)) mbar_wait_teardown(&fullg[s], (issued_parity >> s) & 1u, h.status);
         }
@@ -415,15 +462,17 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
         for (int it = it_begin + ip * it_step; it < it_end && ke > kb; it += IP * it_step) {
             // every item takes an accumulator turn, so that the epilogue can
             // follow the item lanes round-robin; a rejected item (n <= 0)
-            // issues no MMAs
-            const Item w = get_item(h, it, ioff_s, seg_s, cnt_s, ecur);
+            // issues no MMAs.  In a pair the even CTA issues the MMAs of both
+            // (its accumulator buffer is free once both epilogues released
+            // it); the odd CTA only hands its item to its epilogue.
+            const Item w = get_item(h, PAIR ? 2 * it + rank : it, ioff_s, seg_s, cnt_s, ecur);
             const int nm = (w.n + 15) & ~15;
             const int natoms = (nm + 127) / 128;
             bool ok = mbar_wait(&tempty[g * 2 + acc], acc_phase ^ 1, abort_flag, h.status, DEV_TIMEOUT_MMA);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
             const uint32_t d_tmem = gcol + acc * static_cast<uint32_t>(h.n_max);
-            for (int kt = kb; kt < (w.n > 0 ? ke : kb); ++kt) {
+            for (int kt = kb; kt < ((w.n > 0 && rank == 0) ? ke : kb); ++kt) {
                 ok = mbar_wait(&fullg[stage], phase, abort_flag, h.status, DEV_TIMEOUT_MMA);
                 if (!__all_sync(0xffffffffu, ok)) goto mma_done;
                 tc_fence_after();
@@ -452,6 +501,22 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                         // both scale operands arrive as 32x128b copy images
                         const uint32_t sfa_col = sf_base + static_cast<uint32_t>(kt & 1) * 12u;
                         const uint32_t sfb_col = sfa_col + 4u;
+                        if constexpr (PAIR) {
+                            const uint32_t idesc0 = idesc_mxf8f6f4(2 * kBlockM, nm, 5, 0, 0, 0);
+                            if (elect_one()) {
+                                tc_cp_32x128b_x4_pair(sfa_col, sdesc_rows16(smem_u32(sb + L.offSFA)));
+                                for (int a = 0; a < natoms; ++a)
+                                    tc_cp_32x128b_x4_pair(sfb_col + 4u * a, sdesc_rows16(smem_u32(sb + L.offSFB + a * 512)));
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    const uint32_t idesc = idesc0 | (static_cast<uint32_t>(j) << 4) |
+                                                           (static_cast<uint32_t>(j) << 29);
+                                    mma_mxf8f6f4_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sfa_col, sfb_col,
+                                                      (accum_first | j) != 0 ? 1u : 0u);
+                                }
+                                tc_commit_pair(&emptyg[stage], 3);
+                            }
+                        } else {
                         const uint32_t idesc0 = idesc_mxf8f6f4(kBlockM, nm, 5, 0, 0, 0);
                         if (elect_one()) {
                             tc_cp_32x128b_x4(sfa_col, sdesc_rows16(smem_u32(sb + L.offSFA)));
@@ -468,6 +533,7 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                             }
                             tc_commit(&emptyg[stage]);
                         }
+                        }
                     }
                     any = true;
                     __syncwarp();
@@ -480,7 +546,11 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
             if (elect_one()) {
                 item_slot[g * 2 + acc] = w;
                 mbar_arrive(&tfull[g * 2 + acc]);      // release: the slot is visible with the phase
-                tc_commit(&tfull[g * 2 + acc]);
+                if constexpr (PAIR) {
+                    if (rank == 0) tc_commit_pair(&tfull[g * 2 + acc], 3);
+                } else {
+                    tc_commit(&tfull[g * 2 + acc]);
+                }
             }
             __syncwarp();
             if (++acc == static_cast<uint32_t>(NB)) {
@@ -492,7 +562,10 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
         // every tcgen05 operation issued above must finish before TMEM is freed
         if (any) {
             if (elect_one()) {
-                tc_commit(&tdown[g]);
+                if constexpr (PAIR)
+                    tc_commit_pair(&tdown[g], 1);
+                else
+                    tc_commit(&tdown[g]);
                 mbar_wait_teardown(&tdown[g], 0, h.status);
             }
             __syncwarp();
@@ -734,6 +807,9 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                     group_range(h.KT, ks, KS, kb, ke);
                     if (ke > kb) mbar_arrive(&tempty[(g0 + ks) * 2 + acc]);
                 }
+                // the even CTA of a pair refills both CTAs' accumulators (this
+                // warp's TMEM loads are complete: tcgen05.wait::ld)
+                if (PAIR && rank == 1) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&tempty[g0 * 2 + acc]), 0));
             }
         }
     } else if (h.b_producer && warp == 2 * G + 4 * kEpiGroups) {
@@ -749,7 +825,7 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
         bool ok = true;
         int ecur = -1;
         for (int it = it_begin; ok && it < it_end; it += it_step) {
-            const Item w = get_item(h, it, ioff_s, seg_s, cnt_s, ecur);
+            const Item w = get_item(h, PAIR ? 2 * it + rank : it, ioff_s, seg_s, cnt_s, ecur);
             if (w.n <= 0) continue;
             const int nm = (w.n + 15) & ~15;
             const int natoms = (nm + 127) / 128;
@@ -766,7 +842,17 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                 const int kin = (kt - sg * h.kseg_tiles) * kTileElems;
                 const int bx = (sg == 0 ? h.bx0 : (sg == 1 ? h.bx1 : h.bx2)) + kin;
                 uint8_t* sb = base + stage * h.stage_bytes;
-                if (elect_one()) {
+                if constexpr (PAIR) {
+                    // this CTA's half of the token rows and the scale atoms of
+                    // all of them, one box each (boxes of the launch's largest
+                    // item: rows past the half and atoms past the item are
+                    // loaded but not read)
+                    if (elect_one()) {
+                        const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
+                        tma_load_2d_pair(sb + L.offB, &p.tmB, fb, bx, w.b_row0 + rank * (nm >> 1));
+                        tma_load_2d_pair(sb + L.offSFB, &p.tmSFB, fb, 0, static_cast<int>(kt * h.sfb_pitch) + w.b_row0);
+                    }
+                } else if (elect_one()) {
                     if (row_loads) {
                         for (int r = 0; r < w.n; ++r)
                             tma_load_2d(sb + L.offB + r * kBlockK, &p.tmB1, &full[stage], bx, w.b_row0 + r);
@@ -788,7 +874,18 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                 }
             }
         }
-        if (*abort_flag && lane == 0) {
+        if constexpr (PAIR) {
+            // as the weight-side producer: wait until every stage was released
+            for (int i = 0; ok && i < S; ++i) {
+                ok = mbar_wait(&empty[stage], phase ^ 1, abort_flag, h.status, DEV_TIMEOUT_PRODUCER);
+                ok = __all_sync(0xffffffffu, ok);
+                if (++stage == static_cast<uint32_t>(S)) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        if (*abort_flag && lane == 0 && rank == 0) {
             for (int s = 0; s < S; ++s)
                 if (issued & (1u << s)) mbar_wait_teardown(&full[s], (issued_parity >> s) & 1u, h.status);
         }
@@ -797,28 +894,34 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
 
     tc_fence_before();
     __syncthreads();
+    // neither CTA of a pair frees the pair's TMEM or leaves while the other
+    // may still signal its barriers
+    if constexpr (PAIR) cluster_sync_all();
     if (warp == G) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        if constexpr (PAIR)
+            tmem_dealloc_pair(tmem, kTmemCols);
+        else
+            tmem_dealloc(tmem, kTmemCols);
     }
 }
 
 }  // namespace
 
-int gemm_stage_bytes(int n_max) {
-    const SmemLayout l = stage_layout(n_max);
+int gemm_stage_bytes(int n_max, bool pair) {
+    const SmemLayout l = stage_layout(n_max, pair);
     const int bytes = l.offSFB + ((n_max + 127) / 128) * 512;
     return (bytes + 1023) & ~1023;
 }
 
-size_t gemm_smem_bytes(int n_max, int stages, int E, bool xbuf) {
-    return 1024 + static_cast<size_t>(stages) * gemm_stage_bytes(n_max) + (xbuf ? kXbufBytes : 0) + kBarBytes +
+size_t gemm_smem_bytes(int n_max, int stages, int E, bool xbuf, bool pair) {
+    return 1024 + static_cast<size_t>(stages) * gemm_stage_bytes(n_max, pair) + (xbuf ? kXbufBytes : 0) + kBarBytes +
            table_bytes(E);
 }
 
-int gemm_stages(int n_max, int groups, int E, bool xbuf) {
+int gemm_stages(int n_max, int groups, int E, bool xbuf, bool pair) {
     int s = kMaxStagesPerGroup * groups;
-    while (s > 2 * groups && gemm_smem_bytes(n_max, s, E, xbuf) > static_cast<size_t>(kSmemLimit)) --s;
+    while (s > 2 * groups && gemm_smem_bytes(n_max, s, E, xbuf, pair) > static_cast<size_t>(kSmemLimit)) --s;
     return s;
 }
 
@@ -832,9 +935,10 @@ bool gemm_config_ok(int n_max, int groups, int ksplit, int acc_bufs) {
 
 namespace {
 
-template <int KIND, int SET>
+template <int KIND, int SET, bool PAIR = false>
 cudaError_t raise_smem() {
-    return cudaFuncSetAttribute(mx_gemm_kernel<KIND, SET>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    return cudaFuncSetAttribute(mx_gemm_kernel<KIND, SET, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmemLimit);
 }
 
 // The kernel instance whose epilogue covers the launch's output modes: those
@@ -868,22 +972,68 @@ cudaError_t gemm_setup() {
     if (err == cudaSuccess) err = raise_smem<KIND_TF32, SET_F32>();
     if (err == cudaSuccess) err = raise_smem<KIND_BF16, SET_F32>();
     if (err == cudaSuccess) err = raise_smem<KIND_BF16, SET_DUAL>();
+    if (err == cudaSuccess) err = raise_smem<KIND_MX, SET_F32, true>();
+    if (err == cudaSuccess) err = raise_smem<KIND_MX, SET_QUANT, true>();
+    if (err == cudaSuccess) err = raise_smem<KIND_MX, SET_SILU, true>();
     return err;
+}
+
+int gemm_pair_clusters() {
+    static int device = -1, clusters = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev == device) return clusters;
+    // the pair kernels run one CTA per SM (their shared memory): how many
+    // two-CTA clusters of the largest configuration are resident at once
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3((2 + 4 * kEpiGroups + 1) * 32);
+    cfg.dynamicSmemBytes = kSmemLimit;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (raise_smem<KIND_MX, SET_F32, true>() != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&n, mx_gemm_kernel<KIND_MX, SET_F32, true>, &cfg) != cudaSuccess)
+        n = 0;
+    device = dev;
+    clusters = n;
+    return clusters;
 }
 
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s, bool pdl) {
     if (!gemm_config_ok(p.n_max, p.groups, p.ksplit, p.acc_bufs)) return cudaErrorInvalidValue;
     if (p.stages < 2 * p.groups || p.stages > kMaxStagesPerGroup * p.groups) return cudaErrorInvalidValue;
-    const size_t smem = gemm_smem_bytes(p.n_max, p.stages, p.dense ? 0 : p.E, gemm_needs_xbuf(p));
+    const bool pair = p.pair != 0;
+    const size_t smem = gemm_smem_bytes(p.n_max, p.stages, p.dense ? 0 : p.E, gemm_needs_xbuf(p), pair);
     if (smem > static_cast<size_t>(kSmemLimit)) return cudaErrorInvalidValue;
+    if (p.stage_bytes != gemm_stage_bytes(p.n_max, pair)) return cudaErrorInvalidValue;
     if (p.kseg_tiles <= 0 || p.KT > 3 * p.kseg_tiles) return cudaErrorInvalidValue;
-    if (!(p.b_box == 16 || p.b_box == p.n_max)) return cudaErrorInvalidValue;   // boxes must tile the B rows
     if (!p.dense && (p.E <= 0 || p.E > 1024)) return cudaErrorInvalidValue;
     const int set = epi_set(p);
     if (set < 0) return cudaErrorInvalidValue;
     if (p.b_producer && p.groups != 1) return cudaErrorInvalidValue;
     if (p.dense && (p.mt_base < 0 || (p.mt_base + p.m_tiles) * kBlockM > p.a_rows)) return cudaErrorInvalidValue;
     const dim3 g(grid), b((2 * p.groups + 4 * kEpiGroups + (p.b_producer ? 1 : 0)) * 32);
+    if (pair) {
+        // one group of whole items fed by both producers, 16-row token boxes,
+        // whole pairs of weight tiles, scale maps for the paired copies
+        if (p.kind != KIND_MX || p.groups != 1 || p.ksplit != 1 || !p.b_producer || p.b_box != pair_b_rows(p.n_max) ||
+            p.b_row1)
+            return cudaErrorInvalidValue;
+        if (grid < 2 || (grid & 1)) return cudaErrorInvalidValue;
+        if (p.dense ? ((p.m_tiles & 1) || (p.mt_base & 1)) : (p.mt_per_e & 1)) return cudaErrorInvalidValue;
+        if (set == SET_F32) return launch_ex_cluster(mx_gemm_kernel<KIND_MX, SET_F32, true>, g, b, smem, s, pdl, 2, p);
+        if (set == SET_QUANT)
+            return launch_ex_cluster(mx_gemm_kernel<KIND_MX, SET_QUANT, true>, g, b, smem, s, pdl, 2, p);
+        if (set == SET_SILU) return launch_ex_cluster(mx_gemm_kernel<KIND_MX, SET_SILU, true>, g, b, smem, s, pdl, 2, p);
+        return cudaErrorInvalidValue;
+    }
+    if (!(p.b_box == 16 || p.b_box == p.n_max)) return cudaErrorInvalidValue;   // boxes must tile the B rows
     if (p.kind == KIND_TF32) {
         if (set != SET_F32) return cudaErrorInvalidValue;
         return launch_ex(mx_gemm_kernel<KIND_TF32, SET_F32>, g, b, smem, s, pdl, p);

@@ -35,6 +35,27 @@ inline cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// The same with thread-block clusters of `cluster` CTAs along x.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_ex_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                     bool pdl, int cluster, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = pdl ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Device status codes (sticky; read by moe_get_device_status).
 enum : int { DEV_OK = 0, DEV_TIMEOUT_PRODUCER = 1, DEV_TIMEOUT_MMA = 2, DEV_TIMEOUT_EPILOGUE = 3,
              DEV_TIMEOUT_TEARDOWN = 4, DEV_BAD_WORK = 5 };
@@ -122,14 +143,33 @@ struct GemmParams {
     int b_seg_x[3];         // element offset along K of each segment in B's map
     EpiParams epi[2];
     int* status;
+    // CTA pairs (pair != 0): clusters of two CTAs share M = 256 MMAs; work
+    // item i of the launch is the pair of engine items 2i (even CTA) and
+    // 2i + 1 (odd CTA).  Needs one group without K-splits, the token-side
+    // producer, B boxes of pair_b_rows(n_max) rows (each CTA loads half of
+    // an item's token rows), an even grid, and an even number of weight tiles
+    // per expert (grouped) or m_tiles and mt_base even (dense).  The scale
+    // tiles then load through these maps of 16-byte rows: sfa as
+    // [rows/128 * KT * 32][16] in 32-row boxes (one 512-byte atom), sfb as
+    // [KT * sfb_pitch][16] in boxes of 32 * ceil(n_max / 128) rows (all atoms
+    // of an item).
+    int pair;
+    CUtensorMap tmSFA;
+    CUtensorMap tmSFB;
 };
 
-int gemm_stage_bytes(int n_max);
+// Token rows of one CTA of a pair per stage (half of the largest item).
+__host__ __device__ __forceinline__ int pair_b_rows(int n_max) { return ((n_max >> 1) + 15) & ~15; }
+// Shared-memory bytes of one stage; pair: the stage of one CTA of a pair
+// (half of the item's token rows, all of its token scales).
+int gemm_stage_bytes(int n_max, bool pair = false);
 // total shared-memory stages of a launch (all groups); E > 0: grouped items
 // (per-expert tables in shared memory); xbuf: the SiLU exchange buffer and the
 // per-warp staging of MXFP8 output codes (quantising epilogues)
-int gemm_stages(int n_max, int groups, int E, bool xbuf);
-size_t gemm_smem_bytes(int n_max, int stages, int E, bool xbuf);
+int gemm_stages(int n_max, int groups, int E, bool xbuf, bool pair = false);
+size_t gemm_smem_bytes(int n_max, int stages, int E, bool xbuf, bool pair = false);
+// Clusters of two CTAs of the pair kernels that fit on the GPU at once (0: none).
+int gemm_pair_clusters();
 bool gemm_needs_xbuf(const GemmParams& p);
 bool gemm_config_ok(int n_max, int groups, int ksplit, int acc_bufs);
 cudaError_t gemm_setup();   // raise the dynamic shared memory limit once

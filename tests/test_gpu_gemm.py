@@ -88,6 +88,18 @@ def test_gemm_random_against_oracle(M, N, K):
     check(*random_operands(rng, M, N, K), f"M={M} N={N} K={K}")
 
 
+@pytest.mark.parametrize("M,N,K", [(256, 257, 256), (512, 3601, 384), (1024, 4111, 256), (768, 1000, 1024),
+                                   (384, 700, 256)])
+def test_gemm_wide_items_on_cta_pairs(M, N, K):
+    # Batches above 256 tokens form wide items (up to 240 tokens); with an
+    # even number of 128-row weight tiles, two CTAs share each MMA (M = 256,
+    # each CTA loading half of the item's token rows).  Last items of 113,
+    # 1 and 31 tokens (N = 257, 3601, 4111) give pair halves of 56, 8 and 16
+    # rows; M = 384 has an odd tile count and stays unpaired.
+    rng = np.random.default_rng(M * 11 + N * 3 + K)
+    check(*random_operands(rng, M, N, K), f"M={M} N={N} K={K}")
+
+
 def test_gemm_rejects_bad_shapes():
     t = torch.zeros(256, dtype=torch.uint8, device=DEV)
     with pytest.raises(moe.MoeError):
