@@ -68,6 +68,12 @@ namespace {
 #ifndef MOE_PAIR_TOKENS
 #define MOE_PAIR_TOKENS 1024
 #endif
+// tokens per work item at most when the GEMMs run on CTA pairs (a smaller
+// item leaves room for one more shared-memory stage; 8,192 tokens: 240 2.72,
+// 224 2.62, 208 2.65, 192 2.66 ms)
+#ifndef MOE_PAIR_NMAX
+#define MOE_PAIR_NMAX 224
+#endif
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -152,15 +158,15 @@ bool map_mx8(CUtensorMap* m, const void* codes, int64_t rows, int64_t K, int box
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Scale atoms or item-atom planes as rows of 16 bytes, boxes of box_rows
-// rows (32 rows: one 512-byte atom): the paired GEMMs load their scales
-// through these.
-bool map_rows16(CUtensorMap* m, const void* base, int64_t rows, uint32_t box_rows = 32) {
+// Scale atoms or item-atom planes (bytes, a multiple of 256) as rows of 256
+// bytes, boxes of box_rows rows (2 rows: one 512-byte atom): the paired GEMMs
+// load their scales through these.
+bool map_rows256(CUtensorMap* m, const void* base, int64_t bytes, uint32_t box_rows) {
     EncodeTiledFn f = encode_fn();
-    if (!f) return false;
-    cuuint64_t dims[2] = {16, static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {16};
-    cuuint32_t box[2] = {16, box_rows};
+    if (!f || bytes % 256) return false;
+    cuuint64_t dims[2] = {256, static_cast<cuuint64_t>(bytes / 256)};
+    cuuint64_t strides[1] = {256};
+    cuuint32_t box[2] = {256, box_rows};
     cuuint32_t es[2] = {1, 1};
     return f(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
@@ -478,8 +484,8 @@ cudaError_t launch_dense_mx(GemmParams& g, int M, int N, int K, int64_t Np, int 
     g.epi_split = 1 << 30;
     const int items = g.m_tiles * ((N + nmax - 1) / nmax);
     int grid = 0;
-    if (pair_cl > 0 && map_rows16(&g.tmSFA, atoms, static_cast<int64_t>(M) * K / 512) &&
-        map_rows16(&g.tmSFB, planes, static_cast<int64_t>(K / 128) * (Np + 32), 32 * ((nmax + 127) / 128)))
+    if (pair_cl > 0 && map_rows256(&g.tmSFA, atoms, static_cast<int64_t>(M) * K / 32, 2) &&
+        map_rows256(&g.tmSFB, planes, static_cast<int64_t>(K / 128) * (Np + 32) * 16, 2 * ((nmax + 127) / 128)))
         grid = shape_gemm_pair(g, 0, items / 2, sms, pair_cl);
     if (!grid) {
         grid = std::min(items, sms);
@@ -756,10 +762,10 @@ moe_status moe_plan(const moe_config* cfg, const moe_weights* w, int device, voi
     if (ok && !mixed && MOE_PAIR_TOKENS > 0 && p->T_max >= MOE_PAIR_TOKENS) {
         p->pair_clusters = gemm_pair_clusters();
         if (p->pair_clusters > 0)
-            ok = map_rows16(&p->tSA2, p->a2sf, static_cast<int64_t>(p->rowsA2 / 128) * (D / 128) * 32) &&
-                 map_rows16(&p->tSA7, p->w13sf, static_cast<int64_t>(E) * (2 * I / 128) * (L / 128) * 32) &&
-                 map_rows16(&p->tSA8, p->w2sf, static_cast<int64_t>(E) * (L / 128) * (Ip / 128) * 32) &&
-                 map_rows16(&p->tSA10, p->a10sf, static_cast<int64_t>(D / 128) * (p->Kcat / 128) * 32);
+            ok = map_rows256(&p->tSA2, p->a2sf, static_cast<int64_t>(p->rowsA2) * D / 32, 2) &&
+                 map_rows256(&p->tSA7, p->w13sf, static_cast<int64_t>(E) * 2 * I * L / 32, 2) &&
+                 map_rows256(&p->tSA8, p->w2sf, static_cast<int64_t>(E) * L * Ip / 32, 2) &&
+                 map_rows256(&p->tSA10, p->a10sf, static_cast<int64_t>(D) * p->Kcat / 32, 2);
     }
     if (ok && router_stream_ok(p->RK) && router_stream_setup() == cudaSuccess) {
         ok = map_f32_view(&p->tRS, p->router, E, p->RK, p->RK, 128) &&
@@ -794,10 +800,14 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
     const int64_t Tps = Tp + 32, Rps = Rp + 32;   // slots per item-atom scale plane
     // dense GEMMs stream their weights once per token tile: a batch of up to
     // 64 tokens is one tile
-    const int nmax_dense = (T <= 64) ? static_cast<int>(rup(T, 16)) : pick_n_max(T, item_cap(T));
-    // grouped token tile: about 3x the mean tokens per expert, 16..240
+    // wide GEMMs on CTA pairs from MOE_PAIR_TOKENS tokens on (their items
+    // hold up to MOE_PAIR_NMAX tokens)
+    const bool pair_on = p->pair_clusters > 0 && T >= MOE_PAIR_TOKENS;
+    const int cap = pair_on ? std::min(MOE_PAIR_NMAX, kNMax) : kNMax;
+    const int nmax_dense = (T <= 64) ? static_cast<int>(rup(T, 16)) : pick_n_max(T, std::min(item_cap(T), cap));
+    // grouped token tile: about 3x the mean tokens per expert, 16..cap
     const int64_t per_expert = (static_cast<int64_t>(T) * k + E - 1) / E;
-    const int nmax_grp = static_cast<int>(std::min<int64_t>(std::min<int64_t>(std::max<int64_t>(rup(3 * per_expert, 16), 16), kNMax),
+    const int nmax_grp = static_cast<int>(std::min<int64_t>(std::min<int64_t>(std::max<int64_t>(rup(3 * per_expert, 16), 16), cap),
                                                             rup(T, 16)));
     // experts expected to receive tokens (all of them once T * k >> E)
     const int64_t est_experts = std::min<int64_t>(E, static_cast<int64_t>(T) * k);
@@ -863,24 +873,23 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
     bool first_kernel = true;
     // wide GEMMs on CTA pairs: the copy of g with the pair's token and scale
     // maps, if it pairs; returns its grid or 0
-    const bool pair_on = p->pair_clusters > 0 && T >= MOE_PAIR_TOKENS;
     if (pair_on && wide_d && p->pair_dense != nmax_dense) {
         p->pair_dense = 0;
-        const uint32_t sb = 32 * ((nmax_dense + 127) / 128);
+        const uint32_t sb = 2 * ((nmax_dense + 127) / 128);
         if (!map_mx8(&p->tPB2, p->xq, Tp, D, pair_b_rows(nmax_dense)) ||
             !map_mx8(&p->tPB10, p->act, Tp, p->Kcat, pair_b_rows(nmax_dense)) ||
-            !map_rows16(&p->tPS2, p->xsf, static_cast<int64_t>(D / 128) * Tps, sb) ||
-            !map_rows16(&p->tPS10, p->actsf, static_cast<int64_t>(p->Kcat / 128) * Tps, sb))
+            !map_rows256(&p->tPS2, p->xsf, static_cast<int64_t>(D / 128) * Tps * 16, sb) ||
+            !map_rows256(&p->tPS10, p->actsf, static_cast<int64_t>(p->Kcat / 128) * Tps * 16, sb))
             return MOE_ERR_CUDA;
         p->pair_dense = nmax_dense;
     }
     if (pair_on && wide_g && p->pair_grp != nmax_grp) {
         p->pair_grp = 0;
-        const uint32_t sb = 32 * ((nmax_grp + 127) / 128);
+        const uint32_t sb = 2 * ((nmax_grp + 127) / 128);
         if (!map_mx8(&p->tPB7, p->zqp, Rp, L, pair_b_rows(nmax_grp)) ||
             !map_mx8(&p->tPB8, p->hq, Rp, Ip, pair_b_rows(nmax_grp)) ||
-            !map_rows16(&p->tPS7, p->zqpsf, static_cast<int64_t>(L / 128) * Rps, sb) ||
-            !map_rows16(&p->tPS8, p->hqsf, static_cast<int64_t>(Ip / 128) * Rps, sb))
+            !map_rows256(&p->tPS7, p->zqpsf, static_cast<int64_t>(L / 128) * Rps * 16, sb) ||
+            !map_rows256(&p->tPS8, p->hqsf, static_cast<int64_t>(Ip / 128) * Rps * 16, sb))
             return MOE_ERR_CUDA;
         p->pair_grp = nmax_grp;
     }

@@ -149,7 +149,7 @@ __device__ __forceinline__ Item get_item(const Hot& h, int it, const int* ioff, 
         w.mt = m;
         // reject items that would read or write outside the buffers
         if (w.n <= 0 || w.n > h.n_max || w.a_row0 < 0 || (w.a_row0 & (kBlockM - 1)) ||
-            w.a_row0 + kBlockM > h.a_rows || w.b_row0 < 0 || (w.b_row0 & 3) ||
+            w.a_row0 + kBlockM > h.a_rows || w.b_row0 < 0 || (w.b_row0 & 15) ||
             w.b_row0 + ((w.n + 15) & ~15) > h.b_rows || w.mt < 0) {
             w.n = -1;
         }
@@ -393,7 +393,8 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                         // microsecond per stage)
                         if (rank == 0) mbar_arrive_expect_tx(&fullg[stage], tx);
                         tma_load_2d_pair(sb, &p.tmA, fb, ax, w.a_row0);
-                        tma_load_2d_pair(sb + L.offSFA, &p.tmSFA, fb, 0, ((w.a_row0 / kBlockM) * h.KT + kt) * 32);
+                        tma_load_2d_pair(sb + L.offSFA, &p.tmSFA, fb, 0, ((w.a_row0 / kBlockM) * h.KT + kt) * 2);
+
                     }
                 } else if (elect_one()) {
                     mbar_arrive_expect_tx(&fullg[stage], tx);
@@ -850,7 +851,8 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                     if (elect_one()) {
                         const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
                         tma_load_2d_pair(sb + L.offB, &p.tmB, fb, bx, w.b_row0 + rank * (nm >> 1));
-                        tma_load_2d_pair(sb + L.offSFB, &p.tmSFB, fb, 0, static_cast<int>(kt * h.sfb_pitch) + w.b_row0);
+                        tma_load_2d_pair(sb + L.offSFB, &p.tmSFB, fb, 0,
+                                         (static_cast<int>(kt * h.sfb_pitch) + w.b_row0) >> 4);
                     }
                 } else if (elect_one()) {
                     if (row_loads) {

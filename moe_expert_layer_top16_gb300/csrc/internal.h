@@ -149,10 +149,11 @@ struct GemmParams {
     // producer, B boxes of pair_b_rows(n_max) rows (each CTA loads half of
     // an item's token rows), an even grid, and an even number of weight tiles
     // per expert (grouped) or m_tiles and mt_base even (dense).  The scale
-    // tiles then load through these maps of 16-byte rows: sfa as
-    // [rows/128 * KT * 32][16] in 32-row boxes (one 512-byte atom), sfb as
-    // [KT * sfb_pitch][16] in boxes of 32 * ceil(n_max / 128) rows (all atoms
-    // of an item).
+    // tiles then load through these maps of 256-byte rows: sfa as
+    // [rows/128 * KT * 2][256] in 2-row boxes (one 512-byte atom), sfb as
+    // [KT * sfb_pitch / 16][256] in boxes of 2 * ceil(n_max / 128) rows (all
+    // atoms of an item; sfb_pitch and the items' first rows are multiples of
+    // 16).
     int pair;
     CUtensorMap tmSFA;
     CUtensorMap tmSFB;
