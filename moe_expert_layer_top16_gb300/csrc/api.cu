@@ -74,6 +74,24 @@ namespace {
 #ifndef MOE_PAIR_NMAX
 #define MOE_PAIR_NMAX 224
 #endif
+// item lanes (groups) of a paired launch: step 2's dense GEMMs, step 11's,
+// and the grouped ones (0: two lanes when each keeps two accumulators, else
+// one); with two lanes a CTA streams two weight row blocks at once
+#ifndef MOE_PAIR_GROUPS_DENSE
+#define MOE_PAIR_GROUPS_DENSE 1
+#endif
+#ifndef MOE_PAIR_GROUPS_UP
+#define MOE_PAIR_GROUPS_UP 2
+#endif
+#ifndef MOE_PAIR_GROUPS_GRP
+#define MOE_PAIR_GROUPS_GRP 0
+#endif
+// grouped token tile of paired launches: the mean tokens per expert m plus
+// this many tenths of sqrt(m) (a Poisson count's standard deviation), plus 8,
+// at least 80 tokens (0: 3 m as unpaired)
+#ifndef MOE_PAIR_GRP_SD10
+#define MOE_PAIR_GRP_SD10 30
+#endif
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -442,24 +460,43 @@ void shape_gemm(GemmParams& g, int E, int64_t est_items, int grid) {
 // and its scale maps; E > 0 for grouped items.  Returns the grid (an even
 // number of CTAs, at most max_grid), or 0 when the launch stays unpaired
 // (g unchanged).
-int shape_gemm_pair(GemmParams& g, int E, int64_t n_pairs, int max_grid, int clusters) {
+// Item lanes of a paired launch with items of n_max tokens.  One CTA
+// streams its weights at about 24 GB/s from one 128-row block, whatever its
+// stage count, and about twice that from two blocks at once; two lanes pay
+// off unless each would be left with a single accumulator (the epilogue of a
+// lane then stalls its MMAs), which the dense GEMMs' long items tolerate.
+int pair_groups(int want, int n_max) {
+    if (want > 0) return want;
+    return gemm_config_ok(n_max, 2, 1, 2) ? 2 : 1;
+}
+// Accumulator buffers of a paired launch of G lanes with items of n_max
+// tokens (0: its accumulators do not fit in TMEM).
+int pair_acc_bufs(int n_max, int G) {
+    for (int NB = 2; NB >= 1; --NB)
+        if (gemm_config_ok(n_max, G, 1, NB)) return NB;
+    return 0;
+}
+
+int shape_gemm_pair(GemmParams& g, int E, int64_t n_pairs, int max_grid, int clusters, int lanes) {
     if (clusters <= 0 || g.kind != KIND_MX || g.n_max <= kNarrowMax) return 0;
     if (g.dense ? ((g.m_tiles & 1) || (g.mt_base & 1)) : (g.mt_per_e & 1)) return 0;
-    if (!gemm_config_ok(g.n_max, 1, 1, 2)) return 0;
+    const int G = pair_groups(lanes, g.n_max);
+    const int NB = pair_acc_bufs(g.n_max, G);
+    if (NB == 0) return 0;
     const int64_t cl = std::min<int64_t>(std::min<int64_t>(clusters, max_grid / 2), std::max<int64_t>(n_pairs, 1));
     if (cl < 1) return 0;
     GemmParams t = g;
     t.pair = 1;
-    t.groups = 1;
+    t.groups = G;
     t.ksplit = 1;
-    t.acc_bufs = 2;
-    t.b_producer = 1;
+    t.acc_bufs = NB;
+    t.b_producer = G == 1 ? 1 : 0;
     t.b_box = pair_b_rows(t.n_max);
     t.b_row1 = 0;
     t.contiguous = 0;
     t.stage_bytes = gemm_stage_bytes(t.n_max, true);
     const bool xbuf = gemm_needs_xbuf(t);
-    t.stages = gemm_stages(t.n_max, 1, E, xbuf, true);
+    t.stages = gemm_stages(t.n_max, G, E, xbuf, true);
     if (gemm_smem_bytes(t.n_max, t.stages, E, xbuf, true) > static_cast<size_t>(kSmemLimit)) return 0;
     g = t;
     return static_cast<int>(2 * cl);
@@ -469,8 +506,16 @@ int shape_gemm_pair(GemmParams& g, int E, int64_t n_pairs, int max_grid, int clu
 // no-allocation form): items of nmax tokens, wide ones on CTA pairs where
 // that applies.  The caller encodes B with dense_box_rows() rows per box and
 // fills g's output description.
-int dense_pair_clusters(int M, int nmax) {
-    return (MOE_PAIR_TOKENS > 0 && nmax > kNarrowMax && (M / kBlockM) % 2 == 0) ? gemm_pair_clusters() : 0;
+// Token tile of the standalone dense GEMM of N tokens and M weight rows, and
+// the clusters its paired launch may use (*pair_cl = 0: unpaired).
+int dense_nmax(int M, int N, int* pair_cl) {
+    *pair_cl = 0;
+    const int nmax = pick_n_max(N, item_cap(N));
+    if (MOE_PAIR_TOKENS <= 0 || nmax <= kNarrowMax || (M / kBlockM) % 2) return nmax;
+    const int pn = pick_n_max(N, std::min(item_cap(N), std::min(MOE_PAIR_NMAX, kNMax)));
+    if (pn <= kNarrowMax || pair_acc_bufs(pn, pair_groups(MOE_PAIR_GROUPS_UP, pn)) == 0) return nmax;
+    *pair_cl = gemm_pair_clusters();
+    return *pair_cl > 0 ? pn : nmax;
 }
 int dense_box_rows(int nmax, int pair_cl) {
     return nmax <= kNarrowMax ? 16 : (pair_cl > 0 ? pair_b_rows(nmax) : nmax);
@@ -486,7 +531,7 @@ cudaError_t launch_dense_mx(GemmParams& g, int M, int N, int K, int64_t Np, int 
     int grid = 0;
     if (pair_cl > 0 && map_rows256(&g.tmSFA, atoms, static_cast<int64_t>(M) * K / 32, 2) &&
         map_rows256(&g.tmSFB, planes, static_cast<int64_t>(K / 128) * (Np + 32) * 16, 2 * ((nmax + 127) / 128)))
-        grid = shape_gemm_pair(g, 0, items / 2, sms, pair_cl);
+        grid = shape_gemm_pair(g, 0, items / 2, sms, pair_cl, MOE_PAIR_GROUPS_UP);
     if (!grid) {
         grid = std::min(items, sms);
         shape_gemm(g, 0, items, grid);
@@ -807,7 +852,12 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
     const int nmax_dense = (T <= 64) ? static_cast<int>(rup(T, 16)) : pick_n_max(T, std::min(item_cap(T), cap));
     // grouped token tile: about 3x the mean tokens per expert, 16..cap
     const int64_t per_expert = (static_cast<int64_t>(T) * k + E - 1) / E;
-    const int nmax_grp = static_cast<int>(std::min<int64_t>(std::min<int64_t>(std::max<int64_t>(rup(3 * per_expert, 16), 16), cap),
+    int64_t grp_want = 3 * per_expert;
+    if (pair_on && MOE_PAIR_GRP_SD10 > 0)
+        grp_want = std::max<int64_t>(80, per_expert + 8 +
+                                             static_cast<int64_t>(std::ceil(MOE_PAIR_GRP_SD10 * 0.1 *
+                                                                            std::sqrt(static_cast<double>(per_expert)))));
+    const int nmax_grp = static_cast<int>(std::min<int64_t>(std::min<int64_t>(std::max<int64_t>(rup(grp_want, 16), 16), cap),
                                                             rup(T, 16)));
     // experts expected to receive tokens (all of them once T * k >> E)
     const int64_t est_experts = std::min<int64_t>(E, static_cast<int64_t>(T) * k);
@@ -894,13 +944,13 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         p->pair_grp = nmax_grp;
     }
     auto try_pair = [&](GemmParams& g, const CUtensorMap& b16, const CUtensorMap& msfa, const CUtensorMap& msfb,
-                        int E_tab, int64_t n_pairs, int max_grid) -> int {
+                        int E_tab, int64_t n_pairs, int max_grid, int lanes) -> int {
         if (!pair_on) return 0;
         GemmParams t = g;
         t.tmB = b16;
         t.tmSFA = msfa;
         t.tmSFB = msfb;
-        const int grid = shape_gemm_pair(t, E_tab, n_pairs, max_grid, p->pair_clusters);
+        const int grid = shape_gemm_pair(t, E_tab, n_pairs, max_grid, p->pair_clusters, lanes);
         if (grid) g = t;
         return grid;
     };
@@ -954,14 +1004,14 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
             a2s.m_tiles = p->rowsA2 / kBlockM - L / kBlockM;
             const int items_s = a2s.m_tiles * ((T + a2s.n_max - 1) / a2s.n_max);
             a2s_grid = std::max(1, std::min(items_s, p->num_sms - MOE_SPLIT_A2_FREE_SMS));
-            const int pg = try_pair(a2s, p->tPB2, p->tSA2, p->tPS2, 0, items_s / 2, a2s_grid);
+            const int pg = try_pair(a2s, p->tPB2, p->tSA2, p->tPS2, 0, items_s / 2, a2s_grid, MOE_PAIR_GROUPS_DENSE);
             if (pg)
                 a2s_grid = pg;
             else
                 shape_gemm(a2s, 0, items_s, a2s_grid);
         }
         const int items = g.m_tiles * ((T + g.n_max - 1) / g.n_max);
-        int grid = split_a2 ? try_pair(g, p->tPB2, p->tSA2, p->tPS2, 0, items / 2, p->num_sms) : 0;
+        int grid = split_a2 ? try_pair(g, p->tPB2, p->tSA2, p->tPS2, 0, items / 2, p->num_sms, MOE_PAIR_GROUPS_DENSE) : 0;
         if (!grid) {
             grid = std::min(items, p->num_sms);
             shape_gemm(g, 0, items, grid);
@@ -1103,7 +1153,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         g.mt_per_e = 2 * I / kBlockM;
         g.rows_per_e = 2 * I;
         g.epi[0] = EpiParams{EPI_SILU_QUANT, 0, 0, 0, nullptr, 0, p->hq, Ip, p->hqsf, Rps, 1};
-        int grid = try_pair(g, p->tPB7, p->tSA7, p->tPS7, E, est_experts * g.mt_per_e / 2, p->num_sms);
+        int grid = try_pair(g, p->tPB7, p->tSA7, p->tPS7, E, est_experts * g.mt_per_e / 2, p->num_sms, MOE_PAIR_GROUPS_GRP);
         if (!grid) {
             grid = p->num_sms;
             shape_gemm(g, E, est_experts * g.mt_per_e, grid);
@@ -1130,7 +1180,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         g.mt_per_e = L / kBlockM;
         g.rows_per_e = L;
         g.epi[0] = EpiParams{EPI_F32, 0, 0, 0, p->o, L, nullptr, 0, nullptr, 0};
-        int grid = try_pair(g, p->tPB8, p->tSA8, p->tPS8, E, est_experts * g.mt_per_e / 2, p->num_sms);
+        int grid = try_pair(g, p->tPB8, p->tSA8, p->tPS8, E, est_experts * g.mt_per_e / 2, p->num_sms, MOE_PAIR_GROUPS_GRP);
         if (!grid) {
             grid = p->num_sms;
             shape_gemm(g, E, est_experts * g.mt_per_e, grid);
@@ -1169,7 +1219,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         g.epi_split = 1 << 30;
         g.epi[0] = EpiParams{EPI_F32, 0, 0, 0, static_cast<float*>(y), D, nullptr, 0, nullptr, 0, 0, p->out_bf16 ? 1 : 0};
         const int items = g.m_tiles * ((T + g.n_max - 1) / g.n_max);
-        int grid = try_pair(g, p->tPB10, p->tSA10, p->tPS10, 0, items / 2, p->num_sms);
+        int grid = try_pair(g, p->tPB10, p->tSA10, p->tPS10, 0, items / 2, p->num_sms, MOE_PAIR_GROUPS_UP);
         if (!grid) {
             grid = std::min(items, p->num_sms);
             shape_gemm(g, 0, items, grid);
@@ -1341,8 +1391,8 @@ moe_status moe_mx_gemm(const uint8_t* a_codes, const uint8_t* a_scales, int32_t 
     const size_t atom_bytes = static_cast<size_t>(M) * K / 32;
     const size_t plane_bytes = static_cast<size_t>(K / 128) * (Np + 32) * 16;    // item-atom planes
     CUtensorMap tA, tB, tB1;
-    const int nmax = pick_n_max(N, item_cap(N));
-    const int pair_cl = dense_pair_clusters(M, nmax);
+    int pair_cl = 0;
+    const int nmax = dense_nmax(M, N, &pair_cl);
     if (!map_mx4(&tA, a_codes, M, K) || !map_mx8(&tB, b_codes, N, K, dense_box_rows(nmax, pair_cl)) ||
         !map_mx8(&tB1, b_codes, N, K, 1))
         return MOE_ERR_INVALID_ARG;
@@ -1437,8 +1487,8 @@ extern "C" moe_status moe_mx_gemm_noalloc(const uint8_t* a_codes, const uint8_t*
     if (err == cudaSuccess) err = noalloc_scratch(dev, &scratch);
     if (err != cudaSuccess) return cuda_status(err);
     CUtensorMap tA, tB;
-    const int nmax = pick_n_max(N, item_cap(N));
-    const int pair_cl = dense_pair_clusters(M, nmax);
+    int pair_cl = 0;
+    const int nmax = dense_nmax(M, N, &pair_cl);
     if (!map_mx4(&tA, a_codes, M, K) || !map_mx8(&tB, b_codes, N, K, dense_box_rows(nmax, pair_cl)))
         return MOE_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -394,7 +394,12 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                         if (rank == 0) mbar_arrive_expect_tx(&fullg[stage], tx);
                         tma_load_2d_pair(sb, &p.tmA, fb, ax, w.a_row0);
                         tma_load_2d_pair(sb + L.offSFA, &p.tmSFA, fb, 0, ((w.a_row0 / kBlockM) * h.KT + kt) * 2);
-
+                        if (!h.b_producer) {
+                            // several groups: each issues its own token half and scales
+                            tma_load_2d_pair(sb + L.offB, &p.tmB, fb, bx, w.b_row0 + rank * (nm >> 1));
+                            tma_load_2d_pair(sb + L.offSFB, &p.tmSFB, fb, 0,
+                                             (static_cast<int>(kt * h.sfb_pitch) + w.b_row0) >> 4);
+                        }
                     }
                 } else if (elect_one()) {
                     mbar_arrive_expect_tx(&fullg[stage], tx);
@@ -1024,8 +1029,8 @@ cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s, bool pdl)
     if (pair) {
         // one group of whole items fed by both producers, 16-row token boxes,
         // whole pairs of weight tiles, scale maps for the paired copies
-        if (p.kind != KIND_MX || p.groups != 1 || p.ksplit != 1 || !p.b_producer || p.b_box != pair_b_rows(p.n_max) ||
-            p.b_row1)
+        if (p.kind != KIND_MX || p.groups > 2 || p.ksplit != 1 || p.b_producer != (p.groups == 1 ? 1 : 0) ||
+            p.b_box != pair_b_rows(p.n_max) || p.b_row1)
             return cudaErrorInvalidValue;
         if (grid < 2 || (grid & 1)) return cudaErrorInvalidValue;
         if (p.dense ? ((p.m_tiles & 1) || (p.mt_base & 1)) : (p.mt_per_e & 1)) return cudaErrorInvalidValue;

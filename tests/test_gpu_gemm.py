@@ -88,14 +88,14 @@ def test_gemm_random_against_oracle(M, N, K):
     check(*random_operands(rng, M, N, K), f"M={M} N={N} K={K}")
 
 
-@pytest.mark.parametrize("M,N,K", [(256, 257, 256), (512, 3601, 384), (1024, 4111, 256), (768, 1000, 1024),
+@pytest.mark.parametrize("M,N,K", [(256, 257, 256), (512, 3585, 384), (1024, 4063, 256), (768, 1000, 1024),
                                    (384, 700, 256)])
 def test_gemm_wide_items_on_cta_pairs(M, N, K):
-    # Batches above 256 tokens form wide items (up to 240 tokens); with an
-    # even number of 128-row weight tiles, two CTAs share each MMA (M = 256,
-    # each CTA loading half of the item's token rows).  Last items of 113,
-    # 1 and 31 tokens (N = 257, 3601, 4111) give pair halves of 56, 8 and 16
-    # rows; M = 384 has an odd tile count and stays unpaired.
+    # Batches above 256 tokens form wide items; with an even number of
+    # 128-row weight tiles two CTAs share each MMA (M = 256, each CTA loading
+    # half of the item's token rows) and items hold up to 224 tokens.  Last
+    # items of 113, 1 and 31 tokens (N = 257, 3585, 4063) give pair halves of
+    # 56, 8 and 16 rows; M = 384 has an odd tile count and stays unpaired.
     rng = np.random.default_rng(M * 11 + N * 3 + K)
     check(*random_operands(rng, M, N, K), f"M={M} N={N} K={K}")
 
