@@ -53,11 +53,6 @@ namespace {
 #ifndef MOE_SPLIT_A2_TOKENS
 #define MOE_SPLIT_A2_TOKENS 2048
 #endif
-// Where the side stream forks: 0 after the router estimate (beside top-k
-// and the dispatch), 1 after the routed down-projection (beside the combine).
-#ifndef MOE_SPLIT_A2_AT
-#define MOE_SPLIT_A2_AT 0
-#endif
 #ifndef MOE_SPLIT_A2_FREE_SMS
 #define MOE_SPLIT_A2_FREE_SMS 8
 #endif
@@ -893,10 +888,13 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
     // above 128 tokens the router logits are tensor-core estimates from z split
     // into TF32 head + remainder; smaller batches keep z plain
     const bool z_split = p->tc_router && T > 128;
-    // large batches run the shared experts' gate/up (the tiles of step 2 after
-    // the latent projection) on the side stream, beside the routing steps --
-    // not while per-stage events are recorded, which time the steps one by one
-    const bool split_a2 = p->side != nullptr && T >= MOE_SPLIT_A2_TOKENS && !(dbg && dbg->stage_events);
+    // large batches run step 2 as two GEMMs over the same x: the latent
+    // projection, then the shared experts' gate/up.  The second runs on the
+    // side stream beside the routing steps, or, while per-stage events are
+    // recorded (which time the steps one by one), right after the first on
+    // the caller's stream: the same kernels either way.
+    const bool split_a2 = p->side != nullptr && T >= MOE_SPLIT_A2_TOKENS;
+    const bool side_a2 = split_a2 && !(dbg && dbg->stage_events);
     GemmParams a2s;
     int a2s_grid = 0;
     cudaError_t err = cudaSuccess;
@@ -1017,6 +1015,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
             shape_gemm(g, 0, items, grid);
         }
         TRY(launch_gemm(g, grid, s, pdl(true)));
+        if (split_a2 && !side_a2) TRY(launch_gemm(a2s, a2s_grid, s, false));
     }
     // 3. router logits, 4. top-k + gates + bitmaps
     mark(2);
@@ -1051,13 +1050,12 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         else
             TRY(launch_router(p->z, 2 * L, 0, p->router, p->logits, T, E, L, s, pdl(false)));
     }
-    auto fork_a2s = [&]() {
+    if (side_a2) {
         TRY(cudaEventRecord(p->ev_fork, s));
         TRY(cudaStreamWaitEvent(p->side, p->ev_fork, 0));
         TRY(launch_gemm(a2s, a2s_grid, p->side, false));
         TRY(cudaEventRecord(p->ev_join, p->side));
-    };
-    if (split_a2 && MOE_SPLIT_A2_AT == 0) fork_a2s();
+    }
     mark(3);
     {
         TopkArgs a{};
@@ -1187,14 +1185,13 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         }
         TRY(launch_gemm(g, grid, s, pdl(true)));
     }
-    if (split_a2 && MOE_SPLIT_A2_AT == 1) fork_a2s();
     // 10. weighted combine -> MXFP8 into columns [0, L) of the concatenated activation
     mark(9);
     TRY(launch_combine(p->o, p->slot_pos, p->gw, T, k, L, p->act, p->Kcat, p->actsf, Tps, nmax_dense, p->act_bf, s,
                        pdl(false)));
     // 11. y = [cq | h_sq] [P_up | S_down]^T
     mark(10);
-    if (split_a2) TRY(cudaStreamWaitEvent(s, p->ev_join, 0));
+    if (side_a2) TRY(cudaStreamWaitEvent(s, p->ev_join, 0));
     {
         GemmParams g = gemm_base(p->tA10, p->tB10, p->a10sf, p->actsf, Tps, p->Kcat, nmax_dense, D,
                                  static_cast<int>(Tp), p->status);
@@ -1224,7 +1221,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
             grid = std::min(items, p->num_sms);
             shape_gemm(g, 0, items, grid);
         }
-        TRY(launch_gemm(g, grid, s, split_a2 ? false : pdl(true)));
+        TRY(launch_gemm(g, grid, s, side_a2 ? false : pdl(true)));
     }
     mark(MOE_NUM_STAGES);
     if (err == cudaSuccess) p->last_T = T;

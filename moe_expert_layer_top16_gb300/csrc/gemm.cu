@@ -341,9 +341,15 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
         const int ip = g / KS;
         int kb, ke;
         group_range(h.KT, g % KS, KS, kb, ke);
+        // a single-lane pair streams its K tiles as two rings: this producer
+        // the first half of the stages and K tiles, the second producer warp
+        // the rest (one CTA streams a ring at about one stage per 340 ns,
+        // two rings about twice that)
+        const bool dual = PAIR && h.b_producer;
+        if (dual) ke = (h.KT + 1) / 2;
         uint64_t* fullg = full + g * kMaxStagesPerGroup;
         uint64_t* emptyg = empty + g * kMaxStagesPerGroup;
-        const int S = S_all / G + (g < S_all % G ? 1 : 0);
+        const int S = dual ? (S_all + 1) / 2 : S_all / G + (g < S_all % G ? 1 : 0);
         uint8_t* ring = base + (g * (S_all / G) + min(g, S_all % G)) * h.stage_bytes;
         uint32_t stage = 0, phase = 0;
         uint32_t issued = 0, issued_parity = 0;   // per-stage bits for the teardown drain
@@ -394,12 +400,10 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                         if (rank == 0) mbar_arrive_expect_tx(&fullg[stage], tx);
                         tma_load_2d_pair(sb, &p.tmA, fb, ax, w.a_row0);
                         tma_load_2d_pair(sb + L.offSFA, &p.tmSFA, fb, 0, ((w.a_row0 / kBlockM) * h.KT + kt) * 2);
-                        if (!h.b_producer) {
-                            // several groups: each issues its own token half and scales
-                            tma_load_2d_pair(sb + L.offB, &p.tmB, fb, bx, w.b_row0 + rank * (nm >> 1));
-                            tma_load_2d_pair(sb + L.offSFB, &p.tmSFB, fb, 0,
-                                             (static_cast<int>(kt * h.sfb_pitch) + w.b_row0) >> 4);
-                        }
+                        // this CTA's half of the token rows, and all of their scales
+                        tma_load_2d_pair(sb + L.offB, &p.tmB, fb, bx, w.b_row0 + rank * (nm >> 1));
+                        tma_load_2d_pair(sb + L.offSFB, &p.tmSFB, fb, 0,
+                                         (static_cast<int>(kt * h.sfb_pitch) + w.b_row0) >> 4);
                     }
                 } else if (elect_one()) {
                     mbar_arrive_expect_tx(&fullg[stage], tx);
@@ -463,6 +467,17 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
         const uint32_t gcol = tmem + static_cast<uint32_t>(g) * cols_per_group;
         const uint32_t sf_base = gcol + static_cast<uint32_t>(NB * h.n_max);
         uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+        // paired launches: stage and phase of each ring (ring 1: single lane only)
+        const int pS0 = (PAIR && h.b_producer) ? (S + 1) / 2 : S, pS1 = S - pS0;
+        uint32_t pst0 = 0, pph0 = 0, pst1 = 0, pph1 = 0;
+        uint32_t pused = 0;                   // stages consumed so far: the scale columns rotate
+        // scale-column sets of a paired launch (minus one): 4 where the
+        // group's columns leave room, else 2
+        const uint32_t psets = (PAIR && h.b_producer && NB * h.n_max + 4 * 12 <= kTmemCols) ? 3u : 1u;
+        // shared-memory descriptors of stage 0 of this group's ring
+        const uint64_t pdA = PAIR ? sdesc_sw128(smem_u32(ring)) : 0, pdB = PAIR ? sdesc_sw128(smem_u32(ring + L.offB)) : 0;
+        const uint64_t pdSA = PAIR ? sdesc_rows16(smem_u32(ring + L.offSFA)) : 0,
+                       pdSB = PAIR ? sdesc_rows16(smem_u32(ring + L.offSFB)) : 0;
         bool any = false;
         int ecur = -1;
         for (int it = it_begin + ip * it_step; it < it_end && ke > kb; it += IP * it_step) {
@@ -478,6 +493,54 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
             const uint32_t d_tmem = gcol + acc * static_cast<uint32_t>(h.n_max);
+            if constexpr (PAIR) {
+                // one ring per lane, or (single lane) two rings taken in turn:
+                // K tiles 0, KT0, 1, KT0 + 1, ... -- a fixed order
+                const bool dual = h.b_producer != 0;
+                const int KT0 = dual ? (h.KT + 1) / 2 : h.KT, KT1 = h.KT - KT0;
+                const uint32_t idesc0 = idesc_mxf8f6f4(2 * kBlockM, nm, 5, 0, 0, 0);
+                for (int v = 0; v < ((w.n > 0 && rank == 0) ? h.KT : 0); ++v) {
+                    const bool r1 = (v < 2 * KT1) && (v & 1);      // the v-th stage is ring 1's
+                    const uint32_t si = r1 ? pS0 + pst1 : pst0;      // its stage index
+                    // a stage that is already full is seen so by every lane at
+                    // once: the warp-wide vote only on the waiting path
+                    if (!mbar_try_wait(&fullg[si], r1 ? pph1 : pph0)) {
+                        ok = mbar_wait(&fullg[si], r1 ? pph1 : pph0, abort_flag, h.status, DEV_TIMEOUT_MMA);
+                        if (!__all_sync(0xffffffffu, ok)) goto mma_done;
+                    }
+                    // the stage barrier orders the copies' writes before the
+                    // MMAs' reads (both async proxy): no tcgen05 fence per stage.
+                    // Descriptors of stage si: stage 0's plus its offset (the
+                    // start-address field counts 16-byte units)
+                    const uint64_t soff = static_cast<uint64_t>(si) * (static_cast<uint32_t>(h.stage_bytes) >> 4);
+                    const uint64_t adesc = pdA + soff, bdesc = pdB + soff;
+                    // consecutive stages (across items too) use different scale columns
+                    const uint32_t sfa_col = sf_base + (pused++ & psets) * 12u;
+                    const uint32_t sfb_col = sfa_col + 4u;
+                    if (elect_one()) {
+                        tc_cp_32x128b_x4_pair(sfa_col, pdSA + soff);
+                        for (int a = 0; a < natoms; ++a)
+                            tc_cp_32x128b_x4_pair(sfb_col + 4u * a, pdSB + soff + static_cast<uint64_t>(a * (512 >> 4)));
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t idesc = idesc0 | (static_cast<uint32_t>(j) << 4) | (static_cast<uint32_t>(j) << 29);
+                            mma_mxf8f6f4_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sfa_col, sfb_col,
+                                              (v | j) != 0 ? 1u : 0u);
+                        }
+                        tc_commit_pair(&emptyg[si], 3);
+                    }
+                    any = true;
+                    if (r1) {
+                        if (++pst1 == static_cast<uint32_t>(pS1)) {
+                            pst1 = 0;
+                            pph1 ^= 1;
+                        }
+                    } else if (++pst0 == static_cast<uint32_t>(pS0)) {
+                        pst0 = 0;
+                        pph0 ^= 1;
+                    }
+                }
+            } else
             for (int kt = kb; kt < ((w.n > 0 && rank == 0) ? ke : kb); ++kt) {
                 ok = mbar_wait(&fullg[stage], phase, abort_flag, h.status, DEV_TIMEOUT_MMA);
                 if (!__all_sync(0xffffffffu, ok)) goto mma_done;
@@ -507,22 +570,7 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                         // both scale operands arrive as 32x128b copy images
                         const uint32_t sfa_col = sf_base + static_cast<uint32_t>(kt & 1) * 12u;
                         const uint32_t sfb_col = sfa_col + 4u;
-                        if constexpr (PAIR) {
-                            const uint32_t idesc0 = idesc_mxf8f6f4(2 * kBlockM, nm, 5, 0, 0, 0);
-                            if (elect_one()) {
-                                tc_cp_32x128b_x4_pair(sfa_col, sdesc_rows16(smem_u32(sb + L.offSFA)));
-                                for (int a = 0; a < natoms; ++a)
-                                    tc_cp_32x128b_x4_pair(sfb_col + 4u * a, sdesc_rows16(smem_u32(sb + L.offSFB + a * 512)));
-#pragma unroll
-                                for (int j = 0; j < 4; ++j) {
-                                    const uint32_t idesc = idesc0 | (static_cast<uint32_t>(j) << 4) |
-                                                           (static_cast<uint32_t>(j) << 29);
-                                    mma_mxf8f6f4_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sfa_col, sfb_col,
-                                                      (accum_first | j) != 0 ? 1u : 0u);
-                                }
-                                tc_commit_pair(&emptyg[stage], 3);
-                            }
-                        } else {
+                        {
                         const uint32_t idesc0 = idesc_mxf8f6f4(kBlockM, nm, 5, 0, 0, 0);
                         if (elect_one()) {
                             tc_cp_32x128b_x4(sfa_col, sdesc_rows16(smem_u32(sb + L.offSFA)));
@@ -818,7 +866,72 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                 if (PAIR && rank == 1) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&tempty[g0 * 2 + acc]), 0));
             }
         }
-    } else if (h.b_producer && warp == 2 * G + 4 * kEpiGroups) {
+    } else if (PAIR && h.b_producer && warp == 2 * G + 4 * kEpiGroups) {
+        // ------------------------------------------------------------ second ring of a single-lane pair
+        // The second half of every item's K tiles through the second half of
+        // the stages: weight tile, token half and all scales, counted on the
+        // even CTA's stage barrier like producer 0's.
+        const int S0 = (S_all + 1) / 2, S = S_all - S0;
+        const int KT0 = (h.KT + 1) / 2;
+        uint64_t* fullr = full + S0;
+        uint64_t* emptyr = empty + S0;
+        uint8_t* ringr = base + S0 * h.stage_bytes;
+        uint32_t stage = 0, phase = 0;
+        uint32_t issued = 0, issued_parity = 0;
+        bool ok = true;
+        int ecur = -1;
+        const uint32_t tx = 2u * (static_cast<uint32_t>(h.a_tx_bytes) + 512u +
+                                  static_cast<uint32_t>(((h.n_max + 127) / 128) * 512 + h.b_box * kBlockK));
+        for (int it = it_begin; ok && S > 0 && it < it_end; it += it_step) {
+            const Item w = get_item(h, 2 * it + rank, ioff_s, seg_s, cnt_s, ecur);
+            if (w.n <= 0) continue;
+            const int nm = (w.n + 15) & ~15;
+            for (int kt = KT0; kt < h.KT; ++kt) {
+                ok = mbar_wait(&emptyr[stage], phase ^ 1, abort_flag, h.status, DEV_TIMEOUT_PRODUCER);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
+                const int sg = kt / h.kseg_tiles;
+                const int kin = (kt - sg * h.kseg_tiles) * kTileElems;
+                const int ax = (sg == 0 ? h.ax0 : (sg == 1 ? h.ax1 : h.ax2)) + kin;
+                const int bx = (sg == 0 ? h.bx0 : (sg == 1 ? h.bx1 : h.bx2)) + kin;
+                uint8_t* sb = ringr + stage * h.stage_bytes;
+                if (elect_one()) {
+                    const uint32_t fb = mapa_shared(smem_u32(&fullr[stage]), 0);
+                    if (rank == 0) mbar_arrive_expect_tx(&fullr[stage], tx);
+                    tma_load_2d_pair(sb, &p.tmA, fb, ax, w.a_row0);
+                    tma_load_2d_pair(sb + L.offSFA, &p.tmSFA, fb, 0, ((w.a_row0 / kBlockM) * h.KT + kt) * 2);
+                    tma_load_2d_pair(sb + L.offB, &p.tmB, fb, bx, w.b_row0 + rank * (nm >> 1));
+                    tma_load_2d_pair(sb + L.offSFB, &p.tmSFB, fb, 0,
+                                     (static_cast<int>(kt * h.sfb_pitch) + w.b_row0) >> 4);
+                }
+                __syncwarp();
+                issued |= 1u << stage;
+                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == static_cast<uint32_t>(S)) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        // the even CTA's MMAs read this CTA's stages and their commits arrive
+        // on its barriers: before this CTA may exit, every stage must have
+        // been released
+        for (int i = 0; ok && i < S; ++i) {
+            ok = mbar_wait(&emptyr[stage], phase ^ 1, abort_flag, h.status, DEV_TIMEOUT_PRODUCER);
+            ok = __all_sync(0xffffffffu, ok);
+            if (++stage == static_cast<uint32_t>(S)) {
+                stage = 0;
+                phase ^= 1;
+            }
+        }
+        if (*abort_flag && lane == 0 && rank == 0) {
+            for (int s = 0; s < S; ++s)
+                if (issued & (1u << s)) mbar_wait_teardown(&fullr[s], (issued_parity >> s) & 1u, h.status);
+        }
+        __syncwarp();
+    } else if (!PAIR && h.b_producer && warp == 2 * G + 4 * kEpiGroups) {
         // ------------------------------------------------------------ token-side producer (groups == 1)
         // Follows producer 0 stage by stage: the same items and K tiles, the
         // same free stages; it issues the token rows and their scales, whose
@@ -831,7 +944,7 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
         bool ok = true;
         int ecur = -1;
         for (int it = it_begin; ok && it < it_end; it += it_step) {
-            const Item w = get_item(h, PAIR ? 2 * it + rank : it, ioff_s, seg_s, cnt_s, ecur);
+            const Item w = get_item(h, it, ioff_s, seg_s, cnt_s, ecur);
             if (w.n <= 0) continue;
             const int nm = (w.n + 15) & ~15;
             const int natoms = (nm + 127) / 128;
@@ -848,18 +961,7 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                 const int kin = (kt - sg * h.kseg_tiles) * kTileElems;
                 const int bx = (sg == 0 ? h.bx0 : (sg == 1 ? h.bx1 : h.bx2)) + kin;
                 uint8_t* sb = base + stage * h.stage_bytes;
-                if constexpr (PAIR) {
-                    // this CTA's half of the token rows and the scale atoms of
-                    // all of them, one box each (boxes of the launch's largest
-                    // item: rows past the half and atoms past the item are
-                    // loaded but not read)
-                    if (elect_one()) {
-                        const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
-                        tma_load_2d_pair(sb + L.offB, &p.tmB, fb, bx, w.b_row0 + rank * (nm >> 1));
-                        tma_load_2d_pair(sb + L.offSFB, &p.tmSFB, fb, 0,
-                                         (static_cast<int>(kt * h.sfb_pitch) + w.b_row0) >> 4);
-                    }
-                } else if (elect_one()) {
+                if (elect_one()) {
                     if (row_loads) {
                         for (int r = 0; r < w.n; ++r)
                             tma_load_2d(sb + L.offB + r * kBlockK, &p.tmB1, &full[stage], bx, w.b_row0 + r);
@@ -881,18 +983,7 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                 }
             }
         }
-        if constexpr (PAIR) {
-            // as the weight-side producer: wait until every stage was released
-            for (int i = 0; ok && i < S; ++i) {
-                ok = mbar_wait(&empty[stage], phase ^ 1, abort_flag, h.status, DEV_TIMEOUT_PRODUCER);
-                ok = __all_sync(0xffffffffu, ok);
-                if (++stage == static_cast<uint32_t>(S)) {
-                    stage = 0;
-                    phase ^= 1;
-                }
-            }
-        }
-        if (*abort_flag && lane == 0 && rank == 0) {
+        if (*abort_flag && lane == 0) {
             for (int s = 0; s < S; ++s)
                 if (issued & (1u << s)) mbar_wait_teardown(&full[s], (issued_parity >> s) & 1u, h.status);
         }
