@@ -260,6 +260,7 @@ struct ScatterArgs {
     const uint8_t* zq; const uint8_t* zsf; int64_t zsf_pitch; int L;
     uint8_t* zq_perm; uint8_t* zq_perm_sf; int64_t perm_pitch;   // zq_perm_sf: item-atom planes
     int n_max;                // token tile of the grouped GEMM that reads zq_perm
+    int slots_per_warp;       // set by launch_scatter
 };
 cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s, bool pdl = false);
 // out_sf: item-atom planes of a dense GEMM with token tiles of n_max
