@@ -273,6 +273,7 @@ constexpr int kTopkWideTokens = MOE_TOPK_WIDE_TOKENS;  // batches up to this siz
 constexpr int kTopkPerLane = 32;     // E <= 1024
 constexpr int kMaxE = 32 * kTopkPerLane;
 constexpr int kMaxCand = 64;         // candidates ranked exactly per token (two per lane); more: exact pass over all
+constexpr int kRefineGroup = 8;      // candidates whose exact logits share one pass over z
 // Error bound of the fp32 estimate 1 / (1 + __expf(-l)) + b of sigmoid(l) + b
 // for |b| <= 1: __expf errs by at most 2 + floor(1.173 |x|) ulp (CUDA's
 // documented bound), which moves sigmoid by at most sigmoid (1 - sigmoid)
@@ -395,13 +396,13 @@ __device__ __noinline__ void topk_finish(const TopkArgs& a, int t, int lane, con
         if (lane < R) id0 = cand[lane];
         if (lane + 32 < R) id1 = cand[lane + 32];
         if (approx) {
-            // candidates in groups of up to 8 (z is read once per group)
-            for (int c = 0; c < R; c += 8) {
-                const int m = min(8, R - c);
-                int ids[8];
-                float v[8];
+            // candidates in groups of up to kRefineGroup (z is read once per group)
+            for (int c = 0; c < R; c += kRefineGroup) {
+                const int m = min(kRefineGroup, R - c);
+                int ids[kRefineGroup];
+                float v[kRefineGroup];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) ids[u] = cand[min(c + u, R - 1)];
+                for (int u = 0; u < kRefineGroup; ++u) ids[u] = cand[min(c + u, R - 1)];
                 if (m > 4)
                     exact_logits<8>(zt, a.z_lo, a.R, ids, a.L, lane, v);
                 else if (m > 2)
@@ -411,7 +412,7 @@ __device__ __noinline__ void topk_finish(const TopkArgs& a, int t, int lane, con
                 else
                     exact_logits<1>(zt, a.z_lo, a.R, ids, a.L, lane, v);
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
+                for (int u = 0; u < kRefineGroup; ++u) {
                     if (u < m && c + u == lane) l0 = v[u];
                     if (u < m && c + u == lane + 32) l1 = v[u];
                 }
@@ -928,9 +929,22 @@ __global__ void scatter_kernel(ScatterArgs a) {
 
 // ------------------------------------------------------------------ A9: combine + MXFP8
 // c[t][l] = sum_j w[t][j] * o[slot_pos[t][j]][l], slots in order, then MXFP8
-// along l.  CTA (t, chunk) covers 8 blocks of 32 columns of token t; a warp
-// owns one block (its 32 lanes = the 32 elements sharing a scale).
-constexpr int kCombineWarps = 8;
+// along l.  CTA (t, chunk) covers kCombineWarps x 128 columns of token t; a
+// warp owns 128 columns (4 MX blocks), lane i columns 4i..4i+3, so 8 lanes
+// share one scale.  The slots' 16-byte loads are issued 8 at a time before
+// their FMAs (each element's chain still runs j = 0, 1, ... in order); o is
+// read once, with the streaming hint.  L % 128 == 0.  Measured at 8,192
+// tokens: 332 us with a warp per 32 columns and 4-byte loads, 278 us with
+// this layout (2 warps a CTA; 4 warps 279 us, 7 warps 638 us; 16 loads at a
+// time 288 us).
+#ifndef MOE_COMBINE_WARPS
+#define MOE_COMBINE_WARPS 2
+#endif
+constexpr int kCombineWarps = MOE_COMBINE_WARPS;
+#ifndef MOE_COMBINE_BATCH
+#define MOE_COMBINE_BATCH 8
+#endif
+constexpr int kCombineBatch = MOE_COMBINE_BATCH;      // slots whose loads are issued together
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(
     const float* __restrict__ o, const int32_t* __restrict__ slot_pos, const float* __restrict__ w, int T, int k,
     int L, uint8_t* __restrict__ out_q, int64_t ld_q, uint8_t* __restrict__ out_sf, int64_t sf_pitch, int n_max,
@@ -946,21 +960,45 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(
         w_s[threadIdx.x] = w[static_cast<int64_t>(t) * k + threadIdx.x];
     }
     __syncthreads();
-    const int blk = blockIdx.y * kCombineWarps + warp;
-    if (blk >= L / 32) return;
-    const int col = blk * 32 + lane;
-    float acc = 0.0f;
-    for (int j = 0; j < k; ++j) acc = fmaf(w_s[j], o[static_cast<int64_t>(pos_s[j]) * L + col], acc);
+    const int b4 = blockIdx.y * kCombineWarps + warp;
+    if (b4 >= L / 128) return;
+    const int col = b4 * 128 + lane * 4;
+    float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+    for (int j0 = 0; j0 < k; j0 += kCombineBatch) {
+        float4 v[kCombineBatch];
+#pragma unroll
+        for (int u = 0; u < kCombineBatch; ++u)
+            if (j0 + u < k) v[u] = __ldcs(reinterpret_cast<const float4*>(o + static_cast<int64_t>(pos_s[j0 + u]) * L + col));
+#pragma unroll
+        for (int u = 0; u < kCombineBatch; ++u) {
+            if (j0 + u < k) {
+                const float wj = w_s[j0 + u];
+                a0 = fmaf(wj, v[u].x, a0);
+                a1 = fmaf(wj, v[u].y, a1);
+                a2 = fmaf(wj, v[u].z, a2);
+                a3 = fmaf(wj, v[u].w, a3);
+            }
+        }
+    }
     if (out_bf) {                     // mixed precision: the up-projection reads c in bf16
-        out_bf[static_cast<int64_t>(t) * ld_q + col] = __float2bfloat16_rn(acc);
+        __nv_bfloat162* d = reinterpret_cast<__nv_bfloat162*>(out_bf + static_cast<int64_t>(t) * ld_q + col);
+        d[0] = __floats2bfloat162_rn(a0, a1);
+        d[1] = __floats2bfloat162_rn(a2, a3);
         return;
     }
-    uint8_t sc;
-    const uint8_t code = warp_mx8_quant(acc, &sc);
-    out_q[static_cast<int64_t>(t) * ld_q + col] = code;
-    if (lane == 0) {
+    float amax = fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(a2), fabsf(a3)));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    const int e = mx8_exponent(amax);
+    const float inv = exp2i(-e);
+    const uint32_t packed = static_cast<uint32_t>(f32_to_e4m3(a0 * inv)) | (static_cast<uint32_t>(f32_to_e4m3(a1 * inv)) << 8) |
+                            (static_cast<uint32_t>(f32_to_e4m3(a2 * inv)) << 16) |
+                            (static_cast<uint32_t>(f32_to_e4m3(a3 * inv)) << 24);
+    *reinterpret_cast<uint32_t*>(out_q + static_cast<int64_t>(t) * ld_q + col) = packed;
+    if ((lane & 7) == 0) {
         const int b0 = (t / n_max) * n_max;
-        out_sf[sf_atom_offset(b0, t - b0, col, sf_pitch)] = sc;
+        out_sf[sf_atom_offset(b0, t - b0, col, sf_pitch)] = static_cast<uint8_t>(e + 127);
     }
 }
 
@@ -1214,8 +1252,8 @@ cudaError_t launch_scatter(const ScatterArgs& args, cudaStream_t s, bool pdl) {
 cudaError_t launch_combine(const float* o, const int32_t* slot_pos, const float* w, int T, int k, int L,
                            uint8_t* out_q, int64_t ld_q, uint8_t* out_sf, int64_t sf_pitch, int n_max,
                            __nv_bfloat16* out_bf, cudaStream_t s, bool pdl) {
-    if (n_max <= 0) return cudaErrorInvalidValue;
-    dim3 grid(T, (L / 32 + kCombineWarps - 1) / kCombineWarps);
+    if (n_max <= 0 || L % 128 || k > 32 || (ld_q & 3)) return cudaErrorInvalidValue;
+    dim3 grid(T, (L / 128 + kCombineWarps - 1) / kCombineWarps);
     return launch_ex(combine_kernel, grid, dim3(kCombineWarps * 32), 0, s, pdl, o, slot_pos, w, T, k, L, out_q, ld_q,
                      out_sf, sf_pitch, n_max, out_bf);
 }
