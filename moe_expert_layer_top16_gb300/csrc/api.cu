@@ -752,7 +752,7 @@ moe_status moe_plan(const moe_config* cfg, const moe_weights* w, int device, voi
     TRY(palloc(p, &p->xq, Tp * D));
     // token-operand scales of the GEMMs: item-atom planes with 32 spare slots
     TRY(palloc(p, &p->xsf, (D / 128) * (Tp + 32) * 16));
-    TRY(palloc(p, &p->z, sizeof(float) * Tp * 2 * L));     // TF32 high part | remainder
+    TRY(palloc(p, &p->z, sizeof(float) * Tp * 2 * L));     // TF32 high part | fp32 value (plain: the value first)
     if (p->route_hidden) TRY(palloc(p, &p->xr, sizeof(float) * Tp * D));
     TRY(palloc(p, &p->zq, Tp * L));
     TRY(palloc(p, &p->zsf, (L / 128) * Tp * 4));
@@ -885,8 +885,9 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         if (!ok) return MOE_ERR_CUDA;
         p->wide_router = nmax_router;
     }
-    // above 128 tokens the router logits are tensor-core estimates from z split
-    // into TF32 head + remainder; smaller batches keep z plain
+    // above 128 tokens the router logits are tensor-core estimates from the
+    // TF32 head of z (the rows keep the fp32 values beside it for the exact
+    // refinement); smaller batches keep z plain
     const bool z_split = p->tc_router && T > 128;
     // large batches run step 2 as two GEMMs over the same x: the latent
     // projection, then the shared experts' gate/up.  The second runs on the
@@ -989,8 +990,8 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         g.m_tiles = split_a2 ? L / kBlockM : p->rowsA2 / kBlockM;
         g.n_tokens = T;
         g.epi_split = L / kBlockM;
-        // z rows hold L values; the TF32 router estimate also wants them split
-        // into a TF32 head and its remainder (at column L), else they are plain
+        // z rows: for the TF32 router estimate the values' TF32 head, then the
+        // values themselves at column L; else the values only
         g.epi[0] = EpiParams{EPI_QUANT, 0, 0, z_split ? L : 0, p->z, 2 * L, p->zq, L, p->zsf, Tp};
         g.epi[1] = p->mixed ? EpiParams{EPI_SILU_BF16, L / kBlockM, L, 0, nullptr, 0,
                                         reinterpret_cast<uint8_t*>(p->act_bf), p->Kcat, nullptr, 0, 0}
@@ -1231,13 +1232,9 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         const int64_t TK = static_cast<int64_t>(T) * k;
         if (dbg->xq) TRY(cudaMemcpyAsync(dbg->xq, p->xq, static_cast<size_t>(T) * D, cudaMemcpyDeviceToDevice, s));
         if (dbg->xs) TRY(launch_export_sf(p->xsf, Tps, nullptr, T, D / 32, 0, dbg->xs, nmax_dense, nullptr, 0, s));
-        if (dbg->z) {
-            if (z_split)
-                TRY(launch_add_halves(p->z, T, L, dbg->z, s));
-            else
-                TRY(cudaMemcpy2DAsync(dbg->z, sizeof(float) * L, p->z, sizeof(float) * 2 * L, sizeof(float) * L, T,
-                                      cudaMemcpyDeviceToDevice, s));
-        }
+        if (dbg->z)         // split rows keep the fp32 values in their second half
+            TRY(cudaMemcpy2DAsync(dbg->z, sizeof(float) * L, p->z + (z_split ? L : 0), sizeof(float) * 2 * L,
+                                  sizeof(float) * L, T, cudaMemcpyDeviceToDevice, s));
         if (dbg->zq) TRY(cudaMemcpyAsync(dbg->zq, p->zq, static_cast<size_t>(T) * L, cudaMemcpyDeviceToDevice, s));
         if (dbg->zs) TRY(launch_export_sf(p->zsf, Tp, nullptr, T, L / 32, 0, dbg->zs, 0, nullptr, 0, s));
         if (S > 0 && dbg->hsq)

@@ -806,9 +806,8 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
 #pragma unroll
                             for (int i = 0; i < 16; ++i) {
                                 if (i >= nv) break;
-                                const float hi = tf32_round(v[i]);
-                                o[0] = hi;
-                                o[E.f32_split] = v[i] - hi;
+                                o[0] = tf32_round(v[i]);
+                                o[E.f32_split] = v[i];
                                 o += E.ld_f32;
                             }
                         } else {
@@ -828,9 +827,8 @@ __global__ void __launch_bounds__(kGemmMaxThreads, 1) mx_gemm_kernel(const __gri
                             const int64_t row = row0 + i;
                             if (E.out_f32) {
                                 if (E.f32_split) {
-                                    const float hi = tf32_round(v[i]);
-                                    E.out_f32[row * E.ld_f32 + col] = hi;
-                                    E.out_f32[row * E.ld_f32 + col + E.f32_split] = v[i] - hi;
+                                    E.out_f32[row * E.ld_f32 + col] = tf32_round(v[i]);
+                                    E.out_f32[row * E.ld_f32 + col + E.f32_split] = v[i];
                                 } else {
                                     E.out_f32[row * E.ld_f32 + col] = v[i];
                                 }

@@ -85,7 +85,7 @@ struct EpiParams {
     int mode;
     int m_tile0;
     int col0;
-    int f32_split;      // > 0: store the fp32 output as TF32 hi at col and the remainder lo at col + f32_split
+    int f32_split;      // > 0: store the fp32 output rounded to TF32 at col and as it is at col + f32_split
     float* out_f32;     // [rows][ld_f32]
     int64_t ld_f32;
     uint8_t* out_q;     // E4M3 codes [rows][ld_q]
@@ -203,7 +203,8 @@ cudaError_t launch_router_stream(const CUtensorMap& tmR, const CUtensorMap& tmZ,
                                  int c, int* status, cudaStream_t s, bool pdl = false);
 // top-k + gates (kernels.cu).  With refine, the logits are tensor-core
 // estimates z_hi R_hi (both rounded to TF32) and the candidates' exact fp32
-// logits are recomputed from z ([T][z_ld], hi | lo) and R ([E][L]).  The
+// logits are recomputed from z ([T][z_ld], z_hi | z) and R ([E][L]); the
+// remainder z_lo = z - z_hi is exact in fp32 (Sterbenz).  The
 // estimate of expert e for token t is within
 //   delta_te = |z_hi_t| |R_lo_e| + (|z_lo_t| + g_tc (1 + 2^-11) |z_hi_t|
 //              + g_32 (|z_hi_t| + |z_lo_t|)) |R_e|        (2-norms)
@@ -215,8 +216,8 @@ struct TopkArgs {
     const float* bias;
     int T, E, k, softmax;
     int refine;
-    const float* z;         // router input rows (z_ld floats): K = L values, remainders at z_lo (0: none)
-    int z_ld, z_lo;
+    const float* z;         // router input rows (z_ld floats): L TF32 heads, the fp32 values at z_lo (0: the
+    int z_ld, z_lo;         // rows are exactly TF32 and hold only the L values)
     const float* R;         // [E][L]
     const float* rnorm;     // refine: [2][E] upper bounds of |R_e| and |R_lo_e| (2-norms)
     float g_tc, g_32;       // refine: accumulation error coefficients (see above), rounded up
@@ -274,7 +275,6 @@ cudaError_t kernels_setup();   // per-device kernel attributes
 // fp32 [rows][K] -> [rows][2K] = nearest TF32 | exact remainder
 cudaError_t launch_tf32_split(const float* src, int64_t rows, int64_t K, float* dst, cudaStream_t s);
 // [rows][2K] (hi | lo) -> [rows][K] = hi + lo
-cudaError_t launch_add_halves(const float* src, int64_t rows, int64_t K, float* dst, cudaStream_t s);
 // row-major scales [rows][kb] -> item-atom planes [kb/4][pitch] of a dense
 // GEMM with token tiles of n_max
 cudaError_t launch_sf_item_planes(const uint8_t* scales_rm, int64_t rows, int64_t kb, uint8_t* planes, int64_t pitch,

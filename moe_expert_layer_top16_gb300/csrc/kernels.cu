@@ -324,7 +324,7 @@ __device__ __forceinline__ double key64(float l, const float* bias, int e) {
 }
 
 // Exact fp32 logits of NE experts e[0..NE) for the token whose router input
-// row is zt (L values, plus their exact remainders at offset lo when lo > 0):
+// row is zt (its fp32 values at offset lo, or at 0 when lo == 0):
 // lane l runs one FMA chain per expert over elements 4l + 128j .. 4l + 128j
 // + 3, j = 0, 1, ... in order, then a fixed butterfly sums the lanes; every
 // lane returns the values.  The chain of an expert does not depend on NE or
@@ -339,15 +339,9 @@ __device__ __forceinline__ void exact_logits(const float* __restrict__ zt, int l
     float acc[NE];
 #pragma unroll
     for (int u = 0; u < NE; ++u) acc[u] = 0.0f;
+    const float* zv = zt + lo;
     for (int i = 4 * lane; i < L; i += 128) {
-        float4 z4 = __ldg(reinterpret_cast<const float4*>(zt + i));
-        if (lo) {
-            const float4 q = __ldg(reinterpret_cast<const float4*>(zt + lo + i));
-            z4.x += q.x;
-            z4.y += q.y;
-            z4.z += q.z;
-            z4.w += q.w;
-        }
+        const float4 z4 = __ldg(reinterpret_cast<const float4*>(zv + i));
         float4 r4[NE];
 #pragma unroll
         for (int u = 0; u < NE; ++u) r4[u] = __ldg(reinterpret_cast<const float4*>(r[u] + i));
@@ -532,9 +526,10 @@ __device__ __forceinline__ uint32_t hi_bits(float kv, float d) {
 }
 
 // Upper bounds of the 2-norms of the TF32 head (the first L values) and of
-// the exact remainder (L values at offset lo; lo = 0: none, the row is then
-// exactly TF32) of one router input row, from fp32 sums of squares scaled by
-// `infl` (which covers their rounding).  Every lane returns both.
+// the exact remainder z - head (the fp32 values z sit at offset lo; lo = 0:
+// none, the row is then exactly TF32) of one router input row, from fp32 sums
+// of squares scaled by `infl` (which covers their rounding).  Every lane
+// returns both.
 __device__ __forceinline__ void input_norms(const float* __restrict__ zt, int lo, int L, float infl, int lane,
                                             float& nhi, float& nlo) {
     float sh = 0.0f, sl = 0.0f;
@@ -545,7 +540,8 @@ __device__ __forceinline__ void input_norms(const float* __restrict__ zt, int lo
         sh = fmaf(h.z, h.z, sh);
         sh = fmaf(h.w, h.w, sh);
         if (lo) {
-            const float4 q = __ldg(reinterpret_cast<const float4*>(zt + lo + i));
+            const float4 z = __ldg(reinterpret_cast<const float4*>(zt + lo + i));
+            const float4 q = make_float4(z.x - h.x, z.y - h.y, z.z - h.z, z.w - h.w);   // exact
             sl = fmaf(q.x, q.x, sl);
             sl = fmaf(q.y, q.y, sl);
             sl = fmaf(q.z, q.z, sl);
@@ -1107,14 +1103,6 @@ __global__ void tf32_split_kernel(const float* __restrict__ src, int64_t rows, i
     dst[r * 2 * K + K + c] = v - hi;
 }
 
-// [rows][2K] (hi | lo) -> [rows][K] fp32 sums.
-__global__ void add_halves_kernel(const float* __restrict__ src, int64_t rows, int64_t K, float* __restrict__ dst) {
-    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (i >= rows * K) return;
-    const int64_t r = i / K, c = i % K;
-    dst[i] = src[r * 2 * K + c] + src[r * 2 * K + K + c];
-}
-
 // Upper bounds of the 2-norms of router rows and of their TF32 remainders:
 // one warp per row, fp64 sums of squares (relative error below 2^-40 for rows
 // of up to 2^12 values per lane), square roots and the conversion to fp32
@@ -1285,13 +1273,6 @@ cudaError_t launch_tf32_split(const float* src, int64_t rows, int64_t K, float* 
     const int64_t n = rows * K;
     if (n == 0) return cudaSuccess;
     tf32_split_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(src, rows, K, dst);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_add_halves(const float* src, int64_t rows, int64_t K, float* dst, cudaStream_t s) {
-    const int64_t n = rows * K;
-    if (n == 0) return cudaSuccess;
-    add_halves_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(src, rows, K, dst);
     return cudaGetLastError();
 }
 
