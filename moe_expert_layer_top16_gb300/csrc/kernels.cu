@@ -7,6 +7,7 @@
 
 #include "internal.h"
 #include "mx.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 
@@ -534,13 +535,15 @@ __device__ __forceinline__ void input_norms(const float* __restrict__ zt, int lo
                                             float& nhi, float& nlo) {
     float sh = 0.0f, sl = 0.0f;
     for (int i = 4 * lane; i < L; i += 128) {
-        const float4 h = __ldg(reinterpret_cast<const float4*>(zt + i));
+        // with lo > 0 the head is recomputed from the values (the same
+        // rounding that wrote it), so only the values are read
+        const float4 z = __ldg(reinterpret_cast<const float4*>(zt + lo + i));
+        const float4 h = lo ? make_float4(tf32_round(z.x), tf32_round(z.y), tf32_round(z.z), tf32_round(z.w)) : z;
         sh = fmaf(h.x, h.x, sh);
         sh = fmaf(h.y, h.y, sh);
         sh = fmaf(h.z, h.z, sh);
         sh = fmaf(h.w, h.w, sh);
         if (lo) {
-            const float4 z = __ldg(reinterpret_cast<const float4*>(zt + lo + i));
             const float4 q = make_float4(z.x - h.x, z.y - h.y, z.z - h.z, z.w - h.w);   // exact
             sl = fmaf(q.x, q.x, sl);
             sl = fmaf(q.y, q.y, sl);
