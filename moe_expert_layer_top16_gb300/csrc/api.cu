@@ -56,6 +56,15 @@ namespace {
 #ifndef MOE_SPLIT_A2_FREE_SMS
 #define MOE_SPLIT_A2_FREE_SMS 8
 #endif
+// Inside a stream capture (a CUDA graph) the shared experts' gate/up is
+// forked after the routed down-projection instead, beside the combine (HBM-
+// bound while the tensor cores idle), with this many SMs left free of it.
+// Graph replay, 8,192 tokens: 2.346 -> 2.253 ms (8 free: 2.296); launched
+// eagerly that order lost (2.33 -> 2.47 ms: the side kernel then started
+// late), so eager forwards keep the early fork.
+#ifndef MOE_SIDE_LATE_FREE_SMS
+#define MOE_SIDE_LATE_FREE_SMS 32
+#endif
 #ifndef MOE_A_TX_BYTES
 #define MOE_A_TX_BYTES 8192
 #endif
@@ -896,6 +905,8 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
     // the caller's stream: the same kernels either way.
     const bool split_a2 = p->side != nullptr && T >= MOE_SPLIT_A2_TOKENS;
     const bool side_a2 = split_a2 && !(dbg && dbg->stage_events);
+    cudaStreamCaptureStatus capst = cudaStreamCaptureStatusNone;
+    const bool late_fork = side_a2 && cudaStreamIsCapturing(s, &capst) == cudaSuccess && capst == cudaStreamCaptureStatusActive;
     GemmParams a2s;
     int a2s_grid = 0;
     cudaError_t err = cudaSuccess;
@@ -1002,7 +1013,7 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
             a2s.mt_base = L / kBlockM;
             a2s.m_tiles = p->rowsA2 / kBlockM - L / kBlockM;
             const int items_s = a2s.m_tiles * ((T + a2s.n_max - 1) / a2s.n_max);
-            a2s_grid = std::max(1, std::min(items_s, p->num_sms - MOE_SPLIT_A2_FREE_SMS));
+            a2s_grid = std::max(1, std::min(items_s, p->num_sms - (late_fork ? MOE_SIDE_LATE_FREE_SMS : MOE_SPLIT_A2_FREE_SMS)));
             const int pg = try_pair(a2s, p->tPB2, p->tSA2, p->tPS2, 0, items_s / 2, a2s_grid, MOE_PAIR_GROUPS_DENSE);
             if (pg)
                 a2s_grid = pg;
@@ -1051,11 +1062,14 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         else
             TRY(launch_router(p->z, 2 * L, 0, p->router, p->logits, T, E, L, s, pdl(false)));
     }
-    if (side_a2) {
-        TRY(cudaEventRecord(p->ev_fork, s));
+    auto launch_a2s = [&]() {
         TRY(cudaStreamWaitEvent(p->side, p->ev_fork, 0));
         TRY(launch_gemm(a2s, a2s_grid, p->side, false));
         TRY(cudaEventRecord(p->ev_join, p->side));
+    };
+    if (side_a2 && !late_fork) {
+        TRY(cudaEventRecord(p->ev_fork, s));
+        launch_a2s();
     }
     mark(3);
     {
@@ -1187,6 +1201,10 @@ moe_status moe_forward(void* plan, const void* x, int32_t T, void* y, void* stre
         TRY(launch_gemm(g, grid, s, pdl(true)));
     }
     // 10. weighted combine -> MXFP8 into columns [0, L) of the concatenated activation
+    if (late_fork) {
+        TRY(cudaEventRecord(p->ev_fork, s));
+        launch_a2s();
+    }
     mark(9);
     TRY(launch_combine(p->o, p->slot_pos, p->gw, T, k, L, p->act, p->Kcat, p->actsf, Tps, nmax_dense, p->act_bf, s,
                        pdl(false)));
