@@ -6,6 +6,8 @@ bf16 value through the layer's first step; the MXFP4 weight encoder ("Kimi
 K3: 2.8 Trillion Parameters, Four Bits at a Time", section "Four bits from
 the start") over random blocks, planted ties, zeros and extreme exponents.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -45,6 +47,29 @@ def test_quant_x_every_finite_bf16_bit_exact():
     assert (s_gpu == s_ref).all(), f"scale mismatches: {int((s_gpu != s_ref).sum())}"
     mism = np.argwhere(q_gpu != q_ref)
     assert mism.size == 0, f"{len(mism)} code mismatches, first {[(int(bits[r, c]), int(q_gpu[r, c]), int(q_ref[r, c])) for r, c in mism[:8]]}"
+
+
+@pytest.mark.parametrize("route", ["latent", "hidden"])
+def test_quant_x_odd_tile_count_bit_exact(route):
+    # d_model = 384: three 128-wide tiles, so the quantiser's last 256-wide
+    # span has one tile and the upper half of its warp stores nothing; 203
+    # tokens leave a ragged last token tile.  Hidden routing also has the
+    # kernel write x as fp32.
+    wl = dataclasses.replace(synth.workload("tiny"), name="tiny384", d_model=384, route=route)
+    pats = finite_bf16_patterns()
+    rng = np.random.default_rng(11)
+    T = 203
+    bits = rng.choice(pats, size=(T, wl.d_model)).astype(np.uint16)
+    plan, _ = gpu_plan(wl, max_tokens=T)
+    x = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(DEV)
+    dbg = moe.debug_buffers(wl, T, DEV, fields=("xq", "xs"))
+    plan.forward(x, debug=dbg)
+    torch.cuda.synchronize()
+    assert plan.device_status() == moe.MOE_OK
+    xf = (bits.astype(np.uint32) << 16).view(np.float32)
+    q_ref, s_ref = oracle.mxfp8_quantize(xf)
+    assert (dbg["xs"].cpu().numpy() == s_ref).all()
+    assert (dbg["xq"].cpu().numpy() == q_ref).all()
 
 
 def _encoder_inputs():
