@@ -301,9 +301,11 @@ def sampled_y(wl, ol, T, x, g, y, sample):
 
 
 def grouped_item_tokens(T, k, E):
-    """Token rows per work item of the grouped GEMMs at batch size T (the
-    engine's choice: about three times the mean tokens per expert, a multiple
-    of 16 between 16 and 240, at most T rounded up to 16)."""
+    """Rows of the most loaded expert that the item parity compares at batch
+    size T: about three times the mean tokens per expert, a multiple of 16
+    between 16 and 240, at most T rounded up to 16.  The engine's work items
+    hold no more (at most 224 tokens on CTA pairs, 240 unpaired), so the rows
+    cover that expert's first work item whole."""
     per_expert = -(-T * k // E)
     return int(min(max(-(-3 * per_expert // 16) * 16, 16), 240, -(-T // 16) * 16))
 
@@ -315,9 +317,9 @@ def silu(g):
 def run_item_parity(wl, plan, ol, T, n_sample=256, x=None):
     """One forward of T tokens with the full exports, then:
       * the whole-batch exact checks (top-k on the exported logits, dispatch);
-      * the grouped GEMMs element by element on every row of the first work
-        item of the most loaded expert (a full item when that expert has that
-        many tokens): the GPU's MXFP8 activation codes and scales (A7) against
+      * the grouped GEMMs element by element on the most loaded expert's first
+        grouped_item_tokens rows (its first work item whole, and more where
+        its items are smaller): the GPU's MXFP8 activation codes and scales (A7) against
         MXFP8(SiLU(g) u) of the oracle's exact block-scaled products on the
         GPU's own latent codes, and the GPU's expert outputs (A8) against the
         oracle's exact product of the GPU's activation codes, within the

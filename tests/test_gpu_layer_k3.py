@@ -9,9 +9,10 @@ x codes exact, the selected experts' logits exact fp32, every tensor-core
 logit estimate within the layer's proven bound, selections equal to the
 oracle's (no near-tie on these uniform workloads), and y within
 max |err| <= 2e-2 rms(y_ref), sum|err| / sum|y_ref| <= 2e-3.  At 8192 and
-32768 tokens the grouped GEMMs are compared element by element on every row
-of the most loaded expert's first work item (all 240 rows of a full item at
-32768 tokens), and y on at least 256 tokens including that item's.
+32768 tokens the grouped GEMMs are compared element by element on the most
+loaded expert's first rows: its whole segment at 8192 tokens, 240 rows at
+32768 (a full 224-token work item and the next item's first 16 rows), and y
+on at least 256 tokens including those rows' tokens.
 """
 import numpy as np
 import pytest
@@ -59,4 +60,4 @@ def test_sweep_32768(k3):
     accepted, errs, counts, n_item = run_item_parity(wl, plan, ol, 32768)
     assert len(accepted) == 0
     assert counts.sum() == 32768 * 16
-    assert n_item == 240                                    # a full work item, positions 0..239
+    assert n_item == 240                                    # a full 224-token item and 16 rows of the next
