@@ -48,7 +48,9 @@ def test_prefill8192(k3):
     assert n_item == counts.max() and n_item > 146          # the whole segment of the hottest expert
 
 
-@pytest.mark.parametrize("T", [1, 8, 77, 512, 4096])
+# 1024: the first size on CTA pairs; 2048: the first with step 2 split and
+# its second part on the side stream, and two-lane grouped items
+@pytest.mark.parametrize("T", [1, 8, 77, 512, 1024, 2048, 4096])
 def test_sweep(k3, T):
     wl, plan, ol = k3
     accepted, errs, counts = run_sampled_parity(wl, plan, ol, T, np.linspace(0, T - 1, num=min(T, 24)).astype(int))
