@@ -49,9 +49,11 @@ namespace {
 // From this many tokens on, the shared experts' gate/up (the weight tiles of
 // step 2 after the latent projection) runs on a stream of its own beside the
 // routing steps, which leave the tensor cores idle; SMs kept free of it for
-// the routing kernels.
+// the routing kernels.  Both parts then run on CTA pairs (the fused step 2
+// has no paired instance): 1,024 tokens 0.858 -> 0.824 ms with graph replay,
+// 0.872 -> 0.816 ms eager; from 512 tokens the split lost with graph replay.
 #ifndef MOE_SPLIT_A2_TOKENS
-#define MOE_SPLIT_A2_TOKENS 2048
+#define MOE_SPLIT_A2_TOKENS 1024
 #endif
 #ifndef MOE_SPLIT_A2_FREE_SMS
 #define MOE_SPLIT_A2_FREE_SMS 8

@@ -1,8 +1,9 @@
 """The forward's launch paths give bit-identical outputs.
 
 A plain forward launches its kernels with programmatic dependent launch and,
-from 2048 tokens on, runs the shared experts' gate/up on the plan's side
-stream beside the routing steps.  With per-stage events recorded it launches
+from 1024 tokens on, runs the shared experts' gate/up on the plan's side
+stream (beside the routing steps, or, in a captured forward, beside the
+combine).  With per-stage events recorded it launches
 every kernel plainly, one after another, on the caller's stream.  The same
 kernels run on the same data in the same order of accumulation, so y (and
 every intermediate a later step reads) must be equal bit for bit, and

@@ -48,8 +48,8 @@ def test_prefill8192(k3):
     assert n_item == counts.max() and n_item > 146          # the whole segment of the hottest expert
 
 
-# 1024: the first size on CTA pairs; 2048: the first with step 2 split and
-# its second part on the side stream, and two-lane grouped items
+# 1024: the first size on CTA pairs, with step 2 split and its second part
+# on the side stream; 2048: the first above it
 @pytest.mark.parametrize("T", [1, 8, 77, 512, 1024, 2048, 4096])
 def test_sweep(k3, T):
     wl, plan, ol = k3
