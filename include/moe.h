@@ -190,10 +190,12 @@ MOE_API moe_status moe_plan(const moe_config *cfg, const moe_weights *w, int dev
  * default stream); no host synchronisation, no allocation.  1 <= T <=
  * max_tokens.  `dbg` may be NULL.  One plan serves one stream at a time:
  * calls on different streams that overlap race on the plan's workspace.
- * From 2048 tokens on, the shared experts' first GEMM runs on a stream the
- * plan owns, forked from `stream` by an event and joined back into it
- * before the last step, so the call stays one unit of work on `stream`
- * (and can be captured in a CUDA graph). */
+ * From 1024 tokens on (MXFP4 plans), the shared experts' first GEMM runs
+ * on a stream the plan owns, forked from `stream` by an event and joined
+ * back into it before the last step, so the call stays one unit of work on
+ * `stream` (and can be captured in a CUDA graph).  The fork follows the
+ * router when the call is launched directly and the routed down-projection
+ * when `stream` is being captured; the results are the same bit for bit. */
 MOE_API moe_status moe_forward(void *plan, const void *x, int32_t T, void *y, void *stream,
                        const moe_debug *dbg);
 
