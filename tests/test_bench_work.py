@@ -69,3 +69,22 @@ def test_mixed_scheme_bytes():
     work, _, _ = b.algorithmic_work(wl, 64, counts)
     assert work["gemm_down_shared"][0] >= (3584 + 2 * 2 * 2048) * 7168 * 2
     assert b.launches_per_forward(64, wl) == 9 and b.launches_per_forward(64, synth.workload("decode64")) == 10
+
+
+def test_traffic_record_used_only_for_its_sources(tmp_path):
+    # The stored ncu traffic of a workload is reported only while the kernel
+    # sources hash to the value recorded with it; a stale record, a missing
+    # workload or a missing file reads as no capture.
+    import json
+    b = _bench()
+    h = b.kernel_source_hash()
+    assert len(h) == 16 and all(c in "0123456789abcdef" for c in h)
+    rec = {"source_hash": h, "layer_dram_bytes": 123.0, "kernels": {"gemm_gate_up": 100.0}}
+    path = tmp_path / "traffic.json"
+    path.write_text(json.dumps({"w": rec, "old": dict(rec, source_hash="0" * 16)}))
+    b.TRAFFIC_FILE = str(path)
+    assert b.ncu_traffic("w") == (123.0, {"gemm_gate_up": 100.0})
+    assert b.ncu_traffic("old") == (None, None)
+    assert b.ncu_traffic("absent") == (None, None)
+    b.TRAFFIC_FILE = str(tmp_path / "missing.json")
+    assert b.ncu_traffic("w") == (None, None)
